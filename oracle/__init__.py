@@ -1,0 +1,196 @@
+"""CPU oracle for MoE token dispatch and combine (numpy front end over ep_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline use it to check and time against. The product package never imports
+it, and it shares no code with the CUDA library.
+
+Arrays are numpy: ids int32 [T, K], scores float32 [T, K], hidden rows float32
+[T, D] or bf16 bit patterns uint16 [T, D]. Every function below is a thin
+ctypes call into the C source, which cites the passages it follows.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from .build import build_oracle
+
+BF16, F32 = 0, 1
+ERR_BAD_ID, ERR_ROW_OOB = 1, 2
+
+_i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+_u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _kind(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float32:
+        return F32
+    raise TypeError(f"hidden rows must be uint16 (bf16 bits) or float32, got {a.dtype}")
+
+
+class Oracle:
+    """One loaded build of the oracle (mutant=0 is the real one)."""
+
+    def __init__(self, mutant: int = 0):
+        self.mutant = mutant
+        self.lib = C.CDLL(build_oracle(mutant))
+        L = self.lib
+        i64, i32 = C.c_int64, C.c_int32
+        for name, args in {
+            "oracle_ceil_div": [i64, i64],
+            "oracle_pad_tokens": [i64],
+            "oracle_num_max_tokens_pretrain": [i64, i64, i64, i64],
+            "oracle_num_max_tokens_inference": [i64, i64, i64],
+            "oracle_rank_stride": [i64, i64],
+        }.items():
+            f = getattr(L, name)
+            f.argtypes, f.restype = args, i64
+        L.oracle_bf16_from_f32.argtypes, L.oracle_bf16_from_f32.restype = [C.c_float], C.c_uint16
+        L.oracle_f32_from_bf16.argtypes, L.oracle_f32_from_bf16.restype = [C.c_uint16], C.c_float
+        u32p = C.POINTER(C.c_uint32)
+        L.oracle_routing_map.argtypes = [_i32p, _f32p, i64, i64, i32, i32, _u8p, _f32p, u32p]
+        L.oracle_layout.argtypes = [_i32p, i64, i64, i32, i32, i32, _i32p, _i32p, _i32p, _i32p,
+                                    _i32p, _i32p, C.POINTER(C.c_int64), u32p]
+        L.oracle_dispatch.argtypes = [C.c_void_p, i64, _f32p, _i32p, i64, i64, i32, i32, i32,
+                                      C.c_void_p, _f32p, _i32p, _i32p, _i32p, _i32p, _i32p,
+                                      _i32p, _i32p, C.POINTER(C.c_int64), u32p]
+        L.oracle_combine.argtypes = [C.c_void_p, C.c_int, i64, _f32p, _i32p, _i32p, i64, i64,
+                                     i32, i32, C.c_void_p, C.c_int, u32p]
+        for name in ("oracle_routing_map", "oracle_layout", "oracle_dispatch", "oracle_combine"):
+            getattr(L, name).restype = C.c_int
+
+    # -- scalars ------------------------------------------------------------
+    def ceil_div(self, a: int, b: int) -> int:
+        return int(self.lib.oracle_ceil_div(a, b))
+
+    def pad_tokens(self, n: int) -> int:
+        return int(self.lib.oracle_pad_tokens(n))
+
+    def num_max_tokens_pretrain(self, local_batch_size, seq_len, cp, tp) -> int:
+        return int(self.lib.oracle_num_max_tokens_pretrain(local_batch_size, seq_len, cp, tp))
+
+    def num_max_tokens_inference(self, max_num_batched_tokens, cp, tp) -> int:
+        return int(self.lib.oracle_num_max_tokens_inference(max_num_batched_tokens, cp, tp))
+
+    def rank_stride(self, N: int, K: int) -> int:
+        return int(self.lib.oracle_rank_stride(N, K))
+
+    def bf16_from_f32(self, a) -> np.ndarray:
+        a = np.asarray(a, dtype=np.float32).ravel()
+        return np.array([self.lib.oracle_bf16_from_f32(float(v)) for v in a], dtype=np.uint16)
+
+    def f32_from_bf16(self, h) -> np.ndarray:
+        h = np.asarray(h, dtype=np.uint16).ravel()
+        return np.array([self.lib.oracle_f32_from_bf16(int(v)) for v in h], dtype=np.float32)
+
+    # -- arrays -------------------------------------------------------------
+    def routing_map(self, ids, scores, N: int, E: int):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        scores = np.ascontiguousarray(scores, dtype=np.float32)
+        T, K = ids.shape
+        P = self.pad_tokens(N)
+        m = np.zeros((P, E), dtype=np.uint8)
+        pr = np.zeros((P, E), dtype=np.float32)
+        err = C.c_uint32(0)
+        rc = self.lib.oracle_routing_map(ids.ravel(), scores.ravel(), T, N, K, E, m.ravel(),
+                                         pr.ravel(), C.byref(err))
+        if rc:
+            raise OracleError(f"oracle_routing_map rc={rc}")
+        return m.astype(bool), pr, int(err.value)
+
+    def layout(self, ids, N: int, E: int, R: int) -> dict:
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        T, K = ids.shape
+        out = {
+            "cnt": np.zeros(E, np.int32), "expert_offset": np.zeros(E, np.int32),
+            "rows_per_rank": np.zeros(R, np.int32), "rank_prefix": np.zeros(R, np.int32),
+            "tokens_in_rank": np.zeros(R, np.int32), "pos": np.zeros((T, K), np.int32),
+        }
+        S = C.c_int64(0)
+        err = C.c_uint32(0)
+        rc = self.lib.oracle_layout(ids.ravel() if T else np.zeros(1, np.int32), T, N, K, E, R,
+                                    out["cnt"], out["expert_offset"], out["rows_per_rank"],
+                                    out["rank_prefix"], out["tokens_in_rank"],
+                                    out["pos"].ravel() if T else np.zeros(1, np.int32),
+                                    C.byref(S), C.byref(err))
+        if rc:
+            raise OracleError(f"oracle_layout rc={rc}")
+        out["S"] = int(S.value)
+        out["err"] = int(err.value)
+        return out
+
+    def dispatch(self, x, scores, ids, N: int, E: int, R: int, fill: int = 0) -> dict:
+        """Layout plus permute. Receive buffers hold R*S rows; rows that no pair
+        lands on keep the byte ``fill``."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        scores = np.ascontiguousarray(scores, dtype=np.float32)
+        x = np.ascontiguousarray(x)
+        _kind(x)
+        T, K = ids.shape
+        D = x.shape[1]
+        row_bytes = D * x.itemsize
+        S = self.rank_stride(N, K)
+        rows = R * S
+        recv_x = np.full((rows, D), 0, dtype=x.dtype)
+        recv_x.view(np.uint8)[...] = fill
+        recv_scores = np.zeros(rows, np.float32)
+        recv_src = np.full(rows, -1, np.int32)
+        lay = {
+            "cnt": np.zeros(E, np.int32), "expert_offset": np.zeros(E, np.int32),
+            "rows_per_rank": np.zeros(R, np.int32), "rank_prefix": np.zeros(R, np.int32),
+            "tokens_in_rank": np.zeros(R, np.int32), "pos": np.zeros((T, K), np.int32),
+        }
+        Sv = C.c_int64(0)
+        err = C.c_uint32(0)
+        one_i = np.zeros(1, np.int32)
+        rc = self.lib.oracle_dispatch(
+            x.ctypes.data if T else None, row_bytes, scores.ravel() if T else np.zeros(1, np.float32),
+            ids.ravel() if T else one_i, T, N, K, E, R,
+            recv_x.ctypes.data if rows else None,
+            recv_scores if rows else np.zeros(1, np.float32), recv_src if rows else one_i,
+            lay["cnt"], lay["expert_offset"], lay["rows_per_rank"], lay["rank_prefix"],
+            lay["tokens_in_rank"], lay["pos"].ravel() if T else one_i, C.byref(Sv), C.byref(err))
+        if rc:
+            raise OracleError(f"oracle_dispatch rc={rc}")
+        lay.update(S=int(Sv.value), err=int(err.value), recv_x=recv_x, recv_scores=recv_scores,
+                   recv_src=recv_src)
+        return lay
+
+    def combine(self, y, scores, pos, rank_prefix, S: int, R: int, out_dtype: str = "same"):
+        """out[T, D]; out_dtype "same" (y's kind), "bf16" or "f32". Returns (out, err)."""
+        y = np.ascontiguousarray(y)
+        yk = _kind(y)
+        scores = np.ascontiguousarray(scores, dtype=np.float32)
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        rank_prefix = np.ascontiguousarray(rank_prefix, dtype=np.int32)
+        T, K = pos.shape
+        D = y.shape[1]
+        ok = {"same": yk, "bf16": BF16, "f32": F32}[out_dtype]
+        out = np.zeros((T, D), dtype=np.uint16 if ok == BF16 else np.float32)
+        err = C.c_uint32(0)
+        rc = self.lib.oracle_combine(y.ctypes.data if y.size else None, yk, D,
+                                     scores.ravel() if T else np.zeros(1, np.float32),
+                                     pos.ravel() if T else np.zeros(1, np.int32), rank_prefix,
+                                     S, T, K, R, out.ctypes.data if T else None, ok, C.byref(err))
+        if rc:
+            raise OracleError(f"oracle_combine rc={rc}")
+        return out, int(err.value)
+
+
+_default: Oracle | None = None
+
+
+def get() -> Oracle:
+    """The real oracle (built on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle(0)
+    return _default

@@ -1,0 +1,38 @@
+"""Compile the CPU oracle (plain C, gcc) into a shared library beside this file.
+
+Test infrastructure: the oracle is what the CUDA library is checked against.
+``build_oracle(mutant=n)`` builds a deliberately broken copy (n > 0) that the
+CPU tests use to show each pin catches a plausible mistake.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "ep_oracle.c")
+
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-Wall", "-Wextra"]
+
+
+def lib_path(mutant: int = 0) -> str:
+    name = "libep_oracle.so" if mutant == 0 else f"libep_oracle_mutant{mutant}.so"
+    return os.path.join(HERE, "_build", name)
+
+
+def build_oracle(mutant: int = 0, force: bool = False) -> str:
+    out = lib_path(mutant)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(SRC)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", *CFLAGS, f"-DORACLE_MUTANT={mutant}", SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+if __name__ == "__main__":
+    print(build_oracle(force="--force" in sys.argv))

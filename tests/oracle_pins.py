@@ -1,0 +1,353 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each pin takes an oracle build and raises AssertionError when the build
+disagrees with: values the pages print (fixtures under tests/golden/, each
+cited), closed forms, a library routine computing the same quantity another
+way (numpy's stable sort and bincount, torch's bf16 cast), brute force on tiny
+inputs, or an exact result within the fp32 error bound. test_oracle_pins.py
+runs them against the real oracle; test_oracle_mutants.py runs them against
+deliberately broken oracle builds and requires every break to be caught.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _ids(seed, T, E, K):
+    return W.topk_ids_uniform(seed, T, E, K)
+
+
+def _exact_inputs(seed, T, D, K):
+    """Hidden rows and scores whose fp32 products and K-term sums are exact:
+    x = i/8 with |i| <= 64 (exact in bf16), scores = j/64 with 0 <= j <= 64."""
+    xi = (W.u64(seed, 11, T * D) % np.uint64(129)).astype(np.int64) - 64
+    x = (xi.astype(np.float32) / np.float32(8.0)).reshape(T, D)
+    sj = (W.u64(seed, 12, T * K) % np.uint64(65)).astype(np.float32)
+    return x, (sj / np.float32(64.0)).reshape(T, K)
+
+
+def _bf16_bits(a32):
+    """bf16 bit patterns of fp32 values that are exactly representable."""
+    b = np.ascontiguousarray(a32, dtype=np.float32).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0), "value not exact in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
+def _f32_from_bits(h):
+    return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Padding and capacity: worked values from the pages
+# ---------------------------------------------------------------------------
+
+def pin_padding_vectors(o):
+    g = _golden("padding_vectors.json")
+    for c in g["single"]:
+        assert o.pad_tokens(c["n"]) == c["padded"], c
+    for c in g["group"]:
+        assert o.pad_tokens(max(c["counts"])) == c["padded"], c
+
+
+def pin_padding_closed_form(o):
+    # Smallest multiple of 4 not below n, for every n in a range.
+    for n in range(0, 200):
+        p = o.pad_tokens(n)
+        assert p % 4 == 0 and n <= p < n + 4, (n, p)
+
+
+def pin_capacity(o):
+    g = _golden("capacity.json")
+    for c in g["pretrain"]:
+        got = o.num_max_tokens_pretrain(c["local_batch_size"], c["seq_len"], c["cp"], c["tp"])
+        assert got == c["expect"], (c, got)
+    for c in g["inference"]:
+        got = o.num_max_tokens_inference(c["max_num_batched_tokens"], c["cp"], c["tp"])
+        assert got == c["expect"], (c, got)
+
+
+def pin_rank_stride(o):
+    # Worst case for one rank: every pair of every padded token lands there.
+    for N, K in [(13, 2), (16, 2), (8192, 8), (3543, 8), (1, 1), (0, 4)]:
+        assert o.rank_stride(N, K) == ((N + 3) // 4) * 4 * K, (N, K)
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding: hand-worked IEEE cases and torch's cast
+# ---------------------------------------------------------------------------
+
+def pin_bf16_golden(o):
+    for f_hex, h_hex, why in _golden("bf16_rne.json")["cases"]:
+        f = np.array([int(f_hex, 16)], dtype=np.uint32).view(np.float32)
+        got = int(o.bf16_from_f32(f)[0])
+        assert got == int(h_hex, 16), (f_hex, h_hex, hex(got), why)
+
+
+def pin_bf16_vs_torch(o):
+    import torch
+    rng_bits = W.u64(5, 21, 4000).astype(np.uint32)
+    vals = rng_bits.view(np.float32)
+    vals = vals[np.isfinite(vals)]
+    # Add ties and near-ties around random kept values.
+    kept = (W.u64(6, 21, 500) & np.uint64(0x7F7F_0000)).astype(np.uint32)
+    ties = np.concatenate([kept | 0x8000, kept | 0x7FFF, kept | 0x8001,
+                           (kept | 0x1_0000) | 0x8000]).view(np.float32)
+    vals = np.concatenate([vals, ties[np.isfinite(ties)]]).astype(np.float32)
+    ref = torch.from_numpy(vals.copy()).to(torch.bfloat16).view(torch.int16).numpy()
+    got = o.bf16_from_f32(vals).view(np.int16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------------------
+# Layout: counts, prefix sums, positions
+# ---------------------------------------------------------------------------
+
+def _layout_case(seed=1, T=37, N=41, E=16, K=3, R=4):
+    ids = _ids(seed, T, E, K)
+    return ids, N, E, K, R
+
+
+def pin_counts_sum_and_bincount(o):
+    for (T, N, E, K, R) in [(37, 41, 16, 3, 4), (64, 64, 8, 2, 2), (5, 8, 256, 8, 8),
+                            (200, 203, 32, 4, 1)]:
+        ids = _ids(T + E, T, E, K)
+        lay = o.layout(ids, N, E, R)
+        assert int(lay["cnt"].sum()) == T * K                      # sum of counts = T*K
+        assert np.array_equal(lay["cnt"], np.bincount(ids.ravel(), minlength=E))
+        assert int(lay["rank_prefix"][-1]) == T * K                # true total
+        assert lay["err"] == 0
+
+
+def pin_rank_totals_brute(o):
+    ids, N, E, K, R = _layout_case(seed=3, T=29, N=31, E=12, K=4, R=3)
+    T = ids.shape[0]
+    lay = o.layout(ids, N, E, R)
+    eloc = E // R
+    rows = [0] * R
+    toks = [0] * R
+    for t in range(T):
+        seen = set()
+        for k in range(K):
+            r = int(ids[t, k]) // eloc
+            rows[r] += 1
+            seen.add(r)
+        for r in seen:
+            toks[r] += 1
+    assert lay["rows_per_rank"].tolist() == rows
+    assert lay["tokens_in_rank"].tolist() == toks
+    run, pre = 0, []
+    for r in range(R):
+        run += rows[r]
+        pre.append(run)
+    assert lay["rank_prefix"].tolist() == pre
+
+
+def pin_positions_stable_sort(o):
+    # Independent formulation: numpy's stable argsort of the flat pairs by
+    # expert id gives the receive order; the j-th pair of rank r sits at r*S + j.
+    for (seed, T, N, E, K, R) in [(4, 37, 41, 16, 3, 4), (5, 100, 100, 8, 2, 2),
+                                  (6, 13, 16, 256, 8, 8), (7, 300, 301, 64, 6, 8)]:
+        ids = _ids(seed, T, E, K)
+        lay = o.layout(ids, N, E, R)
+        S = lay["S"]
+        flat = ids.ravel().astype(np.int64)
+        order = np.argsort(flat, kind="stable")
+        ranks = flat[order] // (E // R)
+        want = np.empty(T * K, np.int64)
+        for r in range(R):
+            sel = order[ranks == r]
+            want[sel] = r * S + np.arange(sel.size)
+        assert np.array_equal(lay["pos"].ravel().astype(np.int64), want)
+        # expert offsets: first row of each non-empty expert
+        for e in range(E):
+            hits = lay["pos"].ravel()[flat == e]
+            if hits.size:
+                assert int(hits.min()) == int(lay["expert_offset"][e])
+
+
+def pin_positions_bijection(o):
+    ids, N, E, K, R = _layout_case(seed=8, T=61, N=64, E=32, K=5, R=4)
+    lay = o.layout(ids, N, E, R)
+    S = lay["S"]
+    pos = lay["pos"].ravel()
+    assert np.unique(pos).size == pos.size
+    for r in range(R):
+        mine = np.sort(pos[(pos >= r * S) & (pos < (r + 1) * S)])
+        assert np.array_equal(mine, r * S + np.arange(lay["rows_per_rank"][r]))
+
+
+def pin_stride_and_shift(o):
+    # Extents depend only on (N, K): S = pad(N) * K, and changing N moves each
+    # rank's rows by r * (S2 - S1) and nothing else.
+    ids = _ids(9, 13, 16, 2)
+    a = o.layout(ids, 13, 16, 4)
+    b = o.layout(ids, 40, 16, 4)
+    assert a["S"] == 16 * 2 and b["S"] == 40 * 2
+    ra = a["pos"] // a["S"]
+    assert np.array_equal(a["pos"] - ra * a["S"], b["pos"] - ra * b["S"])
+    assert np.array_equal(a["cnt"], b["cnt"])
+
+
+def pin_padded_rows_route_nowhere(o):
+    # Padded rows [T, P) of the routing map are all-False with zero probability;
+    # real rows carry exactly their K ids and scores.
+    T, N, E, K = 13, 13, 8, 2
+    ids = _ids(10, T, E, K)
+    sc = W.topk_scores(10, ids, E, "softmax_all")
+    m, pr, err = o.routing_map(ids, sc, N, E)
+    assert m.shape == (16, E) and err == 0
+    assert not m[T:].any() and not pr[T:].any()
+    for t in range(T):
+        assert sorted(np.nonzero(m[t])[0].tolist()) == sorted(ids[t].tolist())
+        for k in range(K):
+            assert pr[t, ids[t, k]] == sc[t, k]
+    # and the layout never counts a padded row
+    lay = o.layout(ids, N, E, 2)
+    assert int(lay["cnt"].sum()) == T * K
+
+
+def pin_bad_and_duplicate_ids(o):
+    ids = np.array([[3, 3], [8, 1], [-1, 2], [-5, 0]], dtype=np.int32)   # E = 8
+    lay = o.layout(ids, 4, 8, 2)
+    assert lay["err"] & 1
+    assert lay["pos"][1, 0] == -1 and lay["pos"][2, 0] == -1 and lay["pos"][3, 0] == -1
+    assert int(lay["cnt"][3]) == 2 and int(lay["cnt"].sum()) == 5
+    assert lay["pos"][0, 1] == lay["pos"][0, 0] + 1
+
+
+def pin_empty_call(o):
+    ids = np.zeros((0, 4), np.int32)
+    lay = o.layout(ids, 0, 8, 2)
+    assert lay["S"] == 0 and not lay["cnt"].any() and not lay["rank_prefix"].any()
+    lay = o.layout(ids, 6, 8, 2)
+    assert lay["S"] == 8 * 4 and not lay["rows_per_rank"].any()
+
+
+# ---------------------------------------------------------------------------
+# Dispatch and combine
+# ---------------------------------------------------------------------------
+
+def pin_dispatch_rows(o):
+    T, N, E, K, R, D = 23, 26, 16, 3, 4, 8
+    ids = _ids(11, T, E, K)
+    x = W.normal(11, 1, T * D).astype(np.float32).reshape(T, D)
+    sc = W.topk_scores(11, ids, E, "sigmoid_norm")
+    d = o.dispatch(x, sc, ids, N, E, R)
+    for t in range(T):
+        for k in range(K):
+            p = d["pos"][t, k]
+            assert np.array_equal(d["recv_x"][p], x[t])
+            assert d["recv_src"][p] == t * K + k
+            assert d["recv_scores"][p] == sc[t, k]
+    # rows past each rank's true total are untouched
+    used = np.zeros(R * d["S"], bool)
+    used[d["pos"].ravel()] = True
+    assert np.all(d["recv_src"][~used] == -1)
+
+
+def pin_combine_identity_exact(o):
+    # Identity experts: combine(dispatch(x))[t] = sum_k s_k * x_t, exact here.
+    T, N, E, K, R, D = 19, 20, 16, 4, 4, 24
+    ids = _ids(12, T, E, K)
+    x, sc = _exact_inputs(12, T, D, K)
+    want = (sc.astype(np.float64).sum(axis=1)[:, None] * x.astype(np.float64))
+    for kind in ("f32", "bf16"):
+        xin = x if kind == "f32" else _bf16_bits(x)
+        d = o.dispatch(xin, sc, ids, N, E, R)
+        out, err = o.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R, "f32")
+        assert err == 0
+        assert np.array_equal(out.astype(np.float64), want)
+
+
+def pin_combine_scaled_experts_exact(o):
+    # Expert e scales its rows by 2^((e mod 4) - 1): out[t] = sum_k s_k 2^j(e_k) x_t.
+    # Distinct per-expert scales catch a gather from the wrong row or k.
+    T, N, E, K, R, D = 17, 17, 8, 3, 2, 16
+    ids = _ids(13, T, E, K)
+    x, sc = _exact_inputs(13, T, D, K)
+    d = o.dispatch(x, sc, ids, N, E, R)
+    y = d["recv_x"].copy()
+    for t in range(T):
+        for k in range(K):
+            y[d["pos"][t, k]] *= np.float32(2.0 ** ((ids[t, k] % 4) - 1))
+    out, err = o.combine(y, sc, d["pos"], d["rank_prefix"], d["S"], R, "f32")
+    scale = 2.0 ** ((ids % 4) - 1)
+    want = (sc.astype(np.float64) * scale).sum(axis=1)[:, None] * x.astype(np.float64)
+    assert err == 0 and np.array_equal(out.astype(np.float64), want)
+
+
+def pin_combine_error_bound(o):
+    # General inputs: the fp32 chain of K fused multiply-adds is within
+    # K * 2^-24 * sum_k |s_k y_k| of the exact sum (fp64 here), and its bf16
+    # rounding equals torch's bf16 cast of the oracle's own fp32 value.
+    import torch
+    T, N, E, K, R, D = 31, 33, 32, 8, 8, 40
+    ids = W.topk_ids_zipf(14, T, E, K)
+    sc = W.topk_scores(14, ids, E, "sigmoid_norm")
+    x = W.hidden(14, T, D, "bf16")
+    d = o.dispatch(x, sc, ids, N, E, R)
+    out32, _ = o.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R, "f32")
+    outbf, _ = o.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R, "bf16")
+    xf = _f32_from_bits(x).astype(np.float64)
+    s64 = sc.astype(np.float64)
+    exact = s64.sum(axis=1)[:, None] * xf
+    mag = np.abs(s64).sum(axis=1)[:, None] * np.abs(xf)
+    assert np.all(np.abs(out32 - exact) <= K * 2.0 ** -24 * mag + 1e-45)
+    ref = torch.from_numpy(out32).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(outbf.view(np.int16), ref)
+
+
+def pin_unequal_count_invariance(o):
+    # The pages' functional test: with identity experts a token's combined
+    # output depends only on its own routing, so a run padded to the group max
+    # reproduces, bit for bit, the run of the same tokens at their own count
+    # and each token dispatched alone. Combos 8&3, 6&6, 5&3, 13&7.
+    E, K, R, D = 16, 4, 4, 32
+    for a, b in [(8, 3), (6, 6), (5, 3), (13, 7)]:
+        n_group = max(a, b)
+        for T in (a, b):
+            ids = _ids(100 + T, T, E, K)
+            sc = W.topk_scores(100 + T, ids, E, "sigmoid_norm")
+            x = W.hidden(100 + T, T, D, "bf16")
+            outs = []
+            for N in (T, n_group):
+                d = o.dispatch(x, sc, ids, N, E, R)
+                out, err = o.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R)
+                assert err == 0
+                outs.append(out)
+            assert np.array_equal(outs[0], outs[1])
+            for t in range(T):
+                d1 = o.dispatch(x[t:t + 1], sc[t:t + 1], ids[t:t + 1], 1, E, R)
+                o1, _ = o.combine(d1["recv_x"], sc[t:t + 1], d1["pos"], d1["rank_prefix"],
+                                  d1["S"], R)
+                assert np.array_equal(o1[0], outs[0][t])
+
+
+def pin_combine_rejects_rows_past_total(o):
+    # A row beyond its rank's true total (from the prefix sum) contributes
+    # nothing and is reported.
+    T, N, E, K, R, D = 4, 4, 4, 1, 2, 8
+    ids = np.array([[0], [1], [2], [3]], np.int32)
+    x, sc = _exact_inputs(15, T, D, K)
+    d = o.dispatch(x, sc, ids, N, E, R)
+    pos = d["pos"].copy()
+    pos[0, 0] = d["rows_per_rank"][0]        # first garbage row of rank 0
+    out, err = o.combine(d["recv_x"], sc, pos, d["rank_prefix"], d["S"], R, "f32")
+    assert err & 2
+    assert not out[0].any()
+    assert np.array_equal(out[1:], (sc[1:] * x[1:]).astype(np.float32))
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

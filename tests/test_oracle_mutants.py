@@ -1,0 +1,40 @@
+"""Every deliberately broken oracle build must fail at least one pin.
+
+Each mutant plants one plausible mistake in the oracle's C source (a dropped
+term, a wrong sign, an inclusive instead of exclusive offset, a strided
+expert-to-rank map, a stride that ignores padding, an unstable order, bf16
+truncation, pairs counted instead of tokens, the wrong alignment, floor
+instead of ceiling division, padded rows that route somewhere). The pins are
+only trusted if each of these is caught.
+"""
+import pytest
+
+from oracle import Oracle
+from oracle_pins import PINS
+
+MUTANTS = {
+    1: "combine drops the last top-k term",
+    2: "combine subtracts instead of adds",
+    3: "expert offsets inclusive instead of exclusive",
+    4: "expert-to-rank map strided instead of contiguous",
+    5: "per-rank stride ignores the padding to 4",
+    6: "rows handed out in reverse token order",
+    7: "bf16 cast truncates",
+    8: "tokens_in_rank counts pairs",
+    9: "padding to a multiple of 8",
+    10: "capacity uses floor division",
+    11: "padded rows route to experts",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=[MUTANTS[m] for m in sorted(MUTANTS)])
+def test_mutant_is_caught(mutant):
+    o = Oracle(mutant)
+    assert o.lib.oracle_mutant_id() == mutant
+    caught = []
+    for pin in PINS:
+        try:
+            pin(o)
+        except Exception:       # a failed assertion or a rejected call
+            caught.append(pin.__name__)
+    assert caught, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
