@@ -1,0 +1,509 @@
+#!/usr/bin/env python3
+"""Dispatch + combine throughput on one GB300 (tokens/s and achieved HBM GB/s).
+
+One step = one pass of the whole hot path over one batch: the layout (counts,
+prefix sums, positions), the permute into the fixed-stride receive buffer and
+the score-weighted combine back to token order. The expert between dispatch
+and combine is the identity (y = recv_x) and is not timed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload deepseek|mixtral|prefill32k|ragged|tiny]
+
+Prints ONE JSON line (rank 0). Under torchrun (N > 1) each rank runs an
+independent replica on its own GPU (the path has no exchange step: logical
+ranks are partitions of one GPU's buffer), the timed region is bracketed by a
+barrier and synchronisation, and the slowest rank's time is used.
+
+--impl reference times the CPU oracle (single-threaded C, the correctness
+reference) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s & achieved HBM GB/s vs GB300 peak (bf16, 1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "combine_topk_ids_expert_gb300", "csrc", f)
+                  for f in ("layout.cu", "permute.cu", "combine.cu", "ep_kernels.cuh")]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="deepseek", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--permute", choices=["default", "vec", "bulk"], default="default")
+    ap.add_argument("--num-sms", type=int, default=0)
+    ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="approximate CPU time spent timing the oracle")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workload description and algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def workload_desc(w: W.Workload, T: int, N: int) -> dict:
+    return {
+        "workload": (f"{w.name}: T={T} D={w.D} {w.dtype} E={w.E} K={w.K} R={w.R} "
+                     f"num_tokens_per_rank={N} num_max_tokens_per_rank={w.N_max} "
+                     f"ids={w.ids} scores={w.scores}"),
+        "T": T, "D": w.D, "E": w.E, "K": w.K, "R": w.R, "num_tokens_per_rank": N,
+        "num_max_tokens_per_rank": w.N_max,
+    }
+
+
+def algorithmic_bytes(T: int, K: int, D: int, b: int, pairs: int) -> dict:
+    """Bytes the method must move per call (pairs = routed (t, k) pairs)."""
+    row = D * b
+    layout = T * K * 4 + pairs * 4                # ids read once, pos written
+    permute = T * row + pairs * row + pairs * (4 + 4) + pairs * (4 + 4)
+    #          x read    rows written  pos+score read   recv_scores+recv_src written
+    combine = pairs * row + T * row + T * K * (4 + 4)
+    #          rows read    out written  pos+score read
+    return {"layout": layout, "permute": permute, "combine": combine,
+            "step": layout + permute + combine}
+
+
+def measured_peak_hbm() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; otherwise None."""
+    try:
+        lines = open(PROFILE_TRAFFIC).read().splitlines()
+    except OSError:
+        return None
+    src = kernel_source_hash()
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) == 4 and parts[0] == kernel and parts[1] == workload and parts[3] == src:
+            return float(parts[2])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"),
+                              ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_run(w: W.Workload, inp: dict, seconds: float, tokens_per_call: int) -> dict:
+    """Time the oracle (as it stands) on consecutive slices of the workload's
+    tokens until about `seconds` of CPU time have been spent."""
+    import oracle
+    o = oracle.get()
+    x, ids, sc = inp["x"], inp["ids"], inp["scores"]
+    T = ids.shape[0]
+    done = 0
+    t0 = time.perf_counter()
+    start = 0
+    calls = 0
+    while True:
+        n = min(tokens_per_call, T - start)
+        xs, ids_s, sc_s = x[start:start + n], ids[start:start + n], sc[start:start + n]
+        d = o.dispatch(xs, sc_s, ids_s, n, w.E, w.R)
+        o.combine(d["recv_x"], sc_s, d["pos"], d["rank_prefix"], d["S"], w.R)
+        done += n
+        calls += 1
+        start = (start + n) % T
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"tokens": done, "seconds": el, "calls": calls, "tokens_per_call": tokens_per_call}
+
+
+def oracle_tokens_per_call(w: W.Workload) -> int:
+    return 256 if w.D * w.K >= 4096 * 8 else 1024
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gb300(args) -> dict | None:
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import combine_topk_ids_expert_gb300 as ep
+    from combine_topk_ids_expert_gb300.build import build as build_lib
+    if rank == 0:
+        build_lib()
+    barrier(world)
+
+    w = W.WORKLOADS[args.workload]
+    inp = W.make(args.workload, rank=0)
+    T = inp["T"]
+    N = T if w.N is None else w.N
+    if w.T is None:   # ragged: the group max of the 8 source ranks' counts
+        N = max(W.ragged_counts(w))
+    b = w.elem_bytes
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def host(a: np.ndarray):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.pin_memory()
+
+    x_h, ids_h, sc_h = host(inp["x"]), host(inp["ids"]), host(inp["scores"])
+    x = x_h.to(dev).view(tdt) if w.dtype == "bf16" else x_h.to(dev)
+    ids = ids_h.to(dev)
+    sc = sc_h.to(dev)
+    impl = {"default": ep.EP_PERMUTE_DEFAULT, "vec": ep.EP_PERMUTE_VEC,
+            "bulk": ep.EP_PERMUTE_BULK}[args.permute]
+    buf = ep.Buffer(w.N_max, w.D, w.E, w.R, w.K, dtype=tdt, num_sms=args.num_sms,
+                    permute_impl=impl, device=dev)
+    h = buf.handle
+    out = torch.empty((T, w.D), dtype=tdt, device=dev)
+    out_code = ep.EP_BF16 if tdt == torch.bfloat16 else ep.EP_F32
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    d0 = buf.dispatch(x, sc, ids, N)
+    recv_x = d0.recv_x
+    torch.cuda.synchronize(dev)
+    pairs = int(d0.layout.tokens_per_expert.sum().item())
+    assert buf.device_error() == 0
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def step_kernels():
+        ep.ep_dispatch_layout(h, ids, T, N, sptr)
+        ep.ep_dispatch_permute(h, x, sc, sptr)
+        ep.ep_combine(h, recv_x, sc, T, out, out_code, sptr)
+
+    graph = None
+    if args.graph:
+        step_kernels()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                ep.ep_dispatch_layout(h, ids, T, N, s.cuda_stream)
+                ep.ep_dispatch_permute(h, x, sc, s.cuda_stream)
+                ep.ep_combine(h, recv_x, sc, T, out, out_code, s.cuda_stream)
+        stream.wait_stream(s)
+        torch.cuda.synchronize(dev)
+
+    # warm-up
+    for _ in range(args.warmup):
+        flush.zero_()
+        if graph is not None:
+            graph.replay()
+        else:
+            step_kernels()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    launches0 = buf.info()["kernel_launches"]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()                       # L2 flush, outside the events
+        e = ev[i]
+        if graph is not None:
+            e[0].record(stream)
+            graph.replay()
+            e[3].record(stream)
+        else:
+            e[0].record(stream)
+            ep.ep_dispatch_layout(h, ids, T, N, sptr)
+            e[1].record(stream)
+            ep.ep_dispatch_permute(h, x, sc, sptr)
+            e[2].record(stream)
+            ep.ep_combine(h, recv_x, sc, T, out, out_code, sptr)
+            e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop() if rank == 0 else None
+    launches = buf.info()["kernel_launches"] - launches0
+    if graph is not None:
+        launches = K * 4 if T > 0 else 0   # the captured graph holds the same launches
+    assert buf.device_error() == 0
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    total_ms = sum(step_ms)
+    total_ms_max = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms_max / K
+    tok_s = world * T * K / (total_ms_max / 1e3)
+    nbytes = algorithmic_bytes(T, w.K, w.D, b, pairs)
+    peak, peak_src = measured_peak_hbm()
+    res = {"ms_per_step": ms_per_step, "value": tok_s,
+           "step_ms_median": statistics.median(step_ms),
+           "hbm_gbs_step": nbytes["step"] / (ms_per_step / 1e3) / 1e9,
+           "wall_s": wall, "launches": launches, "clocks": clk}
+    if graph is None:
+        lay = [e[0].elapsed_time(e[1]) for e in ev]
+        per = [e[1].elapsed_time(e[2]) for e in ev]
+        com = [e[2].elapsed_time(e[3]) for e in ev]
+        kern = {}
+        for name, arr in (("layout", lay), ("permute", per), ("combine", com)):
+            avg = sum(arr) / len(arr)
+            kern[name] = {"avg_us": avg * 1e3, "median_us": statistics.median(arr) * 1e3,
+                          "algorithmic_bytes": nbytes[name],
+                          "achieved_gbs": nbytes[name] / (avg / 1e3) / 1e9}
+        dom = "permute" if kern["permute"]["avg_us"] >= kern["combine"]["avg_us"] else "combine"
+        ach = kern[dom]["achieved_gbs"]
+        kname = {"permute": f"permute_{buf.info()['permute_impl']}", "combine": "combine"}[dom]
+        res["kernels"] = kern
+        res["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1),
+                           "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                           "peak_source": peak_src,
+                           "traffic": profiled_traffic(kname, args.workload),
+                           "algorithmic_bytes_per_launch": nbytes[dom]}
+    res["bytes"] = nbytes
+    res["pairs"] = pairs
+    res["info"] = buf.info()
+
+    # end to end through the public API with host buffers
+    if not args.no_e2e:
+        out_h = torch.empty((T, w.D), dtype=torch.int16 if tdt == torch.bfloat16 else tdt
+                            ).pin_memory()
+        x_raw = x.view(torch.int16) if tdt == torch.bfloat16 else x
+        Ke = max(3, min(K, 200))
+        for it in range(Ke + 2):
+            if it == 2:
+                torch.cuda.synchronize(dev)
+                barrier(world)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            x_raw.copy_(x_h, non_blocking=True)
+            ids.copy_(ids_h, non_blocking=True)
+            sc.copy_(sc_h, non_blocking=True)
+            buf.dispatch(x, sc, ids, N)
+            buf.combine(recv_x, sc, out=out)
+            out_h.copy_(out.view(torch.int16) if tdt == torch.bfloat16 else out,
+                        non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        h2d = x_h.numel() * x_h.element_size() + ids_h.numel() * 4 + sc_h.numel() * 4
+        d2h = out_h.numel() * out_h.element_size()
+        res["e2e"] = {"value": world * T * Ke / (e2e_ms / 1e3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
+                      "ms_per_step": e2e_ms / Ke}
+        # the e2e output must equal the device-timed path's output
+        torch.cuda.synchronize(dev)
+    buf.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return res if rank == 0 else None
+
+
+def main():
+    args = parse_args()
+    world, rank, _ = dist_env()
+    w = W.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = W.make(args.workload, rank=0)
+        T = inp["T"]
+        N = T if w.N is None else w.N
+        tpc = oracle_tokens_per_call(w)
+        budget = max(1.0, min(args.cpu_seconds, 20.0)) / max(1, args.steps + args.warmup)
+        for _ in range(args.warmup):
+            oracle_sample_run(w, inp, budget, tpc)
+        runs = [oracle_sample_run(w, inp, budget, tpc) for _ in range(args.steps)]
+        tokens = sum(r["tokens"] for r in runs)
+        secs = sum(r["seconds"] for r in runs)
+        v = tokens / secs
+        sample = (f"{args.steps} steps of about {budget:.2f} s, each the oracle's dispatch+combine "
+                  f"over consecutive {tpc}-token slices of the workload (N = slice size)")
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": secs / len(runs) * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "config": workload_desc(w, T, N),
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line))
+        return
+
+    res = run_gb300(args)
+    if rank != 0:
+        return
+    T = W.make(args.workload, rank=0, with_x=False)["T"] if w.T is None else w.T
+    N = T if w.N is None else w.N
+    if w.T is None:
+        N = max(W.ragged_counts(w))
+    cfg = workload_desc(w, T, N)
+    cfg.update({"l2": "flushed between timed steps (memset of 2x L2)",
+                "expert": "identity (y = recv_x), not timed",
+                "permute_impl": {1: "vec", 2: "bulk"}.get(res["info"]["permute_impl"]),
+                "timing": "CUDA graph replay" if args.graph else "eager, per-kernel CUDA events",
+                "parallelism": f"replicas x{args.gpus}"})
+    line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic", "config": cfg,
+            "achieved_hbm_gbs": round(res["hbm_gbs_step"], 1),
+            "hbm_frac_step": round(res["hbm_gbs_step"] / measured_peak_hbm()[0], 4)}
+    if "roofline" in res:
+        line["roofline"] = res["roofline"]
+        line["kernels"] = res["kernels"]
+    if "e2e" in res:
+        line["e2e"] = res["e2e"]
+    line["gpu_launches"] = res["launches"]
+    line["clocks"] = res["clocks"]
+    if not args.no_cpu_baseline:
+        inp = W.make(args.workload, rank=0)
+        tpc = oracle_tokens_per_call(w)
+        r = oracle_sample_run(w, inp, args.cpu_seconds, tpc)
+        line["cpu_baseline"] = {
+            "value": r["tokens"] / r["seconds"], "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": (f"{r['calls']} oracle dispatch+combine calls over consecutive "
+                       f"{tpc}-token slices of the same workload ({r['tokens']} tokens, "
+                       f"{r['seconds']:.1f} s, single thread)")}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

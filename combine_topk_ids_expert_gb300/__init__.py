@@ -1,0 +1,302 @@
+"""GB300-native MoE expert-parallel token dispatch and combine.
+
+A thin binding over libep_gb300.so (the C ABI of include/ep.h). Every step of
+the dispatch/combine path runs in the library's CUDA kernels; this module only
+marshals arguments. PyTorch supplies device memory (the workspace and the
+caller's tensors) and streams.
+
+Module-level functions carry the C names (``ep_dispatch``, ``ep_combine``,
+...) and take a buffer handle and torch tensors. ``Buffer`` wraps them for
+everyday use and returns torch views into the workspace::
+
+    buf = Buffer(num_max_tokens_per_rank=8192, hidden=7168, num_experts=256,
+                 num_ranks=8, topk=8, dtype=torch.bfloat16)
+    d = buf.dispatch(x_TD, topk_scores_TK, topk_expert_ids_TK, num_tokens_per_rank=8192)
+    y = experts(d.recv_x)                    # [R, S, D], rows past each rank's total undefined
+    out_TD = buf.combine(y, topk_scores_TK)  # [T, D]
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import torch
+
+from . import _abi
+from ._abi import (EP_BF16, EP_DEVERR_BAD_ID, EP_DEVERR_ROW_OOB, EP_DEVERR_TIMEOUT, EP_F32,
+                   EP_PERMUTE_BULK, EP_PERMUTE_DEFAULT, EP_PERMUTE_VEC, EpBufferInfo, EpConfig,
+                   EpDispatchOut, EpError, EpLayout, check)
+
+__all__ = [
+    "Buffer", "Layout", "DispatchResult", "EpConfig", "EpError",
+    "ep_buffer_required_bytes", "ep_buffer_init", "ep_buffer_destroy", "ep_dispatch_layout",
+    "ep_dispatch", "ep_dispatch_permute", "ep_combine", "ep_get_device_error",
+    "ep_buffer_query", "ep_pad_tokens", "ep_derive_max_tokens_pretrain",
+    "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
+    "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
+    "EP_DEVERR_BAD_ID", "EP_DEVERR_ROW_OOB", "EP_DEVERR_TIMEOUT", "library_path",
+]
+
+_TORCH_TO_EP = {torch.bfloat16: EP_BF16, torch.float32: EP_F32}
+_EP_TO_TORCH = {EP_BF16: torch.bfloat16, EP_F32: torch.float32}
+
+
+def library_path() -> str:
+    return _abi.LIB_PATH
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check_dtype(t: torch.Tensor, dtype: torch.dtype, name: str) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# ---------------------------------------------------------------------------
+# C-named functions (one call each)
+# ---------------------------------------------------------------------------
+
+def ep_buffer_required_bytes(cfg: EpConfig) -> int:
+    return int(_abi.lib().ep_buffer_required_bytes(C.byref(cfg)))
+
+
+def ep_buffer_init(cfg: EpConfig, workspace: torch.Tensor) -> C.c_void_p:
+    h = C.c_void_p()
+    check(_abi.lib().ep_buffer_init(C.byref(cfg), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), C.byref(h)),
+          "ep_buffer_init")
+    return h
+
+
+def ep_buffer_destroy(handle) -> None:
+    check(_abi.lib().ep_buffer_destroy(handle), "ep_buffer_destroy")
+
+
+def ep_dispatch_layout(handle, topk_expert_ids_TK: torch.Tensor, num_tokens: int,
+                       num_tokens_per_rank: int, stream=None,
+                       host_tokens_per_expert: torch.Tensor | None = None) -> EpLayout:
+    _check_dtype(topk_expert_ids_TK, torch.int32, "topk_expert_ids_TK")
+    host = None
+    if host_tokens_per_expert is not None:
+        _check_dtype(host_tokens_per_expert, torch.int32, "host_tokens_per_expert")
+        if host_tokens_per_expert.is_cuda or not host_tokens_per_expert.is_contiguous():
+            raise ValueError("host_tokens_per_expert must be a contiguous CPU tensor")
+        host = host_tokens_per_expert.data_ptr()
+    out = EpLayout()
+    check(_abi.lib().ep_dispatch_layout(handle, _ptr(topk_expert_ids_TK), num_tokens,
+                                        num_tokens_per_rank, _stream(stream), C.byref(out), host),
+          "ep_dispatch_layout")
+    return out
+
+
+def ep_dispatch(handle, x_TD: torch.Tensor, topk_scores_TK: torch.Tensor,
+                topk_expert_ids_TK: torch.Tensor, num_tokens: int, num_tokens_per_rank: int,
+                stream=None) -> EpDispatchOut:
+    _check_dtype(topk_scores_TK, torch.float32, "topk_scores_TK")
+    _check_dtype(topk_expert_ids_TK, torch.int32, "topk_expert_ids_TK")
+    out = EpDispatchOut()
+    check(_abi.lib().ep_dispatch(handle, _ptr(x_TD), _ptr(topk_scores_TK),
+                                 _ptr(topk_expert_ids_TK), num_tokens, num_tokens_per_rank,
+                                 _stream(stream), C.byref(out)), "ep_dispatch")
+    return out
+
+
+def ep_dispatch_permute(handle, x_TD: torch.Tensor, topk_scores_TK: torch.Tensor,
+                        stream=None) -> EpDispatchOut:
+    _check_dtype(topk_scores_TK, torch.float32, "topk_scores_TK")
+    out = EpDispatchOut()
+    check(_abi.lib().ep_dispatch_permute(handle, _ptr(x_TD), _ptr(topk_scores_TK),
+                                         _stream(stream), C.byref(out)), "ep_dispatch_permute")
+    return out
+
+
+def ep_combine(handle, y_recv: torch.Tensor, topk_scores_TK: torch.Tensor, num_tokens: int,
+               out_TD: torch.Tensor, out_dtype: int, stream=None) -> None:
+    _check_dtype(topk_scores_TK, torch.float32, "topk_scores_TK")
+    check(_abi.lib().ep_combine(handle, _ptr(y_recv), _ptr(topk_scores_TK), num_tokens,
+                                _ptr(out_TD), out_dtype, _stream(stream)), "ep_combine")
+
+
+def ep_get_device_error(handle, stream=None) -> int:
+    v = C.c_uint32(0)
+    check(_abi.lib().ep_get_device_error(handle, _stream(stream), C.byref(v)),
+          "ep_get_device_error")
+    return int(v.value)
+
+
+def ep_buffer_query(handle) -> EpBufferInfo:
+    info = EpBufferInfo()
+    check(_abi.lib().ep_buffer_query(handle, C.byref(info)), "ep_buffer_query")
+    return info
+
+
+def ep_pad_tokens(n: int) -> int:
+    return int(_abi.lib().ep_pad_tokens(n))
+
+
+def ep_derive_max_tokens_pretrain(local_batch_size: int, seq_len: int, cp: int, tp: int) -> int:
+    return int(_abi.lib().ep_derive_max_tokens_pretrain(local_batch_size, seq_len, cp, tp))
+
+
+def ep_derive_max_tokens_inference(max_num_batched_tokens: int, cp: int, tp: int) -> int:
+    return int(_abi.lib().ep_derive_max_tokens_inference(max_num_batched_tokens, cp, tp))
+
+
+def ep_validate_max_tokens(configured: int, derived: int) -> int:
+    return int(_abi.lib().ep_validate_max_tokens(configured, derived))
+
+
+def ep_status_string(status: int) -> str:
+    return _abi.lib().ep_status_string(status).decode()
+
+
+# ---------------------------------------------------------------------------
+# Buffer: workspace ownership plus torch views of the results
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Layout:
+    tokens_per_expert: torch.Tensor   # [E] int32
+    expert_offset: torch.Tensor       # [E] int32
+    rows_per_rank: torch.Tensor       # [R] int32
+    rank_prefix: torch.Tensor         # [R] int32, inclusive
+    tokens_in_rank: torch.Tensor      # [R] int32
+    pos: torch.Tensor                 # [T, K] int32
+    num_tokens: int
+    padded_tokens: int
+    rank_stride: int
+
+
+@dataclass
+class DispatchResult:
+    recv_x: torch.Tensor              # [R, S, D]
+    recv_scores: torch.Tensor         # [R, S] fp32
+    recv_src: torch.Tensor            # [R, S] int32
+    layout: Layout
+
+
+class Buffer:
+    """A dispatcher buffer: one workspace sized from num_max_tokens_per_rank,
+    reused by every call (no allocation after construction)."""
+
+    def __init__(self, num_max_tokens_per_rank: int, hidden: int, num_experts: int,
+                 num_ranks: int, topk: int, dtype: torch.dtype = torch.bfloat16,
+                 num_sms: int = 0, permute_impl: int = EP_PERMUTE_DEFAULT, device=None):
+        if dtype not in _TORCH_TO_EP:
+            raise TypeError(f"dtype must be bfloat16 or float32, got {dtype}")
+        self.cfg = EpConfig(num_max_tokens_per_rank, hidden, num_experts, num_ranks, topk,
+                            _TORCH_TO_EP[dtype], num_sms, permute_impl)
+        nbytes = ep_buffer_required_bytes(self.cfg)
+        if nbytes == 0:
+            raise EpError(_abi.EP_ERR_INVALID_ARG, "ep_buffer_required_bytes")
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        self.device = dev
+        self.dtype = dtype
+        self.E, self.R, self.K, self.D = num_experts, num_ranks, topk, hidden
+        with torch.cuda.device(dev):
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.handle = ep_buffer_init(self.cfg, self.workspace)
+        self._base = self.workspace.data_ptr()
+
+    # -- views -------------------------------------------------------------
+    def _view(self, ptr: int, dtype: torch.dtype, shape: tuple) -> torch.Tensor:
+        n = 1
+        for s in shape:
+            n *= s
+        esize = torch.empty((), dtype=dtype).element_size()
+        off = ptr - self._base
+        return self.workspace[off:off + n * esize].view(dtype).view(*shape)
+
+    def _layout(self, L: EpLayout) -> Layout:
+        T, E, R, K = L.num_tokens, self.E, self.R, self.K
+        i32 = torch.int32
+        return Layout(
+            tokens_per_expert=self._view(L.tokens_per_expert, i32, (E,)),
+            expert_offset=self._view(L.expert_offset, i32, (E,)),
+            rows_per_rank=self._view(L.rows_per_rank, i32, (R,)),
+            rank_prefix=self._view(L.rank_prefix, i32, (R,)),
+            tokens_in_rank=self._view(L.tokens_in_rank, i32, (R,)),
+            pos=self._view(L.pos, i32, (T, K)),
+            num_tokens=T, padded_tokens=L.padded_tokens, rank_stride=L.rank_stride)
+
+    def _dispatch_result(self, d: EpDispatchOut) -> DispatchResult:
+        S = d.layout.rank_stride
+        return DispatchResult(
+            recv_x=self._view(d.recv_x, self.dtype, (self.R, S, self.D)),
+            recv_scores=self._view(d.recv_scores, torch.float32, (self.R, S)),
+            recv_src=self._view(d.recv_src, torch.int32, (self.R, S)),
+            layout=self._layout(d.layout))
+
+    # -- calls -------------------------------------------------------------
+    def dispatch_layout(self, topk_expert_ids_TK: torch.Tensor, num_tokens_per_rank: int,
+                        stream=None, host_counts: bool = False):
+        """Layout only. With host_counts=True also returns the per-expert
+        counts as a CPU tensor (synchronises; refused while capturing)."""
+        host = torch.empty(self.E, dtype=torch.int32) if host_counts else None
+        L = ep_dispatch_layout(self.handle, topk_expert_ids_TK, topk_expert_ids_TK.shape[0],
+                               num_tokens_per_rank, stream, host)
+        lay = self._layout(L)
+        return (lay, host) if host_counts else lay
+
+    def dispatch(self, x_TD: torch.Tensor, topk_scores_TK: torch.Tensor,
+                 topk_expert_ids_TK: torch.Tensor, num_tokens_per_rank: int | None = None,
+                 stream=None) -> DispatchResult:
+        _check_dtype(x_TD, self.dtype, "x_TD")
+        T = x_TD.shape[0]
+        N = T if num_tokens_per_rank is None else num_tokens_per_rank
+        d = ep_dispatch(self.handle, x_TD, topk_scores_TK, topk_expert_ids_TK, T, N, stream)
+        return self._dispatch_result(d)
+
+    def dispatch_permute(self, x_TD: torch.Tensor, topk_scores_TK: torch.Tensor,
+                         stream=None) -> DispatchResult:
+        _check_dtype(x_TD, self.dtype, "x_TD")
+        return self._dispatch_result(ep_dispatch_permute(self.handle, x_TD, topk_scores_TK,
+                                                         stream))
+
+    def combine(self, y_recv: torch.Tensor, topk_scores_TK: torch.Tensor,
+                out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                stream=None) -> torch.Tensor:
+        _check_dtype(y_recv, self.dtype, "y_recv")
+        T = topk_scores_TK.shape[0]
+        if out is None:
+            od = self.dtype if out_dtype is None else out_dtype
+            out = torch.empty((T, self.D), dtype=od, device=self.device)
+        if out.dtype not in _TORCH_TO_EP:
+            raise TypeError(f"out dtype must be bfloat16 or float32, got {out.dtype}")
+        ep_combine(self.handle, y_recv, topk_scores_TK, T, out, _TORCH_TO_EP[out.dtype], stream)
+        return out
+
+    def device_error(self, stream=None) -> int:
+        return ep_get_device_error(self.handle, stream)
+
+    def info(self) -> dict:
+        i = ep_buffer_query(self.handle)
+        return {f: getattr(i, f) for f, _ in EpBufferInfo._fields_}
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None:
+            ep_buffer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

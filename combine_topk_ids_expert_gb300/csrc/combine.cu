@@ -1,0 +1,193 @@
+// combine.cu - weighted un-permute of expert outputs back to token order.
+//
+// Follows "fix(moe): equalize and align per-rank token counts for HybridEP
+// dispatch", section "Fix" (combine() slices the padded rows back off: only
+// rows t < T are produced) and "ep: graph-safe worst-token HT
+// dispatch+combine", section "Internode", item 3 (the true received total is
+// read from the device prefix sum, never the padded row count: a row past
+// its rank's total is never read).
+//
+// For each token t and element d:
+//   acc = +0.0f; for k = 0..K-1 with a valid row p: acc = fmaf(s[t][k], y[p][d], acc)
+//   out[t][d] = acc rounded to the output type (bf16: round to nearest even).
+// A gather: each output element is produced by exactly one thread, in a fixed
+// k order, with no atomics, so results are bitwise reproducible. HBM-bound:
+// reads up to T*K rows, writes T rows.
+#include <cuda_bf16.h>
+
+#include "ep_kernels.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kCombineThreads = 128;
+constexpr int kLoadBatch = 8;   // rows of one token loaded before their FMAs
+
+__device__ __forceinline__ int4 ld_stream_v4(const int4* p)
+{
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Elements per 16-byte vector of the input type (0 = bf16, 1 = fp32).
+template <int IN>
+struct InVec {
+    static constexpr int kElems = IN == 0 ? 8 : 4;
+};
+
+template <int IN>
+__device__ __forceinline__ void fma_vec(float* acc, const int4& r, float w);
+
+template <>
+__device__ __forceinline__ void fma_vec<0>(float* acc, const int4& r, float w)
+{
+    const uint32_t u[4] = {(uint32_t)r.x, (uint32_t)r.y, (uint32_t)r.z, (uint32_t)r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 word.
+        const float lo = __uint_as_float(u[i] << 16);
+        const float hi = __uint_as_float(u[i] & 0xffff0000u);
+        acc[2 * i] = __fmaf_rn(w, lo, acc[2 * i]);
+        acc[2 * i + 1] = __fmaf_rn(w, hi, acc[2 * i + 1]);
+    }
+}
+
+template <>
+__device__ __forceinline__ void fma_vec<1>(float* acc, const int4& r, float w)
+{
+    acc[0] = __fmaf_rn(w, __int_as_float(r.x), acc[0]);
+    acc[1] = __fmaf_rn(w, __int_as_float(r.y), acc[1]);
+    acc[2] = __fmaf_rn(w, __int_as_float(r.z), acc[2]);
+    acc[3] = __fmaf_rn(w, __int_as_float(r.w), acc[3]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x (low address) = lo
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Stores the N = InVec<IN>::kElems accumulators of vector v of token t.
+template <int IN, int OUT>
+__device__ __forceinline__ void store_out(void* out, int64_t t, int64_t D, int64_t v,
+                                          const float* acc)
+{
+    constexpr int N = InVec<IN>::kElems;
+    const int64_t e0 = t * D + v * N;
+    if constexpr (OUT == 0) {
+        uint16_t* o = static_cast<uint16_t*>(out) + e0;
+        if constexpr (N == 8) {
+            int4 w;
+            w.x = (int)pack_bf16x2(acc[0], acc[1]);
+            w.y = (int)pack_bf16x2(acc[2], acc[3]);
+            w.z = (int)pack_bf16x2(acc[4], acc[5]);
+            w.w = (int)pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<int4*>(o) = w;
+        } else {
+            uint2 w;
+            w.x = pack_bf16x2(acc[0], acc[1]);
+            w.y = pack_bf16x2(acc[2], acc[3]);
+            *reinterpret_cast<uint2*>(o) = w;
+        }
+    } else {
+        float* o = static_cast<float*>(out) + e0;
+#pragma unroll
+        for (int i = 0; i < N; i += 4)
+            *reinterpret_cast<float4*>(o + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+    }
+}
+
+template <int IN, int OUT>
+__global__ void __launch_bounds__(kCombineThreads)
+combine_vec_kernel(CombineArgs a)
+{
+    constexpr int N = InVec<IN>::kElems;
+    __shared__ int s_pos[kMaxTopk];
+    __shared__ float s_w[kMaxTopk];
+    const int64_t V = a.D / N;
+    const int4* __restrict__ y = static_cast<const int4*>(a.y);
+
+    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+        if (threadIdx.x < a.K) {
+            const int64_t q = t * a.K + threadIdx.x;
+            int p = a.pos[q];
+            if (p >= 0) {
+                // Keep the row only if it lies inside its rank's true total.
+                const int64_t r = (int64_t)p / a.S;
+                bool ok = r < a.R;
+                if (ok) {
+                    const int lo = (r > 0) ? a.rank_prefix[r - 1] : 0;
+                    ok = ((int64_t)p - r * a.S) < (int64_t)(a.rank_prefix[r] - lo);
+                }
+                if (!ok) {
+                    atomicOr(a.err, kErrRowOob);
+                    p = -1;
+                }
+            }
+            s_pos[threadIdx.x] = p;
+            s_w[threadIdx.x] = a.scores[q];
+        }
+        __syncthreads();
+        for (int64_t v = threadIdx.x; v < V; v += kCombineThreads) {
+            float acc[N];
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i] = 0.0f;
+            for (int k0 = 0; k0 < a.K; k0 += kLoadBatch) {
+                int4 r[kLoadBatch];
+#pragma unroll
+                for (int j = 0; j < kLoadBatch; ++j) {
+                    const int k = k0 + j;
+                    const int p = (k < a.K) ? s_pos[k] : -1;
+                    if (p >= 0) r[j] = ld_stream_v4(y + (int64_t)p * V + v);
+                }
+#pragma unroll
+                for (int j = 0; j < kLoadBatch; ++j) {
+                    const int k = k0 + j;
+                    const int p = (k < a.K) ? s_pos[k] : -1;
+                    if (p >= 0) fma_vec<IN>(acc, r[j], s_w[k]);
+                }
+            }
+            store_out<IN, OUT>(a.out, t, a.D, v, acc);
+        }
+        __syncthreads();
+    }
+}
+
+template <int IN, int OUT>
+cudaError_t occupancy(int* per_sm)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, combine_vec_kernel<IN, OUT>,
+                                                         kCombineThreads, 0);
+}
+
+}  // namespace
+
+cudaError_t plan_combine(int in_dtype, int num_sms, int* grid)
+{
+    int per_sm = 0;
+    cudaError_t e = in_dtype == 0 ? occupancy<0, 0>(&per_sm) : occupancy<1, 1>(&per_sm);
+    if (e != cudaSuccess) return e;
+    *grid = num_sms * (per_sm > 0 ? per_sm : 1);
+    return cudaSuccess;
+}
+
+cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s, int64_t* launches)
+{
+    if (a.T <= 0) return cudaSuccess;
+    const unsigned g = (unsigned)(a.T < grid ? a.T : grid);
+    if (a.in_dtype == 0 && a.out_dtype == 0)
+        combine_vec_kernel<0, 0><<<g, kCombineThreads, 0, s>>>(a);
+    else if (a.in_dtype == 0 && a.out_dtype == 1)
+        combine_vec_kernel<0, 1><<<g, kCombineThreads, 0, s>>>(a);
+    else if (a.in_dtype == 1 && a.out_dtype == 0)
+        combine_vec_kernel<1, 0><<<g, kCombineThreads, 0, s>>>(a);
+    else
+        combine_vec_kernel<1, 1><<<g, kCombineThreads, 0, s>>>(a);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace ep

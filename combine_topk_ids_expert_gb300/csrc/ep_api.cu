@@ -1,0 +1,439 @@
+// ep_api.cu - the C ABI declared in include/ep.h: buffer set-up over a
+// caller-owned workspace, argument checks, and the stream-ordered calls that
+// enqueue the layout, permute and combine kernels.
+//
+// The buffer follows "Unify expert parallel token dispatcher API": the
+// lifetime maximum num_max_tokens_per_rank sizes persistent storage once
+// ("API design"; "Backend behavior": DeepEP and HybridEP preallocate), and
+// each call lays out its current capacity inside it without growing it. The
+// graph-safety rules follow "ep: graph-safe worst-token HT dispatch+combine":
+// no host handshake, no host-mapped counters, counts stay on the device.
+#include <cuda_runtime.h>
+
+#include <new>
+
+#include "ep.h"
+#include "ep_kernels.cuh"
+
+struct ep_buffer {
+    ep_config cfg;
+    int device;
+    int num_sms;
+    int64_t row_bytes;
+    int64_t s_max;          // roundup4(N_max) * K
+    int64_t max_tiles;
+    size_t ws_bytes;
+    // carved device pointers
+    uint8_t* recv_x;
+    float* recv_scores;
+    int32_t* recv_src;
+    int32_t* pos;
+    int32_t* cnt;
+    int32_t* expert_offset;
+    int32_t* rows_per_rank;
+    int32_t* rank_prefix;
+    int32_t* tokens_in_rank;
+    int32_t* tile_cnt;
+    int32_t* tile_pre;
+    int32_t* tile_tok;
+    uint32_t* err;
+    // plans
+    ep::PermutePlan permute;
+    int combine_grid;
+    // state of the last layout on this buffer (host-side scalars only)
+    bool has_layout;
+    int64_t last_T, last_N, last_S;
+    int64_t launches;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+int64_t pad4(int64_t n) { return (n + 3) / 4 * 4; }
+
+int64_t elem_bytes(int32_t dtype) { return dtype == EP_BF16 ? 2 : 4; }
+
+bool is_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Validates a configuration; fills the derived sizes. Host-only.
+bool check_config(const ep_config* c, int64_t* row_bytes, int64_t* s_max, int64_t* max_tiles)
+{
+    if (!c) return false;
+    if (c->num_max_tokens_per_rank < 1 || c->hidden < 1) return false;
+    if (c->dtype != EP_BF16 && c->dtype != EP_F32) return false;
+    if (c->num_experts < 1 || c->num_experts > ep::kMaxExperts) return false;
+    if (c->num_ranks < 1 || c->num_ranks > ep::kMaxRanks) return false;
+    if (c->num_experts % c->num_ranks != 0) return false;
+    if (c->topk < 1 || c->topk > c->num_experts || c->topk > ep::kMaxTopk) return false;
+    if (c->num_sms < 0) return false;
+    if (c->permute_impl < EP_PERMUTE_DEFAULT || c->permute_impl > EP_PERMUTE_BULK) return false;
+    const int64_t rb = c->hidden * elem_bytes(c->dtype);
+    if (rb % 16 != 0) return false;
+    const int64_t s = pad4(c->num_max_tokens_per_rank) * c->topk;
+    // Receive rows and pair indices are int32 on the device.
+    if (s > INT32_MAX / c->num_ranks) return false;
+    if (c->num_max_tokens_per_rank * c->topk > INT32_MAX) return false;
+    *row_bytes = rb;
+    *s_max = s;
+    *max_tiles = ep::layout_tiles(c->num_max_tokens_per_rank, c->topk);
+    return true;
+}
+
+struct Carve {
+    size_t off = 0;
+    size_t take(size_t bytes)
+    {
+        const size_t at = off;
+        off = align_up(off + (bytes ? bytes : 1));
+        return at;
+    }
+};
+
+struct Offsets {
+    size_t recv_x, recv_scores, recv_src, pos, cnt, expert_offset, rows_per_rank, rank_prefix,
+        tokens_in_rank, tile_cnt, tile_pre, tile_tok, err, total;
+};
+
+Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, int64_t max_tiles)
+{
+    const size_t rows = (size_t)c->num_ranks * (size_t)s_max;
+    const size_t E = (size_t)c->num_experts, R = (size_t)c->num_ranks;
+    Carve cv;
+    Offsets o;
+    o.recv_x = cv.take(rows * (size_t)row_bytes);
+    o.recv_scores = cv.take(rows * 4);
+    o.recv_src = cv.take(rows * 4);
+    o.pos = cv.take((size_t)c->num_max_tokens_per_rank * (size_t)c->topk * 4);
+    o.cnt = cv.take(E * 4);
+    o.expert_offset = cv.take(E * 4);
+    o.rows_per_rank = cv.take(R * 4);
+    o.rank_prefix = cv.take(R * 4);
+    o.tokens_in_rank = cv.take(R * 4);
+    o.tile_cnt = cv.take((size_t)max_tiles * E * 4);
+    o.tile_pre = cv.take((size_t)max_tiles * E * 4);
+    o.tile_tok = cv.take((size_t)max_tiles * R * 4);
+    o.err = cv.take(4);
+    o.total = cv.off;
+    return o;
+}
+
+cudaStream_t as_stream(ep_stream_t s) { return static_cast<cudaStream_t>(s); }
+
+// True if the stream is capturing (or the query failed: treat as capturing,
+// so no host synchronisation is attempted).
+bool capturing(cudaStream_t s)
+{
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return true;
+    return st != cudaStreamCaptureStatusNone;
+}
+
+ep_status check_call(const ep_buffer* b, const void* ids, int64_t T, int64_t N)
+{
+    if (!b) return EP_ERR_INVALID_ARG;
+    if (T < 0 || N < T) return EP_ERR_INVALID_ARG;
+    if (N > b->cfg.num_max_tokens_per_rank) return EP_ERR_CAPACITY;
+    if (T > 0 && !ids) return EP_ERR_INVALID_ARG;
+    if (!is_aligned(ids, 4)) return EP_ERR_ALIGNMENT;
+    return EP_OK;
+}
+
+void fill_layout(const ep_buffer* b, ep_layout* out)
+{
+    if (!out) return;
+    out->tokens_per_expert = b->cnt;
+    out->expert_offset = b->expert_offset;
+    out->rows_per_rank = b->rows_per_rank;
+    out->rank_prefix = b->rank_prefix;
+    out->tokens_in_rank = b->tokens_in_rank;
+    out->pos = b->pos;
+    out->num_tokens = b->last_T;
+    out->padded_tokens = pad4(b->last_N);
+    out->rank_stride = b->last_S;
+}
+
+void fill_dispatch(const ep_buffer* b, ep_dispatch_out* out)
+{
+    if (!out) return;
+    out->recv_x = b->recv_x;
+    out->recv_scores = b->recv_scores;
+    out->recv_src = b->recv_src;
+    fill_layout(b, &out->layout);
+}
+
+ep_status enqueue_layout(ep_buffer* b, const int32_t* ids, int64_t T, int64_t N, cudaStream_t s)
+{
+    ep::LayoutArgs a;
+    a.ids = ids;
+    a.T = T;
+    a.S = pad4(N) * b->cfg.topk;
+    a.K = b->cfg.topk;
+    a.E = b->cfg.num_experts;
+    a.R = b->cfg.num_ranks;
+    a.tile_cnt = b->tile_cnt;
+    a.tile_pre = b->tile_pre;
+    a.tile_tok = b->tile_tok;
+    a.cnt = b->cnt;
+    a.expert_offset = b->expert_offset;
+    a.rows_per_rank = b->rows_per_rank;
+    a.rank_prefix = b->rank_prefix;
+    a.tokens_in_rank = b->tokens_in_rank;
+    a.pos = b->pos;
+    a.err = b->err;
+    if (ep::launch_layout(a, s, &b->launches) != cudaSuccess) return EP_ERR_CUDA;
+    b->has_layout = true;
+    b->last_T = T;
+    b->last_N = N;
+    b->last_S = a.S;
+    return EP_OK;
+}
+
+ep_status enqueue_permute(ep_buffer* b, const void* x, const float* scores, cudaStream_t s)
+{
+    ep::PermuteArgs a;
+    a.x = x;
+    a.scores = scores;
+    a.pos = b->pos;
+    a.recv_x = b->recv_x;
+    a.recv_scores = b->recv_scores;
+    a.recv_src = b->recv_src;
+    a.T = b->last_T;
+    a.K = b->cfg.topk;
+    a.row_bytes = b->row_bytes;
+    a.err = b->err;
+    return ep::launch_permute(a, b->permute, s, &b->launches) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status check_rows(const ep_buffer* b, const void* x, const float* scores)
+{
+    if (b->last_T > 0 && (!x || !scores)) return EP_ERR_INVALID_ARG;
+    if (!is_aligned(x, 16) || !is_aligned(scores, 4)) return EP_ERR_ALIGNMENT;
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ep_buffer_required_bytes(const ep_config* cfg)
+{
+    int64_t rb, s_max, tiles;
+    if (!check_config(cfg, &rb, &s_max, &tiles)) return 0;
+    return layout_workspace(cfg, rb, s_max, tiles).total;
+}
+
+ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace_bytes,
+                         ep_buffer** out)
+{
+    if (!out) return EP_ERR_INVALID_ARG;
+    *out = nullptr;
+    int64_t rb, s_max, tiles;
+    if (!check_config(cfg, &rb, &s_max, &tiles)) return EP_ERR_INVALID_ARG;
+    const Offsets o = layout_workspace(cfg, rb, s_max, tiles);
+    if (!workspace || !is_aligned(workspace, kAlign) || workspace_bytes < o.total)
+        return EP_ERR_WORKSPACE;
+
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, workspace) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_WORKSPACE;
+    }
+    if ((attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) ||
+        attr.device != dev)
+        return EP_ERR_WORKSPACE;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return EP_ERR_CUDA;
+
+    ep_buffer* b = new (std::nothrow) ep_buffer();
+    if (!b) return EP_ERR_INVALID_ARG;
+    b->cfg = *cfg;
+    b->device = dev;
+    b->num_sms = (cfg->num_sms > 0 && cfg->num_sms < sms) ? cfg->num_sms : sms;
+    b->row_bytes = rb;
+    b->s_max = s_max;
+    b->max_tiles = tiles;
+    b->ws_bytes = o.total;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    b->recv_x = w + o.recv_x;
+    b->recv_scores = reinterpret_cast<float*>(w + o.recv_scores);
+    b->recv_src = reinterpret_cast<int32_t*>(w + o.recv_src);
+    b->pos = reinterpret_cast<int32_t*>(w + o.pos);
+    b->cnt = reinterpret_cast<int32_t*>(w + o.cnt);
+    b->expert_offset = reinterpret_cast<int32_t*>(w + o.expert_offset);
+    b->rows_per_rank = reinterpret_cast<int32_t*>(w + o.rows_per_rank);
+    b->rank_prefix = reinterpret_cast<int32_t*>(w + o.rank_prefix);
+    b->tokens_in_rank = reinterpret_cast<int32_t*>(w + o.tokens_in_rank);
+    b->tile_cnt = reinterpret_cast<int32_t*>(w + o.tile_cnt);
+    b->tile_pre = reinterpret_cast<int32_t*>(w + o.tile_pre);
+    b->tile_tok = reinterpret_cast<int32_t*>(w + o.tile_tok);
+    b->err = reinterpret_cast<uint32_t*>(w + o.err);
+
+    const int impl = cfg->permute_impl == EP_PERMUTE_DEFAULT ? EP_PERMUTE_BULK : cfg->permute_impl;
+    if (ep::plan_permute(impl, rb, cfg->topk, b->num_sms, &b->permute) != cudaSuccess ||
+        ep::plan_combine(cfg->dtype == EP_BF16 ? 0 : 1, b->num_sms, &b->combine_grid) !=
+            cudaSuccess ||
+        cudaMemset(b->err, 0, sizeof(uint32_t)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        delete b;
+        return EP_ERR_CUDA;
+    }
+    *out = b;
+    return EP_OK;
+}
+
+ep_status ep_buffer_destroy(ep_buffer* buf)
+{
+    delete buf;
+    return EP_OK;
+}
+
+ep_status ep_dispatch_layout(ep_buffer* buf, const int32_t* ids, int64_t T, int64_t N,
+                             ep_stream_t stream, ep_layout* out, int32_t* host_counts)
+{
+    ep_status st = check_call(buf, ids, T, N);
+    if (st != EP_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    if (host_counts && capturing(s)) return EP_ERR_CAPTURE_HOST_SYNC;
+    st = enqueue_layout(buf, ids, T, N, s);
+    if (st != EP_OK) return st;
+    fill_layout(buf, out);
+    if (host_counts) {
+        if (cudaMemcpyAsync(host_counts, buf->cnt, sizeof(int32_t) * buf->cfg.num_experts,
+                            cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+ep_status ep_dispatch(ep_buffer* buf, const void* x, const float* scores, const int32_t* ids,
+                      int64_t T, int64_t N, ep_stream_t stream, ep_dispatch_out* out)
+{
+    ep_status st = check_call(buf, ids, T, N);
+    if (st != EP_OK) return st;
+    if (T > 0 && (!x || !scores)) return EP_ERR_INVALID_ARG;
+    if (!is_aligned(x, 16) || !is_aligned(scores, 4)) return EP_ERR_ALIGNMENT;
+    cudaStream_t s = as_stream(stream);
+    st = enqueue_layout(buf, ids, T, N, s);
+    if (st != EP_OK) return st;
+    st = enqueue_permute(buf, x, scores, s);
+    if (st != EP_OK) return st;
+    fill_dispatch(buf, out);
+    return EP_OK;
+}
+
+ep_status ep_dispatch_permute(ep_buffer* buf, const void* x, const float* scores,
+                              ep_stream_t stream, ep_dispatch_out* out)
+{
+    if (!buf) return EP_ERR_INVALID_ARG;
+    if (!buf->has_layout) return EP_ERR_NO_LAYOUT;
+    ep_status st = check_rows(buf, x, scores);
+    if (st != EP_OK) return st;
+    st = enqueue_permute(buf, x, scores, as_stream(stream));
+    if (st != EP_OK) return st;
+    fill_dispatch(buf, out);
+    return EP_OK;
+}
+
+ep_status ep_combine(ep_buffer* buf, const void* y, const float* scores, int64_t T, void* out,
+                     int32_t out_dtype, ep_stream_t stream)
+{
+    if (!buf) return EP_ERR_INVALID_ARG;
+    if (!buf->has_layout || T != buf->last_T) return EP_ERR_NO_LAYOUT;
+    if (out_dtype != EP_BF16 && out_dtype != EP_F32) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!y || !scores || !out)) return EP_ERR_INVALID_ARG;
+    if (!is_aligned(y, 16) || !is_aligned(out, 16) || !is_aligned(scores, 4))
+        return EP_ERR_ALIGNMENT;
+    ep::CombineArgs a;
+    a.y = y;
+    a.scores = scores;
+    a.pos = buf->pos;
+    a.rank_prefix = buf->rank_prefix;
+    a.out = out;
+    a.T = T;
+    a.K = buf->cfg.topk;
+    a.R = buf->cfg.num_ranks;
+    a.S = buf->last_S;
+    a.D = buf->cfg.hidden;
+    a.in_dtype = buf->cfg.dtype == EP_BF16 ? 0 : 1;
+    a.out_dtype = out_dtype == EP_BF16 ? 0 : 1;
+    a.err = buf->err;
+    if (ep::launch_combine(a, buf->combine_grid, as_stream(stream), &buf->launches) != cudaSuccess)
+        return EP_ERR_CUDA;
+    return EP_OK;
+}
+
+ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flags)
+{
+    if (!buf || !flags) return EP_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (capturing(s)) return EP_ERR_CAPTURE_HOST_SYNC;
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, buf->err, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(buf->err, 0, sizeof v, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return EP_ERR_CUDA;
+    *flags = v;
+    return EP_OK;
+}
+
+ep_status ep_buffer_query(const ep_buffer* buf, ep_buffer_info* info)
+{
+    if (!buf || !info) return EP_ERR_INVALID_ARG;
+    info->workspace_bytes = (int64_t)buf->ws_bytes;
+    info->max_rank_stride = buf->s_max;
+    info->kernel_launches = buf->launches;
+    info->device = buf->device;
+    info->num_sms = buf->num_sms;
+    info->permute_impl = buf->permute.impl;
+    info->permute_grid = buf->permute.grid;
+    info->combine_grid = buf->combine_grid;
+    info->bulk_stages = buf->permute.stages;
+    return EP_OK;
+}
+
+int64_t ep_pad_tokens(int64_t n) { return n < 0 ? -1 : pad4(n); }
+
+int64_t ep_derive_max_tokens_pretrain(int64_t local_batch_size, int64_t seq_len, int64_t cp,
+                                      int64_t tp)
+{
+    if (local_batch_size <= 0 || seq_len <= 0 || cp <= 0 || tp <= 0) return -1;
+    const int64_t shards = cp * tp;
+    return local_batch_size * ((seq_len + shards - 1) / shards);
+}
+
+int64_t ep_derive_max_tokens_inference(int64_t max_num_batched_tokens, int64_t cp, int64_t tp)
+{
+    if (max_num_batched_tokens <= 0 || cp <= 0 || tp <= 0) return -1;
+    const int64_t shards = cp * tp;
+    return (max_num_batched_tokens + shards - 1) / shards;
+}
+
+ep_status ep_validate_max_tokens(int64_t configured, int64_t derived)
+{
+    if (configured <= 0) return EP_ERR_INVALID_ARG;
+    if (configured < derived) return EP_ERR_CAPACITY;
+    return EP_OK;
+}
+
+const char* ep_status_string(ep_status s)
+{
+    switch (s) {
+        case EP_OK: return "ok";
+        case EP_ERR_INVALID_ARG: return "invalid argument";
+        case EP_ERR_CAPACITY: return "num_tokens_per_rank exceeds num_max_tokens_per_rank";
+        case EP_ERR_ALIGNMENT: return "pointer or row size misaligned";
+        case EP_ERR_WORKSPACE: return "workspace too small, misaligned or not device memory";
+        case EP_ERR_CAPTURE_HOST_SYNC: return "synchronous call on a capturing stream";
+        case EP_ERR_CUDA: return "CUDA runtime error";
+        case EP_ERR_NO_LAYOUT: return "no layout for this call on the buffer";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,245 @@
+/*
+ * ep.h - C ABI of the GB300 MoE token dispatch / combine library (libep_gb300.so).
+ *
+ * One process drives one GPU. "Ranks" are R logical partitions of this GPU's
+ * receive buffer: experts are split into R contiguous blocks of E/R experts,
+ * and rank r owns receive rows [r*S, (r+1)*S). Everything here follows the
+ * token-dispatcher pages:
+ *   [titan] "Unify expert parallel token dispatcher API" (pytorch/torchtitan
+ *           pull 3970): sections "API design", "Backend behavior",
+ *           "Capacity derivation".
+ *   [align] "fix(moe): equalize and align per-rank token counts for HybridEP
+ *           dispatch" (NVIDIA-NeMo/Automodel pull 3641): "Problem", "Fix".
+ *   [graph] "ep: graph-safe worst-token HT dispatch+combine (internode +
+ *           intranode)" (uccl pull 18): "Internode" items 1-3, "Intranode".
+ *   [flex]  "Inference: enable flex dispatcher (DeepEP/HybridEP) for prefill"
+ *           (Megatron-LM pull 4321): the SM budget knob.
+ *
+ * Notation: T = materialised tokens (rows of x_TD), N = num_tokens_per_rank
+ * (T <= N <= N_max), P = N rounded up to a multiple of 4, K = top-k,
+ * E = experts, R = logical ranks, D = hidden size, S = P*K receive rows per
+ * rank for the current call.
+ *
+ * Conventions for every call:
+ *  - Pointers named *_TD, *_TK, y_recv, out_TD are DEVICE pointers owned by
+ *    the caller; they must stay valid until the stream work completes.
+ *    Hidden-row pointers (x_TD, y_recv, out_TD) must be 16-byte aligned;
+ *    ids and scores 4-byte aligned. Row-major, densely packed.
+ *  - topk_expert_ids_TK is int32 [T][K]; -1 means "no expert". Any other id
+ *    outside [0, E) is treated as -1 and raises EP_DEVERR_BAD_ID.
+ *    topk_scores_TK is fp32 [T][K]. x_TD is [T][D] of the configured dtype.
+ *  - Calls are stream-ordered and asynchronous; none allocates memory, none
+ *    reads device memory on the host (except the calls documented as
+ *    synchronous, which refuse to run while the stream is capturing), and
+ *    none writes host-mapped memory from a kernel. Every dispatch/combine
+ *    sequence can therefore be captured in a CUDA graph and replayed with new
+ *    routing written into the same input buffers ([graph] "Internode" item 1,
+ *    "Intranode").
+ *  - A host-side argument error returns a status and enqueues nothing.
+ *    Data errors found on the device (bad ids, rows outside a rank's true
+ *    total) set sticky bits in the buffer's device error word; kernels never
+ *    trap and never write out of bounds. Read them with ep_get_device_error.
+ *  - Outputs that live in the workspace (layout arrays, receive buffers) are
+ *    overwritten by the next call on the same buffer. A buffer is not
+ *    thread-safe; use one buffer per concurrent stream of calls.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EP_API __attribute__((visibility("default")))
+#else
+#define EP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t passed as an opaque pointer (NULL = the legacy default stream). */
+typedef void* ep_stream_t;
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,       /* bad shape, null pointer, bad enum */
+    EP_ERR_CAPACITY = 2,          /* num_tokens_per_rank > num_max_tokens_per_rank, or sizes overflow */
+    EP_ERR_ALIGNMENT = 3,         /* pointer or row size not aligned as documented */
+    EP_ERR_WORKSPACE = 4,         /* workspace too small, misaligned or not device memory */
+    EP_ERR_CAPTURE_HOST_SYNC = 5, /* a synchronous call was made on a capturing stream */
+    EP_ERR_CUDA = 6,              /* a CUDA runtime call or launch failed */
+    EP_ERR_NO_LAYOUT = 7          /* combine/permute before any layout on this buffer, or T differs */
+} ep_status;
+
+typedef enum { EP_BF16 = 0, EP_F32 = 1 } ep_dtype;
+
+typedef enum {
+    EP_PERMUTE_DEFAULT = 0,       /* the library's choice */
+    EP_PERMUTE_VEC = 1,           /* 16-byte vector loads/stores through registers */
+    EP_PERMUTE_BULK = 2           /* bulk async copies staged through shared memory */
+} ep_permute_impl;
+
+/* Device error word bits (sticky until ep_get_device_error clears them). */
+#define EP_DEVERR_BAD_ID 0x1u     /* an id outside [-1, E) was seen; treated as -1 */
+#define EP_DEVERR_ROW_OOB 0x2u    /* combine met a row outside its rank's true total; skipped */
+#define EP_DEVERR_TIMEOUT 0x4u    /* a bounded device-side wait gave up; outputs invalid */
+
+/* Lifetime configuration ([titan] "API design": the dispatcher configuration
+ * carries the lifetime maximum num_max_tokens_per_rank; persistent storage is
+ * sized from it once and never grows inside dispatch). */
+typedef struct {
+    int64_t num_max_tokens_per_rank; /* N_max >= 1 */
+    int64_t hidden;                  /* D >= 1; D * element size must be a multiple of 16 */
+    int32_t num_experts;             /* E, 1 <= E <= 1024, E % R == 0 */
+    int32_t num_ranks;               /* R, 1 <= R <= 64 logical ranks */
+    int32_t topk;                    /* K, 1 <= K <= min(E, 64) */
+    int32_t dtype;                   /* ep_dtype of x_TD and the receive buffer */
+    int32_t num_sms;                 /* SMs the copy kernels may use; 0 = all ([flex]) */
+    int32_t permute_impl;            /* ep_permute_impl */
+} ep_config;
+
+/* Opaque handle; the library owns this host-side object, the caller owns the workspace. */
+typedef struct ep_buffer ep_buffer;
+
+/* Layout of one call. All pointers are device pointers into the workspace. */
+typedef struct {
+    int32_t* tokens_per_expert; /* [E] pairs routed to each expert: [titan] "API design"
+                                   num_local_tokens_per_expert_E; [graph] "Internode" item 2 */
+    int32_t* expert_offset;     /* [E] first receive row of expert e: r(e)*S + counts of the
+                                   lower experts of the same rank */
+    int32_t* rows_per_rank;     /* [R] receive rows used by rank r (its true total) */
+    int32_t* rank_prefix;       /* [R] inclusive prefix of rows_per_rank; the last entry is the
+                                   true received total ([graph] "Internode" item 3) */
+    int32_t* tokens_in_rank;    /* [R] distinct tokens with at least one expert on rank r */
+    int32_t* pos;               /* [T][K] receive row of pair (t,k), or -1; rows of one expert
+                                   follow ascending t*K+k */
+    int64_t num_tokens;         /* T */
+    int64_t padded_tokens;      /* P = roundup4(N) ([align] "Problem" item 2, "Fix") */
+    int64_t rank_stride;        /* S = P*K rows per rank ([titan] "Backend behavior") */
+} ep_layout;
+
+/* Result of a dispatch: views into the workspace. recv_x is [R*S][D] of the
+ * configured dtype (rank r's rows start at r*S), recv_scores fp32 [R*S] and
+ * recv_src int32 [R*S] (source pair index t*K+k). Only rows
+ * [r*S, r*S + rows_per_rank[r]) of each rank are defined; the tail of each
+ * rank's block holds stale data from earlier calls and must not be read. */
+typedef struct {
+    void* recv_x;
+    float* recv_scores;
+    int32_t* recv_src;
+    ep_layout layout;
+} ep_dispatch_out;
+
+/* Read-only facts about a buffer (for tuning and for counting launches). */
+typedef struct {
+    int64_t workspace_bytes;    /* bytes the buffer uses from the workspace */
+    int64_t max_rank_stride;    /* S_max = roundup4(N_max) * K */
+    int64_t kernel_launches;    /* kernels this buffer has launched so far */
+    int32_t device;             /* CUDA device the buffer was created on */
+    int32_t num_sms;            /* SMs the copy kernels use */
+    int32_t permute_impl;       /* resolved ep_permute_impl */
+    int32_t permute_grid;       /* CTAs of the permute kernel */
+    int32_t combine_grid;       /* CTAs of the combine kernel */
+    int32_t bulk_stages;        /* shared-memory row slots per CTA of the bulk permute */
+} ep_buffer_info;
+
+/* Bytes of device workspace ep_buffer_init needs for this configuration, or 0
+ * if the configuration is invalid. Host-only; never touches the GPU.
+ * Sized once from N_max ([titan] "API design"; "Backend behavior": persistent
+ * buffers are preallocated): receive rows R * roundup4(N_max) * K of D
+ * elements, their scores and sources, the [N_max][K] positions and the
+ * layout arrays. */
+EP_API size_t ep_buffer_required_bytes(const ep_config* cfg);
+
+/* Create a buffer over caller-owned device workspace. workspace must be
+ * device memory on the current device, 256-byte aligned, at least
+ * ep_buffer_required_bytes(cfg) bytes, and must outlive the buffer. The
+ * current device at this call is the buffer's device. Synchronous (clears
+ * the device error word). Returns EP_ERR_INVALID_ARG for a bad cfg,
+ * EP_ERR_WORKSPACE for an unusable workspace, EP_ERR_CUDA if no device. */
+EP_API ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace_bytes,
+                         ep_buffer** out);
+
+/* Release the host-side handle. Does not free the workspace. NULL is a no-op. */
+EP_API ep_status ep_buffer_destroy(ep_buffer* buf);
+
+/* Dispatch layout ([titan] "API design"; [graph] "Internode" items 2-3):
+ * per-expert counts, per-rank totals, their inclusive prefix, distinct
+ * tokens per rank, expert offsets and the receive row of every (t, k) pair,
+ * computed on the device from topk_expert_ids_TK [T][K]. num_tokens = T,
+ * num_tokens_per_rank = N (0 <= T <= N <= N_max); rows T..P-1 are padding
+ * that routes to no expert ([align] "Fix"). Fills *out (may be NULL).
+ * host_tokens_per_expert: NULL for worst-token mode (counts stay on the
+ * device, fully asynchronous); non-NULL for exact mode ([graph] "Internode"
+ * item 1, num_worst_tokens == 0): the E counts are copied to this host array
+ * and the call synchronizes the stream; refused with EP_ERR_CAPTURE_HOST_SYNC
+ * while the stream is capturing. */
+EP_API ep_status ep_dispatch_layout(ep_buffer* buf, const int32_t* topk_expert_ids_TK, int64_t num_tokens,
+                             int64_t num_tokens_per_rank, ep_stream_t stream, ep_layout* out,
+                             int32_t* host_tokens_per_expert);
+
+/* Dispatch = layout + permute ([titan] "API design" dispatch(x_TD,
+ * topk_scores_TK, topk_expert_ids_TK, ..., num_tokens_per_rank);
+ * "Backend behavior": the current capacity sets the per-rank stride of the
+ * preallocated buffer and sizes the permute output). For every pair with a
+ * row p: recv_x[p] = x_TD[t], recv_scores[p] = topk_scores_TK[t][k],
+ * recv_src[p] = t*K + k. Fills *out (may be NULL). */
+EP_API ep_status ep_dispatch(ep_buffer* buf, const void* x_TD, const float* topk_scores_TK,
+                      const int32_t* topk_expert_ids_TK, int64_t num_tokens,
+                      int64_t num_tokens_per_rank, ep_stream_t stream, ep_dispatch_out* out);
+
+/* The permute half of ep_dispatch alone, using the layout of the last
+ * ep_dispatch_layout / ep_dispatch on this buffer (same T; x_TD and
+ * topk_scores_TK have that T). EP_ERR_NO_LAYOUT if there is none. */
+EP_API ep_status ep_dispatch_permute(ep_buffer* buf, const void* x_TD, const float* topk_scores_TK,
+                              ep_stream_t stream, ep_dispatch_out* out);
+
+/* Combine ([align] "Fix": combine() slices the padded rows back off;
+ * [graph] "Internode" item 3: the true total comes from the device prefix
+ * sum). Uses the layout of the last dispatch on this buffer; num_tokens must
+ * equal its T. y_recv is the expert output in the receive layout
+ * ([R*S][D], configured dtype; may alias recv_x). For t < T:
+ *   out_TD[t][d] = round( fma-chain over k = 0..K-1 with pos >= 0 of
+ *                         topk_scores_TK[t][k] * y_recv[pos[t][k]][d] )
+ * accumulated in fp32 from +0 in ascending k with one fused multiply-add
+ * per term, no atomics, then rounded to out_dtype (bf16: round to nearest
+ * even; fp32: unchanged). A token with no expert gets a +0 row. Rows of
+ * y_recv beyond a rank's true total are never read (EP_DEVERR_ROW_OOB).
+ * out_TD is [T][D] of out_dtype. */
+EP_API ep_status ep_combine(ep_buffer* buf, const void* y_recv, const float* topk_scores_TK,
+                     int64_t num_tokens, void* out_TD, int32_t out_dtype, ep_stream_t stream);
+
+/* Synchronously read and clear the device error word (EP_DEVERR_* bits).
+ * Refused with EP_ERR_CAPTURE_HOST_SYNC while the stream is capturing. */
+EP_API ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flags);
+
+/* Read-only facts about buf. */
+EP_API ep_status ep_buffer_query(const ep_buffer* buf, ep_buffer_info* info);
+
+/* roundup4(n): the padded per-rank token count ([align] "Problem" item 2, "Fix"). */
+EP_API int64_t ep_pad_tokens(int64_t n);
+
+/* [titan] "Capacity derivation", Pretraining: local_batch_size *
+ * ceil_div(seq_len, cp * tp). Returns -1 if any argument is not positive. */
+EP_API int64_t ep_derive_max_tokens_pretrain(int64_t local_batch_size, int64_t seq_len, int64_t cp,
+                                      int64_t tp);
+
+/* [titan] "Capacity derivation", vLLM inference: ceil_div(max_num_batched_tokens,
+ * cp * tp). Returns -1 if any argument is not positive. */
+EP_API int64_t ep_derive_max_tokens_inference(int64_t max_num_batched_tokens, int64_t cp, int64_t tp);
+
+/* [titan] "Capacity derivation": an explicitly configured num_max_tokens_per_rank
+ * must be positive and at least the derived requirement. Returns EP_OK,
+ * EP_ERR_INVALID_ARG (not positive) or EP_ERR_CAPACITY (too small). */
+EP_API ep_status ep_validate_max_tokens(int64_t configured, int64_t derived);
+
+/* Static description of a status code. */
+EP_API const char* ep_status_string(ep_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */
