@@ -31,7 +31,7 @@ __all__ = [
     "Buffer", "Layout", "DispatchResult", "EpConfig", "EpError",
     "ep_buffer_required_bytes", "ep_buffer_init", "ep_buffer_destroy", "ep_dispatch_layout",
     "ep_dispatch", "ep_dispatch_permute", "ep_combine", "ep_get_device_error",
-    "ep_buffer_query", "ep_pad_tokens", "ep_derive_max_tokens_pretrain",
+    "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_pad_tokens", "ep_derive_max_tokens_pretrain",
     "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
     "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
     "EP_DEVERR_BAD_ID", "EP_DEVERR_ROW_OOB", "EP_DEVERR_TIMEOUT", "library_path",
@@ -144,6 +144,28 @@ def ep_buffer_query(handle) -> EpBufferInfo:
     info = EpBufferInfo()
     check(_abi.lib().ep_buffer_query(handle, C.byref(info)), "ep_buffer_query")
     return info
+
+
+def ep_dispatch_layout_noalloc(topk_expert_ids_TK: torch.Tensor, num_tokens: int,
+                               num_tokens_per_rank: int, topk: int, num_experts: int,
+                               num_ranks: int, tokens_per_expert: torch.Tensor,
+                               expert_offset: torch.Tensor, rows_per_rank: torch.Tensor,
+                               rank_prefix: torch.Tensor, tokens_in_rank: torch.Tensor,
+                               pos: torch.Tensor, error_flags: torch.Tensor | None = None,
+                               stream=None) -> None:
+    """The layout without a buffer, for callers that cannot allocate device
+    memory: the caller supplies every output tensor (int32, on the device);
+    the library uses its own fixed device scratch and allocates nothing."""
+    for name, t in (("topk_expert_ids_TK", topk_expert_ids_TK),
+                    ("tokens_per_expert", tokens_per_expert), ("expert_offset", expert_offset),
+                    ("rows_per_rank", rows_per_rank), ("rank_prefix", rank_prefix),
+                    ("tokens_in_rank", tokens_in_rank), ("pos", pos)):
+        _check_dtype(t, torch.int32, name)
+    check(_abi.lib().ep_dispatch_layout_noalloc(
+        _ptr(topk_expert_ids_TK), num_tokens, num_tokens_per_rank, topk, num_experts,
+        num_ranks, _ptr(tokens_per_expert), _ptr(expert_offset), _ptr(rows_per_rank),
+        _ptr(rank_prefix), _ptr(tokens_in_rank), _ptr(pos), _ptr(error_flags),
+        _stream(stream)), "ep_dispatch_layout_noalloc")
 
 
 def ep_pad_tokens(n: int) -> int:

@@ -218,6 +218,32 @@ EP_API ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_
 /* Read-only facts about buf. */
 EP_API ep_status ep_buffer_query(const ep_buffer* buf, ep_buffer_info* info);
 
+/* The dispatch layout of ep_dispatch_layout, for callers that cannot allocate
+ * device memory or keep a workspace (for example an op inside a host framework
+ * that owns every device allocation and only hands it input and output
+ * tensors). The source pages have no counterpart: it exists for such callers.
+ * No buffer is involved and nothing is allocated: the caller passes
+ * topk_expert_ids_TK [T][K] and the outputs (device pointers, 4-byte aligned):
+ * tokens_per_expert [E], expert_offset [E], rows_per_rank [R], rank_prefix [R],
+ * tokens_in_rank [R] and pos [T][K], with the same meaning and values as the
+ * ep_layout fields; error_flags (nullable) is a device word the kernels OR
+ * EP_DEVERR_BAD_ID into (the caller zeroes it). The kernels' other global
+ * memory is a library-owned 4 MiB device array per GPU, held until the
+ * process exits; a call whose tile tables need more,
+ *   ceil(T / max(1, 2048/K)) * (2*E + R) * 4 bytes (plus alignment),
+ * is rejected with EP_ERR_CAPACITY (about 516k tokens at E=256, R=8, K=8;
+ * about 126k at E=1024, R=64, K=8). The first call on each device (with that
+ * device current) looks up the array's device address; make it before any
+ * stream capture. All calls share the array, so calls whose GPU work overlaps
+ * (other streams or threads) race: serialize them. Asynchronous on stream. */
+EP_API ep_status ep_dispatch_layout_noalloc(const int32_t* topk_expert_ids_TK, int64_t num_tokens,
+                                            int64_t num_tokens_per_rank, int32_t topk,
+                                            int32_t num_experts, int32_t num_ranks,
+                                            int32_t* tokens_per_expert, int32_t* expert_offset,
+                                            int32_t* rows_per_rank, int32_t* rank_prefix,
+                                            int32_t* tokens_in_rank, int32_t* pos,
+                                            uint32_t* error_flags, ep_stream_t stream);
+
 /* roundup4(n): the padded per-rank token count ([align] "Problem" item 2, "Fix"). */
 EP_API int64_t ep_pad_tokens(int64_t n);
 
