@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--workload", default="deepseek", choices=sorted(W.WORKLOADS))
     ap.add_argument("--permute", choices=["default", "vec", "bulk"], default="default")
     ap.add_argument("--num-sms", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T (and N) of the workload: smaller cases for profiling")
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -72,6 +74,16 @@ def workload_desc(w: W.Workload, T: int, N: int) -> dict:
         "T": T, "D": w.D, "E": w.E, "K": w.K, "R": w.R, "num_tokens_per_rank": N,
         "num_max_tokens_per_rank": w.N_max,
     }
+
+
+def workload_tokens(args, w: W.Workload) -> tuple[int, int]:
+    """(T, N) of the benched call: the workload's own, or --tokens for both."""
+    if args.tokens > 0:
+        return args.tokens, args.tokens
+    if w.T is None:   # ragged: source rank 0, padded to the group max of the 8 counts
+        counts = W.ragged_counts(w)
+        return counts[0], max(counts)
+    return w.T, w.N
 
 
 def algorithmic_bytes(T: int, K: int, D: int, b: int, pairs: int) -> dict:
@@ -264,11 +276,8 @@ def run_gb300(args) -> dict | None:
     barrier(world)
 
     w = W.WORKLOADS[args.workload]
-    inp = W.make(args.workload, rank=0)
-    T = inp["T"]
-    N = T if w.N is None else w.N
-    if w.T is None:   # ragged: the group max of the 8 source ranks' counts
-        N = max(W.ragged_counts(w))
+    T, N = workload_tokens(args, w)
+    inp = W.make(args.workload, rank=0, T=T)
     b = w.elem_bytes
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
 
@@ -282,7 +291,8 @@ def run_gb300(args) -> dict | None:
     sc = sc_h.to(dev)
     impl = {"default": ep.EP_PERMUTE_DEFAULT, "vec": ep.EP_PERMUTE_VEC,
             "bulk": ep.EP_PERMUTE_BULK}[args.permute]
-    buf = ep.Buffer(w.N_max, w.D, w.E, w.R, w.K, dtype=tdt, num_sms=args.num_sms,
+    n_max = args.tokens if args.tokens > 0 else w.N_max   # smaller workspace when profiling
+    buf = ep.Buffer(n_max, w.D, w.E, w.R, w.K, dtype=tdt, num_sms=args.num_sms,
                     permute_impl=impl, device=dev)
     h = buf.handle
     out = torch.empty((T, w.D), dtype=tdt, device=dev)
@@ -290,8 +300,11 @@ def run_gb300(args) -> dict | None:
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
+    n_launch0 = buf.info()["kernel_launches"]
     d0 = buf.dispatch(x, sc, ids, N)
     recv_x = d0.recv_x
+    buf.combine(recv_x, sc, out=out)
+    per_step_launches = buf.info()["kernel_launches"] - n_launch0
     torch.cuda.synchronize(dev)
     pairs = int(d0.layout.tokens_per_expert.sum().item())
     assert buf.device_error() == 0
@@ -299,23 +312,20 @@ def run_gb300(args) -> dict | None:
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
-    def step_kernels():
-        ep.ep_dispatch_layout(h, ids, T, N, sptr)
-        ep.ep_dispatch_permute(h, x, sc, sptr)
-        ep.ep_combine(h, recv_x, sc, T, out, out_code, sptr)
+    def step_kernels(stream_ptr):
+        ep.ep_dispatch(h, x, sc, ids, T, N, stream_ptr)
+        ep.ep_combine(h, recv_x, sc, T, out, out_code, stream_ptr)
 
     graph = None
     if args.graph:
-        step_kernels()
+        step_kernels(sptr)
         torch.cuda.synchronize(dev)
         graph = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(dev)
         s.wait_stream(stream)
         with torch.cuda.stream(s):
             with torch.cuda.graph(graph, stream=s):
-                ep.ep_dispatch_layout(h, ids, T, N, s.cuda_stream)
-                ep.ep_dispatch_permute(h, x, sc, s.cuda_stream)
-                ep.ep_combine(h, recv_x, sc, T, out, out_code, s.cuda_stream)
+                step_kernels(s.cuda_stream)
         stream.wait_stream(s)
         torch.cuda.synchronize(dev)
 
@@ -325,11 +335,11 @@ def run_gb300(args) -> dict | None:
         if graph is not None:
             graph.replay()
         else:
-            step_kernels()
+            step_kernels(sptr)
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
@@ -340,28 +350,24 @@ def run_gb300(args) -> dict | None:
     for i in range(K):
         flush.zero_()                       # L2 flush, outside the events
         e = ev[i]
+        e[0].record(stream)
         if graph is not None:
-            e[0].record(stream)
             graph.replay()
-            e[3].record(stream)
         else:
-            e[0].record(stream)
-            ep.ep_dispatch_layout(h, ids, T, N, sptr)
+            ep.ep_dispatch(h, x, sc, ids, T, N, sptr)
             e[1].record(stream)
-            ep.ep_dispatch_permute(h, x, sc, sptr)
-            e[2].record(stream)
             ep.ep_combine(h, recv_x, sc, T, out, out_code, sptr)
-            e[3].record(stream)
+        e[2].record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - wall0
     clk = clocks.stop() if rank == 0 else None
     launches = buf.info()["kernel_launches"] - launches0
     if graph is not None:
-        launches = K * 4 if T > 0 else 0   # the captured graph holds the same launches
+        launches = K * per_step_launches
     assert buf.device_error() == 0
 
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     total_ms = sum(step_ms)
     total_ms_max = max_over_ranks(total_ms, world)
     ms_per_step = total_ms_max / K
@@ -373,24 +379,24 @@ def run_gb300(args) -> dict | None:
            "hbm_gbs_step": nbytes["step"] / (ms_per_step / 1e3) / 1e9,
            "wall_s": wall, "launches": launches, "clocks": clk}
     if graph is None:
-        lay = [e[0].elapsed_time(e[1]) for e in ev]
-        per = [e[1].elapsed_time(e[2]) for e in ev]
-        com = [e[2].elapsed_time(e[3]) for e in ev]
+        dis = [e[0].elapsed_time(e[1]) for e in ev]
+        com = [e[1].elapsed_time(e[2]) for e in ev]
         kern = {}
-        for name, arr in (("layout", lay), ("permute", per), ("combine", com)):
+        for name, arr, nb in (("dispatch", dis, nbytes["layout"] + nbytes["permute"]),
+                              ("combine", com, nbytes["combine"])):
             avg = sum(arr) / len(arr)
             kern[name] = {"avg_us": avg * 1e3, "median_us": statistics.median(arr) * 1e3,
-                          "algorithmic_bytes": nbytes[name],
-                          "achieved_gbs": nbytes[name] / (avg / 1e3) / 1e9}
-        dom = "permute" if kern["permute"]["avg_us"] >= kern["combine"]["avg_us"] else "combine"
+                          "algorithmic_bytes": nb, "achieved_gbs": nb / (avg / 1e3) / 1e9}
+        dom = "dispatch" if kern["dispatch"]["avg_us"] >= kern["combine"]["avg_us"] else "combine"
         ach = kern[dom]["achieved_gbs"]
-        kname = {"permute": f"permute_{buf.info()['permute_impl']}", "combine": "combine"}[dom]
+        impl_name = {1: "vec", 2: "bulk"}[buf.info()["permute_impl"]]
+        kname = {"dispatch": f"dispatch_{impl_name}", "combine": "combine"}[dom]
         res["kernels"] = kern
-        res["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1),
+        res["roofline"] = {"bound": "hbm", "kernel": kname, "achieved": round(ach, 1),
                            "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
                            "peak_source": peak_src,
                            "traffic": profiled_traffic(kname, args.workload),
-                           "algorithmic_bytes_per_launch": nbytes[dom]}
+                           "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
     res["bytes"] = nbytes
     res["pairs"] = pairs
     res["info"] = buf.info()
@@ -440,9 +446,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        inp = W.make(args.workload, rank=0)
-        T = inp["T"]
-        N = T if w.N is None else w.N
+        T, N = workload_tokens(args, w)
+        inp = W.make(args.workload, rank=0, T=T)
         tpc = oracle_tokens_per_call(w)
         budget = max(1.0, min(args.cpu_seconds, 20.0)) / max(1, args.steps + args.warmup)
         for _ in range(args.warmup):
@@ -469,10 +474,7 @@ def main():
     res = run_gb300(args)
     if rank != 0:
         return
-    T = W.make(args.workload, rank=0, with_x=False)["T"] if w.T is None else w.T
-    N = T if w.N is None else w.N
-    if w.T is None:
-        N = max(W.ragged_counts(w))
+    T, N = workload_tokens(args, w)
     cfg = workload_desc(w, T, N)
     cfg.update({"l2": "flushed between timed steps (memset of 2x L2)",
                 "expert": "identity (y = recv_x), not timed",
@@ -493,7 +495,7 @@ def main():
     line["gpu_launches"] = res["launches"]
     line["clocks"] = res["clocks"]
     if not args.no_cpu_baseline:
-        inp = W.make(args.workload, rank=0)
+        inp = W.make(args.workload, rank=0, T=T)
         tpc = oracle_tokens_per_call(w)
         r = oracle_sample_run(w, inp, args.cpu_seconds, tpc)
         line["cpu_baseline"] = {

@@ -15,22 +15,13 @@
 // reads up to T*K rows, writes T rows.
 #include <cuda_bf16.h>
 
-#include "ep_kernels.cuh"
+#include "ep_device.cuh"
 
 namespace ep {
 namespace {
 
 constexpr int kCombineThreads = 128;
 constexpr int kLoadBatch = 8;   // rows of one token loaded before their FMAs
-
-__device__ __forceinline__ int4 ld_stream_v4(const int4* p)
-{
-    int4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // Elements per 16-byte vector of the input type (0 = bf16, 1 = fp32).
 template <int IN>
@@ -107,20 +98,21 @@ combine_vec_kernel(CombineArgs a)
     constexpr int N = InVec<IN>::kElems;
     __shared__ int s_pos[kMaxTopk];
     __shared__ float s_w[kMaxTopk];
+    griddep_wait();
     const int64_t V = a.D / N;
     const int4* __restrict__ y = static_cast<const int4*>(a.y);
 
     for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
         if (threadIdx.x < a.K) {
             const int64_t q = t * a.K + threadIdx.x;
-            int p = a.pos[q];
+            int p = __ldcg(a.pos + q);
             if (p >= 0) {
                 // Keep the row only if it lies inside its rank's true total.
                 const int64_t r = (int64_t)p / a.S;
                 bool ok = r < a.R;
                 if (ok) {
-                    const int lo = (r > 0) ? a.rank_prefix[r - 1] : 0;
-                    ok = ((int64_t)p - r * a.S) < (int64_t)(a.rank_prefix[r] - lo);
+                    const int lo = (r > 0) ? __ldcg(a.rank_prefix + r - 1) : 0;
+                    ok = ((int64_t)p - r * a.S) < (int64_t)(__ldcg(a.rank_prefix + r) - lo);
                 }
                 if (!ok) {
                     atomicOr(a.err, kErrRowOob);
@@ -128,7 +120,7 @@ combine_vec_kernel(CombineArgs a)
                 }
             }
             s_pos[threadIdx.x] = p;
-            s_w[threadIdx.x] = a.scores[q];
+            s_w[threadIdx.x] = __ldcg(a.scores + q);
         }
         __syncthreads();
         for (int64_t v = threadIdx.x; v < V; v += kCombineThreads) {
@@ -141,7 +133,7 @@ combine_vec_kernel(CombineArgs a)
                 for (int j = 0; j < kLoadBatch; ++j) {
                     const int k = k0 + j;
                     const int p = (k < a.K) ? s_pos[k] : -1;
-                    if (p >= 0) r[j] = ld_stream_v4(y + (int64_t)p * V + v);
+                    if (p >= 0) r[j] = ld_cg_v4(y + (int64_t)p * V + v);
                 }
 #pragma unroll
                 for (int j = 0; j < kLoadBatch; ++j) {
@@ -154,6 +146,7 @@ combine_vec_kernel(CombineArgs a)
         }
         __syncthreads();
     }
+    griddep_launch_dependents();
 }
 
 template <int IN, int OUT>
@@ -174,20 +167,14 @@ cudaError_t plan_combine(int in_dtype, int num_sms, int* grid)
     return cudaSuccess;
 }
 
-cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s, int64_t* launches)
+cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& o)
 {
     if (a.T <= 0) return cudaSuccess;
-    const unsigned g = (unsigned)(a.T < grid ? a.T : grid);
-    if (a.in_dtype == 0 && a.out_dtype == 0)
-        combine_vec_kernel<0, 0><<<g, kCombineThreads, 0, s>>>(a);
-    else if (a.in_dtype == 0 && a.out_dtype == 1)
-        combine_vec_kernel<0, 1><<<g, kCombineThreads, 0, s>>>(a);
-    else if (a.in_dtype == 1 && a.out_dtype == 0)
-        combine_vec_kernel<1, 0><<<g, kCombineThreads, 0, s>>>(a);
-    else
-        combine_vec_kernel<1, 1><<<g, kCombineThreads, 0, s>>>(a);
-    ++*launches;
-    return cudaGetLastError();
+    const dim3 g((unsigned)(a.T < grid ? a.T : grid)), b(kCombineThreads);
+    if (a.in_dtype == 0 && a.out_dtype == 0) return launch_kernel(combine_vec_kernel<0, 0>, g, b, 0, o, a);
+    if (a.in_dtype == 0 && a.out_dtype == 1) return launch_kernel(combine_vec_kernel<0, 1>, g, b, 0, o, a);
+    if (a.in_dtype == 1 && a.out_dtype == 0) return launch_kernel(combine_vec_kernel<1, 0>, g, b, 0, o, a);
+    return launch_kernel(combine_vec_kernel<1, 1>, g, b, 0, o, a);
 }
 
 }  // namespace ep

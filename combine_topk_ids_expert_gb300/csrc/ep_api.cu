@@ -10,6 +10,8 @@
 // no host handshake, no host-mapped counters, counts stay on the device.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <new>
 
 #include "ep.h"
@@ -21,7 +23,9 @@ struct ep_buffer {
     int num_sms;
     int64_t row_bytes;
     int64_t s_max;          // roundup4(N_max) * K
-    int64_t max_tiles;
+    int64_t max_tiles;      // layout tiles the tables hold
+    int ep_stride;          // row stride of the tile tables: roundup4(E)
+    bool pdl;               // launch with programmatic dependent launch
     size_t ws_bytes;
     // carved device pointers
     uint8_t* recv_x;
@@ -78,7 +82,7 @@ bool check_config(const ep_config* c, int64_t* row_bytes, int64_t* s_max, int64_
     if (c->num_max_tokens_per_rank * c->topk > INT32_MAX) return false;
     *row_bytes = rb;
     *s_max = s;
-    *max_tiles = ep::layout_tiles(c->num_max_tokens_per_rank, c->topk);
+    *max_tiles = ep::max_tiles(c->num_max_tokens_per_rank, c->topk);
     return true;
 }
 
@@ -101,6 +105,7 @@ Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, i
 {
     const size_t rows = (size_t)c->num_ranks * (size_t)s_max;
     const size_t E = (size_t)c->num_experts, R = (size_t)c->num_ranks;
+    const size_t Ep = (size_t)ep::round_up4(c->num_experts);
     Carve cv;
     Offsets o;
     o.recv_x = cv.take(rows * (size_t)row_bytes);
@@ -112,8 +117,8 @@ Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, i
     o.rows_per_rank = cv.take(R * 4);
     o.rank_prefix = cv.take(R * 4);
     o.tokens_in_rank = cv.take(R * 4);
-    o.tile_cnt = cv.take((size_t)max_tiles * E * 4);
-    o.tile_pre = cv.take((size_t)max_tiles * E * 4);
+    o.tile_cnt = cv.take((size_t)max_tiles * Ep * 4);
+    o.tile_pre = cv.take((size_t)max_tiles * Ep * 4);
     o.tile_tok = cv.take((size_t)max_tiles * R * 4);
     o.err = cv.take(4);
     o.total = cv.off;
@@ -164,15 +169,20 @@ void fill_dispatch(const ep_buffer* b, ep_dispatch_out* out)
     fill_layout(b, &out->layout);
 }
 
-ep_status enqueue_layout(ep_buffer* b, const int32_t* ids, int64_t T, int64_t N, cudaStream_t s)
+ep::LaunchOpts opts(ep_buffer* b, cudaStream_t s) { return ep::LaunchOpts{s, b->pdl, &b->launches}; }
+
+ep::LayoutArgs layout_args(ep_buffer* b, const int32_t* ids, int64_t T, int64_t N)
 {
     ep::LayoutArgs a;
     a.ids = ids;
     a.T = T;
     a.S = pad4(N) * b->cfg.topk;
+    a.tpt = ep::tokens_per_tile(T, b->cfg.topk, b->num_sms);
+    a.ntiles = (int)ep::tile_count(T, a.tpt);
     a.K = b->cfg.topk;
     a.E = b->cfg.num_experts;
     a.R = b->cfg.num_ranks;
+    a.Ep = b->ep_stride;
     a.tile_cnt = b->tile_cnt;
     a.tile_pre = b->tile_pre;
     a.tile_tok = b->tile_tok;
@@ -183,15 +193,10 @@ ep_status enqueue_layout(ep_buffer* b, const int32_t* ids, int64_t T, int64_t N,
     a.tokens_in_rank = b->tokens_in_rank;
     a.pos = b->pos;
     a.err = b->err;
-    if (ep::launch_layout(a, s, &b->launches) != cudaSuccess) return EP_ERR_CUDA;
-    b->has_layout = true;
-    b->last_T = T;
-    b->last_N = N;
-    b->last_S = a.S;
-    return EP_OK;
+    return a;
 }
 
-ep_status enqueue_permute(ep_buffer* b, const void* x, const float* scores, cudaStream_t s)
+ep::PermuteArgs permute_args(ep_buffer* b, const void* x, const float* scores)
 {
     ep::PermuteArgs a;
     a.x = x;
@@ -204,7 +209,50 @@ ep_status enqueue_permute(ep_buffer* b, const void* x, const float* scores, cuda
     a.K = b->cfg.topk;
     a.row_bytes = b->row_bytes;
     a.err = b->err;
-    return ep::launch_permute(a, b->permute, s, &b->launches) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return a;
+}
+
+void remember_layout(ep_buffer* b, int64_t T, int64_t N)
+{
+    b->has_layout = true;
+    b->last_T = T;
+    b->last_N = N;
+    b->last_S = pad4(N) * b->cfg.topk;
+}
+
+ep_status enqueue_layout(ep_buffer* b, const int32_t* ids, int64_t T, int64_t N, cudaStream_t s)
+{
+    if (ep::launch_layout(layout_args(b, ids, T, N), opts(b, s)) != cudaSuccess) return EP_ERR_CUDA;
+    remember_layout(b, T, N);
+    return EP_OK;
+}
+
+ep_status enqueue_permute(ep_buffer* b, const void* x, const float* scores, cudaStream_t s)
+{
+    return ep::launch_permute(permute_args(b, x, scores), b->permute, opts(b, s)) == cudaSuccess
+               ? EP_OK
+               : EP_ERR_CUDA;
+}
+
+// Layout counts, then positions + permute fused into one kernel when the call
+// fits it, else the positions and permute kernels one after the other.
+ep_status enqueue_dispatch(ep_buffer* b, const void* x, const float* scores, const int32_t* ids,
+                           int64_t T, int64_t N, cudaStream_t s)
+{
+    const ep::LayoutArgs la = layout_args(b, ids, T, N);
+    const ep::LaunchOpts o = opts(b, s);
+    if (b->permute.impl == EP_PERMUTE_BULK) {
+        if (ep::launch_layout_counts(la, o) != cudaSuccess) return EP_ERR_CUDA;
+        remember_layout(b, T, N);
+        const cudaError_t e = ep::launch_dispatch_fused(la, permute_args(b, x, scores), b->permute, o);
+        if (e == cudaSuccess) return EP_OK;
+        if (e != cudaErrorNotSupported) return EP_ERR_CUDA;
+        if (ep::launch_layout_positions(la, o) != cudaSuccess) return EP_ERR_CUDA;
+        return enqueue_permute(b, x, scores, s);
+    }
+    if (ep::launch_layout(la, o) != cudaSuccess) return EP_ERR_CUDA;
+    remember_layout(b, T, N);
+    return enqueue_permute(b, x, scores, s);
 }
 
 ep_status check_rows(const ep_buffer* b, const void* x, const float* scores)
@@ -257,6 +305,11 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     b->row_bytes = rb;
     b->s_max = s_max;
     b->max_tiles = tiles;
+    b->ep_stride = ep::round_up4(cfg->num_experts);
+    {
+        const char* v = std::getenv("EP_PDL");
+        b->pdl = !(v && std::strcmp(v, "0") == 0);
+    }
     b->ws_bytes = o.total;
     uint8_t* w = static_cast<uint8_t*>(workspace);
     b->recv_x = w + o.recv_x;
@@ -274,7 +327,8 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     b->err = reinterpret_cast<uint32_t*>(w + o.err);
 
     const int impl = cfg->permute_impl == EP_PERMUTE_DEFAULT ? EP_PERMUTE_BULK : cfg->permute_impl;
-    if (ep::plan_permute(impl, rb, cfg->topk, b->num_sms, &b->permute) != cudaSuccess ||
+    if (ep::plan_permute(impl, rb, cfg->topk, cfg->num_experts, b->num_sms, &b->permute) !=
+            cudaSuccess ||
         ep::plan_combine(cfg->dtype == EP_BF16 ? 0 : 1, b->num_sms, &b->combine_grid) !=
             cudaSuccess ||
         cudaMemset(b->err, 0, sizeof(uint32_t)) != cudaSuccess ||
@@ -318,10 +372,7 @@ ep_status ep_dispatch(ep_buffer* buf, const void* x, const float* scores, const 
     if (st != EP_OK) return st;
     if (T > 0 && (!x || !scores)) return EP_ERR_INVALID_ARG;
     if (!is_aligned(x, 16) || !is_aligned(scores, 4)) return EP_ERR_ALIGNMENT;
-    cudaStream_t s = as_stream(stream);
-    st = enqueue_layout(buf, ids, T, N, s);
-    if (st != EP_OK) return st;
-    st = enqueue_permute(buf, x, scores, s);
+    st = enqueue_dispatch(buf, x, scores, ids, T, N, as_stream(stream));
     if (st != EP_OK) return st;
     fill_dispatch(buf, out);
     return EP_OK;
@@ -363,7 +414,7 @@ ep_status ep_combine(ep_buffer* buf, const void* y, const float* scores, int64_t
     a.in_dtype = buf->cfg.dtype == EP_BF16 ? 0 : 1;
     a.out_dtype = out_dtype == EP_BF16 ? 0 : 1;
     a.err = buf->err;
-    if (ep::launch_combine(a, buf->combine_grid, as_stream(stream), &buf->launches) != cudaSuccess)
+    if (ep::launch_combine(a, buf->combine_grid, opts(buf, as_stream(stream))) != cudaSuccess)
         return EP_ERR_CUDA;
     return EP_OK;
 }

@@ -1,0 +1,211 @@
+// ep_device.cuh - device helpers shared by the layout, permute and combine
+// kernels: programmatic-dependent-launch controls, id checks, mbarrier and
+// bulk-async-copy wrappers (hand-written PTX), and the stable per-tile
+// position pass.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ep_kernels.cuh"
+
+namespace ep {
+
+// ---- programmatic dependent launch -----------------------------------------
+// Every kernel is launched so that it may start while its predecessor in the
+// stream finishes. It must call griddep_wait() before touching memory the
+// predecessor may write or read; it calls griddep_launch_dependents() once its
+// own successor may start its prologue. Both are no-ops for a normal launch.
+
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- loads of data another kernel wrote ----------------------------------
+// Kernels may start before their predecessor finishes (above), so data written
+// by an earlier kernel is read with L2-coherent loads (ld.global.cg), never
+// through the non-coherent L1 path.
+
+__device__ __forceinline__ int4 ld_cg_v4(const void* p)
+{
+    int4 v;
+    asm volatile("ld.global.cg.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ---- ids ---------------------------------------------------------------------
+
+__device__ __forceinline__ int valid_id(int e, int E) { return (e >= -1 && e < E) ? e : -1; }
+
+__device__ __forceinline__ unsigned lanemask_lt(int lane) { return (1u << lane) - 1u; }
+
+// ---- mbarrier and bulk async copies ------------------------------------------
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bounded waits (then kErrTimeout)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0u;
+}
+
+// False if the phase has not completed by the deadline (%globaltimer ns).
+__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t deadline)
+{
+    while (true) {
+        for (int it = 0; it < 64; ++it)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() > deadline) return false;
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_until(bar, parity, globaltimer_ns() + kWaitLimitNs);
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ---- stable positions of one layout tile ------------------------------------
+//
+// Receive row of each pair of tile `tile` (tokens [t0, t1), flat pairs
+// [p0, p0 + np)): expert_offset[e] + tile_pre[tile][e] + (pairs with the same
+// expert in the earlier warps' segments) + (peers in lower lanes of the same
+// 32-pair chunk). Warp w owns the flat pairs [w*seg, w*seg + seg) of the tile,
+// so the order is the flat pair order t*K + k. Called by all kLayoutThreads
+// threads of the block; s_base holds kLayoutWarps * Ep ints. Writes the rows
+// to pos_out (global) and, if s_pos is given, to s_pos[i] (shared).
+__device__ __forceinline__ void tile_positions(const LayoutArgs& a, int tile, int* s_base,
+                                               int32_t* pos_out, int* s_pos)
+{
+    const int64_t t0 = (int64_t)tile * a.tpt;
+    const int64_t t1 = min(a.T, t0 + a.tpt);
+    const int64_t p0 = t0 * a.K;
+    const int np = (int)((t1 - t0) * a.K);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int E = a.E, Ep = a.Ep;
+    const int seg = (((np + kLayoutWarps - 1) / kLayoutWarps) + 31) & ~31;
+    const int w_begin = warp * seg;
+    const int w_end = min(np, w_begin + seg);
+    int* mine = s_base + warp * Ep;
+
+    for (int i = threadIdx.x; i < kLayoutWarps * Ep; i += blockDim.x) s_base[i] = 0;
+    __syncthreads();
+
+    // Pass 1: per-warp histogram (one writer per row, one add per peer group).
+    for (int c = w_begin; c < w_begin + seg; c += 32) {
+        const int i = c + lane;
+        const int e = (i < w_end) ? valid_id(__ldcg(a.ids + p0 + i), E) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // Exclusive prefix over warps, seeded with the expert's first row and the
+    // counts of all earlier tiles.
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int base = __ldcg(a.expert_offset + e) + __ldcg(a.tile_pre + (int64_t)tile * Ep + e);
+#pragma unroll
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int c = s_base[w * Ep + e];
+            s_base[w * Ep + e] = base;
+            base += c;
+        }
+    }
+    __syncthreads();
+
+    // Pass 2: running base of the expert + rank among equal ids in lower lanes.
+    for (int c = w_begin; c < w_begin + seg; c += 32) {
+        const int i = c + lane;
+        const bool in = i < w_end;
+        const int e = in ? valid_id(__ldcg(a.ids + p0 + i), E) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int b = (e >= 0) ? mine[e] : 0;
+        if (in) {
+            const int p = (e >= 0) ? b + __popc(peers & lanemask_lt(lane)) : -1;
+            pos_out[p0 + i] = p;
+            if (s_pos) s_pos[i] = p;
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] = b + __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+}
+
+}  // namespace ep

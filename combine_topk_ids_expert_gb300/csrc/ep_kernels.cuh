@@ -1,5 +1,6 @@
-// ep_kernels.cuh - internal interface between the C ABI (ep_api.cu) and the
-// sm_103a kernels (layout.cu, permute.cu, combine.cu). Not installed.
+// ep_kernels.cuh - internal interface between the C ABI (ep_api.cu,
+// layout_noalloc.cu) and the sm_103a kernels (layout.cu, permute.cu,
+// combine.cu). Not installed.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -7,23 +8,44 @@
 
 namespace ep {
 
-// Limits the kernels are written for (checked by ep_buffer_init).
-constexpr int kMaxExperts = 1024;   // one scan element per thread of a 1024-thread block
+// Limits the kernels are written for (checked on the host).
+constexpr int kMaxExperts = 1024;   // one scan column per thread of a 1024-thread block
 constexpr int kMaxRanks = 64;       // per-token rank sets are 64-bit masks
 constexpr int kMaxTopk = 64;        // per-token positions staged in shared memory
 
-// Layout tiles: each CTA of the count and position kernels owns a contiguous
-// run of tokens holding about kLayoutPairs (token, k) pairs.
+// Layout tiles: CTA `tile` of the count and position kernels owns tokens
+// [tile*tpt, min(T, (tile+1)*tpt)). Tile tables have rows of Ep = roundup4(E)
+// ints so the scan can read them as 16-byte vectors.
 constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
-constexpr int kLayoutPairs = 2048;
-inline int64_t layout_tokens_per_tile(int K) {
-    int64_t t = kLayoutPairs / K;
-    return t > 0 ? t : 1;
+constexpr int kMaxTilePairs = 8192;   // pairs one tile may hold (fused kernel's shared table)
+constexpr int kTileBaseCap = 256;     // tiles per call before large calls add more
+
+inline int round_up4(int e) { return (e + 3) / 4 * 4; }
+
+// Tokens per tile for a call of T tokens: about one tile per SM, more tiles
+// when a tile would exceed kMaxTilePairs pairs.
+inline int64_t tokens_per_tile(int64_t T, int K, int num_sms)
+{
+    if (T <= 0) return 1;
+    int64_t tiles = num_sms < kTileBaseCap ? num_sms : kTileBaseCap;
+    const int64_t need = (T * K + kMaxTilePairs - 1) / kMaxTilePairs;
+    if (need > tiles) tiles = need;
+    if (tiles > T) tiles = T;
+    if (tiles < 1) tiles = 1;
+    return (T + tiles - 1) / tiles;
 }
-inline int64_t layout_tiles(int64_t T, int K) {
-    const int64_t tpt = layout_tokens_per_tile(K);
-    return (T + tpt - 1) / tpt;
+
+inline int64_t tile_count(int64_t T, int64_t tpt) { return T <= 0 ? 0 : (T + tpt - 1) / tpt; }
+
+// Upper bound of tile_count over every T <= n_max (any SM count), for sizing.
+inline int64_t max_tiles(int64_t n_max, int K)
+{
+    int64_t t = kTileBaseCap;
+    const int64_t need = (n_max * K + kMaxTilePairs - 1) / kMaxTilePairs;
+    if (need > t) t = need;
+    if (t > n_max) t = n_max;
+    return t < 1 ? 1 : t;
 }
 
 // Device error word bits (same values as EP_DEVERR_* in ep.h).
@@ -35,9 +57,11 @@ struct LayoutArgs {
     const int32_t* ids;        // [T][K]
     int64_t T;
     int64_t S;                 // rows per rank for this call
-    int K, E, R;
-    int32_t* tile_cnt;         // [tiles][E] per-tile expert counts (scratch)
-    int32_t* tile_pre;         // [tiles][E] exclusive prefix over tiles (scratch)
+    int64_t tpt;               // tokens per tile
+    int ntiles;
+    int K, E, R, Ep;
+    int32_t* tile_cnt;         // [tiles][Ep] per-tile expert counts (scratch)
+    int32_t* tile_pre;         // [tiles][Ep] exclusive prefix over tiles (scratch)
     int32_t* tile_tok;         // [tiles][R] per-tile distinct-token counts (scratch)
     int32_t* cnt;              // [E]
     int32_t* expert_offset;    // [E]
@@ -47,8 +71,22 @@ struct LayoutArgs {
     int32_t* pos;              // [T][K]
     uint32_t* err;
 };
-// Enqueues the layout kernels; adds the number of kernels launched to *launches.
-cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s, int64_t* launches);
+
+// Launch options shared by every kernel: programmatic dependent launch lets a
+// kernel start while its predecessor in the stream drains.
+struct LaunchOpts {
+    cudaStream_t stream;
+    bool pdl;
+    int64_t* launches;         // incremented per kernel launched
+};
+
+// count + scan: fills cnt, expert_offset, rows_per_rank, rank_prefix,
+// tokens_in_rank and the tile tables.
+cudaError_t launch_layout_counts(const LayoutArgs& a, const LaunchOpts& o);
+// positions of every pair (after launch_layout_counts).
+cudaError_t launch_layout_positions(const LayoutArgs& a, const LaunchOpts& o);
+// all three.
+cudaError_t launch_layout(const LayoutArgs& a, const LaunchOpts& o);
 
 struct PermuteArgs {
     const void* x;             // [T][row_bytes]
@@ -64,14 +102,21 @@ struct PermuteArgs {
 };
 struct PermutePlan {
     int impl;                  // 1 = vec, 2 = bulk
-    int grid;
-    int stages;                // bulk: shared-memory row slots per CTA
-    int smem_bytes;            // bulk: dynamic shared memory per CTA
+    int grid;                  // standalone permute kernels
+    int stages;                // bulk: shared-memory row slots per CTA (standalone)
+    int smem_bytes;            // bulk: dynamic shared memory per CTA (standalone)
+    int fused_smem_cap;        // fused layout+permute: max dynamic shared memory per CTA
 };
-// Chooses grid and staging for a row size on the current device.
-cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int num_sms, PermutePlan* plan);
-cudaError_t launch_permute(const PermuteArgs& a, const PermutePlan& plan, cudaStream_t s,
-                           int64_t* launches);
+// Chooses grids and staging for a row size on the current device.
+cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms,
+                         PermutePlan* plan);
+cudaError_t launch_permute(const PermuteArgs& a, const PermutePlan& plan, const LaunchOpts& o);
+
+// Positions + bulk permute in one kernel, one CTA per layout tile, after
+// launch_layout_counts. Returns cudaErrorNotSupported when the call does not
+// fit the fused kernel (then the caller runs positions + permute separately).
+cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
+                                  const PermutePlan& plan, const LaunchOpts& o);
 
 struct CombineArgs {
     const void* y;             // [R*S][D] of in_dtype
@@ -87,6 +132,26 @@ struct CombineArgs {
     uint32_t* err;
 };
 cudaError_t plan_combine(int in_dtype, int num_sms, int* grid);
-cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s, int64_t* launches);
+cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& o);
+
+// Launches kernel with an optional programmatic-dependent-launch attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          const LaunchOpts& o, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = o.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = o.pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+    if (e == cudaSuccess && o.launches) ++*o.launches;
+    return e;
+}
 
 }  // namespace ep

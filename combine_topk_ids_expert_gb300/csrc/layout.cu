@@ -8,53 +8,63 @@
 // written to device memory, and a device prefix sum holding the true
 // received total). Nothing is copied to the host and nothing waits on it.
 //
-// Three kernels, all sized from T and K only:
-//   count : one CTA per tile of tokens; warp-aggregated shared-memory
-//           histogram (__match_any_sync groups equal expert ids so one lane
-//           per group adds the group size), plus distinct tokens per rank.
-//   scan  : one CTA; column prefix of the tile histograms, per-expert totals,
-//           expert offsets within each rank, per-rank totals and their
-//           inclusive prefix.
+// Kernels, sized from T and K only:
+//   count : one CTA per tile of tokens (about one tile per SM); warp-
+//           aggregated shared-memory histogram (__match_any_sync groups equal
+//           expert ids so one lane per group adds the group size), plus the
+//           distinct tokens per rank.
+//   scan  : one CTA of 1024 threads; column prefix of the tile histograms read
+//           as 16-byte vectors by row groups, per-expert totals, expert offsets
+//           within each rank, per-rank totals and their inclusive prefix.
 //   pos   : one CTA per tile; stable rank of each pair among the pairs of the
-//           same expert (flat order t*K+k), from per-warp histograms, their
-//           prefix over warps, the tile prefix and the expert offset.
-#include "ep_kernels.cuh"
+//           same expert in flat order t*K+k (tile_positions). The bulk
+//           dispatch fuses this pass into its permute kernel instead.
+#include "ep_device.cuh"
 
 namespace ep {
 namespace {
 
-__device__ __forceinline__ int valid_id(int e, int E) { return (e >= -1 && e < E) ? e : -1; }
-
-__device__ __forceinline__ unsigned lanemask_lt(int lane) { return (1u << lane) - 1u; }
+constexpr int kCountUnroll = 4;
 
 __global__ void __launch_bounds__(kLayoutThreads)
-layout_count_kernel(LayoutArgs a, int64_t tpt)
+layout_count_kernel(LayoutArgs a)
 {
     __shared__ int s_hist[kMaxExperts];
     __shared__ int s_tok[kMaxRanks];
+    griddep_wait();
+    griddep_launch_dependents();
     const int tile = blockIdx.x;
-    const int64_t t0 = (int64_t)tile * tpt;
-    const int64_t t1 = min(a.T, t0 + tpt);
+    const int64_t t0 = (int64_t)tile * a.tpt;
+    const int64_t t1 = min(a.T, t0 + a.tpt);
     const int64_t p0 = t0 * a.K;
     const int np = (int)((t1 - t0) * a.K);
     const int lane = threadIdx.x & 31;
 
-    for (int i = threadIdx.x; i < a.E; i += blockDim.x) s_hist[i] = 0;
+    for (int i = threadIdx.x; i < a.Ep; i += blockDim.x) s_hist[i] = 0;
     if (threadIdx.x < a.R) s_tok[threadIdx.x] = 0;
     __syncthreads();
 
-    // Full warps walk the tile so every lane takes part in __match_any_sync.
+    // Full warps walk the tile so every lane takes part in __match_any_sync;
+    // each thread loads kCountUnroll ids before matching them.
     const int np32 = (np + 31) & ~31;
     bool bad = false;
-    for (int i = threadIdx.x; i < np32; i += blockDim.x) {
-        int e = -1;
-        if (i < np) {
-            const int raw = __ldg(a.ids + p0 + i);
-            e = valid_id(raw, a.E);
-            bad |= (e != raw);
+    for (int base = 0; base < np32; base += kCountUnroll * kLayoutThreads) {
+        int e[kCountUnroll];
+#pragma unroll
+        for (int j = 0; j < kCountUnroll; ++j) {
+            const int i = base + j * kLayoutThreads + (int)threadIdx.x;
+            const int raw = (i < np) ? __ldcg(a.ids + p0 + i) : -1;
+            e[j] = valid_id(raw, a.E);
+            bad |= (e[j] != raw);
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[e], __popc(peers));
+#pragma unroll
+        for (int j = 0; j < kCountUnroll; ++j) {
+            const int warp_first = base + j * kLayoutThreads + ((int)threadIdx.x & ~31);
+            if (warp_first < np32) {
+                const unsigned peers = __match_any_sync(0xffffffffu, e[j]);
+                if (e[j] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[e[j]], __popc(peers));
+            }
+        }
     }
     if (bad) atomicOr(a.err, kErrBadId);
 
@@ -62,8 +72,9 @@ layout_count_kernel(LayoutArgs a, int64_t tpt)
     const int eloc = a.E / a.R;
     for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
         unsigned long long mask = 0ull;
+#pragma unroll 8
         for (int k = 0; k < a.K; ++k) {
-            const int e = valid_id(__ldg(a.ids + t * a.K + k), a.E);
+            const int e = valid_id(__ldcg(a.ids + t * a.K + k), a.E);
             if (e >= 0) mask |= 1ull << (e / eloc);
         }
         while (mask) {
@@ -73,42 +84,93 @@ layout_count_kernel(LayoutArgs a, int64_t tpt)
     }
     __syncthreads();
 
-    for (int e = threadIdx.x; e < a.E; e += blockDim.x)
-        a.tile_cnt[(int64_t)tile * a.E + e] = s_hist[e];
+    for (int e = threadIdx.x; e < a.Ep; e += blockDim.x)
+        a.tile_cnt[(int64_t)tile * a.Ep + e] = s_hist[e];
     if (threadIdx.x < a.R) a.tile_tok[(int64_t)tile * a.R + threadIdx.x] = s_tok[threadIdx.x];
 }
 
-// One CTA of 1024 threads: thread e owns expert e (E <= 1024).
-__global__ void __launch_bounds__(1024)
-layout_scan_kernel(LayoutArgs a, int ntiles)
+__device__ __forceinline__ int4 add4(int4 a, int4 b)
 {
+    return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// One CTA of 1024 threads. Thread (g, q) owns columns 4q..4q+3 of the rows of
+// row group g; the groups' sums are scanned per column in shared memory.
+__global__ void __launch_bounds__(1024)
+layout_scan_kernel(LayoutArgs a)
+{
+    __shared__ int s_grp[4096];          // [groups][Ep], groups * Ep <= 4096
+    __shared__ int s_tok[1024];          // [groups2][R]
     __shared__ int s_incl[kMaxExperts];
     __shared__ int s_warp[32];
+    griddep_wait();
+    griddep_launch_dependents();
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int32_t* __restrict__ tc = a.tile_cnt;
-    int32_t* __restrict__ tp = a.tile_pre;
+    const int G = a.ntiles, Ep = a.Ep, Q = Ep / 4;
+    int NG = 1024 / Q;
+    if (NG > 64) NG = 64;
+    const int g = tid / Q, q = tid % Q;
+    const bool active = g < NG;
+    const int RG = (G + NG - 1) / NG;
+    const int r0 = min(G, g * RG), r1 = min(G, r0 + RG);
+    const int4* tc = reinterpret_cast<const int4*>(a.tile_cnt);
+    int4* tp = reinterpret_cast<int4*>(a.tile_pre);
 
-    // Column prefix over tiles (exclusive) and the expert's total.
-    int total = 0;
-    if (tid < a.E) {
-        int64_t idx = tid;
+    // Row-group sums of the tile histograms.
+    int4 acc = make_int4(0, 0, 0, 0);
+    if (active) {
 #pragma unroll 8
-        for (int tile = 0; tile < ntiles; ++tile, idx += a.E) {
-            const int c = tc[idx];
-            tp[idx] = total;
-            total += c;
+        for (int r = r0; r < r1; ++r) acc = add4(acc, ld_cg_v4(tc + (int64_t)r * Q + q));
+        s_grp[g * Ep + 4 * q + 0] = acc.x;
+        s_grp[g * Ep + 4 * q + 1] = acc.y;
+        s_grp[g * Ep + 4 * q + 2] = acc.z;
+        s_grp[g * Ep + 4 * q + 3] = acc.w;
+    }
+    // Distinct tokens per rank: thread (g2, r) sums rows g2, g2 + NG2, ...
+    const int NG2 = 1024 / a.R;
+    if (tid < NG2 * a.R) {
+        const int g2 = tid / a.R, r = tid % a.R;
+        int s = 0;
+#pragma unroll 4
+        for (int row = g2; row < G; row += NG2) s += __ldcg(a.tile_tok + (int64_t)row * a.R + r);
+        s_tok[tid] = s;
+    }
+    __syncthreads();
+
+    // Exclusive scan of the group sums down each column; the column total is
+    // the expert's count.
+    int total = 0;
+    if (tid < Ep) {
+        for (int gg = 0; gg < NG; ++gg) {
+            const int v = s_grp[gg * Ep + tid];
+            s_grp[gg * Ep + tid] = total;
+            total += v;
         }
-        a.cnt[tid] = total;
     }
     if (tid < a.R) {
         int s = 0;
-        for (int tile = 0; tile < ntiles; ++tile) s += a.tile_tok[(int64_t)tile * a.R + tid];
+        for (int g2 = 0; g2 < NG2; ++g2) s += s_tok[g2 * a.R + tid];
         a.tokens_in_rank[tid] = s;
     }
+    __syncthreads();
+
+    // Exclusive prefix of every tile row: the group's base plus its earlier rows.
+    if (active) {
+        int4 run = make_int4(s_grp[g * Ep + 4 * q + 0], s_grp[g * Ep + 4 * q + 1],
+                             s_grp[g * Ep + 4 * q + 2], s_grp[g * Ep + 4 * q + 3]);
+#pragma unroll 4
+        for (int r = r0; r < r1; ++r) {
+            const int4 v = ld_cg_v4(tc + (int64_t)r * Q + q);
+            tp[(int64_t)r * Q + q] = run;
+            run = add4(run, v);
+        }
+    }
+    if (tid < a.E) a.cnt[tid] = total;
 
     // Inclusive scan of the per-expert totals over e (warp shuffles, then warp sums).
-    int v = total;
+    int v = (tid < a.E) ? total : 0;
+    const int own = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, v, d);
@@ -136,7 +198,7 @@ layout_scan_kernel(LayoutArgs a, int ntiles)
     if (tid < a.E) {
         const int r = tid / eloc;
         const int base = (r > 0) ? s_incl[r * eloc - 1] : 0;
-        a.expert_offset[tid] = (int32_t)((int64_t)r * a.S + (v - total - base));
+        a.expert_offset[tid] = (int32_t)((int64_t)r * a.S + (v - own - base));
     }
     if (tid < a.R) {
         const int hi = s_incl[(tid + 1) * eloc - 1];
@@ -147,81 +209,35 @@ layout_scan_kernel(LayoutArgs a, int ntiles)
 }
 
 __global__ void __launch_bounds__(kLayoutThreads)
-layout_pos_kernel(LayoutArgs a, int64_t tpt)
+layout_pos_kernel(LayoutArgs a)
 {
-    __shared__ int s_base[kLayoutWarps * kMaxExperts];   // [warp][expert]
-    const int tile = blockIdx.x;
-    const int64_t t0 = (int64_t)tile * tpt;
-    const int64_t t1 = min(a.T, t0 + tpt);
-    const int64_t p0 = t0 * a.K;
-    const int np = (int)((t1 - t0) * a.K);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int E = a.E;
-
-    // Warp w owns the flat pairs [w*seg, w*seg + seg) of the tile; seg is a
-    // multiple of 32 so every chunk is a full warp.
-    const int seg = (((np + kLayoutWarps - 1) / kLayoutWarps) + 31) & ~31;
-    const int w_begin = warp * seg;
-    const int w_end = min(np, w_begin + seg);
-    int* mine = s_base + warp * E;
-
-    for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) s_base[i] = 0;
-    __syncthreads();
-
-    // Pass 1: per-warp histogram (one writer per row; no atomics).
-    for (int c = w_begin; c < w_begin + seg; c += 32) {
-        const int i = c + lane;
-        const int e = (i < w_end) ? valid_id(__ldg(a.ids + p0 + i), E) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
-        __syncwarp();
-    }
-    __syncthreads();
-
-    // Exclusive prefix over warps, seeded with the expert offset and the
-    // counts of all earlier tiles.
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int base = a.expert_offset[e] + a.tile_pre[(int64_t)tile * E + e];
-#pragma unroll
-        for (int w = 0; w < kLayoutWarps; ++w) {
-            const int c = s_base[w * E + e];
-            s_base[w * E + e] = base;
-            base += c;
-        }
-    }
-    __syncthreads();
-
-    // Pass 2: row = running base of the expert + rank among equal ids in lower lanes.
-    for (int c = w_begin; c < w_begin + seg; c += 32) {
-        const int i = c + lane;
-        const bool in = i < w_end;
-        const int e = in ? valid_id(__ldg(a.ids + p0 + i), E) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int b = (e >= 0) ? mine[e] : 0;
-        if (in) a.pos[p0 + i] = (e >= 0) ? b + __popc(peers & lanemask_lt(lane)) : -1;
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] = b + __popc(peers);
-        __syncwarp();
-    }
+    __shared__ int s_base[kLayoutWarps * kMaxExperts];
+    griddep_wait();
+    griddep_launch_dependents();
+    tile_positions(a, blockIdx.x, s_base, a.pos, nullptr);
 }
 
 }  // namespace
 
-cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s, int64_t* launches)
+cudaError_t launch_layout_counts(const LayoutArgs& a, const LaunchOpts& o)
 {
-    const int64_t tpt = layout_tokens_per_tile(a.K);
-    const int64_t ntiles = layout_tiles(a.T, a.K);
-    if (ntiles > 0) {
-        layout_count_kernel<<<(unsigned)ntiles, kLayoutThreads, 0, s>>>(a, tpt);
-        ++*launches;
-    }
-    layout_scan_kernel<<<1, 1024, 0, s>>>(a, (int)ntiles);
-    ++*launches;
-    if (ntiles > 0) {
-        layout_pos_kernel<<<(unsigned)ntiles, kLayoutThreads, 0, s>>>(a, tpt);
-        ++*launches;
-    }
-    return cudaGetLastError();
+    cudaError_t e = cudaSuccess;
+    if (a.ntiles > 0)
+        e = launch_kernel(layout_count_kernel, dim3(a.ntiles), dim3(kLayoutThreads), 0, o, a);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(layout_scan_kernel, dim3(1), dim3(1024), 0, o, a);
+}
+
+cudaError_t launch_layout_positions(const LayoutArgs& a, const LaunchOpts& o)
+{
+    if (a.ntiles <= 0) return cudaSuccess;
+    return launch_kernel(layout_pos_kernel, dim3(a.ntiles), dim3(kLayoutThreads), 0, o, a);
+}
+
+cudaError_t launch_layout(const LayoutArgs& a, const LaunchOpts& o)
+{
+    cudaError_t e = launch_layout_counts(a, o);
+    return e != cudaSuccess ? e : launch_layout_positions(a, o);
 }
 
 }  // namespace ep

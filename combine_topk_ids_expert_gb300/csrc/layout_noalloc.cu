@@ -41,11 +41,16 @@ void* g_scratch_addr[kCachedDevices];   // device address of g_layout_scratch, p
 
 size_t seg(size_t bytes) { return (bytes + kSegAlign - 1) / kSegAlign * kSegAlign; }
 
+// Tiles of max(1, 2048/K) tokens: a fixed tiling, so the scratch bound
+// depends on the call's sizes only.
+int64_t noalloc_tokens_per_tile(int K) { return 2048 / K > 0 ? 2048 / K : 1; }
+
 // Bytes of scratch the layout of T tokens needs (tile tables plus one word).
 size_t scratch_needed(int64_t T, int K, int E, int R)
 {
-    const size_t tiles = (size_t)ep::layout_tiles(T, K);
-    return 2 * seg(tiles * (size_t)E * 4) + seg(tiles * (size_t)R * 4) + seg(4);
+    const size_t tiles = (size_t)ep::tile_count(T, noalloc_tokens_per_tile(K));
+    const size_t Ep = (size_t)ep::round_up4(E);
+    return 2 * seg(tiles * Ep * 4) + seg(tiles * (size_t)R * 4) + seg(4);
 }
 
 // Device address of g_layout_scratch on the current device, looked up once per device.
@@ -97,19 +102,21 @@ extern "C" ep_status ep_dispatch_layout_noalloc(
     void* base = nullptr;
     if (scratch_address(&base) != cudaSuccess) return EP_ERR_CUDA;
     uint8_t* p = static_cast<uint8_t*>(base);
-    const size_t tiles = (size_t)ep::layout_tiles(T, K);
-
     ep::LayoutArgs a;
     a.ids = topk_expert_ids_TK;
     a.T = T;
     a.S = S;
+    a.tpt = noalloc_tokens_per_tile(K);
+    a.ntiles = (int)ep::tile_count(T, a.tpt);
     a.K = K;
     a.E = E;
     a.R = R;
+    a.Ep = ep::round_up4(E);
+    const size_t tiles = (size_t)a.ntiles;
     a.tile_cnt = reinterpret_cast<int32_t*>(p);
-    p += seg(tiles * (size_t)E * 4);
+    p += seg(tiles * (size_t)a.Ep * 4);
     a.tile_pre = reinterpret_cast<int32_t*>(p);
-    p += seg(tiles * (size_t)E * 4);
+    p += seg(tiles * (size_t)a.Ep * 4);
     a.tile_tok = reinterpret_cast<int32_t*>(p);
     p += seg(tiles * (size_t)R * 4);
     a.cnt = tokens_per_expert;
@@ -121,7 +128,7 @@ extern "C" ep_status ep_dispatch_layout_noalloc(
     // Without a caller word, bad-id reports land in a scratch word nobody reads.
     a.err = error_flags ? error_flags : reinterpret_cast<uint32_t*>(p);
     int64_t launches = 0;
-    if (ep::launch_layout(a, static_cast<cudaStream_t>(stream), &launches) != cudaSuccess)
-        return EP_ERR_CUDA;
+    const ep::LaunchOpts o{static_cast<cudaStream_t>(stream), true, &launches};
+    if (ep::launch_layout(a, o) != cudaSuccess) return EP_ERR_CUDA;
     return EP_OK;
 }

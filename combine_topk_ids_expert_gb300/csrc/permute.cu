@@ -4,19 +4,27 @@
 // Follows "Unify expert parallel token dispatcher API", section "Backend
 // behavior" (HybridEP: non-blocking dispatch sizes the fused-permute output by
 // the current capacity; DeepEP: the current capacity is the per-rank layout
-// stride). Positions come from the layout kernels; this file only moves data.
+// stride).
 //
-// The kernel is HBM-bound: it reads T rows and writes up to T*K rows. Two
-// implementations:
-//   vec  : a CTA per token (grid-stride); each thread loads its 16-byte
-//          vectors of the row once (non-coherent, no L1 allocation) and stores
-//          them to every destination row.
-//   bulk : one warp per CTA drives bulk async copies: a row goes global ->
-//          shared memory once (completion tracked by an mbarrier), then each
-//          lane k copies it shared -> global to its destination row; a ring of
-//          row slots keeps several loads and stores in flight per SM. No
-//          multicast, no cluster: plain 1-D bulk copies within one CTA.
-#include "ep_kernels.cuh"
+// HBM-bound: reads T rows and writes up to T*K rows. Three kernels:
+//   dispatch_fused : the default. One CTA (8 warps) per layout tile, about one
+//                    per SM. Thread 0 starts bulk async loads of the tile's
+//                    rows into a shared-memory ring *before* waiting for the
+//                    layout scan (the rows do not depend on it), then all
+//                    warps compute the tile's positions into shared memory,
+//                    then warp 0 streams the rows out: lane k issues the bulk
+//                    store of destination k; warps 1-7 write scores and
+//                    sources. Completion of loads is tracked by mbarriers
+//                    (bounded waits); a slot is reused only after its stores
+//                    have read it (cp.async.bulk.wait_group.read).
+//   permute_bulk   : the same ring for a standalone permute (positions from
+//                    global memory, prefetched two tokens ahead), one warp per
+//                    CTA, one CTA per SM, tokens strided by the grid.
+//   permute_vec    : a CTA per token (grid-stride); each thread loads its
+//                    16-byte vectors of the row once and stores them to every
+//                    destination row.
+// No multicast and no clusters: plain 1-D bulk copies within one CTA.
+#include "ep_device.cuh"
 
 namespace ep {
 namespace {
@@ -25,22 +33,16 @@ constexpr int kVecThreads = 128;
 constexpr int kBulkLag = 4;            // store groups in flight before a slot is reused
 constexpr int kBulkMaxStages = 32;
 constexpr int kBulkSmemBudget = 200 * 1024;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bounded mbarrier wait (then EP_DEVERR_TIMEOUT)
+constexpr int kFusedSmemCap = 227 * 1024 - 1024;   // dynamic shared memory of the fused kernel
 
-__device__ __forceinline__ int4 ld_stream_v4(const int4* p)
-{
-    int4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
+int slot_bytes_of(int64_t row_bytes) { return (int)((row_bytes + 127) / 128 * 128); }
 
 template <int U>
 __global__ void __launch_bounds__(kVecThreads)
 permute_vec_kernel(PermuteArgs a)
 {
     __shared__ int s_pos[kMaxTopk];
+    griddep_wait();
     const int64_t V = a.row_bytes / 16;
     const int4* __restrict__ x = static_cast<const int4*>(a.x);
     int4* __restrict__ rx = static_cast<int4*>(a.recv_x);
@@ -48,10 +50,10 @@ permute_vec_kernel(PermuteArgs a)
     for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
         if (threadIdx.x < a.K) {
             const int64_t q = t * a.K + threadIdx.x;
-            const int p = a.pos[q];
+            const int p = __ldcg(a.pos + q);
             s_pos[threadIdx.x] = p;
             if (p >= 0) {
-                a.recv_scores[p] = a.scores[q];
+                a.recv_scores[p] = __ldcg(a.scores + q);
                 a.recv_src[p] = (int32_t)q;
             }
         }
@@ -62,7 +64,7 @@ permute_vec_kernel(PermuteArgs a)
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + (int64_t)u * kVecThreads;
-                if (v < V) r[u] = ld_stream_v4(src + v);
+                if (v < V) r[u] = ld_cg_v4(src + v);
             }
             for (int k = 0; k < a.K; ++k) {
                 const int p = s_pos[k];
@@ -77,98 +79,18 @@ permute_vec_kernel(PermuteArgs a)
         }
         __syncthreads();
     }
+    griddep_launch_dependents();
 }
 
-// ---- bulk async copy helpers (inline PTX) ---------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p)
+// Lets loads already issued land before the CTA's shared memory is released
+// (after a timed-out wait), under one shared deadline.
+__device__ void drain_loads(uint32_t bar0, int stages, int64_t from, int64_t to)
 {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0u;
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait: false if the phase has not completed by the deadline
-// (nanoseconds of %globaltimer).
-__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t deadline)
-{
-    while (true) {
-        for (int it = 0; it < 64; ++it)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() > deadline) return false;
-    }
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_until(bar, parity, globaltimer_ns() + kWaitLimitNs);
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    for (int64_t m = from; m < to; ++m)
+        if (!mbar_wait_until(bar0 + 8u * (uint32_t)(m % stages), (uint32_t)((m / stages) & 1),
+                             deadline))
+            break;
 }
 
 // One warp per CTA. Lane 0 issues the row loads; lane k < K issues the store
@@ -182,6 +104,7 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
     const int lane = threadIdx.x;
     const int64_t G = gridDim.x;
     const int64_t b = blockIdx.x;
+    griddep_wait();
     if (b >= a.T) return;
     const int64_t n_my = (a.T - 1 - b) / G + 1;
     const uint32_t bytes = static_cast<uint32_t>(a.row_bytes);
@@ -215,8 +138,8 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
         w = 0.f;
         if (i < n_my && lane < K) {
             const int64_t q = (b + i * G) * K + lane;
-            p = __ldg(a.pos + q);
-            w = __ldg(a.scores + q);
+            p = __ldcg(a.pos + q);
+            w = __ldcg(a.scores + q);
         }
     };
     int p_cur, p_nxt;
@@ -231,17 +154,15 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
         float w_nn;
         fetch(i + 2, p_nn, w_nn);
         const int s = (int)(i % stages);
-        const uint32_t parity = (uint32_t)((i / stages) & 1);
-        if (!mbar_wait(bar0 + 8u * s, parity)) {
+        if (!mbar_wait(bar0 + 8u * s, (uint32_t)((i / stages) & 1))) {
             ok = false;
             break;
         }
         if (p_cur >= 0) {
             bulk_s2g(rx + (int64_t)p_cur * a.row_bytes, slot0 + (uint32_t)s * (uint32_t)slot_bytes,
                      bytes);
-            const int64_t q = (b + i * G) * K + lane;
             a.recv_scores[p_cur] = w_cur;
-            a.recv_src[p_cur] = (int32_t)q;
+            a.recv_src[p_cur] = (int32_t)((b + i * G) * K + lane);
         }
         bulk_commit();
         const int64_t j = i - kBulkLag;
@@ -256,18 +177,94 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
         w_nxt = w_nn;
     }
     bulk_wait_all();
-    if (!ok) {
-        if (lane == 0) {
+    if (!ok && lane == 0) {
+        atomicOr(a.err, kErrTimeout);
+        int64_t issued_hi = (i - kBulkLag) + stages;   // loads issued for tokens < issued_hi
+        if (issued_hi < n_pro) issued_hi = n_pro;
+        drain_loads(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my);
+    }
+    griddep_launch_dependents();
+}
+
+// Positions + permute of one layout tile per CTA (see the file comment).
+// Shared memory: [stages slots of slot_bytes][kLayoutWarps * Ep ints][tile pairs ints].
+__global__ void __launch_bounds__(kLayoutThreads, 1)
+dispatch_fused_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kBulkMaxStages];
+    int* s_base = reinterpret_cast<int*>(smem + (size_t)stages * slot_bytes);
+    int* s_pos = s_base + kLayoutWarps * L.Ep;
+    const int tile = blockIdx.x;
+    const int64_t t0 = (int64_t)tile * L.tpt;
+    const int64_t t1 = min(L.T, t0 + L.tpt);
+    const int n_my = (int)(t1 - t0);
+    const int64_t p0 = t0 * L.K;
+    const int K = L.K;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bytes = static_cast<uint32_t>(a.row_bytes);
+    const uint32_t slot0 = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
+    uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
+    const int n_pro = n_my < stages ? n_my : stages;
+
+    auto issue_load = [&](int i) {
+        const int s = i % stages;
+        const uint32_t bar = bar0 + 8u * s;
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(slot0 + (uint32_t)s * (uint32_t)slot_bytes, x + (t0 + i) * a.row_bytes, bytes,
+                 bar);
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(bar0 + 8u * s, 1u);
+        fence_mbar_init();
+        // The rows do not depend on the layout: start them before waiting for it.
+        for (int i = 0; i < n_pro; ++i) issue_load(i);
+    }
+
+    griddep_wait();                                   // counts and offsets are ready
+    tile_positions(L, tile, s_base, L.pos, s_pos);    // ends with __syncthreads
+    griddep_launch_dependents();
+
+    if (warp == 0) {
+        bool ok = true;
+        int i = 0;
+        for (; i < n_my; ++i) {
+            const int s = i % stages;
+            if (!mbar_wait(bar0 + 8u * s, (uint32_t)((i / stages) & 1))) {
+                ok = false;
+                break;
+            }
+            if (lane < K) {
+                const int p = s_pos[i * K + lane];
+                if (p >= 0)
+                    bulk_s2g(rx + (int64_t)p * a.row_bytes,
+                             slot0 + (uint32_t)s * (uint32_t)slot_bytes, bytes);
+            }
+            bulk_commit();
+            const int j = i - kBulkLag;
+            if (j >= 0 && j + stages < n_my) {
+                bulk_wait_read<kBulkLag>();
+                __syncwarp();
+                if (lane == 0) issue_load(j + stages);
+            }
+        }
+        bulk_wait_all();
+        if (!ok && lane == 0) {
             atomicOr(a.err, kErrTimeout);
-            // Let loads already issued land before the CTA's shared memory is
-            // released, under one shared deadline.
-            int64_t issued_hi = (i - kBulkLag) + stages;   // loads issued for tokens < issued_hi
+            int issued_hi = (i - kBulkLag) + stages;
             if (issued_hi < n_pro) issued_hi = n_pro;
-            const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
-            for (int64_t m = i; m < n_my && m < issued_hi; ++m)
-                if (!mbar_wait_until(bar0 + 8u * (uint32_t)(m % stages),
-                                     (uint32_t)((m / stages) & 1), deadline))
-                    break;
+            drain_loads(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my);
+        }
+    } else {
+        const int np = n_my * K;
+        for (int j = threadIdx.x - 32; j < np; j += kLayoutThreads - 32) {
+            const int p = s_pos[j];
+            if (p >= 0) {
+                a.recv_scores[p] = __ldcg(a.scores + p0 + j);
+                a.recv_src[p] = (int32_t)(p0 + j);
+            }
         }
     }
 }
@@ -283,17 +280,20 @@ int vec_unroll(int64_t row_bytes)
 
 }  // namespace
 
-cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int num_sms, PermutePlan* plan)
+cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms,
+                         PermutePlan* plan)
 {
+    (void)E;
     plan->impl = impl;
     plan->stages = 0;
     plan->smem_bytes = 0;
-    const int slot = (int)((row_bytes + 127) / 128 * 128);
+    plan->fused_smem_cap = 0;
+    const int slot = slot_bytes_of(row_bytes);
     if (impl == 2) {
         int stages = kBulkSmemBudget / slot;
         if (stages > kBulkMaxStages) stages = kBulkMaxStages;
         if (stages < kBulkLag + 2 || row_bytes > (1 << 20) || K > 32) {
-            plan->impl = impl = 1;   // rows too large for a useful ring: vector path
+            plan->impl = impl = 1;   // rows too large for a useful ring, or K > a warp
         } else {
             plan->stages = stages;
             plan->smem_bytes = stages * slot;
@@ -301,6 +301,10 @@ cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int num_sms, Permut
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  plan->smem_bytes);
             if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(dispatch_fused_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemCap);
+            if (e != cudaSuccess) return e;
+            plan->fused_smem_cap = kFusedSmemCap;
             plan->grid = num_sms;
             return cudaSuccess;
         }
@@ -323,29 +327,40 @@ cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int num_sms, Permut
     return cudaSuccess;
 }
 
-cudaError_t launch_permute(const PermuteArgs& a, const PermutePlan& plan, cudaStream_t s,
-                           int64_t* launches)
+cudaError_t launch_permute(const PermuteArgs& a, const PermutePlan& plan, const LaunchOpts& o)
 {
     if (a.T <= 0) return cudaSuccess;
     const unsigned grid = (unsigned)(a.T < plan.grid ? a.T : plan.grid);
-    if (plan.impl == 2) {
-        permute_bulk_kernel<<<grid, 32, plan.smem_bytes, s>>>(a, plan.stages,
-                                                              (int)((a.row_bytes + 127) / 128 * 128));
-    } else {
-        switch (vec_unroll(a.row_bytes)) {
-#define EP_LAUNCH(U)                                                        \
-    case U:                                                                 \
-        permute_vec_kernel<U><<<grid, kVecThreads, 0, s>>>(a);              \
-        break;
-            EP_LAUNCH(1) EP_LAUNCH(2) EP_LAUNCH(3) EP_LAUNCH(4)
-            EP_LAUNCH(5) EP_LAUNCH(6) EP_LAUNCH(7) EP_LAUNCH(8)
+    if (plan.impl == 2)
+        return launch_kernel(permute_bulk_kernel, dim3(grid), dim3(32), (size_t)plan.smem_bytes, o,
+                             a, plan.stages, slot_bytes_of(a.row_bytes));
+    switch (vec_unroll(a.row_bytes)) {
+#define EP_LAUNCH(U) \
+    case U:          \
+        return launch_kernel(permute_vec_kernel<U>, dim3(grid), dim3(kVecThreads), 0, o, a);
+        EP_LAUNCH(1) EP_LAUNCH(2) EP_LAUNCH(3) EP_LAUNCH(4)
+        EP_LAUNCH(5) EP_LAUNCH(6) EP_LAUNCH(7) EP_LAUNCH(8)
 #undef EP_LAUNCH
-            default:
-                return cudaErrorInvalidValue;
-        }
+        default:
+            return cudaErrorInvalidValue;
     }
-    ++*launches;
-    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
+                                  const PermutePlan& plan, const LaunchOpts& o)
+{
+    if (plan.impl != 2 || plan.fused_smem_cap <= 0 || l.K > 32) return cudaErrorNotSupported;
+    if (l.ntiles <= 0) return cudaSuccess;
+    const int64_t tile_pairs = l.tpt * l.K;
+    if (tile_pairs > kMaxTilePairs) return cudaErrorNotSupported;
+    const int slot = slot_bytes_of(p.row_bytes);
+    const int64_t fixed = ((int64_t)kLayoutWarps * l.Ep + tile_pairs) * 4;
+    int64_t stages = (plan.fused_smem_cap - fixed) / slot;
+    if (stages > kBulkMaxStages) stages = kBulkMaxStages;
+    if (stages < kBulkLag + 2) return cudaErrorNotSupported;
+    const size_t smem = (size_t)(stages * slot + fixed);
+    return launch_kernel(dispatch_fused_kernel, dim3(l.ntiles), dim3(kLayoutThreads), smem, o, l,
+                         p, (int)stages, slot);
 }
 
 }  // namespace ep

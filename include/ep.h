@@ -230,7 +230,7 @@ EP_API ep_status ep_buffer_query(const ep_buffer* buf, ep_buffer_info* info);
  * EP_DEVERR_BAD_ID into (the caller zeroes it). The kernels' other global
  * memory is a library-owned 4 MiB device array per GPU, held until the
  * process exits; a call whose tile tables need more,
- *   ceil(T / max(1, 2048/K)) * (2*E + R) * 4 bytes (plus alignment),
+ *   ceil(T / max(1, 2048/K)) * (2*roundup4(E) + R) * 4 bytes (plus alignment),
  * is rejected with EP_ERR_CAPACITY (about 516k tokens at E=256, R=8, K=8;
  * about 126k at E=1024, R=64, K=8). The first call on each device (with that
  * device current) looks up the array's device address; make it before any
