@@ -40,7 +40,8 @@ METRIC = "dispatch+combine tokens/s & achieved HBM GB/s vs GB300 peak (bf16, 1 G
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "combine_topk_ids_expert_gb300", "csrc", f)
-                  for f in ("layout.cu", "permute.cu", "combine.cu", "ep_kernels.cuh")]
+                  for f in ("layout.cu", "permute.cu", "combine.cu", "ep_kernels.cuh",
+                            "ep_device.cuh")]
 
 
 def parse_args():
@@ -125,6 +126,8 @@ def profiled_traffic(kernel: str, workload: str) -> float | None:
         return None
     src = kernel_source_hash()
     for ln in lines:
+        if ln.lstrip().startswith("#"):
+            continue
         parts = ln.split()
         if len(parts) == 4 and parts[0] == kernel and parts[1] == workload and parts[3] == src:
             return float(parts[2])
