@@ -167,9 +167,15 @@ cudaError_t plan_combine(int in_dtype, int num_sms, int* grid)
     return cudaSuccess;
 }
 
-cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& o)
+cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& opts)
 {
     if (a.T <= 0) return cudaSuccess;
+    // The combine follows the expert (or, with an identity expert, the permute)
+    // and would only start early to wait: launch it in plain stream order. In a
+    // captured graph an early-launched combine behind the bulk permute measured
+    // slower than a plain dependency.
+    LaunchOpts o = opts;
+    o.pdl = false;
     const dim3 g((unsigned)(a.T < grid ? a.T : grid)), b(kCombineThreads);
     if (a.in_dtype == 0 && a.out_dtype == 0) return launch_kernel(combine_vec_kernel<0, 0>, g, b, 0, o, a);
     if (a.in_dtype == 0 && a.out_dtype == 1) return launch_kernel(combine_vec_kernel<0, 1>, g, b, 0, o, a);

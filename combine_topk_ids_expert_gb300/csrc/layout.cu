@@ -25,6 +25,7 @@ namespace ep {
 namespace {
 
 constexpr int kCountUnroll = 4;
+constexpr int kScanRows = 10;   // tile rows a scan thread holds in registers
 
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_count_kernel(LayoutArgs a)
@@ -117,11 +118,20 @@ layout_scan_kernel(LayoutArgs a)
     const int4* tc = reinterpret_cast<const int4*>(a.tile_cnt);
     int4* tp = reinterpret_cast<int4*>(a.tile_pre);
 
-    // Row-group sums of the tile histograms.
+    // Row-group sums of the tile histograms. The group's rows are loaded into
+    // registers in one round (kScanRows at a time) and kept for the prefix pass.
+    int4 rows[kScanRows];
     int4 acc = make_int4(0, 0, 0, 0);
     if (active) {
-#pragma unroll 8
-        for (int r = r0; r < r1; ++r) acc = add4(acc, ld_cg_v4(tc + (int64_t)r * Q + q));
+        for (int c0 = r0; c0 < r1; c0 += kScanRows) {
+#pragma unroll
+            for (int j = 0; j < kScanRows; ++j) {
+                const int r = c0 + j;
+                rows[j] = (r < r1) ? ld_cg_v4(tc + (int64_t)r * Q + q) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < kScanRows; ++j) acc = add4(acc, rows[j]);
+        }
         s_grp[g * Ep + 4 * q + 0] = acc.x;
         s_grp[g * Ep + 4 * q + 1] = acc.y;
         s_grp[g * Ep + 4 * q + 2] = acc.z;
@@ -155,15 +165,26 @@ layout_scan_kernel(LayoutArgs a)
     }
     __syncthreads();
 
-    // Exclusive prefix of every tile row: the group's base plus its earlier rows.
+    // Exclusive prefix of every tile row: the group's base plus its earlier rows
+    // (from registers when the group fits one chunk, else reloaded).
     if (active) {
         int4 run = make_int4(s_grp[g * Ep + 4 * q + 0], s_grp[g * Ep + 4 * q + 1],
                              s_grp[g * Ep + 4 * q + 2], s_grp[g * Ep + 4 * q + 3]);
-#pragma unroll 4
-        for (int r = r0; r < r1; ++r) {
-            const int4 v = ld_cg_v4(tc + (int64_t)r * Q + q);
-            tp[(int64_t)r * Q + q] = run;
-            run = add4(run, v);
+        if (r1 - r0 <= kScanRows) {
+#pragma unroll
+            for (int j = 0; j < kScanRows; ++j) {
+                const int r = r0 + j;
+                if (r < r1) {
+                    tp[(int64_t)r * Q + q] = run;
+                    run = add4(run, rows[j]);
+                }
+            }
+        } else {
+            for (int r = r0; r < r1; ++r) {
+                const int4 v = ld_cg_v4(tc + (int64_t)r * Q + q);
+                tp[(int64_t)r * Q + q] = run;
+                run = add4(run, v);
+            }
         }
     }
     if (tid < a.E) a.cnt[tid] = total;

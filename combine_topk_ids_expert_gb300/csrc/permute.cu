@@ -225,7 +225,6 @@ dispatch_fused_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
 
     griddep_wait();                                   // counts and offsets are ready
     tile_positions(L, tile, s_base, L.pos, s_pos);    // ends with __syncthreads
-    griddep_launch_dependents();
 
     if (warp == 0) {
         bool ok = true;
@@ -267,6 +266,7 @@ dispatch_fused_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
             }
         }
     }
+    griddep_launch_dependents();
 }
 
 int vec_unroll(int64_t row_bytes)
