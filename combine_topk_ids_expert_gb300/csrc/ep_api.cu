@@ -26,6 +26,7 @@ struct ep_buffer {
     int64_t max_tiles;      // layout tiles the tables hold
     int ep_stride;          // row stride of the tile tables: roundup4(E)
     bool pdl;               // launch with programmatic dependent launch
+    int64_t test_skip_load; // test hook (EP_TEST_SKIP_LOAD), -1 = off
     size_t ws_bytes;
     // carved device pointers
     uint8_t* recv_x;
@@ -209,6 +210,7 @@ ep::PermuteArgs permute_args(ep_buffer* b, const void* x, const float* scores)
     a.K = b->cfg.topk;
     a.row_bytes = b->row_bytes;
     a.err = b->err;
+    a.skip_load = b->test_skip_load;
     return a;
 }
 
@@ -309,6 +311,9 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     {
         const char* v = std::getenv("EP_PDL");
         b->pdl = !(v && std::strcmp(v, "0") == 0);
+        // Test hook: make one bounded wait of the bulk permute run out.
+        const char* t = std::getenv("EP_TEST_SKIP_LOAD");
+        b->test_skip_load = (t && *t) ? std::strtoll(t, nullptr, 10) : -1;
     }
     b->ws_bytes = o.total;
     uint8_t* w = static_cast<uint8_t*>(workspace);

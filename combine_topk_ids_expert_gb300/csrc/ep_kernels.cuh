@@ -99,6 +99,10 @@ struct PermuteArgs {
     int K;
     int64_t row_bytes;         // multiple of 16
     uint32_t* err;
+    // Test hook for the bounded-wait path: CTA 0 of the bulk kernels never
+    // issues the load of its local token with this index, so that token's wait
+    // runs out (EP_DEVERR_TIMEOUT). -1 (the default) disables it.
+    int64_t skip_load;
 };
 struct PermutePlan {
     int impl;                  // 1 = vec, 2 = bulk

@@ -82,15 +82,16 @@ permute_vec_kernel(PermuteArgs a)
     griddep_launch_dependents();
 }
 
-// Lets loads already issued land before the CTA's shared memory is released
-// (after a timed-out wait), under one shared deadline.
-__device__ void drain_loads(uint32_t bar0, int stages, int64_t from, int64_t to)
+// After a timed-out wait: lets every load this CTA issued (tokens [from, to)
+// except `skipped`, which was never issued) land before the CTA's shared memory
+// is released, under one shared deadline.
+__device__ void drain_loads(uint32_t bar0, int stages, int64_t from, int64_t to, int64_t skipped)
 {
     const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
     for (int64_t m = from; m < to; ++m)
-        if (!mbar_wait_until(bar0 + 8u * (uint32_t)(m % stages), (uint32_t)((m / stages) & 1),
-                             deadline))
-            break;
+        if (m != skipped)
+            mbar_wait_until(bar0 + 8u * (uint32_t)(m % stages), (uint32_t)((m / stages) & 1),
+                            deadline);
 }
 
 // One warp per CTA. Lane 0 issues the row loads; lane k < K issues the store
@@ -120,7 +121,9 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
     }
     __syncwarp();
 
+    const int64_t skipped = (b == 0) ? a.skip_load : -1;
     auto issue_load = [&](int64_t i) {
+        if (i == skipped) return;
         const int s = (int)(i % stages);
         const uint32_t bar = bar0 + 8u * s;
         mbar_expect_tx(bar, bytes);
@@ -181,7 +184,7 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
         atomicOr(a.err, kErrTimeout);
         int64_t issued_hi = (i - kBulkLag) + stages;   // loads issued for tokens < issued_hi
         if (issued_hi < n_pro) issued_hi = n_pro;
-        drain_loads(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my);
+        drain_loads(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my, skipped);
     }
     griddep_launch_dependents();
 }
@@ -209,7 +212,9 @@ dispatch_fused_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
     uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
     const int n_pro = n_my < stages ? n_my : stages;
 
+    const int64_t skipped = (tile == 0) ? a.skip_load : -1;
     auto issue_load = [&](int i) {
+        if (i == skipped) return;
         const int s = i % stages;
         const uint32_t bar = bar0 + 8u * s;
         mbar_expect_tx(bar, bytes);
@@ -254,7 +259,7 @@ dispatch_fused_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
             atomicOr(a.err, kErrTimeout);
             int issued_hi = (i - kBulkLag) + stages;
             if (issued_hi < n_pro) issued_hi = n_pro;
-            drain_loads(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my);
+            drain_loads(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my, skipped);
         }
     } else {
         const int np = n_my * K;

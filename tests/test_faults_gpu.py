@@ -166,3 +166,29 @@ def test_bad_ids_are_reported_and_contained(orc):
     assert np.array_equal(to_np(d.layout.pos), ref["pos"])
     assert to_np(d.layout.pos)[3, 1] == -1 and to_np(d.layout.pos)[4, 0] == -1
     buf.close()
+
+
+def test_bounded_wait_runs_out_and_reports(orc, monkeypatch):
+    # The bulk permute waits on an mbarrier for each row load with a 2 s limit.
+    # EP_TEST_SKIP_LOAD makes CTA 0 never issue one load, so that wait runs
+    # out: the kernel must set EP_DEVERR_TIMEOUT, let its other loads land and
+    # return, leaving the context usable. Nothing faults or hangs.
+    monkeypatch.setenv("EP_TEST_SKIP_LOAD", "0")
+    buf = ep.Buffer(64, D, E, R, K, dtype=torch.bfloat16, permute_impl=ep.EP_PERMUTE_BULK)
+    monkeypatch.delenv("EP_TEST_SKIP_LOAD")
+    x, ids, sc = small(T=40, seed=8)
+    xd, idd, scd = to_dev(x), to_dev(ids), to_dev(sc)
+    buf.dispatch(xd, scd, idd, 40)
+    torch.cuda.synchronize()
+    assert buf.device_error() & ep.EP_DEVERR_TIMEOUT
+    buf.close()
+    # The same GPU context keeps working: a fresh buffer is oracle-exact.
+    good = ep.Buffer(64, D, E, R, K, dtype=torch.bfloat16, permute_impl=ep.EP_PERMUTE_BULK)
+    d = good.dispatch(xd, scd, idd, 40)
+    out = good.combine(d.recv_x, scd)
+    torch.cuda.synchronize()
+    assert good.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, 40, E, R)
+    want, _ = orc.combine(ref["recv_x"], sc, ref["pos"], ref["rank_prefix"], ref["S"], R)
+    assert_combine_equal(to_np(out), want)
+    good.close()
