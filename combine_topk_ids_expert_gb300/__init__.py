@@ -30,7 +30,8 @@ from ._abi import (EP_BF16, EP_DEVERR_BAD_ID, EP_DEVERR_ROW_OOB, EP_DEVERR_TIMEO
 __all__ = [
     "Buffer", "Layout", "DispatchResult", "EpConfig", "EpError",
     "ep_buffer_required_bytes", "ep_buffer_init", "ep_buffer_destroy", "ep_dispatch_layout",
-    "ep_dispatch", "ep_dispatch_permute", "ep_combine", "ep_get_device_error",
+    "ep_dispatch", "ep_dispatch_permute", "ep_combine", "ep_combine_backward",
+    "ep_dispatch_backward", "ep_get_device_error",
     "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_pad_tokens", "ep_derive_max_tokens_pretrain",
     "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
     "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
@@ -131,6 +132,31 @@ def ep_combine(handle, y_recv: torch.Tensor, topk_scores_TK: torch.Tensor, num_t
     _check_dtype(topk_scores_TK, torch.float32, "topk_scores_TK")
     check(_abi.lib().ep_combine(handle, _ptr(y_recv), _ptr(topk_scores_TK), num_tokens,
                                 _ptr(out_TD), out_dtype, _stream(stream)), "ep_combine")
+
+
+def ep_combine_backward(handle, grad_out_TD: torch.Tensor, y_recv: torch.Tensor | None,
+                        topk_scores_TK: torch.Tensor, num_tokens: int, grad_y_recv: torch.Tensor,
+                        grad_scores_TK: torch.Tensor | None = None, stream=None) -> None:
+    _check_dtype(topk_scores_TK, torch.float32, "topk_scores_TK")
+    if grad_scores_TK is not None:
+        _check_dtype(grad_scores_TK, torch.float32, "grad_scores_TK")
+    check(_abi.lib().ep_combine_backward(handle, _ptr(grad_out_TD), _ptr(y_recv),
+                                         _ptr(topk_scores_TK), num_tokens, _ptr(grad_y_recv),
+                                         _ptr(grad_scores_TK), _stream(stream)),
+          "ep_combine_backward")
+
+
+def ep_dispatch_backward(handle, grad_recv_x: torch.Tensor,
+                         grad_recv_scores: torch.Tensor | None, num_tokens: int,
+                         grad_x_TD: torch.Tensor, grad_x_dtype: int,
+                         grad_scores_TK: torch.Tensor | None = None, stream=None) -> None:
+    for name, t in (("grad_recv_scores", grad_recv_scores), ("grad_scores_TK", grad_scores_TK)):
+        if t is not None:
+            _check_dtype(t, torch.float32, name)
+    check(_abi.lib().ep_dispatch_backward(handle, _ptr(grad_recv_x), _ptr(grad_recv_scores),
+                                          num_tokens, _ptr(grad_x_TD), grad_x_dtype,
+                                          _ptr(grad_scores_TK), _stream(stream)),
+          "ep_dispatch_backward")
 
 
 def ep_get_device_error(handle, stream=None) -> int:
@@ -248,6 +274,7 @@ class Buffer:
 
     def _layout(self, L: EpLayout) -> Layout:
         T, E, R, K = L.num_tokens, self.E, self.R, self.K
+        self._stride = L.rank_stride
         i32 = torch.int32
         return Layout(
             tokens_per_expert=self._view(L.tokens_per_expert, i32, (E,)),
@@ -260,6 +287,7 @@ class Buffer:
 
     def _dispatch_result(self, d: EpDispatchOut) -> DispatchResult:
         S = d.layout.rank_stride
+        self._stride = S
         return DispatchResult(
             recv_x=self._view(d.recv_x, self.dtype, (self.R, S, self.D)),
             recv_scores=self._view(d.recv_scores, torch.float32, (self.R, S)),
@@ -304,6 +332,38 @@ class Buffer:
             raise TypeError(f"out dtype must be bfloat16 or float32, got {out.dtype}")
         ep_combine(self.handle, y_recv, topk_scores_TK, T, out, _TORCH_TO_EP[out.dtype], stream)
         return out
+
+    def combine_backward(self, grad_out: torch.Tensor, y_recv: torch.Tensor | None,
+                         topk_scores_TK: torch.Tensor, grad_y: torch.Tensor | None = None,
+                         want_scores: bool = True, stream=None):
+        """(grad_y [R, S, D], grad_scores [T, K] or None) for the last dispatch.
+        grad_y rows that no pair references are left as they were."""
+        _check_dtype(grad_out, self.dtype, "grad_out")
+        T = topk_scores_TK.shape[0]
+        if grad_y is None:
+            S = self._last_stride()
+            grad_y = torch.empty((self.R, S, self.D), dtype=self.dtype, device=self.device)
+        gs = torch.empty((T, self.K), dtype=torch.float32, device=self.device) \
+            if want_scores else None
+        ep_combine_backward(self.handle, grad_out, y_recv, topk_scores_TK, T, grad_y, gs, stream)
+        return grad_y, gs
+
+    def dispatch_backward(self, grad_recv_x: torch.Tensor, num_tokens: int,
+                          grad_recv_scores: torch.Tensor | None = None,
+                          out_dtype: torch.dtype | None = None, stream=None):
+        """(grad_x [T, D], grad_scores [T, K] or None) for the last dispatch."""
+        _check_dtype(grad_recv_x, self.dtype, "grad_recv_x")
+        od = self.dtype if out_dtype is None else out_dtype
+        gx = torch.empty((num_tokens, self.D), dtype=od, device=self.device)
+        gs = None
+        if grad_recv_scores is not None:
+            gs = torch.empty((num_tokens, self.K), dtype=torch.float32, device=self.device)
+        ep_dispatch_backward(self.handle, grad_recv_x, grad_recv_scores, num_tokens, gx,
+                             _TORCH_TO_EP[od], gs, stream)
+        return gx, gs
+
+    def _last_stride(self) -> int:
+        return self._stride
 
     def device_error(self, stream=None) -> int:
         return ep_get_device_error(self.handle, stream)

@@ -120,7 +120,9 @@ combine_vec_kernel(CombineArgs a)
                 }
             }
             s_pos[threadIdx.x] = p;
-            s_w[threadIdx.x] = __ldcg(a.scores + q);
+            s_w[threadIdx.x] = a.unit_weights ? 1.0f : __ldcg(a.scores + q);
+            if (a.gather_out)
+                a.gather_out[q] = (p >= 0 && a.gather_in) ? __ldcg(a.gather_in + p) : 0.0f;
         }
         __syncthreads();
         for (int64_t v = threadIdx.x; v < V; v += kCombineThreads) {
@@ -143,6 +145,138 @@ combine_vec_kernel(CombineArgs a)
                 }
             }
             store_out<IN, OUT>(a.out, t, a.D, v, acc);
+        }
+        __syncthreads();
+    }
+    griddep_launch_dependents();
+}
+
+// Unpacks the N elements of a 16-byte vector of the input type to fp32.
+template <int IN>
+__device__ __forceinline__ void unpack(const int4& r, float* f)
+{
+    if constexpr (IN == 0) {
+        const uint32_t u[4] = {(uint32_t)r.x, (uint32_t)r.y, (uint32_t)r.z, (uint32_t)r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(u[i] << 16);
+            f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        }
+    } else {
+        f[0] = __int_as_float(r.x);
+        f[1] = __int_as_float(r.y);
+        f[2] = __int_as_float(r.z);
+        f[3] = __int_as_float(r.w);
+    }
+}
+
+// Packs N fp32 values to a 16-byte vector of the type (bf16: round to nearest even).
+template <int IN>
+__device__ __forceinline__ int4 pack(const float* f)
+{
+    if constexpr (IN == 0) {
+        return make_int4((int)pack_bf16x2(f[0], f[1]), (int)pack_bf16x2(f[2], f[3]),
+                         (int)pack_bf16x2(f[4], f[5]), (int)pack_bf16x2(f[6], f[7]));
+    } else {
+        return make_int4(__float_as_int(f[0]), __float_as_int(f[1]), __float_as_int(f[2]),
+                         __float_as_int(f[3]));
+    }
+}
+
+// Backward of combine, one CTA per token (grid-stride): for each valid pair,
+// grad_y[pos][d] = s * grad_out[t][d] (one fp32 product, rounded to the row
+// type) and, if requested, grad_scores[t][k] = <grad_out[t], y[pos]>: per-thread
+// fp32 FMA chains over the thread's vectors, then a fixed butterfly across the
+// warp and a fixed sum over warps (deterministic, order documented).
+template <int IN>
+__global__ void __launch_bounds__(kCombineThreads)
+combine_backward_kernel(CombineBwdArgs a)
+{
+    constexpr int N = InVec<IN>::kElems;
+    constexpr int kWarps = kCombineThreads / 32;
+    __shared__ int s_pos[kMaxTopk];
+    __shared__ float s_w[kMaxTopk];
+    __shared__ float s_red[kWarps][kLoadBatch];
+    griddep_wait();
+    const int64_t V = a.D / N;
+    const int4* __restrict__ gout = static_cast<const int4*>(a.grad_out);
+    const int4* __restrict__ y = static_cast<const int4*>(a.y);
+    int4* __restrict__ gy = static_cast<int4*>(a.grad_y);
+    const bool want_scores = a.grad_scores != nullptr;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+        if (threadIdx.x < a.K) {
+            const int64_t q = t * a.K + threadIdx.x;
+            int p = __ldcg(a.pos + q);
+            if (p >= 0) {
+                const int64_t r = (int64_t)p / a.S;
+                bool ok = r < a.R;
+                if (ok) {
+                    const int lo = (r > 0) ? __ldcg(a.rank_prefix + r - 1) : 0;
+                    ok = ((int64_t)p - r * a.S) < (int64_t)(__ldcg(a.rank_prefix + r) - lo);
+                }
+                if (!ok) {
+                    atomicOr(a.err, kErrRowOob);
+                    p = -1;
+                }
+            }
+            s_pos[threadIdx.x] = p;
+            s_w[threadIdx.x] = __ldcg(a.scores + q);
+        }
+        __syncthreads();
+        for (int k0 = 0; k0 < a.K; k0 += kLoadBatch) {
+            float part[kLoadBatch];
+#pragma unroll
+            for (int j = 0; j < kLoadBatch; ++j) part[j] = 0.0f;
+            for (int64_t v = threadIdx.x; v < V; v += kCombineThreads) {
+                float gf[N];
+                unpack<IN>(ld_cg_v4(gout + t * V + v), gf);
+                int4 yv[kLoadBatch];
+                if (want_scores) {
+#pragma unroll
+                    for (int j = 0; j < kLoadBatch; ++j) {
+                        const int k = k0 + j;
+                        const int p = (k < a.K) ? s_pos[k] : -1;
+                        if (p >= 0) yv[j] = ld_cg_v4(y + (int64_t)p * V + v);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kLoadBatch; ++j) {
+                    const int k = k0 + j;
+                    const int p = (k < a.K) ? s_pos[k] : -1;
+                    if (p < 0) continue;
+                    float o[N];
+#pragma unroll
+                    for (int e = 0; e < N; ++e) o[e] = __fmul_rn(s_w[k], gf[e]);
+                    gy[(int64_t)p * V + v] = pack<IN>(o);
+                    if (want_scores) {
+                        float yf[N];
+                        unpack<IN>(yv[j], yf);
+#pragma unroll
+                        for (int e = 0; e < N; ++e) part[j] = __fmaf_rn(gf[e], yf[e], part[j]);
+                    }
+                }
+            }
+            if (want_scores) {
+#pragma unroll
+                for (int j = 0; j < kLoadBatch; ++j)
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        part[j] += __shfl_xor_sync(0xffffffffu, part[j], off);
+                if (lane == 0)
+#pragma unroll
+                    for (int j = 0; j < kLoadBatch; ++j) s_red[warp][j] = part[j];
+                __syncthreads();
+                if (threadIdx.x < kLoadBatch && k0 + (int)threadIdx.x < a.K) {
+                    const int k = k0 + threadIdx.x;
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) sum += s_red[w][threadIdx.x];
+                    a.grad_scores[t * a.K + k] = (s_pos[k] >= 0) ? sum : 0.0f;
+                }
+                __syncthreads();
+            }
         }
         __syncthreads();
     }
@@ -181,6 +315,16 @@ cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& opt
     if (a.in_dtype == 0 && a.out_dtype == 1) return launch_kernel(combine_vec_kernel<0, 1>, g, b, 0, o, a);
     if (a.in_dtype == 1 && a.out_dtype == 0) return launch_kernel(combine_vec_kernel<1, 0>, g, b, 0, o, a);
     return launch_kernel(combine_vec_kernel<1, 1>, g, b, 0, o, a);
+}
+
+cudaError_t launch_combine_backward(const CombineBwdArgs& a, int grid, const LaunchOpts& opts)
+{
+    if (a.T <= 0) return cudaSuccess;
+    LaunchOpts o = opts;
+    o.pdl = false;
+    const dim3 g((unsigned)(a.T < grid ? a.T : grid)), b(kCombineThreads);
+    if (a.dtype == 0) return launch_kernel(combine_backward_kernel<0>, g, b, 0, o, a);
+    return launch_kernel(combine_backward_kernel<1>, g, b, 0, o, a);
 }
 
 }  // namespace ep

@@ -419,6 +419,74 @@ ep_status ep_combine(ep_buffer* buf, const void* y, const float* scores, int64_t
     a.in_dtype = buf->cfg.dtype == EP_BF16 ? 0 : 1;
     a.out_dtype = out_dtype == EP_BF16 ? 0 : 1;
     a.err = buf->err;
+    a.unit_weights = false;
+    a.gather_in = nullptr;
+    a.gather_out = nullptr;
+    if (ep::launch_combine(a, buf->combine_grid, opts(buf, as_stream(stream))) != cudaSuccess)
+        return EP_ERR_CUDA;
+    return EP_OK;
+}
+
+ep_status ep_combine_backward(ep_buffer* buf, const void* grad_out, const void* y,
+                              const float* scores, int64_t T, void* grad_y, float* grad_scores,
+                              ep_stream_t stream)
+{
+    if (!buf) return EP_ERR_INVALID_ARG;
+    if (!buf->has_layout || T != buf->last_T) return EP_ERR_NO_LAYOUT;
+    if (T > 0 && (!grad_out || !scores || !grad_y || (grad_scores && !y)))
+        return EP_ERR_INVALID_ARG;
+    if (!is_aligned(grad_out, 16) || !is_aligned(y, 16) || !is_aligned(grad_y, 16) ||
+        !is_aligned(scores, 4) || !is_aligned(grad_scores, 4))
+        return EP_ERR_ALIGNMENT;
+    ep::CombineBwdArgs a;
+    a.grad_out = grad_out;
+    a.y = y;
+    a.scores = scores;
+    a.pos = buf->pos;
+    a.rank_prefix = buf->rank_prefix;
+    a.grad_y = grad_y;
+    a.grad_scores = grad_scores;
+    a.T = T;
+    a.K = buf->cfg.topk;
+    a.R = buf->cfg.num_ranks;
+    a.S = buf->last_S;
+    a.D = buf->cfg.hidden;
+    a.dtype = buf->cfg.dtype == EP_BF16 ? 0 : 1;
+    a.err = buf->err;
+    if (ep::launch_combine_backward(a, buf->combine_grid, opts(buf, as_stream(stream))) !=
+        cudaSuccess)
+        return EP_ERR_CUDA;
+    return EP_OK;
+}
+
+ep_status ep_dispatch_backward(ep_buffer* buf, const void* grad_recv_x,
+                               const float* grad_recv_scores, int64_t T, void* grad_x,
+                               int32_t grad_x_dtype, float* grad_scores, ep_stream_t stream)
+{
+    if (!buf) return EP_ERR_INVALID_ARG;
+    if (!buf->has_layout || T != buf->last_T) return EP_ERR_NO_LAYOUT;
+    if (grad_x_dtype != EP_BF16 && grad_x_dtype != EP_F32) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!grad_recv_x || !grad_x)) return EP_ERR_INVALID_ARG;
+    if (!is_aligned(grad_recv_x, 16) || !is_aligned(grad_x, 16) ||
+        !is_aligned(grad_recv_scores, 4) || !is_aligned(grad_scores, 4))
+        return EP_ERR_ALIGNMENT;
+    ep::CombineArgs a;
+    a.y = grad_recv_x;
+    a.scores = nullptr;
+    a.pos = buf->pos;
+    a.rank_prefix = buf->rank_prefix;
+    a.out = grad_x;
+    a.T = T;
+    a.K = buf->cfg.topk;
+    a.R = buf->cfg.num_ranks;
+    a.S = buf->last_S;
+    a.D = buf->cfg.hidden;
+    a.in_dtype = buf->cfg.dtype == EP_BF16 ? 0 : 1;
+    a.out_dtype = grad_x_dtype == EP_BF16 ? 0 : 1;
+    a.err = buf->err;
+    a.unit_weights = true;
+    a.gather_in = grad_recv_scores;
+    a.gather_out = grad_scores;
     if (ep::launch_combine(a, buf->combine_grid, opts(buf, as_stream(stream))) != cudaSuccess)
         return EP_ERR_CUDA;
     return EP_OK;

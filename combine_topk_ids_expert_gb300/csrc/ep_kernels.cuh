@@ -134,9 +134,31 @@ struct CombineArgs {
     int64_t D;
     int in_dtype, out_dtype;   // 0 = bf16, 1 = fp32
     uint32_t* err;
+    // Dispatch backward reuses the combine gather: weights of 1 (scores unused),
+    // and gather_out[t][k] = gather_in[pos[t][k]] (0 without a valid row).
+    bool unit_weights;
+    const float* gather_in;    // [R*S] or null
+    float* gather_out;         // [T][K] or null
 };
 cudaError_t plan_combine(int in_dtype, int num_sms, int* grid);
 cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& o);
+
+struct CombineBwdArgs {
+    const void* grad_out;      // [T][D] of dtype
+    const void* y;             // [R*S][D] of dtype (read only when grad_scores is set)
+    const float* scores;       // [T][K]
+    const int32_t* pos;        // [T][K]
+    const int32_t* rank_prefix;// [R]
+    void* grad_y;              // [R*S][D] of dtype
+    float* grad_scores;        // [T][K] or null
+    int64_t T;
+    int K, R;
+    int64_t S;
+    int64_t D;
+    int dtype;                 // 0 = bf16, 1 = fp32
+    uint32_t* err;
+};
+cudaError_t launch_combine_backward(const CombineBwdArgs& a, int grid, const LaunchOpts& o);
 
 // Launches kernel with an optional programmatic-dependent-launch attribute.
 template <typename... KArgs, typename... Args>

@@ -211,6 +211,34 @@ EP_API ep_status ep_dispatch_permute(ep_buffer* buf, const void* x_TD, const flo
 EP_API ep_status ep_combine(ep_buffer* buf, const void* y_recv, const float* topk_scores_TK,
                      int64_t num_tokens, void* out_TD, int32_t out_dtype, ep_stream_t stream);
 
+/* Backward of ep_combine, for training ([align] "Testing": the unequal-count
+ * run must reproduce the equal-count run bit for bit in the forward AND the
+ * backward pass; the page does not spell the backward out, it is the
+ * derivative of the combine). Uses the layout of the last dispatch on this
+ * buffer; num_tokens must equal its T. grad_out_TD is [T][D] and y_recv,
+ * grad_y_recv are [R*S][D], all of the configured dtype. For every valid pair:
+ *   grad_y_recv[pos[t][k]][d] = topk_scores_TK[t][k] * grad_out_TD[t][d]
+ *   (one fp32 product, rounded to the dtype; rows no pair references are not
+ *   written), and, when grad_scores_TK (fp32 [T][K]) is non-NULL,
+ *   grad_scores_TK[t][k] = sum_d grad_out_TD[t][d] * y_recv[pos[t][k]][d]
+ *   (fp32 per-thread FMA chains reduced in a fixed order: deterministic; 0 for
+ *   a pair without a valid row). y_recv is read only for grad_scores_TK. */
+EP_API ep_status ep_combine_backward(ep_buffer* buf, const void* grad_out_TD, const void* y_recv,
+                                     const float* topk_scores_TK, int64_t num_tokens,
+                                     void* grad_y_recv, float* grad_scores_TK, ep_stream_t stream);
+
+/* Backward of ep_dispatch (same source as ep_combine_backward). grad_recv_x is
+ * [R*S][D] of the configured dtype; grad_x_TD [T][D] of grad_x_dtype:
+ *   grad_x_TD[t][d] = sum over valid k (ascending, fp32 from +0) of
+ *                     grad_recv_x[pos[t][k]][d], rounded to grad_x_dtype;
+ * and, when grad_scores_TK is non-NULL, grad_scores_TK[t][k] =
+ * grad_recv_scores[pos[t][k]] (0 without a valid row or without
+ * grad_recv_scores): the scores' gradient through recv_scores. */
+EP_API ep_status ep_dispatch_backward(ep_buffer* buf, const void* grad_recv_x,
+                                      const float* grad_recv_scores, int64_t num_tokens,
+                                      void* grad_x_TD, int32_t grad_x_dtype,
+                                      float* grad_scores_TK, ep_stream_t stream);
+
 /* Synchronously read and clear the device error word (EP_DEVERR_* bits).
  * Refused with EP_ERR_CAPTURE_HOST_SYNC while the stream is capturing. */
 EP_API ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flags);

@@ -64,7 +64,13 @@ class Oracle:
                                       _i32p, _i32p, C.POINTER(C.c_int64), u32p]
         L.oracle_combine.argtypes = [C.c_void_p, C.c_int, i64, _f32p, _i32p, _i32p, i64, i64,
                                      i32, i32, C.c_void_p, C.c_int, u32p]
-        for name in ("oracle_routing_map", "oracle_layout", "oracle_dispatch", "oracle_combine"):
+        vp = C.c_void_p
+        L.oracle_combine_backward.argtypes = [vp, C.c_int, vp, C.c_int, i64, _f32p, _i32p, _i32p,
+                                              i64, i64, i32, i32, vp, vp, u32p]
+        L.oracle_dispatch_backward.argtypes = [vp, C.c_int, i64, vp, _i32p, _i32p, i64, i64, i32,
+                                               i32, vp, C.c_int, vp, u32p]
+        for name in ("oracle_routing_map", "oracle_layout", "oracle_dispatch", "oracle_combine",
+                     "oracle_combine_backward", "oracle_dispatch_backward"):
             getattr(L, name).restype = C.c_int
 
     # -- scalars ------------------------------------------------------------
@@ -183,6 +189,57 @@ class Oracle:
         if rc:
             raise OracleError(f"oracle_combine rc={rc}")
         return out, int(err.value)
+
+
+    # -- backward ------------------------------------------------------------
+    def combine_backward(self, grad_out, y, scores, pos, rank_prefix, S: int, R: int,
+                         grad_y_fill: int = 0):
+        """(grad_y [R*S, D] of y's kind, grad_scores [T, K] fp32, err). Rows of
+        grad_y that no valid pair references keep the byte grad_y_fill."""
+        grad_out = np.ascontiguousarray(grad_out)
+        y = np.ascontiguousarray(y)
+        scores = np.ascontiguousarray(scores, dtype=np.float32)
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        rank_prefix = np.ascontiguousarray(rank_prefix, dtype=np.int32)
+        T, K = pos.shape
+        D = y.shape[1]
+        grad_y = np.zeros_like(y)
+        grad_y.view(np.uint8)[...] = grad_y_fill
+        gs = np.zeros((T, K), np.float32)
+        err = C.c_uint32(0)
+        rc = self.lib.oracle_combine_backward(
+            grad_out.ctypes.data if T else None, _kind(grad_out), y.ctypes.data if y.size else None,
+            _kind(y), D, scores.ravel() if T else np.zeros(1, np.float32),
+            pos.ravel() if T else np.zeros(1, np.int32), rank_prefix, S, T, K, R,
+            grad_y.ctypes.data if grad_y.size else None, gs.ctypes.data if T else None,
+            C.byref(err))
+        if rc:
+            raise OracleError(f"oracle_combine_backward rc={rc}")
+        return grad_y, gs, int(err.value)
+
+    def dispatch_backward(self, grad_recv, grad_recv_scores, pos, rank_prefix, S: int, R: int,
+                          out_dtype: str = "same"):
+        """(grad_x [T, D], grad_scores [T, K] fp32 or None, err)."""
+        grad_recv = np.ascontiguousarray(grad_recv)
+        gk = _kind(grad_recv)
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        rank_prefix = np.ascontiguousarray(rank_prefix, dtype=np.int32)
+        T, K = pos.shape
+        D = grad_recv.shape[1]
+        ok = {"same": gk, "bf16": BF16, "f32": F32}[out_dtype]
+        gx = np.zeros((T, D), dtype=np.uint16 if ok == BF16 else np.float32)
+        grs = None if grad_recv_scores is None else np.ascontiguousarray(grad_recv_scores,
+                                                                          dtype=np.float32)
+        gs = None if grs is None else np.zeros((T, K), np.float32)
+        err = C.c_uint32(0)
+        rc = self.lib.oracle_dispatch_backward(
+            grad_recv.ctypes.data if grad_recv.size else None, gk, D,
+            None if grs is None else grs.ctypes.data, pos.ravel() if T else np.zeros(1, np.int32),
+            rank_prefix, S, T, K, R, gx.ctypes.data if T else None, ok,
+            None if gs is None or not T else gs.ctypes.data, C.byref(err))
+        if rc:
+            raise OracleError(f"oracle_dispatch_backward rc={rc}")
+        return gx, gs, int(err.value)
 
 
 _default: Oracle | None = None

@@ -443,5 +443,112 @@ int oracle_combine(const void* y, int y_kind, int64_t D, const float* scores,
     return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Backward of combine and dispatch.                                          */
+/* ------------------------------------------------------------------------ */
+
+static int row_ok(int64_t p, const int32_t* rank_prefix_R, int64_t S, int32_t R)
+{
+    if (p < 0) return 0;
+    int64_t r = (S > 0) ? p / S : R;
+    if (r >= R) return 0;
+    int64_t lo = (r > 0) ? rank_prefix_R[r - 1] : 0;
+    return p - r * S < (int64_t)rank_prefix_R[r] - lo;
+}
+
+static void store_elem(void* base, int kind, int64_t i, float v)
+{
+    if (kind == ORC_BF16)
+        ((uint16_t*)base)[i] = oracle_bf16_from_f32(v);
+    else
+        ((float*)base)[i] = v;
+}
+
+/* Backward of combine. The pages require the backward pass to be reproduced
+ * bit for bit like the forward ([align] "Testing": unequal-count forward AND
+ * backward bitwise-match the equal-count run) but do not spell it out; it is
+ * the derivative of out[t] = sum_k s[t][k] * y[pos[t][k]]:
+ *   grad_y[pos[t][k]][d] = s[t][k] * grad_out[t][d]   (one fp32 product,
+ *                          rounded to y's kind), for every valid pair;
+ *   grad_scores[t][k]    = sum_d grad_out[t][d] * y[pos[t][k]][d], summed in
+ *                          fp64 in ascending d and rounded once to fp32
+ *                          (0 for a pair without a valid row).
+ * Rows of grad_y that no valid pair references are left as the caller filled
+ * them. A pair whose row lies outside its rank's true total raises
+ * ORC_ERR_ROW_OOB and contributes nothing. grad_scores may be NULL. */
+int oracle_combine_backward(const void* grad_out, int g_kind, const void* y, int y_kind,
+                            int64_t D, const float* scores, const int32_t* pos_TK,
+                            const int32_t* rank_prefix_R, int64_t S, int64_t T, int32_t K,
+                            int32_t R, void* grad_y, float* grad_scores, uint32_t* err)
+{
+    if (T < 0 || D <= 0 || K <= 0 || R <= 0 || S < 0) return ORC_EINVAL;
+    if ((g_kind != ORC_BF16 && g_kind != ORC_F32) || (y_kind != ORC_BF16 && y_kind != ORC_F32))
+        return ORC_EINVAL;
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t k = 0; k < K; ++k) {
+            int64_t p = pos_TK[t * K + k];
+            double dot = 0.0;
+            if (p >= 0 && !row_ok(p, rank_prefix_R, S, R)) {
+                *err |= ORC_ERR_ROW_OOB;
+                p = -1;
+            }
+            if (p >= 0) {
+#if ORACLE_MUTANT == 12
+                float s = scores[t * K];                /* mutant: always the first score */
+#else
+                float s = scores[t * K + k];
+#endif
+                for (int64_t d = 0; d < D; ++d) {
+                    float g = load_elem(grad_out, g_kind, t * D + d);
+                    store_elem(grad_y, y_kind, p * D + d, s * g);
+                    dot += (double)g * (double)load_elem(y, y_kind, p * D + d);
+                }
+            }
+            if (grad_scores) grad_scores[t * K + k] = (float)dot;
+        }
+    return ORC_OK;
+}
+
+/* Backward of dispatch: the derivative of recv_x[pos[t][k]] = x[t] and
+ * recv_scores[pos[t][k]] = s[t][k]:
+ *   grad_x[t][d]      = sum over valid k (ascending) of grad_recv[pos[t][k]][d],
+ *                       accumulated in fp32 from +0 (the same chain as
+ *                       combine with unit weights) and rounded to grad_x's kind;
+ *   grad_scores[t][k] = grad_recv_scores[pos[t][k]] (0 without a valid row).
+ * grad_recv_scores and grad_scores may be NULL (then that part is skipped). */
+int oracle_dispatch_backward(const void* grad_recv, int g_kind, int64_t D,
+                             const float* grad_recv_scores, const int32_t* pos_TK,
+                             const int32_t* rank_prefix_R, int64_t S, int64_t T, int32_t K,
+                             int32_t R, void* grad_x, int x_kind, float* grad_scores,
+                             uint32_t* err)
+{
+    if (T < 0 || D <= 0 || K <= 0 || R <= 0 || S < 0) return ORC_EINVAL;
+    if ((g_kind != ORC_BF16 && g_kind != ORC_F32) || (x_kind != ORC_BF16 && x_kind != ORC_F32))
+        return ORC_EINVAL;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t d = 0; d < D; ++d) {
+            float acc = 0.0f;
+#if ORACLE_MUTANT == 13
+            for (int32_t k = 1; k < K; ++k) {           /* mutant: drops the first term */
+#else
+            for (int32_t k = 0; k < K; ++k) {
+#endif
+                int64_t p = pos_TK[t * K + k];
+                if (!row_ok(p, rank_prefix_R, S, R)) continue;
+                acc = fmaf(1.0f, load_elem(grad_recv, g_kind, p * D + d), acc);
+            }
+            store_elem(grad_x, x_kind, t * D + d, acc);
+        }
+        for (int32_t k = 0; k < K; ++k) {
+            int64_t p = pos_TK[t * K + k];
+            int ok = row_ok(p, rank_prefix_R, S, R);
+            if (p >= 0 && !ok) *err |= ORC_ERR_ROW_OOB;
+            if (grad_scores)
+                grad_scores[t * K + k] = (ok && grad_recv_scores) ? grad_recv_scores[p] : 0.0f;
+        }
+    }
+    return ORC_OK;
+}
+
 /* Number of deliberately broken builds the tests can request (ORACLE_MUTANT). */
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -350,4 +350,110 @@ def pin_combine_rejects_rows_past_total(o):
     assert np.array_equal(out[1:], (sc[1:] * x[1:]).astype(np.float32))
 
 
+# ---------------------------------------------------------------------------
+# Backward: adjoint identities, finite differences, invariance
+# ---------------------------------------------------------------------------
+
+def _exact_grad(seed, T, D):
+    gi = (W.u64(seed, 13, T * D) % np.uint64(65)).astype(np.int64) - 32
+    return (gi.astype(np.float32) / np.float32(4.0)).reshape(T, D)
+
+
+def pin_combine_backward_adjoint(o):
+    # combine is linear in y: <combine(y), g> = <y, combine_backward_y(g)>,
+    # exact in fp64 for dyadic fp32 data.
+    T, N, E, K, R, D = 21, 24, 16, 4, 4, 12
+    ids = _ids(30, T, E, K)
+    x, sc = _exact_inputs(30, T, D, K)
+    g = _exact_grad(30, T, D)
+    d = o.dispatch(x, sc, ids, N, E, R)
+    out, _ = o.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R, "f32")
+    gy, _, err = o.combine_backward(g, d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R)
+    assert err == 0
+    lhs = float((out.astype(np.float64) * g).sum())
+    valid = np.zeros(R * d["S"], bool)
+    valid[d["pos"].ravel()] = True
+    rhs = float((d["recv_x"][valid].astype(np.float64) * gy[valid]).sum())
+    assert lhs == rhs
+
+
+def pin_combine_backward_scores_by_difference(o):
+    # grad_scores[t][k] is the change of <out, g> per unit change of s[t][k],
+    # measured with the forward combine (exact for dyadic data).
+    T, N, E, K, R, D = 9, 12, 8, 3, 2, 16
+    ids = _ids(31, T, E, K)
+    x, sc = _exact_inputs(31, T, D, K)
+    g = _exact_grad(31, T, D)
+    d = o.dispatch(x, sc, ids, N, E, R)
+    _, gs, _ = o.combine_backward(g, d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R)
+    base, _ = o.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R, "f32")
+    delta = np.float32(1.0 / 64.0)
+    for t in range(T):
+        for k in range(K):
+            s2 = sc.copy()
+            s2[t, k] += delta
+            o2, _ = o.combine(d["recv_x"], s2, d["pos"], d["rank_prefix"], d["S"], R, "f32")
+            diff = float(((o2.astype(np.float64) - base) * g).sum())
+            assert diff == float(delta) * float(gs[t, k]), (t, k)
+
+
+def pin_combine_backward_grad_y_rounding(o):
+    # bf16 grad_y is the bf16 rounding (torch's cast) of the fp32 product s * g.
+    import torch
+    T, N, E, K, R, D = 11, 12, 8, 2, 2, 32
+    ids = _ids(32, T, E, K)
+    sc = W.topk_scores(32, ids, E, "sigmoid_norm")
+    x = W.hidden(32, T, D, "bf16")
+    g = W.hidden(33, T, D, "bf16")
+    d = o.dispatch(x, sc, ids, N, E, R)
+    gy, _, _ = o.combine_backward(g, d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R)
+    gf = _f32_from_bits(g)
+    for t in range(T):
+        for k in range(K):
+            want = torch.from_numpy((sc[t, k] * gf[t]).astype(np.float32)).to(torch.bfloat16)
+            assert np.array_equal(gy[d["pos"][t, k]].view(np.int16),
+                                  want.view(torch.int16).numpy())
+
+
+def pin_dispatch_backward_adjoint(o):
+    # dispatch is linear in x and in s: <dispatch(x), G> = <x, grad_x> and
+    # <recv_scores, h> = <s, grad_scores>, exact for dyadic fp32 data.
+    T, N, E, K, R, D = 19, 20, 16, 4, 4, 10
+    ids = _ids(34, T, E, K)
+    x, sc = _exact_inputs(34, T, D, K)
+    d = o.dispatch(x, sc, ids, N, E, R)
+    rows = R * d["S"]
+    G = _exact_grad(35, rows, D)
+    h = _exact_grad(36, rows, 1).ravel()
+    gx, gs, err = o.dispatch_backward(G, h, d["pos"], d["rank_prefix"], d["S"], R)
+    assert err == 0
+    valid = np.zeros(rows, bool)
+    valid[d["pos"].ravel()] = True
+    lhs = float((d["recv_x"][valid].astype(np.float64) * G[valid]).sum())
+    assert lhs == float((x.astype(np.float64) * gx).sum())
+    lhs_s = float((d["recv_scores"][valid].astype(np.float64) * h[valid]).sum())
+    assert lhs_s == float((sc.astype(np.float64) * gs).sum())
+
+
+def pin_backward_unequal_count_invariance(o):
+    # [align] "Testing": forward AND backward reproduce the equal-count run
+    # bit for bit. Per-token gradients do not depend on N or on other tokens.
+    E, K, R, D = 16, 4, 4, 32
+    for a, b in [(8, 3), (5, 3), (13, 7)]:
+        T = b
+        ids = _ids(200 + T, T, E, K)
+        sc = W.topk_scores(200 + T, ids, E, "sigmoid_norm")
+        x = W.hidden(200 + T, T, D, "bf16")
+        g = W.hidden(300 + T, T, D, "bf16")
+        res = []
+        for N in (T, max(a, b)):
+            d = o.dispatch(x, sc, ids, N, E, R)
+            gy, gs, _ = o.combine_backward(g, d["recv_x"], sc, d["pos"], d["rank_prefix"],
+                                           d["S"], R)
+            gx, _, _ = o.dispatch_backward(gy, None, d["pos"], d["rank_prefix"], d["S"], R)
+            res.append((gs, gx))
+        assert np.array_equal(res[0][0].view(np.uint32), res[1][0].view(np.uint32))
+        assert np.array_equal(res[0][1], res[1][1])
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -24,6 +24,8 @@ MUTANTS = {
     9: "padding to a multiple of 8",
     10: "capacity uses floor division",
     11: "padded rows route to experts",
+    12: "combine backward scales every row by the first score",
+    13: "dispatch backward drops the first term",
 }
 
 
