@@ -243,13 +243,23 @@ def dist_env():
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """The slowest rank's value (all ranks call it). NCCL reduces a CUDA
+    tensor; other backends (gloo, used by the CPU tests) a host tensor."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(tokens_per_rank_step: int, steps: int, rank_ms: float, world: int) -> float:
+    """Whole-job tokens/s of `world` independent replicas: all ranks' tokens
+    over the slowest rank's time (weak scaling)."""
+    slowest = max_over_ranks(rank_ms, world)
+    return world * tokens_per_rank_step * steps / (slowest / 1e3)
 
 
 def barrier(world: int):
@@ -374,7 +384,7 @@ def run_gb300(args) -> dict | None:
     total_ms = sum(step_ms)
     total_ms_max = max_over_ranks(total_ms, world)
     ms_per_step = total_ms_max / K
-    tok_s = world * T * K / (total_ms_max / 1e3)
+    tok_s = replica_throughput(T, K, total_ms, world)
     nbytes = algorithmic_bytes(T, w.K, w.D, b, pairs)
     peak, peak_src = measured_peak_hbm()
     res = {"ms_per_step": ms_per_step, "value": tok_s,
