@@ -24,8 +24,8 @@ import torch
 
 from . import _abi
 from ._abi import (EP_BF16, EP_DEVERR_BAD_ID, EP_DEVERR_ROW_OOB, EP_DEVERR_TIMEOUT, EP_F32,
-                   EP_PERMUTE_BULK, EP_PERMUTE_DEFAULT, EP_PERMUTE_VEC, EpBufferInfo, EpConfig,
-                   EpDispatchOut, EpError, EpLayout, check)
+                   EP_LAYOUT_PACKED, EP_LAYOUT_STRIDED, EP_PERMUTE_BULK, EP_PERMUTE_DEFAULT,
+                   EP_PERMUTE_VEC, EpBufferInfo, EpConfig, EpDispatchOut, EpError, EpLayout, check)
 
 __all__ = [
     "Buffer", "Layout", "DispatchResult", "EpConfig", "EpError",
@@ -35,6 +35,7 @@ __all__ = [
     "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_pad_tokens", "ep_derive_max_tokens_pretrain",
     "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
     "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
+    "EP_LAYOUT_STRIDED", "EP_LAYOUT_PACKED",
     "EP_DEVERR_BAD_ID", "EP_DEVERR_ROW_OOB", "EP_DEVERR_TIMEOUT", "library_path",
 ]
 
@@ -229,13 +230,14 @@ class Layout:
     num_tokens: int
     padded_tokens: int
     rank_stride: int
+    packed: bool
 
 
 @dataclass
 class DispatchResult:
-    recv_x: torch.Tensor              # [R, S, D]
-    recv_scores: torch.Tensor         # [R, S] fp32
-    recv_src: torch.Tensor            # [R, S] int32
+    recv_x: torch.Tensor              # [R, S, D] (strided) or [R*S, D] (packed)
+    recv_scores: torch.Tensor         # [R, S] or [R*S] fp32
+    recv_src: torch.Tensor            # [R, S] or [R*S] int32
     layout: Layout
 
 
@@ -245,11 +247,14 @@ class Buffer:
 
     def __init__(self, num_max_tokens_per_rank: int, hidden: int, num_experts: int,
                  num_ranks: int, topk: int, dtype: torch.dtype = torch.bfloat16,
-                 num_sms: int = 0, permute_impl: int = EP_PERMUTE_DEFAULT, device=None):
+                 num_sms: int = 0, permute_impl: int = EP_PERMUTE_DEFAULT, device=None,
+                 layout: str = "strided"):
         if dtype not in _TORCH_TO_EP:
             raise TypeError(f"dtype must be bfloat16 or float32, got {dtype}")
+        mode = {"strided": EP_LAYOUT_STRIDED, "packed": EP_LAYOUT_PACKED}[layout]
         self.cfg = EpConfig(num_max_tokens_per_rank, hidden, num_experts, num_ranks, topk,
-                            _TORCH_TO_EP[dtype], num_sms, permute_impl)
+                            _TORCH_TO_EP[dtype], num_sms, permute_impl, mode)
+        self.packed = mode == EP_LAYOUT_PACKED
         nbytes = ep_buffer_required_bytes(self.cfg)
         if nbytes == 0:
             raise EpError(_abi.EP_ERR_INVALID_ARG, "ep_buffer_required_bytes")
@@ -283,15 +288,17 @@ class Buffer:
             rank_prefix=self._view(L.rank_prefix, i32, (R,)),
             tokens_in_rank=self._view(L.tokens_in_rank, i32, (R,)),
             pos=self._view(L.pos, i32, (T, K)),
-            num_tokens=T, padded_tokens=L.padded_tokens, rank_stride=L.rank_stride)
+            num_tokens=T, padded_tokens=L.padded_tokens, rank_stride=L.rank_stride,
+            packed=bool(L.packed))
 
     def _dispatch_result(self, d: EpDispatchOut) -> DispatchResult:
         S = d.layout.rank_stride
         self._stride = S
+        lead = (self.R * S,) if self.packed else (self.R, S)
         return DispatchResult(
-            recv_x=self._view(d.recv_x, self.dtype, (self.R, S, self.D)),
-            recv_scores=self._view(d.recv_scores, torch.float32, (self.R, S)),
-            recv_src=self._view(d.recv_src, torch.int32, (self.R, S)),
+            recv_x=self._view(d.recv_x, self.dtype, lead + (self.D,)),
+            recv_scores=self._view(d.recv_scores, torch.float32, lead),
+            recv_src=self._view(d.recv_src, torch.int32, lead),
             layout=self._layout(d.layout))
 
     # -- calls -------------------------------------------------------------
@@ -342,7 +349,8 @@ class Buffer:
         T = topk_scores_TK.shape[0]
         if grad_y is None:
             S = self._last_stride()
-            grad_y = torch.empty((self.R, S, self.D), dtype=self.dtype, device=self.device)
+            lead = (self.R * S,) if self.packed else (self.R, S)
+            grad_y = torch.empty(lead + (self.D,), dtype=self.dtype, device=self.device)
         gs = torch.empty((T, self.K), dtype=torch.float32, device=self.device) \
             if want_scores else None
         ep_combine_backward(self.handle, grad_out, y_recv, topk_scores_TK, T, grad_y, gs, stream)

@@ -27,6 +27,9 @@ EP_PERMUTE_DEFAULT = 0
 EP_PERMUTE_VEC = 1
 EP_PERMUTE_BULK = 2
 
+EP_LAYOUT_STRIDED = 0
+EP_LAYOUT_PACKED = 1
+
 EP_DEVERR_BAD_ID = 0x1
 EP_DEVERR_ROW_OOB = 0x2
 EP_DEVERR_TIMEOUT = 0x4
@@ -42,6 +45,7 @@ class EpConfig(C.Structure):
         ("dtype", C.c_int32),
         ("num_sms", C.c_int32),
         ("permute_impl", C.c_int32),
+        ("layout_mode", C.c_int32),
     ]
 
 
@@ -56,6 +60,7 @@ class EpLayout(C.Structure):
         ("num_tokens", C.c_int64),
         ("padded_tokens", C.c_int64),
         ("rank_stride", C.c_int64),
+        ("packed", C.c_int32),
     ]
 
 

@@ -106,18 +106,10 @@ combine_vec_kernel(CombineArgs a)
         if (threadIdx.x < a.K) {
             const int64_t q = t * a.K + threadIdx.x;
             int p = __ldcg(a.pos + q);
-            if (p >= 0) {
-                // Keep the row only if it lies inside its rank's true total.
-                const int64_t r = (int64_t)p / a.S;
-                bool ok = r < a.R;
-                if (ok) {
-                    const int lo = (r > 0) ? __ldcg(a.rank_prefix + r - 1) : 0;
-                    ok = ((int64_t)p - r * a.S) < (int64_t)(__ldcg(a.rank_prefix + r) - lo);
-                }
-                if (!ok) {
-                    atomicOr(a.err, kErrRowOob);
-                    p = -1;
-                }
+            // Keep the row only if it lies inside its rank's true total.
+            if (p >= 0 && !row_valid(p, a.S, a.R, a.rank_prefix, a.packed)) {
+                atomicOr(a.err, kErrRowOob);
+                p = -1;
             }
             s_pos[threadIdx.x] = p;
             s_w[threadIdx.x] = a.unit_weights ? 1.0f : __ldcg(a.scores + q);
@@ -209,17 +201,10 @@ combine_backward_kernel(CombineBwdArgs a)
         if (threadIdx.x < a.K) {
             const int64_t q = t * a.K + threadIdx.x;
             int p = __ldcg(a.pos + q);
-            if (p >= 0) {
-                const int64_t r = (int64_t)p / a.S;
-                bool ok = r < a.R;
-                if (ok) {
-                    const int lo = (r > 0) ? __ldcg(a.rank_prefix + r - 1) : 0;
-                    ok = ((int64_t)p - r * a.S) < (int64_t)(__ldcg(a.rank_prefix + r) - lo);
-                }
-                if (!ok) {
-                    atomicOr(a.err, kErrRowOob);
-                    p = -1;
-                }
+            // Keep the row only if it lies inside its rank's true total.
+            if (p >= 0 && !row_valid(p, a.S, a.R, a.rank_prefix, a.packed)) {
+                atomicOr(a.err, kErrRowOob);
+                p = -1;
             }
             s_pos[threadIdx.x] = p;
             s_w[threadIdx.x] = __ldcg(a.scores + q);

@@ -75,6 +75,7 @@ bool check_config(const ep_config* c, int64_t* row_bytes, int64_t* s_max, int64_
     if (c->topk < 1 || c->topk > c->num_experts || c->topk > ep::kMaxTopk) return false;
     if (c->num_sms < 0) return false;
     if (c->permute_impl < EP_PERMUTE_DEFAULT || c->permute_impl > EP_PERMUTE_BULK) return false;
+    if (c->layout_mode != EP_LAYOUT_STRIDED && c->layout_mode != EP_LAYOUT_PACKED) return false;
     const int64_t rb = c->hidden * elem_bytes(c->dtype);
     if (rb % 16 != 0) return false;
     const int64_t s = pad4(c->num_max_tokens_per_rank) * c->topk;
@@ -159,6 +160,7 @@ void fill_layout(const ep_buffer* b, ep_layout* out)
     out->num_tokens = b->last_T;
     out->padded_tokens = pad4(b->last_N);
     out->rank_stride = b->last_S;
+    out->packed = b->cfg.layout_mode == EP_LAYOUT_PACKED ? 1 : 0;
 }
 
 void fill_dispatch(const ep_buffer* b, ep_dispatch_out* out)
@@ -194,6 +196,7 @@ ep::LayoutArgs layout_args(ep_buffer* b, const int32_t* ids, int64_t T, int64_t 
     a.tokens_in_rank = b->tokens_in_rank;
     a.pos = b->pos;
     a.err = b->err;
+    a.packed = b->cfg.layout_mode == EP_LAYOUT_PACKED;
     return a;
 }
 
@@ -419,6 +422,7 @@ ep_status ep_combine(ep_buffer* buf, const void* y, const float* scores, int64_t
     a.in_dtype = buf->cfg.dtype == EP_BF16 ? 0 : 1;
     a.out_dtype = out_dtype == EP_BF16 ? 0 : 1;
     a.err = buf->err;
+    a.packed = buf->cfg.layout_mode == EP_LAYOUT_PACKED;
     a.unit_weights = false;
     a.gather_in = nullptr;
     a.gather_out = nullptr;
@@ -453,6 +457,7 @@ ep_status ep_combine_backward(ep_buffer* buf, const void* grad_out, const void* 
     a.D = buf->cfg.hidden;
     a.dtype = buf->cfg.dtype == EP_BF16 ? 0 : 1;
     a.err = buf->err;
+    a.packed = buf->cfg.layout_mode == EP_LAYOUT_PACKED;
     if (ep::launch_combine_backward(a, buf->combine_grid, opts(buf, as_stream(stream))) !=
         cudaSuccess)
         return EP_ERR_CUDA;
@@ -484,6 +489,7 @@ ep_status ep_dispatch_backward(ep_buffer* buf, const void* grad_recv_x,
     a.in_dtype = buf->cfg.dtype == EP_BF16 ? 0 : 1;
     a.out_dtype = grad_x_dtype == EP_BF16 ? 0 : 1;
     a.err = buf->err;
+    a.packed = buf->cfg.layout_mode == EP_LAYOUT_PACKED;
     a.unit_weights = true;
     a.gather_in = grad_recv_scores;
     a.gather_out = grad_scores;

@@ -41,6 +41,21 @@ __device__ __forceinline__ int4 ld_cg_v4(const void* p)
     return v;
 }
 
+// Whether receive row p holds data: inside its rank's true total, read from
+// the device prefix sum ("ep: graph-safe worst-token HT dispatch+combine",
+// "Internode" item 3): p - r*S < rank_prefix[r] - rank_prefix[r-1] for
+// r = p / S (strided), or p < rank_prefix[R-1] (packed).
+__device__ __forceinline__ bool row_valid(int p, int64_t S, int R, const int32_t* rank_prefix,
+                                          bool packed)
+{
+    if (p < 0) return false;
+    if (packed) return p < __ldcg(rank_prefix + R - 1);
+    const int64_t r = (int64_t)p / S;
+    if (r >= R) return false;
+    const int lo = (r > 0) ? __ldcg(rank_prefix + r - 1) : 0;
+    return ((int64_t)p - r * S) < (int64_t)(__ldcg(rank_prefix + r) - lo);
+}
+
 // ---- ids ---------------------------------------------------------------------
 
 __device__ __forceinline__ int valid_id(int e, int E) { return (e >= -1 && e < E) ? e : -1; }

@@ -70,6 +70,7 @@ struct LayoutArgs {
     int32_t* tokens_in_rank;   // [R]
     int32_t* pos;              // [T][K]
     uint32_t* err;
+    bool packed;               // ranks back to back instead of r*S
 };
 
 // Launch options shared by every kernel: programmatic dependent launch lets a
@@ -134,6 +135,7 @@ struct CombineArgs {
     int64_t D;
     int in_dtype, out_dtype;   // 0 = bf16, 1 = fp32
     uint32_t* err;
+    bool packed;               // row validity: p < total instead of per-rank ranges
     // Dispatch backward reuses the combine gather: weights of 1 (scores unused),
     // and gather_out[t][k] = gather_in[pos[t][k]] (0 without a valid row).
     bool unit_weights;
@@ -157,6 +159,7 @@ struct CombineBwdArgs {
     int64_t D;
     int dtype;                 // 0 = bf16, 1 = fp32
     uint32_t* err;
+    bool packed;
 };
 cudaError_t launch_combine_backward(const CombineBwdArgs& a, int grid, const LaunchOpts& o);
 

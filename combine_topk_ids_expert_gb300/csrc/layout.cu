@@ -217,9 +217,13 @@ layout_scan_kernel(LayoutArgs a)
     // inclusive prefix of its first expert's predecessor ends.
     const int eloc = a.E / a.R;
     if (tid < a.E) {
-        const int r = tid / eloc;
-        const int base = (r > 0) ? s_incl[r * eloc - 1] : 0;
-        a.expert_offset[tid] = (int32_t)((int64_t)r * a.S + (v - own - base));
+        if (a.packed) {
+            a.expert_offset[tid] = v - own;              // after every lower expert
+        } else {
+            const int r = tid / eloc;
+            const int base = (r > 0) ? s_incl[r * eloc - 1] : 0;
+            a.expert_offset[tid] = (int32_t)((int64_t)r * a.S + (v - own - base));
+        }
     }
     if (tid < a.R) {
         const int hi = s_incl[(tid + 1) * eloc - 1];

@@ -81,6 +81,11 @@ typedef enum {
     EP_PERMUTE_BULK = 2           /* bulk async copies staged through shared memory */
 } ep_permute_impl;
 
+typedef enum {
+    EP_LAYOUT_STRIDED = 0,        /* worst-token mode: rank r's rows start at r*S */
+    EP_LAYOUT_PACKED = 1          /* exact mode: ranks back to back, rows [0, true total) */
+} ep_layout_mode;
+
 /* Device error word bits (sticky until ep_get_device_error clears them). */
 #define EP_DEVERR_BAD_ID 0x1u     /* an id outside [-1, E) was seen; treated as -1 */
 #define EP_DEVERR_ROW_OOB 0x2u    /* combine met a row outside its rank's true total; skipped */
@@ -98,6 +103,16 @@ typedef struct {
     int32_t dtype;                   /* ep_dtype of x_TD and the receive buffer */
     int32_t num_sms;                 /* SMs the copy kernels may use; 0 = all ([flex]) */
     int32_t permute_impl;            /* ep_permute_impl */
+    int32_t layout_mode;             /* ep_layout_mode: where each rank's rows start.
+                                        STRIDED ([titan] "Backend behavior": the current
+                                        capacity is the per-rank stride; [graph] worst-token
+                                        mode): rank r owns rows [r*S, r*S + rows_per_rank[r]).
+                                        PACKED ([graph] num_worst_tokens == 0, receive sized
+                                        by the true counts): rank r owns rows
+                                        [rank_prefix[r-1], rank_prefix[r]), expert e starts
+                                        after all lower experts, the valid rows are exactly
+                                        [0, rank_prefix[R-1]); read the counts with exact
+                                        mode (host_tokens_per_expert) to size consumers. */
 } ep_config;
 
 /* Opaque handle; the library owns this host-side object, the caller owns the workspace. */
@@ -117,7 +132,9 @@ typedef struct {
                                    follow ascending t*K+k */
     int64_t num_tokens;         /* T */
     int64_t padded_tokens;      /* P = roundup4(N) ([align] "Problem" item 2, "Fix") */
-    int64_t rank_stride;        /* S = P*K rows per rank ([titan] "Backend behavior") */
+    int64_t rank_stride;        /* S = P*K rows reserved per rank ([titan] "Backend behavior");
+                                   the strided layout's per-rank stride */
+    int32_t packed;             /* 1 if rows are placed by EP_LAYOUT_PACKED */
 } ep_layout;
 
 /* Result of a dispatch: views into the workspace. recv_x is [R*S][D] of the

@@ -57,18 +57,18 @@ class Oracle:
         L.oracle_f32_from_bf16.argtypes, L.oracle_f32_from_bf16.restype = [C.c_uint16], C.c_float
         u32p = C.POINTER(C.c_uint32)
         L.oracle_routing_map.argtypes = [_i32p, _f32p, i64, i64, i32, i32, _u8p, _f32p, u32p]
-        L.oracle_layout.argtypes = [_i32p, i64, i64, i32, i32, i32, _i32p, _i32p, _i32p, _i32p,
-                                    _i32p, _i32p, C.POINTER(C.c_int64), u32p]
-        L.oracle_dispatch.argtypes = [C.c_void_p, i64, _f32p, _i32p, i64, i64, i32, i32, i32,
+        L.oracle_layout.argtypes = [_i32p, i64, i64, i32, i32, i32, i32, _i32p, _i32p, _i32p,
+                                    _i32p, _i32p, _i32p, C.POINTER(C.c_int64), u32p]
+        L.oracle_dispatch.argtypes = [C.c_void_p, i64, _f32p, _i32p, i64, i64, i32, i32, i32, i32,
                                       C.c_void_p, _f32p, _i32p, _i32p, _i32p, _i32p, _i32p,
                                       _i32p, _i32p, C.POINTER(C.c_int64), u32p]
         L.oracle_combine.argtypes = [C.c_void_p, C.c_int, i64, _f32p, _i32p, _i32p, i64, i64,
-                                     i32, i32, C.c_void_p, C.c_int, u32p]
+                                     i32, i32, i32, C.c_void_p, C.c_int, u32p]
         vp = C.c_void_p
         L.oracle_combine_backward.argtypes = [vp, C.c_int, vp, C.c_int, i64, _f32p, _i32p, _i32p,
-                                              i64, i64, i32, i32, vp, vp, u32p]
+                                              i64, i64, i32, i32, i32, vp, vp, u32p]
         L.oracle_dispatch_backward.argtypes = [vp, C.c_int, i64, vp, _i32p, _i32p, i64, i64, i32,
-                                               i32, vp, C.c_int, vp, u32p]
+                                               i32, i32, vp, C.c_int, vp, u32p]
         for name in ("oracle_routing_map", "oracle_layout", "oracle_dispatch", "oracle_combine",
                      "oracle_combine_backward", "oracle_dispatch_backward"):
             getattr(L, name).restype = C.c_int
@@ -112,7 +112,7 @@ class Oracle:
             raise OracleError(f"oracle_routing_map rc={rc}")
         return m.astype(bool), pr, int(err.value)
 
-    def layout(self, ids, N: int, E: int, R: int) -> dict:
+    def layout(self, ids, N: int, E: int, R: int, packed: bool = False) -> dict:
         ids = np.ascontiguousarray(ids, dtype=np.int32)
         T, K = ids.shape
         out = {
@@ -123,7 +123,7 @@ class Oracle:
         S = C.c_int64(0)
         err = C.c_uint32(0)
         rc = self.lib.oracle_layout(ids.ravel() if T else np.zeros(1, np.int32), T, N, K, E, R,
-                                    out["cnt"], out["expert_offset"], out["rows_per_rank"],
+                                    int(packed), out["cnt"], out["expert_offset"], out["rows_per_rank"],
                                     out["rank_prefix"], out["tokens_in_rank"],
                                     out["pos"].ravel() if T else np.zeros(1, np.int32),
                                     C.byref(S), C.byref(err))
@@ -133,7 +133,8 @@ class Oracle:
         out["err"] = int(err.value)
         return out
 
-    def dispatch(self, x, scores, ids, N: int, E: int, R: int, fill: int = 0) -> dict:
+    def dispatch(self, x, scores, ids, N: int, E: int, R: int, fill: int = 0,
+                 packed: bool = False) -> dict:
         """Layout plus permute. Receive buffers hold R*S rows; rows that no pair
         lands on keep the byte ``fill``."""
         ids = np.ascontiguousarray(ids, dtype=np.int32)
@@ -159,7 +160,7 @@ class Oracle:
         one_i = np.zeros(1, np.int32)
         rc = self.lib.oracle_dispatch(
             x.ctypes.data if T else None, row_bytes, scores.ravel() if T else np.zeros(1, np.float32),
-            ids.ravel() if T else one_i, T, N, K, E, R,
+            ids.ravel() if T else one_i, T, N, K, E, R, int(packed),
             recv_x.ctypes.data if rows else None,
             recv_scores if rows else np.zeros(1, np.float32), recv_src if rows else one_i,
             lay["cnt"], lay["expert_offset"], lay["rows_per_rank"], lay["rank_prefix"],
@@ -167,10 +168,11 @@ class Oracle:
         if rc:
             raise OracleError(f"oracle_dispatch rc={rc}")
         lay.update(S=int(Sv.value), err=int(err.value), recv_x=recv_x, recv_scores=recv_scores,
-                   recv_src=recv_src)
+                   recv_src=recv_src, packed=bool(packed))
         return lay
 
-    def combine(self, y, scores, pos, rank_prefix, S: int, R: int, out_dtype: str = "same"):
+    def combine(self, y, scores, pos, rank_prefix, S: int, R: int, out_dtype: str = "same",
+                packed: bool = False):
         """out[T, D]; out_dtype "same" (y's kind), "bf16" or "f32". Returns (out, err)."""
         y = np.ascontiguousarray(y)
         yk = _kind(y)
@@ -185,7 +187,8 @@ class Oracle:
         rc = self.lib.oracle_combine(y.ctypes.data if y.size else None, yk, D,
                                      scores.ravel() if T else np.zeros(1, np.float32),
                                      pos.ravel() if T else np.zeros(1, np.int32), rank_prefix,
-                                     S, T, K, R, out.ctypes.data if T else None, ok, C.byref(err))
+                                     S, T, K, R, int(packed), out.ctypes.data if T else None, ok,
+                                     C.byref(err))
         if rc:
             raise OracleError(f"oracle_combine rc={rc}")
         return out, int(err.value)
@@ -193,7 +196,7 @@ class Oracle:
 
     # -- backward ------------------------------------------------------------
     def combine_backward(self, grad_out, y, scores, pos, rank_prefix, S: int, R: int,
-                         grad_y_fill: int = 0):
+                         grad_y_fill: int = 0, packed: bool = False):
         """(grad_y [R*S, D] of y's kind, grad_scores [T, K] fp32, err). Rows of
         grad_y that no valid pair references keep the byte grad_y_fill."""
         grad_out = np.ascontiguousarray(grad_out)
@@ -210,7 +213,7 @@ class Oracle:
         rc = self.lib.oracle_combine_backward(
             grad_out.ctypes.data if T else None, _kind(grad_out), y.ctypes.data if y.size else None,
             _kind(y), D, scores.ravel() if T else np.zeros(1, np.float32),
-            pos.ravel() if T else np.zeros(1, np.int32), rank_prefix, S, T, K, R,
+            pos.ravel() if T else np.zeros(1, np.int32), rank_prefix, S, T, K, R, int(packed),
             grad_y.ctypes.data if grad_y.size else None, gs.ctypes.data if T else None,
             C.byref(err))
         if rc:
@@ -218,7 +221,7 @@ class Oracle:
         return grad_y, gs, int(err.value)
 
     def dispatch_backward(self, grad_recv, grad_recv_scores, pos, rank_prefix, S: int, R: int,
-                          out_dtype: str = "same"):
+                          out_dtype: str = "same", packed: bool = False):
         """(grad_x [T, D], grad_scores [T, K] fp32 or None, err)."""
         grad_recv = np.ascontiguousarray(grad_recv)
         gk = _kind(grad_recv)
@@ -235,7 +238,7 @@ class Oracle:
         rc = self.lib.oracle_dispatch_backward(
             grad_recv.ctypes.data if grad_recv.size else None, gk, D,
             None if grs is None else grs.ctypes.data, pos.ravel() if T else np.zeros(1, np.int32),
-            rank_prefix, S, T, K, R, gx.ctypes.data if T else None, ok,
+            rank_prefix, S, T, K, R, int(packed), gx.ctypes.data if T else None, ok,
             None if gs is None or not T else gs.ctypes.data, C.byref(err))
         if rc:
             raise OracleError(f"oracle_dispatch_backward rc={rc}")

@@ -217,13 +217,18 @@ int oracle_routing_map(const int32_t* ids, const float* scores, int64_t T, int64
  *                       pages do not fix one, and combine does not depend on
  *                       it).
  *   *S_out              rows per rank for this call, P * K.
+ * packed = 0 (worst-token mode, [graph] "Internode" items 2-3): rank r's rows
+ * start at r * S. packed = 1 (exact mode, [graph] num_worst_tokens == 0, where
+ * the receive side is sized by the true counts): ranks follow each other with
+ * no gap, so expert e starts at the counts of all lower experts and the valid
+ * rows are exactly [0, rank_prefix[R-1]).
  * The steps follow the plain definition: pad (rows T..P-1 get -1), count,
  * scan, then hand out rows with a running cursor per expert in flat order.
  */
 int oracle_layout(const int32_t* ids, int64_t T, int64_t N, int32_t K, int32_t E, int32_t R,
-                  int32_t* cnt_E, int32_t* expert_offset_E, int32_t* rows_per_rank_R,
-                  int32_t* rank_prefix_R, int32_t* tokens_in_rank_R, int32_t* pos_TK,
-                  int64_t* S_out, uint32_t* err)
+                  int32_t packed, int32_t* cnt_E, int32_t* expert_offset_E,
+                  int32_t* rows_per_rank_R, int32_t* rank_prefix_R, int32_t* tokens_in_rank_R,
+                  int32_t* pos_TK, int64_t* S_out, uint32_t* err)
 {
     if (check_shape(T, N, K, E, R) != ORC_OK) return ORC_EINVAL;
     int64_t P = oracle_pad_tokens(N);
@@ -265,12 +270,19 @@ int oracle_layout(const int32_t* ids, int64_t T, int64_t N, int32_t K, int32_t E
         rank_prefix_R[r] = run;
     }
 
-    /* Step 3: first row of each expert inside its rank's block of S rows. */
+    /* Step 3: first row of each expert: inside its rank's block of S rows
+     * (strided), or after every lower expert (packed). */
     for (int32_t e = 0; e < E; ++e) {
         int32_t r = rank_of(e, E, R);
-        int64_t off = (int64_t)r * S;
+#if ORACLE_MUTANT == 14
+        int64_t off = (int64_t)r * S;                   /* mutant: packed mode ignored */
         for (int32_t f = 0; f < e; ++f)
             if (rank_of(f, E, R) == r) off += cnt_E[f];
+#else
+        int64_t off = packed ? 0 : (int64_t)r * S;
+        for (int32_t f = 0; f < e; ++f)
+            if (packed || rank_of(f, E, R) == r) off += cnt_E[f];
+#endif
 #if ORACLE_MUTANT == 3
         off += cnt_E[e];                            /* mutant: inclusive offset */
 #endif
@@ -320,13 +332,14 @@ int oracle_layout(const int32_t* ids, int64_t T, int64_t N, int32_t K, int32_t E
  * The layout outputs are written as oracle_layout writes them.
  */
 int oracle_dispatch(const void* x, int64_t row_bytes, const float* scores, const int32_t* ids,
-                    int64_t T, int64_t N, int32_t K, int32_t E, int32_t R, void* recv_x,
+                    int64_t T, int64_t N, int32_t K, int32_t E, int32_t R, int32_t packed,
+                    void* recv_x,
                     float* recv_scores, int32_t* recv_src, int32_t* cnt_E,
                     int32_t* expert_offset_E, int32_t* rows_per_rank_R, int32_t* rank_prefix_R,
                     int32_t* tokens_in_rank_R, int32_t* pos_TK, int64_t* S_out, uint32_t* err)
 {
     if (row_bytes <= 0) return ORC_EINVAL;
-    int rc = oracle_layout(ids, T, N, K, E, R, cnt_E, expert_offset_E, rows_per_rank_R,
+    int rc = oracle_layout(ids, T, N, K, E, R, packed, cnt_E, expert_offset_E, rows_per_rank_R,
                            rank_prefix_R, tokens_in_rank_R, pos_TK, S_out, err);
     if (rc != ORC_OK) return rc;
     const uint8_t* xb = (const uint8_t*)x;
@@ -387,6 +400,19 @@ static float load_elem(const void* base, int kind, int64_t i)
 /* Combine: weighted un-permute back to token order.                          */
 /* ------------------------------------------------------------------------ */
 
+/* Whether receive row p holds data: inside its rank's true total ([graph]
+ * "Internode" item 3), i.e. p - r*S < rank_prefix[r] - rank_prefix[r-1] for
+ * r = p / S (strided), or p < rank_prefix[R-1] (packed). */
+static int row_ok(int64_t p, const int32_t* rank_prefix_R, int64_t S, int32_t R, int32_t packed)
+{
+    if (p < 0) return 0;
+    if (packed) return p < (int64_t)rank_prefix_R[R - 1];
+    int64_t r = (S > 0) ? p / S : R;
+    if (r >= R) return 0;
+    int64_t lo = (r > 0) ? rank_prefix_R[r - 1] : 0;
+    return p - r * S < (int64_t)rank_prefix_R[r] - lo;
+}
+
 /* Combine for one call. [align] "Fix" (combine() slices the padded rows
  * back off) and [graph] "Internode" item 3 (the true received total comes
  * from the device prefix sum, not the padded row count).
@@ -405,7 +431,7 @@ static float load_elem(const void* base, int kind, int64_t i)
  */
 int oracle_combine(const void* y, int y_kind, int64_t D, const float* scores,
                    const int32_t* pos_TK, const int32_t* rank_prefix_R, int64_t S, int64_t T,
-                   int32_t K, int32_t R, void* out, int out_kind, uint32_t* err)
+                   int32_t K, int32_t R, int32_t packed, void* out, int out_kind, uint32_t* err)
 {
     if (T < 0 || D <= 0 || K <= 0 || R <= 0 || S < 0) return ORC_EINVAL;
     if ((y_kind != ORC_BF16 && y_kind != ORC_F32) || (out_kind != ORC_BF16 && out_kind != ORC_F32))
@@ -420,10 +446,7 @@ int oracle_combine(const void* y, int y_kind, int64_t D, const float* scores,
 #endif
                 int64_t p = pos_TK[t * K + k];
                 if (p < 0) continue;
-                int64_t r = (S > 0) ? p / S : R;
-                int64_t lo = (r > 0 && r < R) ? rank_prefix_R[r - 1] : 0;
-                int64_t rows = (r < R) ? (int64_t)rank_prefix_R[r] - lo : 0;
-                if (r >= R || p - r * S >= rows) {
+                if (!row_ok(p, rank_prefix_R, S, R, packed)) {
                     *err |= ORC_ERR_ROW_OOB;
                     continue;
                 }
@@ -446,15 +469,6 @@ int oracle_combine(const void* y, int y_kind, int64_t D, const float* scores,
 /* ------------------------------------------------------------------------ */
 /* Backward of combine and dispatch.                                          */
 /* ------------------------------------------------------------------------ */
-
-static int row_ok(int64_t p, const int32_t* rank_prefix_R, int64_t S, int32_t R)
-{
-    if (p < 0) return 0;
-    int64_t r = (S > 0) ? p / S : R;
-    if (r >= R) return 0;
-    int64_t lo = (r > 0) ? rank_prefix_R[r - 1] : 0;
-    return p - r * S < (int64_t)rank_prefix_R[r] - lo;
-}
 
 static void store_elem(void* base, int kind, int64_t i, float v)
 {
@@ -479,7 +493,8 @@ static void store_elem(void* base, int kind, int64_t i, float v)
 int oracle_combine_backward(const void* grad_out, int g_kind, const void* y, int y_kind,
                             int64_t D, const float* scores, const int32_t* pos_TK,
                             const int32_t* rank_prefix_R, int64_t S, int64_t T, int32_t K,
-                            int32_t R, void* grad_y, float* grad_scores, uint32_t* err)
+                            int32_t R, int32_t packed, void* grad_y, float* grad_scores,
+                            uint32_t* err)
 {
     if (T < 0 || D <= 0 || K <= 0 || R <= 0 || S < 0) return ORC_EINVAL;
     if ((g_kind != ORC_BF16 && g_kind != ORC_F32) || (y_kind != ORC_BF16 && y_kind != ORC_F32))
@@ -488,7 +503,7 @@ int oracle_combine_backward(const void* grad_out, int g_kind, const void* y, int
         for (int32_t k = 0; k < K; ++k) {
             int64_t p = pos_TK[t * K + k];
             double dot = 0.0;
-            if (p >= 0 && !row_ok(p, rank_prefix_R, S, R)) {
+            if (p >= 0 && !row_ok(p, rank_prefix_R, S, R, packed)) {
                 *err |= ORC_ERR_ROW_OOB;
                 p = -1;
             }
@@ -519,8 +534,8 @@ int oracle_combine_backward(const void* grad_out, int g_kind, const void* y, int
 int oracle_dispatch_backward(const void* grad_recv, int g_kind, int64_t D,
                              const float* grad_recv_scores, const int32_t* pos_TK,
                              const int32_t* rank_prefix_R, int64_t S, int64_t T, int32_t K,
-                             int32_t R, void* grad_x, int x_kind, float* grad_scores,
-                             uint32_t* err)
+                             int32_t R, int32_t packed, void* grad_x, int x_kind,
+                             float* grad_scores, uint32_t* err)
 {
     if (T < 0 || D <= 0 || K <= 0 || R <= 0 || S < 0) return ORC_EINVAL;
     if ((g_kind != ORC_BF16 && g_kind != ORC_F32) || (x_kind != ORC_BF16 && x_kind != ORC_F32))
@@ -534,14 +549,14 @@ int oracle_dispatch_backward(const void* grad_recv, int g_kind, int64_t D,
             for (int32_t k = 0; k < K; ++k) {
 #endif
                 int64_t p = pos_TK[t * K + k];
-                if (!row_ok(p, rank_prefix_R, S, R)) continue;
+                if (!row_ok(p, rank_prefix_R, S, R, packed)) continue;
                 acc = fmaf(1.0f, load_elem(grad_recv, g_kind, p * D + d), acc);
             }
             store_elem(grad_x, x_kind, t * D + d, acc);
         }
         for (int32_t k = 0; k < K; ++k) {
             int64_t p = pos_TK[t * K + k];
-            int ok = row_ok(p, rank_prefix_R, S, R);
+            int ok = row_ok(p, rank_prefix_R, S, R, packed);
             if (p >= 0 && !ok) *err |= ORC_ERR_ROW_OOB;
             if (grad_scores)
                 grad_scores[t * K + k] = (ok && grad_recv_scores) ? grad_recv_scores[p] : 0.0f;

@@ -456,4 +456,55 @@ def pin_backward_unequal_count_invariance(o):
         assert np.array_equal(res[0][1], res[1][1])
 
 
+# ---------------------------------------------------------------------------
+# Packed (exact-mode) layout
+# ---------------------------------------------------------------------------
+
+def pin_packed_positions_global_sort(o):
+    # Packed rows: the j-th pair of numpy's stable argsort by expert sits at row j;
+    # the rows fill exactly [0, true total).
+    for (seed, T, N, E, K, R) in [(50, 37, 41, 16, 3, 4), (51, 13, 16, 256, 8, 8),
+                                  (52, 120, 123, 32, 4, 1)]:
+        ids = _ids(seed, T, E, K)
+        lay = o.layout(ids, N, E, R, packed=True)
+        order = np.argsort(ids.ravel(), kind="stable")
+        want = np.empty(T * K, np.int64)
+        want[order] = np.arange(T * K)
+        assert np.array_equal(lay["pos"].ravel().astype(np.int64), want)
+        assert int(lay["rank_prefix"][-1]) == T * K
+
+
+def pin_packed_relation_to_strided(o):
+    # The packed row of a pair is its strided row moved from r*S to the start
+    # of rank r's rows in the packed buffer (the exclusive rank prefix).
+    ids = _ids(53, 29, 16, 4)
+    st = o.layout(ids, 31, 16, 4)
+    pk = o.layout(ids, 31, 16, 4, packed=True)
+    r = st["pos"] // st["S"]
+    start = np.concatenate([[0], st["rank_prefix"][:-1]])[r]
+    assert np.array_equal(pk["pos"], st["pos"] - r * st["S"] + start)
+
+
+def pin_packed_combine_and_backward_match_strided(o):
+    T, N, E, K, R, D = 23, 24, 16, 4, 4, 16
+    ids = _ids(54, T, E, K)
+    sc = W.topk_scores(54, ids, E, "sigmoid_norm")
+    x = W.hidden(54, T, D, "bf16")
+    g = W.hidden(55, T, D, "bf16")
+    res = []
+    for packed in (False, True):
+        d = o.dispatch(x, sc, ids, N, E, R, packed=packed)
+        out, err = o.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R,
+                             packed=packed)
+        gy, gs, _ = o.combine_backward(g, d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"],
+                                       R, packed=packed)
+        gx, _, _ = o.dispatch_backward(gy, None, d["pos"], d["rank_prefix"], d["S"], R,
+                                       packed=packed)
+        assert err == 0
+        res.append((out, gs, gx))
+    for a, b in zip(*res):
+        assert np.array_equal(a.view(np.uint16) if a.dtype == np.uint16 else a.view(np.uint32),
+                              b.view(np.uint16) if b.dtype == np.uint16 else b.view(np.uint32))
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

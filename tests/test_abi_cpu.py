@@ -106,7 +106,7 @@ def test_required_bytes():
     dict(num_ranks=128, num_experts=256),  # R above 64
     dict(hidden=7), dict(hidden=0),        # row bytes not a multiple of 16
     dict(num_max_tokens_per_rank=0),
-    dict(dtype=5), dict(permute_impl=9), dict(num_sms=-1),
+    dict(dtype=5), dict(permute_impl=9), dict(num_sms=-1), dict(layout_mode=2),
     dict(num_max_tokens_per_rank=1 << 28),  # rows overflow int32
 ])
 def test_required_bytes_rejects(bad):

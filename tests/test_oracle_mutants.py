@@ -26,6 +26,7 @@ MUTANTS = {
     11: "padded rows route to experts",
     12: "combine backward scales every row by the first score",
     13: "dispatch backward drops the first term",
+    14: "packed layout placed like the strided one",
 }
 
 

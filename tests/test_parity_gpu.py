@@ -13,8 +13,8 @@ import torch
 
 import combine_topk_ids_expert_gb300 as ep
 import workloads as W
-from gpu_util import (assert_combine_equal, assert_layout_equal, assert_recv_equal, to_dev,
-                      to_np, torch_dtype)
+from gpu_util import (assert_combine_equal, assert_layout_equal, assert_recv_equal, bits,
+                      to_dev, to_np, torch_dtype)
 
 pytestmark = pytest.mark.gpu
 
@@ -160,3 +160,41 @@ def test_unequal_count_runs_match(orc):
                 outs.append(to_np(buf.combine(d.recv_x, scd)))
                 assert d.layout.padded_tokens == ((N + 3) // 4) * 4
             assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
+@pytest.mark.parametrize("case", ["tiny_T13_N16", "ds_small_tiles", "k3_e48_r4_f32",
+                                  "k40_e64_r8", "e1024_r64"])
+def test_parity_packed_layout(orc, case, impl):
+    # Exact-mode layout: ranks back to back, valid rows exactly [0, true total);
+    # forward and backward against the oracle's packed definition.
+    seed, T, N, N_max, D, dtype, E, K, R, ik, sk = CASES[case]
+    x, ids, sc = case_inputs(seed, T, D, dtype, E, K, ik, sk)
+    g = W.hidden(seed + 5, T, D, dtype)
+    buf = ep.Buffer(N_max, D, E, R, K, dtype=torch_dtype(dtype), permute_impl=impl,
+                    layout="packed")
+    xd, idd, scd, gd = to_dev(x), to_dev(ids), to_dev(sc), to_dev(g)
+    d = buf.dispatch(xd, scd, idd, N)
+    out = buf.combine(d.recv_x, scd)
+    grad_y, _ = buf.combine_backward(gd, d.recv_x, scd, want_scores=False)
+    grad_x, _ = buf.dispatch_backward(grad_y, T)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, N, E, R, packed=True)
+    assert d.layout.packed
+    assert_layout_equal(d.layout, ref)
+    total = int(ref["rank_prefix"][-1])
+    assert np.array_equal(bits(to_np(d.recv_x)[:total]), bits(ref["recv_x"][:total]))
+    assert np.array_equal(to_np(d.recv_src)[:total], ref["recv_src"][:total])
+    assert np.array_equal(to_np(d.recv_scores)[:total].view(np.uint32),
+                          ref["recv_scores"][:total].view(np.uint32))
+    want, _ = orc.combine(ref["recv_x"], sc, ref["pos"], ref["rank_prefix"], ref["S"], R,
+                          packed=True)
+    assert_combine_equal(to_np(out), want)
+    gy_ref, _, _ = orc.combine_backward(g, ref["recv_x"], sc, ref["pos"], ref["rank_prefix"],
+                                        ref["S"], R, packed=True)
+    assert np.array_equal(bits(to_np(grad_y)[:total]), bits(gy_ref[:total]))
+    gx_ref, _, _ = orc.dispatch_backward(gy_ref, None, ref["pos"], ref["rank_prefix"], ref["S"],
+                                         R, packed=True)
+    assert np.array_equal(bits(to_np(grad_x)), bits(gx_ref))
+    buf.close()
