@@ -272,6 +272,16 @@ def barrier(world: int):
 # the GPU arm
 # ---------------------------------------------------------------------------
 
+def step_calls(args, w: W.Workload) -> tuple[list[dict], int]:
+    """The dispatch+combine calls of one step and their shared N: one call, or
+    one per source rank of the ragged workload (padded to the group max)."""
+    if args.tokens > 0 or w.T is not None:
+        T, N = workload_tokens(args, w)
+        return [W.make(args.workload, rank=0, T=T)], N
+    counts = W.ragged_counts(w)
+    return [W.make(args.workload, rank=r) for r in range(w.ragged_ranks)], max(counts)
+
+
 def run_gb300(args) -> dict | None:
     import torch
 
@@ -289,45 +299,56 @@ def run_gb300(args) -> dict | None:
     barrier(world)
 
     w = W.WORKLOADS[args.workload]
-    T, N = workload_tokens(args, w)
-    inp = W.make(args.workload, rank=0, T=T)
+    inps, N = step_calls(args, w)
+    Ts = [c["T"] for c in inps]
+    T_step = sum(Ts)
+    n_calls = len(inps)
     b = w.elem_bytes
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    raw = torch.int16 if tdt == torch.bfloat16 else tdt
 
     def host(a: np.ndarray):
         t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
         return t.pin_memory()
 
-    x_h, ids_h, sc_h = host(inp["x"]), host(inp["ids"]), host(inp["scores"])
-    x = x_h.to(dev).view(tdt) if w.dtype == "bf16" else x_h.to(dev)
-    ids = ids_h.to(dev)
-    sc = sc_h.to(dev)
+    xh = [host(c["x"]) for c in inps]
+    idh = [host(c["ids"]) for c in inps]
+    sch = [host(c["scores"]) for c in inps]
+    xs = [t.to(dev).view(tdt) if tdt == torch.bfloat16 else t.to(dev) for t in xh]
+    idss = [t.to(dev) for t in idh]
+    scs = [t.to(dev) for t in sch]
+    outs = [torch.empty((T, w.D), dtype=tdt, device=dev) for T in Ts]
     impl = {"default": ep.EP_PERMUTE_DEFAULT, "vec": ep.EP_PERMUTE_VEC,
             "bulk": ep.EP_PERMUTE_BULK}[args.permute]
     n_max = args.tokens if args.tokens > 0 else w.N_max   # smaller workspace when profiling
     buf = ep.Buffer(n_max, w.D, w.E, w.R, w.K, dtype=tdt, num_sms=args.num_sms,
                     permute_impl=impl, device=dev)
     h = buf.handle
-    out = torch.empty((T, w.D), dtype=tdt, device=dev)
     out_code = ep.EP_BF16 if tdt == torch.bfloat16 else ep.EP_F32
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
+    # One untimed pass: routed pairs per call, launches per step, reference outputs.
     n_launch0 = buf.info()["kernel_launches"]
-    d0 = buf.dispatch(x, sc, ids, N)
-    recv_x = d0.recv_x
-    buf.combine(recv_x, sc, out=out)
+    pairs = []
+    recv_x = None
+    for i in range(n_calls):
+        d = buf.dispatch(xs[i], scs[i], idss[i], N)
+        recv_x = d.recv_x
+        buf.combine(recv_x, scs[i], out=outs[i])
+        pairs.append(int(d.layout.tokens_per_expert.sum().item()))
     per_step_launches = buf.info()["kernel_launches"] - n_launch0
     torch.cuda.synchronize(dev)
-    pairs = int(d0.layout.tokens_per_expert.sum().item())
     assert buf.device_error() == 0
+    ref_outs = [o.clone() for o in outs]
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
     def step_kernels(stream_ptr):
-        ep.ep_dispatch(h, x, sc, ids, T, N, stream_ptr)
-        ep.ep_combine(h, recv_x, sc, T, out, out_code, stream_ptr)
+        for i in range(n_calls):
+            ep.ep_dispatch(h, xs[i], scs[i], idss[i], Ts[i], N, stream_ptr)
+            ep.ep_combine(h, recv_x, scs[i], Ts[i], outs[i], out_code, stream_ptr)
 
     graph = None
     if args.graph:
@@ -342,7 +363,6 @@ def run_gb300(args) -> dict | None:
         stream.wait_stream(s)
         torch.cuda.synchronize(dev)
 
-    # warm-up
     for _ in range(args.warmup):
         flush.zero_()
         if graph is not None:
@@ -352,7 +372,9 @@ def run_gb300(args) -> dict | None:
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # events per step: start, then after each call's dispatch and combine
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(1 + 2 * n_calls)]
+          for _ in range(K)]
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
@@ -360,17 +382,19 @@ def run_gb300(args) -> dict | None:
     barrier(world)
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for i in range(K):
+    for it in range(K):
         flush.zero_()                       # L2 flush, outside the events
-        e = ev[i]
+        e = ev[it]
         e[0].record(stream)
         if graph is not None:
             graph.replay()
+            e[-1].record(stream)
         else:
-            ep.ep_dispatch(h, x, sc, ids, T, N, sptr)
-            e[1].record(stream)
-            ep.ep_combine(h, recv_x, sc, T, out, out_code, sptr)
-        e[2].record(stream)
+            for i in range(n_calls):
+                ep.ep_dispatch(h, xs[i], scs[i], idss[i], Ts[i], N, sptr)
+                e[1 + 2 * i].record(stream)
+                ep.ep_combine(h, recv_x, scs[i], Ts[i], outs[i], out_code, sptr)
+                e[2 + 2 * i].record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - wall0
@@ -379,27 +403,39 @@ def run_gb300(args) -> dict | None:
     if graph is not None:
         launches = K * per_step_launches
     assert buf.device_error() == 0
+    for o, r in zip(outs, ref_outs):
+        assert torch.equal(o.view(raw), r.view(raw)), "timed steps changed the output"
 
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
     total_ms = sum(step_ms)
     total_ms_max = max_over_ranks(total_ms, world)
     ms_per_step = total_ms_max / K
-    tok_s = replica_throughput(T, K, total_ms, world)
-    nbytes = algorithmic_bytes(T, w.K, w.D, b, pairs)
+    tok_s = replica_throughput(T_step, K, total_ms, world)
+    nb = [algorithmic_bytes(T, w.K, w.D, b, p) for T, p in zip(Ts, pairs)]
+    nbytes = {k: sum(x[k] for x in nb) for k in nb[0]}
     peak, peak_src = measured_peak_hbm()
     res = {"ms_per_step": ms_per_step, "value": tok_s,
            "step_ms_median": statistics.median(step_ms),
            "hbm_gbs_step": nbytes["step"] / (ms_per_step / 1e3) / 1e9,
-           "wall_s": wall, "launches": launches, "clocks": clk}
+           "wall_s": wall, "launches": launches, "clocks": clk, "T_step": T_step,
+           "calls_per_step": n_calls}
     if graph is None:
-        dis = [e[0].elapsed_time(e[1]) for e in ev]
-        com = [e[1].elapsed_time(e[2]) for e in ev]
+        dis, com = [], []
+        for e in ev:
+            prev = e[0]
+            d_ms = c_ms = 0.0
+            for i in range(n_calls):
+                d_ms += prev.elapsed_time(e[1 + 2 * i])
+                c_ms += e[1 + 2 * i].elapsed_time(e[2 + 2 * i])
+                prev = e[2 + 2 * i]
+            dis.append(d_ms)
+            com.append(c_ms)
         kern = {}
-        for name, arr, nb in (("dispatch", dis, nbytes["layout"] + nbytes["permute"]),
-                              ("combine", com, nbytes["combine"])):
+        for name, arr, nbk in (("dispatch", dis, nbytes["layout"] + nbytes["permute"]),
+                               ("combine", com, nbytes["combine"])):
             avg = sum(arr) / len(arr)
             kern[name] = {"avg_us": avg * 1e3, "median_us": statistics.median(arr) * 1e3,
-                          "algorithmic_bytes": nb, "achieved_gbs": nb / (avg / 1e3) / 1e9}
+                          "algorithmic_bytes": nbk, "achieved_gbs": nbk / (avg / 1e3) / 1e9}
         dom = "dispatch" if kern["dispatch"]["avg_us"] >= kern["combine"]["avg_us"] else "combine"
         ach = kern[dom]["achieved_gbs"]
         impl_name = {1: "vec", 2: "bulk"}[buf.info()["permute_impl"]]
@@ -411,73 +447,76 @@ def run_gb300(args) -> dict | None:
                            "traffic": profiled_traffic(kname, args.workload),
                            "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
     res["bytes"] = nbytes
-    res["pairs"] = pairs
+    res["pairs"] = sum(pairs)
     res["info"] = buf.info()
 
-    # End to end through the public API with host buffers: every step copies its
+    # End to end through the public API with host buffers: every call copies its
     # inputs from pinned host memory and its output back, inside the timed region.
-    # Steps are pipelined on three streams (H2D of step i+1, compute of step i,
-    # D2H of step i-1) over double-buffered device inputs and outputs.
+    # Calls are pipelined on three streams (H2D of call j+1, compute of call j,
+    # D2H of call j-1) over double-buffered device inputs and outputs.
     if not args.no_e2e:
-        raw = torch.int16 if tdt == torch.bfloat16 else tdt
-        ref_out = out.clone()
-        xs = [torch.empty_like(x) for _ in range(2)]
-        idss = [torch.empty_like(ids) for _ in range(2)]
-        scs = [torch.empty_like(sc) for _ in range(2)]
-        outs = [torch.empty_like(out) for _ in range(2)]
-        outs_h = [torch.empty((T, w.D), dtype=raw).pin_memory() for _ in range(2)]
+        Tm = max(Ts)
+        dx = [torch.empty((Tm, w.D), dtype=tdt, device=dev) for _ in range(2)]
+        did = [torch.empty((Tm, w.K), dtype=torch.int32, device=dev) for _ in range(2)]
+        dsc = [torch.empty((Tm, w.K), dtype=torch.float32, device=dev) for _ in range(2)]
+        dout = [torch.empty((Tm, w.D), dtype=tdt, device=dev) for _ in range(2)]
+        hout = [torch.empty((Tm, w.D), dtype=raw).pin_memory() for _ in range(2)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         s_cmp = stream
 
-        def run_pipeline(n):
-            ev_in = [torch.cuda.Event() for _ in range(n)]
-            ev_cmp = [torch.cuda.Event() for _ in range(n)]
-            ev_out = [torch.cuda.Event() for _ in range(n)]
-            for i in range(n):
-                bsel = i % 2
+        def run_pipeline(n_units):
+            ev_in = [torch.cuda.Event() for _ in range(n_units)]
+            ev_cmp = [torch.cuda.Event() for _ in range(n_units)]
+            ev_out = [torch.cuda.Event() for _ in range(n_units)]
+            for j in range(n_units):
+                i, bs = j % n_calls, j % 2
+                T = Ts[i]
                 with torch.cuda.stream(s_in):
-                    if i >= 2:
-                        s_in.wait_event(ev_cmp[i - 2])
-                    (xs[bsel].view(raw) if tdt == torch.bfloat16 else xs[bsel]).copy_(
-                        x_h, non_blocking=True)
-                    idss[bsel].copy_(ids_h, non_blocking=True)
-                    scs[bsel].copy_(sc_h, non_blocking=True)
-                    ev_in[i].record(s_in)
-                s_cmp.wait_event(ev_in[i])
-                if i >= 2:
-                    s_cmp.wait_event(ev_out[i - 2])
-                ep.ep_dispatch(h, xs[bsel], scs[bsel], idss[bsel], T, N, s_cmp.cuda_stream)
-                ep.ep_combine(h, recv_x, scs[bsel], T, outs[bsel], out_code, s_cmp.cuda_stream)
-                ev_cmp[i].record(s_cmp)
+                    if j >= 2:
+                        s_in.wait_event(ev_cmp[j - 2])
+                    dx[bs][:T].view(raw).copy_(xh[i], non_blocking=True)
+                    did[bs][:T].copy_(idh[i], non_blocking=True)
+                    dsc[bs][:T].copy_(sch[i], non_blocking=True)
+                    ev_in[j].record(s_in)
+                s_cmp.wait_event(ev_in[j])
+                if j >= 2:
+                    s_cmp.wait_event(ev_out[j - 2])
+                ep.ep_dispatch(h, dx[bs][:T], dsc[bs][:T], did[bs][:T], T, N, s_cmp.cuda_stream)
+                ep.ep_combine(h, recv_x, dsc[bs][:T], T, dout[bs][:T], out_code,
+                              s_cmp.cuda_stream)
+                ev_cmp[j].record(s_cmp)
                 with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_cmp[i])
-                    outs_h[bsel].copy_(outs[bsel].view(raw) if tdt == torch.bfloat16
-                                       else outs[bsel], non_blocking=True)
-                    ev_out[i].record(s_out)
-            return ev_out[n - 1]
+                    s_out.wait_event(ev_cmp[j])
+                    hout[bs][:T].copy_(dout[bs][:T].view(raw), non_blocking=True)
+                    ev_out[j].record(s_out)
+            return ev_out[n_units - 1]
 
-        run_pipeline(4)                      # warm-up
+        run_pipeline(2 * n_calls + 2)        # warm-up
         torch.cuda.synchronize(dev)
         Ke = max(3, min(K, 300))
+        n_units = Ke * n_calls
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(s_in)
         s_cmp.wait_event(e0)
         s_out.wait_event(e0)
-        last = run_pipeline(Ke)
+        last = run_pipeline(n_units)
         s_out.wait_event(last)
         e1.record(s_out)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-        got = outs_h[(Ke - 1) % 2]
-        assert torch.equal(got, ref_out.view(raw).cpu()), "e2e output differs from the device path"
-        h2d = x_h.numel() * x_h.element_size() + ids_h.numel() * 4 + sc_h.numel() * 4
-        d2h = outs_h[0].numel() * outs_h[0].element_size()
-        res["e2e"] = {"value": world * T * Ke / (e2e_ms / 1e3), "unit": "tokens/s",
-                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
-                      "ms_per_step": e2e_ms / Ke,
-                      "pipeline": "H2D(i+1) | dispatch+combine(i) | D2H(i-1), 3 streams"}
+        jl = n_units - 1
+        il, bl = jl % n_calls, jl % 2
+        assert torch.equal(hout[bl][:Ts[il]], ref_outs[il].view(raw).cpu()), \
+            "e2e output differs from the device path"
+        h2d = sum(x.numel() * x.element_size() + a.numel() * 4 + c.numel() * 4
+                  for x, a, c in zip(xh, idh, sch))
+        d2h = sum(T * w.D * b for T in Ts)
+        res["e2e"] = {"value": replica_throughput(T_step, Ke, e0.elapsed_time(e1), world),
+                      "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "steps": Ke, "ms_per_step": e2e_ms / Ke,
+                      "pipeline": "H2D(j+1) | dispatch+combine(j) | D2H(j-1), 3 streams"}
     buf.close()
     if world > 1:
         import torch.distributed as dist
@@ -522,7 +561,10 @@ def main():
     if rank != 0:
         return
     T, N = workload_tokens(args, w)
+    if res.get("calls_per_step", 1) > 1:
+        T = res["T_step"]
     cfg = workload_desc(w, T, N)
+    cfg["calls_per_step"] = res.get("calls_per_step", 1)
     cfg.update({"l2": "flushed between timed steps (memset of 2x L2)",
                 "expert": "identity (y = recv_x), not timed",
                 "permute_impl": {1: "vec", 2: "bulk"}.get(res["info"]["permute_impl"]),
