@@ -69,8 +69,10 @@ class Oracle:
                                               i64, i64, i32, i32, i32, vp, vp, u32p]
         L.oracle_dispatch_backward.argtypes = [vp, C.c_int, i64, vp, _i32p, _i32p, i64, i64, i32,
                                                i32, i32, vp, C.c_int, vp, u32p]
+        L.oracle_expert_gemm.argtypes = [vp, vp, _i32p, _i32p, i32, i64, i64, vp]
         for name in ("oracle_routing_map", "oracle_layout", "oracle_dispatch", "oracle_combine",
-                     "oracle_combine_backward", "oracle_dispatch_backward"):
+                     "oracle_combine_backward", "oracle_dispatch_backward",
+                     "oracle_expert_gemm"):
             getattr(L, name).restype = C.c_int
 
     # -- scalars ------------------------------------------------------------
@@ -243,6 +245,23 @@ class Oracle:
         if rc:
             raise OracleError(f"oracle_dispatch_backward rc={rc}")
         return gx, gs, int(err.value)
+
+
+    # -- expert consumer -----------------------------------------------------
+    def expert_gemm(self, x, w, cnt, expert_offset, fill: int = 0):
+        """y [rows, dout] bf16 bits: each expert's rows times its weight
+        matrix transposed (fp64 sum, one rounding); other rows keep `fill`."""
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        w = np.ascontiguousarray(w, dtype=np.uint16)
+        cnt = np.ascontiguousarray(cnt, dtype=np.int32)
+        off = np.ascontiguousarray(expert_offset, dtype=np.int32)
+        E, dout, din = w.shape
+        y = np.full((x.shape[0], dout), fill, dtype=np.uint16)
+        rc = self.lib.oracle_expert_gemm(x.ctypes.data, w.ctypes.data, cnt, off, E, din, dout,
+                                         y.ctypes.data)
+        if rc:
+            raise OracleError(f"oracle_expert_gemm rc={rc}")
+        return y
 
 
 _default: Oracle | None = None

@@ -565,5 +565,44 @@ int oracle_dispatch_backward(const void* grad_recv, int g_kind, int64_t D,
     return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Expert consumer: grouped GEMM over each expert's receive rows.             */
+/* ------------------------------------------------------------------------ */
+
+/* The expert computation between dispatch and combine, as a grouped linear
+ * layer driven by the device-side counts ([graph] "Internode" item 2: per-
+ * expert counts stay on the device for the consumers; "Tests": layout ->
+ * dispatch -> expert -> combine). For every expert e and each of its rows
+ * p = expert_offset[e] + j, j < cnt[e]:
+ *     y[p][o] = sum_i x[p][i] * w[e][o][i]      (o < dout, i < din)
+ * summed exactly in fp64 (products of bf16 values are exact) in ascending i
+ * and rounded once to bf16. x and y are in the receive layout (rows of
+ * din / dout bf16 values), w is [E][dout][din] bf16. Rows of y that belong to
+ * no expert are left as the caller filled them. */
+int oracle_expert_gemm(const uint16_t* x, const uint16_t* w, const int32_t* cnt_E,
+                       const int32_t* expert_offset_E, int32_t E, int64_t din, int64_t dout,
+                       uint16_t* y)
+{
+    if (E <= 0 || din <= 0 || dout <= 0) return ORC_EINVAL;
+    for (int32_t e = 0; e < E; ++e) {
+#if ORACLE_MUTANT == 15
+        const uint16_t* we = w + (int64_t)((e + 1) % E) * dout * din;   /* mutant: next expert */
+#else
+        const uint16_t* we = w + (int64_t)e * dout * din;
+#endif
+        for (int64_t j = 0; j < cnt_E[e]; ++j) {
+            int64_t p = (int64_t)expert_offset_E[e] + j;
+            for (int64_t o = 0; o < dout; ++o) {
+                double acc = 0.0;
+                for (int64_t i = 0; i < din; ++i)
+                    acc += (double)oracle_f32_from_bf16(x[p * din + i]) *
+                           (double)oracle_f32_from_bf16(we[o * din + i]);
+                y[p * dout + o] = oracle_bf16_from_f32((float)acc);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
 /* Number of deliberately broken builds the tests can request (ORACLE_MUTANT). */
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -507,4 +507,47 @@ def pin_packed_combine_and_backward_match_strided(o):
                               b.view(np.uint16) if b.dtype == np.uint16 else b.view(np.uint32))
 
 
+# ---------------------------------------------------------------------------
+# Expert consumer (grouped GEMM)
+# ---------------------------------------------------------------------------
+
+def _gemm_case(seed=60, T=29, N=32, E=8, K=2, R=2, din=32, dout=24):
+    ids = _ids(seed, T, E, K)
+    sc = W.topk_scores(seed, ids, E, "sigmoid_norm")
+    x = W.hidden(seed, T, din, "bf16")
+    return ids, sc, x, N, E, K, R, din, dout
+
+
+def pin_expert_gemm_vs_numpy(o):
+    # Each expert's rows times its weights, against numpy's fp64 matmul of the
+    # same bf16 values, rounded once by torch's bf16 cast.
+    import torch
+    ids, sc, x, N, E, K, R, din, dout = _gemm_case()
+    d = o.dispatch(x, sc, ids, N, E, R)
+    w = W.hidden(61, E * dout, din, "bf16").reshape(E, dout, din)
+    y = o.expert_gemm(d["recv_x"], w, d["cnt"], d["expert_offset"], fill=0xFFFF)
+    xf = _f32_from_bits(d["recv_x"]).astype(np.float64)
+    wf = _f32_from_bits(w).astype(np.float64)
+    covered = np.zeros(y.shape[0], bool)
+    for e in range(E):
+        lo, n = int(d["expert_offset"][e]), int(d["cnt"][e])
+        ref = xf[lo:lo + n] @ wf[e].T
+        want = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16)
+        assert np.array_equal(y[lo:lo + n].view(np.int16), want.view(torch.int16).numpy())
+        covered[lo:lo + n] = True
+    assert np.all(y[~covered] == 0xFFFF)              # rows of no expert untouched
+
+
+def pin_expert_gemm_identity_weights(o):
+    # W_e = [I | 0] (dout <= din): every expert copies the first dout columns.
+    ids, sc, x, N, E, K, R, din, dout = _gemm_case(seed=62, din=32, dout=16)
+    d = o.dispatch(x, sc, ids, N, E, R)
+    eye = np.zeros((dout, din), np.float32)
+    eye[np.arange(dout), np.arange(dout)] = 1.0
+    w = np.broadcast_to(_bf16_bits(eye), (E, dout, din)).copy()
+    y = o.expert_gemm(d["recv_x"], w, d["cnt"], d["expert_offset"])
+    rows = d["pos"].ravel()
+    assert np.array_equal(y[rows], d["recv_x"][rows, :dout])
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

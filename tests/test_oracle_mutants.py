@@ -27,6 +27,7 @@ MUTANTS = {
     12: "combine backward scales every row by the first score",
     13: "dispatch backward drops the first term",
     14: "packed layout placed like the strided one",
+    15: "expert GEMM uses the next expert's weights",
 }
 
 
