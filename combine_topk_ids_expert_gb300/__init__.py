@@ -31,7 +31,7 @@ __all__ = [
     "Buffer", "Layout", "DispatchResult", "EpConfig", "EpError",
     "ep_buffer_required_bytes", "ep_buffer_init", "ep_buffer_destroy", "ep_dispatch_layout",
     "ep_dispatch", "ep_dispatch_permute", "ep_combine", "ep_combine_backward",
-    "ep_dispatch_backward", "ep_get_device_error",
+    "ep_dispatch_backward", "ep_expert_gemm", "ep_get_device_error",
     "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_pad_tokens", "ep_derive_max_tokens_pretrain",
     "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
     "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
@@ -158,6 +158,14 @@ def ep_dispatch_backward(handle, grad_recv_x: torch.Tensor,
                                           num_tokens, _ptr(grad_x_TD), grad_x_dtype,
                                           _ptr(grad_scores_TK), _stream(stream)),
           "ep_dispatch_backward")
+
+
+def ep_expert_gemm(handle, x_recv: torch.Tensor, weights: torch.Tensor, din: int, dout: int,
+                   y_recv: torch.Tensor, stream=None) -> None:
+    for name, t in (("x_recv", x_recv), ("weights", weights), ("y_recv", y_recv)):
+        _check_dtype(t, torch.bfloat16, name)
+    check(_abi.lib().ep_expert_gemm(handle, _ptr(x_recv), _ptr(weights), din, dout, _ptr(y_recv),
+                                    _stream(stream)), "ep_expert_gemm")
 
 
 def ep_get_device_error(handle, stream=None) -> int:
@@ -369,6 +377,23 @@ class Buffer:
         ep_dispatch_backward(self.handle, grad_recv_x, grad_recv_scores, num_tokens, gx,
                              _TORCH_TO_EP[od], gs, stream)
         return gx, gs
+
+    def expert_gemm(self, x_recv: torch.Tensor, weights: torch.Tensor,
+                    y_recv: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """y = x * W_e^T over each expert's receive rows (weights [E, dout, din]),
+        from the counts of the last dispatch on this buffer. Returns y_recv with
+        the receive layout's leading shape and dout columns."""
+        E, dout, din = weights.shape
+        if E != self.E:
+            raise ValueError(f"weights must have {self.E} experts, got {E}")
+        if x_recv.shape[-1] != din:
+            raise ValueError(f"x_recv has {x_recv.shape[-1]} columns, weights expect {din}")
+        S = self._last_stride()
+        lead = (self.R * S,) if self.packed else (self.R, S)
+        if y_recv is None:
+            y_recv = torch.empty(lead + (dout,), dtype=torch.bfloat16, device=self.device)
+        ep_expert_gemm(self.handle, x_recv, weights, din, dout, y_recv, stream)
+        return y_recv
 
     def _last_stride(self) -> int:
         return self._stride

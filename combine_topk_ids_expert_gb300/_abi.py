@@ -105,6 +105,8 @@ SIGNATURES = {
                                       C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
     "ep_dispatch_backward": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
                                        C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
+    "ep_expert_gemm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64,
+                                 C.c_void_p, C.c_void_p]),
     "ep_get_device_error": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
     "ep_buffer_query": (C.c_int, [C.c_void_p, C.POINTER(EpBufferInfo)]),
     "ep_dispatch_layout_noalloc": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_int32,

@@ -498,6 +498,33 @@ ep_status ep_dispatch_backward(ep_buffer* buf, const void* grad_recv_x,
     return EP_OK;
 }
 
+ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights, int64_t din,
+                         int64_t dout, void* y_recv, ep_stream_t stream)
+{
+    if (!buf) return EP_ERR_INVALID_ARG;
+    if (!buf->has_layout) return EP_ERR_NO_LAYOUT;
+    if (buf->cfg.dtype != EP_BF16) return EP_ERR_INVALID_ARG;
+    if (din < 64 || din % 64 != 0 || dout < 128 || dout % 128 != 0) return EP_ERR_INVALID_ARG;
+    if (!x_recv || !weights || !y_recv) return EP_ERR_INVALID_ARG;
+    if (!is_aligned(x_recv, 16) || !is_aligned(weights, 16) || !is_aligned(y_recv, 16))
+        return EP_ERR_ALIGNMENT;
+    const int64_t rows = (int64_t)buf->cfg.num_ranks * buf->last_S;
+    if (rows <= 0) return EP_OK;
+    if ((int64_t)buf->cfg.num_experts * dout > INT32_MAX) return EP_ERR_CAPACITY;
+    ep::GemmArgs a;
+    a.cnt = buf->cnt;
+    a.expert_offset = buf->expert_offset;
+    a.y = y_recv;
+    a.din = din;
+    a.dout = dout;
+    a.E = buf->cfg.num_experts;
+    a.err = buf->err;
+    const cudaError_t e =
+        ep::launch_expert_gemm(a, x_recv, rows, weights, buf->num_sms, opts(buf, as_stream(stream)));
+    if (e == cudaErrorInvalidValue) return EP_ERR_INVALID_ARG;
+    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
 ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flags)
 {
     if (!buf || !flags) return EP_ERR_INVALID_ARG;

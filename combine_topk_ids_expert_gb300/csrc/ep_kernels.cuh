@@ -163,6 +163,20 @@ struct CombineBwdArgs {
 };
 cudaError_t launch_combine_backward(const CombineBwdArgs& a, int grid, const LaunchOpts& o);
 
+// Expert consumer: grouped GEMM y[p] = x[p] * W_e^T over each expert's rows,
+// driven by the device counts and offsets (expert_gemm.cu).
+struct GemmArgs {
+    const int32_t* cnt;            // [E] rows per expert
+    const int32_t* expert_offset;  // [E] first receive row of each expert
+    void* y;                       // [rows][dout] bf16
+    int64_t din, dout;             // din % 64 == 0, dout % 128 == 0
+    int E;
+    uint32_t* err;
+};
+// x: [rows][din] bf16 receive rows; w: [E][dout][din] bf16.
+cudaError_t launch_expert_gemm(const GemmArgs& a, const void* x, int64_t rows, const void* w,
+                               int grid, const LaunchOpts& o);
+
 // Launches kernel with an optional programmatic-dependent-launch attribute.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

@@ -256,6 +256,24 @@ EP_API ep_status ep_dispatch_backward(ep_buffer* buf, const void* grad_recv_x,
                                       void* grad_x_TD, int32_t grad_x_dtype,
                                       float* grad_scores_TK, ep_stream_t stream);
 
+/* The expert consumer between dispatch and combine: a grouped GEMM driven by
+ * the per-expert counts and offsets that the last layout on this buffer left
+ * on the device ([graph] "Internode" item 2: counts stay on the device so
+ * consumers never touch the host; "Tests": layout -> dispatch -> expert ->
+ * combine). For every expert e and each of its rows p = expert_offset[e] + j,
+ * j < tokens_per_expert[e]:
+ *     y_recv[p][o] = sum_i x_recv[p][i] * weights[e][o][i]
+ * with bf16 inputs, fp32 accumulation on the tensor cores (tcgen05) and one
+ * round to bf16. x_recv is [R*S][din] and y_recv [R*S][dout] in the receive
+ * layout (strided or packed; x_recv may be recv_x with din = D), weights is
+ * [E][dout][din]; all bf16 device memory, 16-byte aligned. din % 64 == 0,
+ * dout % 128 == 0; bf16 buffers only (EP_ERR_INVALID_ARG otherwise). Rows of
+ * y_recv that belong to no expert are not written. Summation order inside the
+ * tensor cores is the hardware's: results are within the fp32 summation bound
+ * of the exact product, not bitwise fixed across GPU models. */
+EP_API ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights,
+                                int64_t din, int64_t dout, void* y_recv, ep_stream_t stream);
+
 /* Synchronously read and clear the device error word (EP_DEVERR_* bits).
  * Refused with EP_ERR_CAPTURE_HOST_SYNC while the stream is capturing. */
 EP_API ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flags);

@@ -1,0 +1,134 @@
+"""The tcgen05 grouped GEMM (expert consumer) against the oracle.
+
+y[p] = x[p] * W_e^T over each expert's receive rows, driven by the device
+counts of the last dispatch. The tensor cores' summation order is the
+hardware's, so each output is compared with the oracle's value (fp64 sum,
+one bf16 rounding) within |gpu - oracle| <= 2^-7 max(|gpu|, |oracle|) +
+2 din 2^-24 m, m = sum_i |x_i w_i|: the fp32 summation bound, plus one bf16
+ulp because the two sides round different sums and may land on neighbours.
+Rows that belong to no expert must keep their contents.
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_topk_ids_expert_gb300 as ep
+import workloads as W
+from gpu_util import assert_combine_equal, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 0x7FC1   # a bf16 NaN pattern no GEMM output produces
+
+
+def f32(h):
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+def check_gemm(orc, y_gpu, x_ref, w, cnt, off):
+    y_ref = orc.expert_gemm(x_ref, w, cnt, off, fill=SENTINEL)
+    xf, wf = np.abs(f32(x_ref).astype(np.float64)), np.abs(f32(w).astype(np.float64))
+    din = w.shape[2]
+    covered = np.zeros(y_ref.shape[0], bool)
+    for e in range(w.shape[0]):
+        lo, n = int(off[e]), int(cnt[e])
+        if n == 0:
+            continue
+        covered[lo:lo + n] = True
+        g = f32(y_gpu[lo:lo + n]).astype(np.float64)
+        r = f32(y_ref[lo:lo + n]).astype(np.float64)
+        mag = xf[lo:lo + n] @ wf[e].T
+        tol = 2.0 ** -7 * np.maximum(np.abs(r), np.abs(g)) + 2.0 * din * 2.0 ** -24 * mag + 1e-30
+        bad = np.abs(g - r) > tol
+        assert not bad.any(), (f"expert {e}: {int(bad.sum())} outputs outside the bound, "
+                               f"e.g. gpu {g[bad][:4]} oracle {r[bad][:4]} tol {tol[bad][:4]}")
+    assert np.all(y_gpu[~covered] == SENTINEL), "rows of no expert were written"
+
+
+CASES = {
+    # name: (seed, T, N, din, dout, E, K, R, ids, layout)
+    "bn256_zipf":   (70, 300, 300, 256, 256, 16, 4, 4, "zipf", "strided"),
+    "bn128":        (71, 250, 252, 128, 128, 8, 2, 2, "uniform", "strided"),
+    "bn128_384":    (72, 180, 180, 192, 384, 8, 2, 1, "uniform", "strided"),
+    "packed":       (73, 300, 301, 256, 256, 16, 4, 4, "zipf", "packed"),
+    "ds_like":      (74, 1000, 1003, 1024, 512, 32, 8, 8, "zipf", "strided"),
+    "many_empty":   (75, 37, 40, 128, 256, 256, 8, 8, "uniform", "strided"),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_expert_gemm_parity(orc, case):
+    seed, T, N, din, dout, E, K, R, ik, layout = CASES[case]
+    x = W.hidden(seed, T, din, "bf16")
+    ids, sc = W.routing(seed, T, E, K, ik, "sigmoid_norm")
+    w = W.hidden(seed + 1, E * dout, din, "bf16").reshape(E, dout, din)
+    buf = ep.Buffer(N, din, E, R, K, dtype=torch.bfloat16, layout=layout)
+    d = buf.dispatch(to_dev(x), to_dev(sc), to_dev(ids), N)
+    S = d.layout.rank_stride
+    y = torch.full((R * S, dout), SENTINEL, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    buf.expert_gemm(d.recv_x.reshape(R * S, din), to_dev(w), y_recv=y)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, N, E, R, packed=(layout == "packed"))
+    check_gemm(orc, to_np(y), ref["recv_x"], w, ref["cnt"], ref["expert_offset"])
+    buf.close()
+
+
+def test_gemm_output_feeds_combine(orc):
+    # layout -> dispatch -> expert GEMM (D -> D) -> combine on the device, as the
+    # worst-token page's graph test chains them; combine of the GEMM's output is
+    # bit-exact against the oracle's combine of the same rows.
+    T, N, D, E, K, R = 400, 400, 256, 16, 4, 4
+    x = W.hidden(80, T, D, "bf16")
+    ids, sc = W.routing(80, T, E, K, "zipf", "sigmoid_norm")
+    w = W.hidden(81, E * D, D, "bf16").reshape(E, D, D)
+    buf = ep.Buffer(N, D, E, R, K, dtype=torch.bfloat16)
+    scd = to_dev(sc)
+    d = buf.dispatch(to_dev(x), scd, to_dev(ids), N)
+    y = buf.expert_gemm(d.recv_x, to_dev(w))
+    out = buf.combine(y, scd)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, N, E, R)
+    y_np = to_np(y.reshape(-1, D))
+    want, _ = orc.combine(y_np, sc, ref["pos"], ref["rank_prefix"], ref["S"], R)
+    assert_combine_equal(to_np(out), want)
+    buf.close()
+
+
+def test_gemm_graph_replay_fresh_routing(orc):
+    # Captured once; each replay's tile list follows that replay's counts.
+    T, N, D, E, K, R = 256, 256, 128, 8, 2, 2
+    buf = ep.Buffer(N, D, E, R, K, dtype=torch.bfloat16)
+    x = W.hidden(90, T, D, "bf16")
+    w = W.hidden(91, E * 128, D, "bf16").reshape(E, 128, D)
+    xd, wd = to_dev(x), to_dev(w)
+    ids_d = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    sc_d = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    S = ep.ep_pad_tokens(N) * K
+    y = torch.empty((R * S, 128), dtype=torch.bfloat16, device="cuda")
+    ids0, sc0 = W.routing(92, T, E, K, "zipf", "sigmoid_norm")
+    ids_d.copy_(torch.from_numpy(ids0))
+    sc_d.copy_(torch.from_numpy(sc0))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d = buf.dispatch(xd, sc_d, ids_d, N, stream=s)
+        buf.expert_gemm(d.recv_x, wd, y_recv=y, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        d = buf.dispatch(xd, sc_d, ids_d, N, stream=s)
+        buf.expert_gemm(d.recv_x, wd, y_recv=y, stream=s)
+    for i in range(4):
+        ids_i, sc_i = W.routing(93 + i, T, E, K, "zipf" if i % 2 else "uniform", "sigmoid_norm")
+        ids_d.copy_(torch.from_numpy(ids_i))
+        sc_d.copy_(torch.from_numpy(sc_i))
+        y.view(torch.int16).fill_(SENTINEL)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = orc.dispatch(x, sc_i, ids_i, N, E, R)
+        check_gemm(orc, to_np(y), ref["recv_x"], w, ref["cnt"], ref["expert_offset"])
+    assert buf.device_error() == 0
+    buf.close()
