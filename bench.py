@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (and N) of the workload: smaller cases for profiling")
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
+    ap.add_argument("--gemm", type=int, default=0, metavar="DOUT",
+                    help="instead: time the expert grouped GEMM (D -> DOUT) on the receive rows")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -524,8 +526,82 @@ def run_gb300(args) -> dict | None:
     return res if rank == 0 else None
 
 
+def measured_peak_bf16(sustained: bool) -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(p) as f:
+            return float(json.load(f)[key]), f"measured (MEASURED_PEAKS.json {key})"
+    except Exception:
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
+def run_gemm(args) -> None:
+    """Times the expert consumer: y = x W_e^T over every expert's receive rows
+    (bf16, fp32 accumulation on the tensor cores), after one dispatch."""
+    import torch
+
+    import combine_topk_ids_expert_gb300 as ep
+    from combine_topk_ids_expert_gb300.build import build as build_lib
+    build_lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = W.WORKLOADS[args.workload]
+    inps, N = step_calls(args, w)
+    inp = inps[0]
+    T = inp["T"]
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(inp["ids"]).to(dev)
+    sc = torch.from_numpy(inp["scores"]).to(dev)
+    n_max = args.tokens if args.tokens > 0 else w.N_max
+    buf = ep.Buffer(n_max, w.D, w.E, w.R, w.K, dtype=torch.bfloat16, device=dev)
+    d = buf.dispatch(x, sc, ids, N)
+    torch.cuda.synchronize(dev)
+    pairs = int(d.layout.tokens_per_expert.sum().item())
+    dout = args.gemm
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    wts = (torch.randn((w.E, dout, w.D), generator=g, device=dev, dtype=torch.float32) * 0.03
+           ).to(torch.bfloat16)
+    y = torch.empty(d.recv_x.shape[:-1] + (dout,), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        buf.expert_gemm(d.recv_x, wts, y_recv=y)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    launches0 = buf.info()["kernel_launches"]
+    clocks = ClockSampler(0)
+    clocks.start()
+    for e0, e1 in ev:
+        e0.record()
+        buf.expert_gemm(d.recv_x, wts, y_recv=y)
+        e1.record()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    assert buf.device_error() == 0
+    ms = [a.elapsed_time(b) for a, b in ev]
+    avg = sum(ms) / K
+    flops = 2.0 * pairs * w.D * dout
+    tf = flops / (avg / 1e3) / 1e12
+    peak, src = measured_peak_bf16(sustained=False)
+    line = {"metric": "expert grouped GEMM TFLOP/s (bf16 in, fp32 accumulate, tcgen05)",
+            "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+            "ms_per_step": avg, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name} receive rows ({pairs} routed pairs) x "
+                                   f"W[{w.E}, {dout}, {w.D}]",
+                       "rows": pairs, "din": w.D, "dout": dout, "experts": w.E},
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_source": src},
+            "gpu_launches": buf.info()["kernel_launches"] - launches0, "clocks": clk}
+    buf.close()
+    print(json.dumps(line))
+
+
 def main():
     args = parse_args()
+    if args.gemm and args.impl == "gb300":
+        run_gemm(args)
+        return
     world, rank, _ = dist_env()
     w = W.WORKLOADS[args.workload]
 

@@ -13,10 +13,11 @@
 //   - warp 0 (one thread) streams 64-wide K slices of the row block and of
 //     the expert's weights into a 4-stage shared-memory ring with TMA tensor
 //     copies (128-byte swizzle), completion on mbarriers;
-//   - warp 1 owns a BN-column fp32 accumulator in tensor memory (TMEM) and
-//     one thread issues tcgen05.mma (M=128, N=BN, K=16, bf16 inputs, fp32
+//   - warp 1 owns two BN-column fp32 accumulators in tensor memory (TMEM)
+//     and one thread issues tcgen05.mma (M=128, N=BN, K=16, bf16 inputs, fp32
 //     accumulate) from shared-memory descriptors, committing each stage back
-//     to the ring and the finished tile to the epilogue;
+//     to the ring and each finished tile to the epilogue; tiles alternate
+//     between the accumulators so the epilogue overlaps the next tile;
 //   - warps 2-5 read the accumulator with tcgen05.ld (each warp its 32-lane
 //     quarter), round to bf16 and store the rows that belong to the expert.
 // Every wait is bounded; on a timeout the CTA reports EP_DEVERR_TIMEOUT,
@@ -47,7 +48,8 @@ struct Tile {
     // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                        ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-    static constexpr uint32_t kTmemCols = BN;
+    // Two accumulators, so the epilogue of one tile overlaps the MMAs of the next.
+    static constexpr uint32_t kTmemCols = 2 * BN;
 };
 
 // Shared-memory matrix descriptor for a K-major tile written by TMA with the
@@ -189,10 +191,10 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
     const uint32_t full0 = smem_u32(bars);                 // kStages
     const uint32_t empty0 = full0 + 8u * kStages;          // kStages
-    const uint32_t accum_full = empty0 + 8u * kStages;
-    const uint32_t accum_empty = accum_full + 8u;
-    const uint32_t drain = accum_empty + 8u;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 3);
+    const uint32_t accum_full0 = empty0 + 8u * kStages;    // 2: one per accumulator
+    const uint32_t accum_empty0 = accum_full0 + 16u;       // 2
+    const uint32_t drain = accum_empty0 + 16u;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     int* s_mtile = const_cast<int*>(reinterpret_cast<volatile int*>(s_abort + 1));   // [E + 1]
 
@@ -206,8 +208,10 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
             mbar_init(full0 + 8u * s, 1u);
             mbar_init(empty0 + 8u * s, 1u);
         }
-        mbar_init(accum_full, 1u);
-        mbar_init(accum_empty, (uint32_t)kEpilogueThreads);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accum_full0 + 8u * b, 1u);
+            mbar_init(accum_empty0 + 8u * b, (uint32_t)kEpilogueThreads);
+        }
         mbar_init(drain, 1u);
         *s_abort = 0;
         fence_mbar_init();
@@ -269,8 +273,10 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         int g = 0, tl = 0;
         bool issued = false;
         for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x, ++tl) {
-            if (!wait_or_abort(accum_empty, (uint32_t)((tl & 1) ^ 1), s_abort)) break;
+            const int acc = tl & 1, use = tl >> 1;      // accumulator and its use count
+            if (!wait_or_abort(accum_empty0 + 8u * acc, (uint32_t)((use & 1) ^ 1), s_abort)) break;
             tc_fence_after();
+            const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
             bool ok = true;
             for (int k = 0; k < k_iters; ++k, ++g) {
                 const int s = g % kStages;
@@ -282,14 +288,14 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
                 const uint32_t sa = tiles_u32 + (uint32_t)s * C::kStageBytes;
 #pragma unroll
                 for (int j = 0; j < kBK / kUmmaK; ++j)
-                    umma_bf16(tmem, sw128_desc(sa + j * kUmmaK * 2),
+                    umma_bf16(d_tmem, sw128_desc(sa + j * kUmmaK * 2),
                               sw128_desc(sa + C::kBytesA + j * kUmmaK * 2), C::kIdesc,
                               (k | j) != 0 ? 1u : 0u);
                 issued = true;
                 umma_commit(empty0 + 8u * s);   // frees the stage once these MMAs finish
             }
             if (!ok) break;
-            umma_commit(accum_full);            // the tile's accumulator is complete
+            umma_commit(accum_full0 + 8u * acc);   // the tile's accumulator is complete
         }
         if (issued) {   // every MMA this thread issued has finished before TMEM is freed
             umma_commit(drain);
@@ -303,8 +309,10 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         uint16_t* y = static_cast<uint16_t*>(a.y);
         int tl = 0;
         for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x, ++tl) {
-            if (!wait_or_abort(accum_full, (uint32_t)(tl & 1), s_abort)) break;
+            const int acc = tl & 1, use = tl >> 1;
+            if (!wait_or_abort(accum_full0 + 8u * acc, (uint32_t)(use & 1), s_abort)) break;
             tc_fence_after();
+            const uint32_t t_acc = t_lane + (uint32_t)(acc * BN);
             const int mt = t / n_blocks, nb = t % n_blocks;
             const int e = expert_of(s_mtile, E, mt);
             const int m_in = (mt - s_mtile[e]) * kBM;
@@ -313,7 +321,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 uint32_t v[32];
-                tmem_ld32(t_lane + (uint32_t)c, v);
+                tmem_ld32(t_acc + (uint32_t)c, v);
                 tmem_wait_ld();
                 if (r_in < rows) {
                     int4* dst = reinterpret_cast<int4*>(y + row * a.dout + nb * BN + c);
@@ -329,7 +337,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
                 }
             }
             tc_fence_before();
-            mbar_arrive(accum_empty);
+            mbar_arrive(accum_empty0 + 8u * acc);
         }
     }
 
@@ -382,7 +390,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
 template <int BN>
 size_t gemm_smem_bytes(int E)
 {
-    return 1024 + (size_t)kStages * Tile<BN>::kStageBytes + 8 * (2 * kStages + 3) + 8 +
+    return 1024 + (size_t)kStages * Tile<BN>::kStageBytes + 8 * (2 * kStages + 5) + 8 +
            4 * (size_t)(E + 1);
 }
 
