@@ -70,9 +70,12 @@ class Oracle:
         L.oracle_dispatch_backward.argtypes = [vp, C.c_int, i64, vp, _i32p, _i32p, i64, i64, i32,
                                                i32, i32, vp, C.c_int, vp, u32p]
         L.oracle_expert_gemm.argtypes = [vp, vp, _i32p, _i32p, i32, i64, i64, vp]
+        L.oracle_dispatch_dedup.argtypes = [vp, i64, _f32p, _i32p, i64, i64, i32, i32, i32, vp,
+                                            _i32p, _i32p, _f32p, _i32p, _i32p, u32p]
+        L.oracle_dedup_expand.argtypes = [vp, i64, _i32p, _i32p, _i32p, i64, i32, i32, i32, vp]
         for name in ("oracle_routing_map", "oracle_layout", "oracle_dispatch", "oracle_combine",
                      "oracle_combine_backward", "oracle_dispatch_backward",
-                     "oracle_expert_gemm"):
+                     "oracle_expert_gemm", "oracle_dispatch_dedup", "oracle_dedup_expand"):
             getattr(L, name).restype = C.c_int
 
     # -- scalars ------------------------------------------------------------
@@ -261,6 +264,58 @@ class Oracle:
                                          y.ctypes.data)
         if rc:
             raise OracleError(f"oracle_expert_gemm rc={rc}")
+        return y
+
+
+    # -- per-rank dedupe --------------------------------------------------------
+    def dispatch_dedup(self, x, scores, ids, N: int, E: int, R: int, fill: int = 0) -> dict:
+        """One receive row per (token, rank): recv_tok_x [R*P, D], recv_tok_src
+        [R*P], recv_topk_idx [R*P, K], recv_topk_w [R*P, K], tok_pos [T, R],
+        tokens_in_rank [R]; rows past each rank's total keep `fill`."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        scores = np.ascontiguousarray(scores, dtype=np.float32)
+        x = np.ascontiguousarray(x)
+        _kind(x)
+        T, K = ids.shape
+        D = x.shape[1]
+        rows = R * self.pad_tokens(N)
+        rx = np.zeros((max(rows, 1), D), dtype=x.dtype)
+        rx.view(np.uint8)[...] = fill
+        src = np.full(max(rows, 1), -1, np.int32)
+        idx = np.full((max(rows, 1), K), -2, np.int32)
+        wts = np.zeros((max(rows, 1), K), np.float32)
+        tpos = np.zeros((max(T, 1), R), np.int32)
+        tir = np.zeros(R, np.int32)
+        err = C.c_uint32(0)
+        rc = self.lib.oracle_dispatch_dedup(
+            x.ctypes.data if T else None, D * x.itemsize,
+            scores.ravel() if T else np.zeros(1, np.float32),
+            ids.ravel() if T else np.zeros(1, np.int32), T, N, K, E, R, rx.ctypes.data,
+            src, idx.ravel(), wts.ravel(), tpos.ravel(), tir, C.byref(err))
+        if rc:
+            raise OracleError(f"oracle_dispatch_dedup rc={rc}")
+        return {"recv_tok_x": rx[:rows], "recv_tok_src": src[:rows], "recv_topk_idx": idx[:rows],
+                "recv_topk_w": wts[:rows], "tok_pos": tpos[:T], "tokens_in_rank": tir,
+                "P": self.pad_tokens(N), "err": int(err.value)}
+
+    def dedup_expand(self, recv_tok_x, tok_pos, pos, ids, E: int, R: int, rows: int,
+                     fill: int = 0):
+        """Expert-layout rows y [rows, D] from the dedupe rows."""
+        recv_tok_x = np.ascontiguousarray(recv_tok_x)
+        tok_pos = np.ascontiguousarray(tok_pos, dtype=np.int32)
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        T, K = ids.shape
+        D = recv_tok_x.shape[1]
+        y = np.zeros((rows, D), dtype=recv_tok_x.dtype)
+        y.view(np.uint8)[...] = fill
+        rc = self.lib.oracle_dedup_expand(recv_tok_x.ctypes.data, D * recv_tok_x.itemsize,
+                                          tok_pos.ravel() if T else np.zeros(1, np.int32),
+                                          pos.ravel() if T else np.zeros(1, np.int32),
+                                          ids.ravel() if T else np.zeros(1, np.int32), T, K, E,
+                                          R, y.ctypes.data)
+        if rc:
+            raise OracleError(f"oracle_dedup_expand rc={rc}")
         return y
 
 

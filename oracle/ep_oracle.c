@@ -566,6 +566,98 @@ int oracle_dispatch_backward(const void* grad_recv, int g_kind, int64_t D,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Per-rank dedupe: one row per (token, destination rank).                     */
+/* ------------------------------------------------------------------------ */
+
+/* Dispatch with one receive row per distinct (token, rank), the transport
+ * format of a dispatcher that sends a token to a rank once however many of
+ * that rank's experts it selected ([titan] "Backend behavior": DeepEP's
+ * per-rank layout; [graph] "Internode": per-rank token counts). Rank r owns
+ * rows [r*P, r*P + tokens_in_rank[r]); its rows are the tokens with at least
+ * one expert on r, in ascending token order (reading: the stable order, as
+ * for expert rows). For row q of token t on rank r:
+ *   recv_tok_x[q] = x[t], recv_tok_src[q] = t,
+ *   recv_topk_idx[q][k] = e - r*E_loc if pair (t,k) routes to expert e of
+ *                         rank r, else -1 (a local expert index),
+ *   recv_topk_w[q][k]   = scores[t][k] for those pairs, else 0;
+ * and tok_pos[t][r] = q, or -1 when t has no expert on r. Receive buffers hold
+ * R * P rows (P = oracle_pad_tokens(N)). */
+int oracle_dispatch_dedup(const void* x, int64_t row_bytes, const float* scores,
+                          const int32_t* ids, int64_t T, int64_t N, int32_t K, int32_t E,
+                          int32_t R, void* recv_tok_x, int32_t* recv_tok_src,
+                          int32_t* recv_topk_idx, float* recv_topk_w, int32_t* tok_pos_TR,
+                          int32_t* tokens_in_rank_R, uint32_t* err)
+{
+    if (check_shape(T, N, K, E, R) != ORC_OK || row_bytes <= 0) return ORC_EINVAL;
+    const int64_t P = oracle_pad_tokens(N);
+    const int32_t eloc = E / R;
+    for (int32_t r = 0; r < R; ++r) {
+        int64_t q = (int64_t)r * P;
+        for (int64_t t = 0; t < T; ++t) {
+            int hit = 0;
+            for (int32_t k = 0; k < K; ++k) {
+                int32_t e = ids[t * K + k];
+                if (e < -1 || e >= E) {
+                    *err |= ORC_ERR_BAD_ID;
+                    e = -1;
+                }
+                if (e >= 0 && rank_of(e, E, R) == r) hit = 1;
+            }
+            if (!hit) {
+                tok_pos_TR[t * R + r] = -1;
+                continue;
+            }
+#if ORACLE_MUTANT == 16
+            for (int32_t dup = 0; dup < K; ++dup) {     /* mutant: one row per pair */
+                if (dup > 0) {
+                    int32_t e = ids[t * K + dup];
+                    if (e < 0 || e >= E || rank_of(e, E, R) != r) continue;
+                }
+#endif
+            if (q >= (int64_t)(r + 1) * P) return ORC_EINVAL;   /* a rank never exceeds P rows */
+            tok_pos_TR[t * R + r] = (int32_t)q;
+            memcpy((uint8_t*)recv_tok_x + q * row_bytes, (const uint8_t*)x + t * row_bytes,
+                   (size_t)row_bytes);
+            recv_tok_src[q] = (int32_t)t;
+            for (int32_t k = 0; k < K; ++k) {
+                int32_t e = ids[t * K + k];
+                int mine = e >= 0 && e < E && rank_of(e, E, R) == r;
+                recv_topk_idx[q * K + k] = mine ? e - r * eloc : -1;
+                recv_topk_w[q * K + k] = mine ? scores[t * K + k] : 0.0f;
+            }
+            ++q;
+#if ORACLE_MUTANT == 16
+            }
+#endif
+        }
+        tokens_in_rank_R[r] = (int32_t)(q - (int64_t)r * P);
+    }
+    return ORC_OK;
+}
+
+/* The receiver's expansion of the dedupe rows into the expert layout of
+ * oracle_dispatch: for every pair (t,k) with a receive row p = pos[t][k],
+ *   y[p] = recv_tok_x[tok_pos[t][r(e)]]
+ * where e = ids[t][k]. y holds the expert layout's rows (R * S of row_bytes). */
+int oracle_dedup_expand(const void* recv_tok_x, int64_t row_bytes, const int32_t* tok_pos_TR,
+                        const int32_t* pos_TK, const int32_t* ids, int64_t T, int32_t K,
+                        int32_t E, int32_t R, void* y)
+{
+    if (T < 0 || K <= 0 || E <= 0 || R <= 0 || E % R != 0 || row_bytes <= 0) return ORC_EINVAL;
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t k = 0; k < K; ++k) {
+            const int64_t p = pos_TK[t * K + k];
+            const int32_t e = ids[t * K + k];
+            if (p < 0 || e < 0 || e >= E) continue;
+            const int64_t q = tok_pos_TR[t * R + rank_of(e, E, R)];
+            if (q < 0) return ORC_EINVAL;
+            memcpy((uint8_t*)y + p * row_bytes, (const uint8_t*)recv_tok_x + q * row_bytes,
+                   (size_t)row_bytes);
+        }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Expert consumer: grouped GEMM over each expert's receive rows.             */
 /* ------------------------------------------------------------------------ */
 

@@ -550,4 +550,50 @@ def pin_expert_gemm_identity_weights(o):
     assert np.array_equal(y[rows], d["recv_x"][rows, :dout])
 
 
+# ---------------------------------------------------------------------------
+# Per-rank dedupe
+# ---------------------------------------------------------------------------
+
+def pin_dedup_rows_brute(o):
+    # Rank r's rows are exactly the tokens with an expert on r, in token order;
+    # their count is the layout's tokens_in_rank; idx/w follow the pairs.
+    T, N, E, K, R, D = 31, 33, 16, 4, 4, 8
+    ids = _ids(70, T, E, K)
+    sc = W.topk_scores(70, ids, E, "sigmoid_norm")
+    x = W.hidden(70, T, D, "bf16")
+    dd = o.dispatch_dedup(x, sc, ids, N, E, R)
+    lay = o.layout(ids, N, E, R)
+    assert np.array_equal(dd["tokens_in_rank"], lay["tokens_in_rank"])
+    P, eloc = dd["P"], E // R
+    for r in range(R):
+        toks = [t for t in range(T) if any(int(e) // eloc == r for e in ids[t])]
+        rows = np.arange(r * P, r * P + len(toks))
+        assert dd["recv_tok_src"][rows].tolist() == toks
+        for q, t in zip(rows, toks):
+            assert np.array_equal(dd["recv_tok_x"][q], x[t])
+            assert dd["tok_pos"][t, r] == q
+            for k in range(K):
+                e = int(ids[t, k])
+                mine = e // eloc == r
+                assert dd["recv_topk_idx"][q, k] == (e - r * eloc if mine else -1)
+                assert dd["recv_topk_w"][q, k] == (sc[t, k] if mine else 0.0)
+        others = [t for t in range(T) if t not in toks]
+        assert all(dd["tok_pos"][t, r] == -1 for t in others)
+
+
+def pin_dedup_expand_reproduces_dispatch(o):
+    # The receiver's expansion of the dedupe rows equals the per-expert
+    # dispatch bit for bit on every routed row.
+    T, N, E, K, R, D = 45, 48, 32, 8, 8, 16
+    ids = W.topk_ids_zipf(71, T, E, K)
+    sc = W.topk_scores(71, ids, E, "sigmoid_norm")
+    x = W.hidden(71, T, D, "bf16")
+    d = o.dispatch(x, sc, ids, N, E, R)
+    dd = o.dispatch_dedup(x, sc, ids, N, E, R)
+    y = o.dedup_expand(dd["recv_tok_x"], dd["tok_pos"], d["pos"], ids, E, R, R * d["S"])
+    rows = d["pos"].ravel()
+    assert np.array_equal(y[rows], d["recv_x"][rows])
+    assert int(dd["tokens_in_rank"].sum()) < T * K           # duplicates were folded
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -28,6 +28,7 @@ MUTANTS = {
     13: "dispatch backward drops the first term",
     14: "packed layout placed like the strided one",
     15: "expert GEMM uses the next expert's weights",
+    16: "dedupe writes one row per pair instead of per rank",
 }
 
 
