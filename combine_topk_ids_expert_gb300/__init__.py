@@ -25,13 +25,15 @@ import torch
 from . import _abi
 from ._abi import (EP_BF16, EP_DEVERR_BAD_ID, EP_DEVERR_ROW_OOB, EP_DEVERR_TIMEOUT, EP_F32,
                    EP_LAYOUT_PACKED, EP_LAYOUT_STRIDED, EP_PERMUTE_BULK, EP_PERMUTE_DEFAULT,
-                   EP_PERMUTE_VEC, EpBufferInfo, EpConfig, EpDispatchOut, EpError, EpLayout, check)
+                   EP_PERMUTE_VEC, EpBufferInfo, EpConfig, EpDedupOut, EpDispatchOut, EpError,
+                   EpLayout, check)
 
 __all__ = [
     "Buffer", "Layout", "DispatchResult", "EpConfig", "EpError",
     "ep_buffer_required_bytes", "ep_buffer_init", "ep_buffer_destroy", "ep_dispatch_layout",
     "ep_dispatch", "ep_dispatch_permute", "ep_combine", "ep_combine_backward",
-    "ep_dispatch_backward", "ep_expert_gemm", "ep_get_device_error",
+    "ep_dispatch_backward", "ep_dispatch_dedup", "ep_dedup_expand", "ep_expert_gemm",
+    "ep_get_device_error", "DedupResult",
     "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_pad_tokens", "ep_derive_max_tokens_pretrain",
     "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
     "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
@@ -160,6 +162,25 @@ def ep_dispatch_backward(handle, grad_recv_x: torch.Tensor,
           "ep_dispatch_backward")
 
 
+def ep_dispatch_dedup(handle, x_TD: torch.Tensor, topk_scores_TK: torch.Tensor,
+                      topk_expert_ids_TK: torch.Tensor, num_tokens: int, num_tokens_per_rank: int,
+                      stream=None) -> EpDedupOut:
+    _check_dtype(topk_scores_TK, torch.float32, "topk_scores_TK")
+    _check_dtype(topk_expert_ids_TK, torch.int32, "topk_expert_ids_TK")
+    out = EpDedupOut()
+    check(_abi.lib().ep_dispatch_dedup(handle, _ptr(x_TD), _ptr(topk_scores_TK),
+                                       _ptr(topk_expert_ids_TK), num_tokens, num_tokens_per_rank,
+                                       _stream(stream), C.byref(out)), "ep_dispatch_dedup")
+    return out
+
+
+def ep_dedup_expand(handle, topk_expert_ids_TK: torch.Tensor, y_recv: torch.Tensor,
+                    stream=None) -> None:
+    _check_dtype(topk_expert_ids_TK, torch.int32, "topk_expert_ids_TK")
+    check(_abi.lib().ep_dedup_expand(handle, _ptr(topk_expert_ids_TK), _ptr(y_recv),
+                                     _stream(stream)), "ep_dedup_expand")
+
+
 def ep_expert_gemm(handle, x_recv: torch.Tensor, weights: torch.Tensor, din: int, dout: int,
                    y_recv: torch.Tensor, stream=None) -> None:
     for name, t in (("x_recv", x_recv), ("weights", weights), ("y_recv", y_recv)):
@@ -247,6 +268,16 @@ class DispatchResult:
     recv_scores: torch.Tensor         # [R, S] or [R*S] fp32
     recv_src: torch.Tensor            # [R, S] or [R*S] int32
     layout: Layout
+
+
+@dataclass
+class DedupResult:
+    recv_x: torch.Tensor              # [R, P, D]: one row per distinct (token, rank)
+    recv_tok_src: torch.Tensor        # [R, P] int32 source token
+    recv_topk_idx: torch.Tensor       # [R, P, K] int32 local expert index or -1
+    recv_topk_w: torch.Tensor         # [R, P, K] fp32 score or 0
+    tok_pos: torch.Tensor             # [T, R] int32 row of (t, r) or -1
+    layout: Layout                    # tokens_in_rank[r] = rank r's rows
 
 
 class Buffer:
@@ -377,6 +408,35 @@ class Buffer:
         ep_dispatch_backward(self.handle, grad_recv_x, grad_recv_scores, num_tokens, gx,
                              _TORCH_TO_EP[od], gs, stream)
         return gx, gs
+
+    def dispatch_dedup(self, x_TD: torch.Tensor, topk_scores_TK: torch.Tensor,
+                       topk_expert_ids_TK: torch.Tensor, num_tokens_per_rank: int | None = None,
+                       stream=None) -> DedupResult:
+        """One receive row per distinct (token, rank)."""
+        _check_dtype(x_TD, self.dtype, "x_TD")
+        T = x_TD.shape[0]
+        N = T if num_tokens_per_rank is None else num_tokens_per_rank
+        d = ep_dispatch_dedup(self.handle, x_TD, topk_scores_TK, topk_expert_ids_TK, T, N, stream)
+        P, R, K = d.rows_per_rank_stride, self.R, self.K
+        lay = self._layout(d.layout)
+        return DedupResult(
+            recv_x=self._view(d.recv_x, self.dtype, (R, P, self.D)),
+            recv_tok_src=self._view(d.recv_tok_src, torch.int32, (R, P)),
+            recv_topk_idx=self._view(d.recv_topk_idx, torch.int32, (R, P, K)),
+            recv_topk_w=self._view(d.recv_topk_w, torch.float32, (R, P, K)),
+            tok_pos=self._view(d.tok_pos, torch.int32, (T, R)),
+            layout=lay)
+
+    def dedup_expand(self, topk_expert_ids_TK: torch.Tensor, y_recv: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+        """The receiver's expansion of the last dedupe dispatch into per-expert rows
+        (a tensor shaped like a dispatch's recv_x), ready for combine."""
+        S = self._last_stride()
+        lead = (self.R * S,) if self.packed else (self.R, S)
+        if y_recv is None:
+            y_recv = torch.empty(lead + (self.D,), dtype=self.dtype, device=self.device)
+        ep_dedup_expand(self.handle, topk_expert_ids_TK, y_recv, stream)
+        return y_recv
 
     def expert_gemm(self, x_recv: torch.Tensor, weights: torch.Tensor,
                     y_recv: torch.Tensor | None = None, stream=None) -> torch.Tensor:

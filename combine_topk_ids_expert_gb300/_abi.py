@@ -73,6 +73,18 @@ class EpDispatchOut(C.Structure):
     ]
 
 
+class EpDedupOut(C.Structure):
+    _fields_ = [
+        ("recv_x", C.c_void_p),
+        ("recv_tok_src", C.c_void_p),
+        ("recv_topk_idx", C.c_void_p),
+        ("recv_topk_w", C.c_void_p),
+        ("tok_pos", C.c_void_p),
+        ("rows_per_rank_stride", C.c_int64),
+        ("layout", EpLayout),
+    ]
+
+
 class EpBufferInfo(C.Structure):
     _fields_ = [
         ("workspace_bytes", C.c_int64),
@@ -105,6 +117,9 @@ SIGNATURES = {
                                       C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
     "ep_dispatch_backward": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
                                        C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
+    "ep_dispatch_dedup": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
+                                    C.c_int64, C.c_void_p, C.POINTER(EpDedupOut)]),
+    "ep_dedup_expand": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "ep_expert_gemm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64,
                                  C.c_void_p, C.c_void_p]),
     "ep_get_device_error": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),

@@ -1,0 +1,240 @@
+// dedup.cu - per-rank dedupe: one receive row per distinct (token, rank), and
+// the receiver's expansion of those rows into the per-expert layout.
+//
+// A dispatcher that sends each token to a destination rank once, however
+// many of that rank's experts it selected, moves fewer rows ("Unify expert
+// parallel token dispatcher API", "Backend behavior": DeepEP's per-rank
+// layout; "ep: graph-safe worst-token HT dispatch+combine", "Internode":
+// per-rank counts on the device). Rank r owns rows [r*P, r*P +
+// tokens_in_rank[r]) in ascending token order; each row carries its source
+// token and, per k, the local expert index (or -1) and the score (or 0).
+//
+// Kernels (after the layout's count and scan, which also leave each tile's
+// exclusive prefix of distinct tokens per rank):
+//   dedup_pos    : one CTA per layout tile; warp ballots rank each token among
+//                  the tile's tokens that hit rank r, in token order.
+//   dedup_copy   : a CTA per token (grid-stride); the row is loaded once in
+//                  16-byte vectors and stored to each destination rank's row.
+//   dedup_expand : a CTA per token; copies each pair's dedupe row to its
+//                  per-expert receive row (the receiver's expansion).
+#include "ep_device.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kCopyThreads = 128;
+
+__device__ __forceinline__ unsigned long long rank_mask(const int32_t* ids, int64_t t, int K,
+                                                        int E, int eloc)
+{
+    unsigned long long m = 0ull;
+#pragma unroll 8
+    for (int k = 0; k < K; ++k) {
+        const int e = valid_id(__ldcg(ids + t * K + k), E);
+        if (e >= 0) m |= 1ull << (e / eloc);
+    }
+    return m;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+dedup_pos_kernel(LayoutArgs l, DedupArgs a)
+{
+    __shared__ int s_base[kLayoutWarps][kMaxRanks];
+    griddep_wait();
+    griddep_launch_dependents();
+    const int tile = blockIdx.x;
+    const int64_t t0 = (int64_t)tile * l.tpt;
+    const int64_t t1 = min(l.T, t0 + l.tpt);
+    const int n = (int)(t1 - t0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int R = a.R, eloc = a.E / a.R;
+    const int seg = (((n + kLayoutWarps - 1) / kLayoutWarps) + 31) & ~31;
+    const int w_begin = warp * seg;
+    const int w_end = min(n, w_begin + seg);
+
+    for (int i = threadIdx.x; i < kLayoutWarps * kMaxRanks; i += blockDim.x)
+        s_base[i / kMaxRanks][i % kMaxRanks] = 0;
+    __syncthreads();
+
+    // Pass 1: tokens of this warp's segment that hit each rank.
+    for (int c = w_begin; c < w_begin + seg; c += 32) {
+        const int i = c + lane;
+        const unsigned long long m = (i < w_end) ? rank_mask(a.ids, t0 + i, a.K, a.E, eloc) : 0ull;
+        for (int r = 0; r < R; ++r) {
+            const unsigned b = __ballot_sync(0xffffffffu, (m >> r) & 1ull);
+            if (lane == 0) s_base[warp][r] += __popc(b);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // Exclusive prefix over warps, seeded with the rank's base row and the
+    // distinct tokens of all earlier tiles.
+    if (threadIdx.x < R) {
+        const int r = threadIdx.x;
+        int base = (int)((int64_t)r * a.P) + __ldcg(l.tile_tok_pre + (int64_t)tile * R + r);
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int c = s_base[w][r];
+            s_base[w][r] = base;
+            base += c;
+        }
+    }
+    __syncthreads();
+
+    // Pass 2: row = running base + tokens hitting the rank in lower lanes.
+    for (int c = w_begin; c < w_begin + seg; c += 32) {
+        const int i = c + lane;
+        const bool in = i < w_end;
+        const unsigned long long m = in ? rank_mask(a.ids, t0 + i, a.K, a.E, eloc) : 0ull;
+        for (int r = 0; r < R; ++r) {
+            const bool bit = (m >> r) & 1ull;
+            const unsigned b = __ballot_sync(0xffffffffu, bit);
+            const int base = s_base[warp][r];
+            if (in) a.tok_pos[(t0 + i) * R + r] = bit ? base + __popc(b & lanemask_lt(lane)) : -1;
+            __syncwarp();
+            if (lane == 0) s_base[warp][r] = base + __popc(b);
+            __syncwarp();
+        }
+    }
+}
+
+template <int U>
+__global__ void __launch_bounds__(kCopyThreads)
+dedup_copy_kernel(DedupArgs a)
+{
+    __shared__ int s_row[kMaxRanks];
+    __shared__ int s_rank[kMaxRanks];
+    __shared__ int s_n;
+    griddep_wait();
+    const int64_t V = a.row_bytes / 16;
+    const int eloc = a.E / a.R;
+    const int4* __restrict__ x = static_cast<const int4*>(a.x);
+    int4* __restrict__ rx = static_cast<int4*>(a.recv_x);
+
+    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+        if (threadIdx.x == 0) {
+            int n = 0;
+            for (int r = 0; r < a.R; ++r) {
+                const int q = __ldcg(a.tok_pos + t * a.R + r);
+                if (q >= 0) {
+                    s_row[n] = q;
+                    s_rank[n] = r;
+                    ++n;
+                }
+            }
+            s_n = n;
+        }
+        __syncthreads();
+        const int n = s_n;
+        // Per destination row: source token, local expert index and score per k.
+        for (int j = threadIdx.x; j < n * a.K; j += kCopyThreads) {
+            const int d = j / a.K, k = j % a.K;
+            const int q = s_row[d], r = s_rank[d];
+            const int e = valid_id(__ldcg(a.ids + t * a.K + k), a.E);
+            const bool mine = e >= 0 && e / eloc == r;
+            a.recv_topk_idx[(int64_t)q * a.K + k] = mine ? e - r * eloc : -1;
+            a.recv_topk_w[(int64_t)q * a.K + k] = mine ? __ldcg(a.scores + t * a.K + k) : 0.0f;
+            if (k == 0) a.recv_tok_src[q] = (int32_t)t;
+        }
+        const int4* src = x + t * V;
+        for (int64_t v0 = threadIdx.x; v0 < V; v0 += (int64_t)U * kCopyThreads) {
+            int4 r4[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + (int64_t)u * kCopyThreads;
+                if (v < V) r4[u] = ld_cg_v4(src + v);
+            }
+            for (int d = 0; d < n; ++d) {
+                int4* dst = rx + (int64_t)s_row[d] * V;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = v0 + (int64_t)u * kCopyThreads;
+                    if (v < V) dst[v] = r4[u];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    griddep_launch_dependents();
+}
+
+__global__ void __launch_bounds__(kCopyThreads)
+dedup_expand_kernel(DedupArgs a, const int32_t* pos, void* y)
+{
+    __shared__ int s_dst[kMaxTopk];
+    __shared__ int s_src[kMaxTopk];
+    griddep_wait();
+    const int64_t V = a.row_bytes / 16;
+    const int eloc = a.E / a.R;
+    const int4* __restrict__ rx = static_cast<const int4*>(a.recv_x);
+    int4* __restrict__ out = static_cast<int4*>(y);
+
+    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+        if (threadIdx.x < a.K) {
+            const int64_t q = t * a.K + threadIdx.x;
+            const int p = __ldcg(pos + q);
+            const int e = valid_id(__ldcg(a.ids + q), a.E);
+            int src = -1;
+            if (p >= 0 && e >= 0) {
+                src = __ldcg(a.tok_pos + t * a.R + e / eloc);
+                if (src < 0) atomicOr(a.err, kErrRowOob);   // ids differ from the dispatch's
+            }
+            s_dst[threadIdx.x] = (src >= 0) ? p : -1;
+            s_src[threadIdx.x] = src;
+        }
+        __syncthreads();
+        for (int k = 0; k < a.K; ++k) {
+            const int p = s_dst[k];
+            if (p < 0) continue;
+            const int4* s = rx + (int64_t)s_src[k] * V;
+            int4* d = out + (int64_t)p * V;
+            for (int64_t v = threadIdx.x; v < V; v += kCopyThreads) d[v] = ld_cg_v4(s + v);
+        }
+        __syncthreads();
+    }
+    griddep_launch_dependents();
+}
+
+int copy_unroll(int64_t row_bytes)
+{
+    int64_t u = (row_bytes / 16 + kCopyThreads - 1) / kCopyThreads;
+    return (int)(u < 1 ? 1 : (u > 8 ? 8 : u));
+}
+
+int copy_grid(int64_t T)
+{
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t g = (int64_t)(sms > 0 ? sms : 1) * 8;
+    return (int)(T < g ? T : g);
+}
+
+}  // namespace
+
+cudaError_t launch_dedup(const LayoutArgs& l, const DedupArgs& a, const LaunchOpts& o)
+{
+    if (a.T <= 0) return cudaSuccess;
+    cudaError_t e = launch_kernel(dedup_pos_kernel, dim3(l.ntiles), dim3(kLayoutThreads), 0, o, l, a);
+    if (e != cudaSuccess) return e;
+    const dim3 g(copy_grid(a.T)), b(kCopyThreads);
+    switch (copy_unroll(a.row_bytes)) {
+#define EP_COPY(U) \
+    case U:        \
+        return launch_kernel(dedup_copy_kernel<U>, g, b, 0, o, a);
+        EP_COPY(1) EP_COPY(2) EP_COPY(3) EP_COPY(4) EP_COPY(5) EP_COPY(6) EP_COPY(7) EP_COPY(8)
+#undef EP_COPY
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_dedup_expand(const DedupArgs& a, const int32_t* pos, void* y,
+                                const LaunchOpts& o)
+{
+    if (a.T <= 0) return cudaSuccess;
+    return launch_kernel(dedup_expand_kernel, dim3(copy_grid(a.T)), dim3(kCopyThreads), 0, o, a,
+                         pos, y);
+}
+
+}  // namespace ep

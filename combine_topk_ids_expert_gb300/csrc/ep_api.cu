@@ -41,12 +41,16 @@ struct ep_buffer {
     int32_t* tile_cnt;
     int32_t* tile_pre;
     int32_t* tile_tok;
+    int32_t* tile_tok_pre;
+    int32_t* tok_pos;
+    int32_t* tok_src;
     uint32_t* err;
     // plans
     ep::PermutePlan permute;
     int combine_grid;
     // state of the last layout on this buffer (host-side scalars only)
     bool has_layout;
+    bool last_dedup;        // the last dispatch wrote dedupe rows
     int64_t last_T, last_N, last_S;
     int64_t launches;
 };
@@ -100,7 +104,7 @@ struct Carve {
 
 struct Offsets {
     size_t recv_x, recv_scores, recv_src, pos, cnt, expert_offset, rows_per_rank, rank_prefix,
-        tokens_in_rank, tile_cnt, tile_pre, tile_tok, err, total;
+        tokens_in_rank, tile_cnt, tile_pre, tile_tok, tile_tok_pre, tok_pos, tok_src, err, total;
 };
 
 Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, int64_t max_tiles)
@@ -122,6 +126,9 @@ Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, i
     o.tile_cnt = cv.take((size_t)max_tiles * Ep * 4);
     o.tile_pre = cv.take((size_t)max_tiles * Ep * 4);
     o.tile_tok = cv.take((size_t)max_tiles * R * 4);
+    o.tile_tok_pre = cv.take((size_t)max_tiles * R * 4);
+    o.tok_pos = cv.take((size_t)c->num_max_tokens_per_rank * R * 4);
+    o.tok_src = cv.take(R * (size_t)pad4(c->num_max_tokens_per_rank) * 4);
     o.err = cv.take(4);
     o.total = cv.off;
     return o;
@@ -189,6 +196,7 @@ ep::LayoutArgs layout_args(ep_buffer* b, const int32_t* ids, int64_t T, int64_t 
     a.tile_cnt = b->tile_cnt;
     a.tile_pre = b->tile_pre;
     a.tile_tok = b->tile_tok;
+    a.tile_tok_pre = nullptr;
     a.cnt = b->cnt;
     a.expert_offset = b->expert_offset;
     a.rows_per_rank = b->rows_per_rank;
@@ -220,6 +228,7 @@ ep::PermuteArgs permute_args(ep_buffer* b, const void* x, const float* scores)
 void remember_layout(ep_buffer* b, int64_t T, int64_t N)
 {
     b->has_layout = true;
+    b->last_dedup = false;
     b->last_T = T;
     b->last_N = N;
     b->last_S = pad4(N) * b->cfg.topk;
@@ -332,6 +341,9 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     b->tile_cnt = reinterpret_cast<int32_t*>(w + o.tile_cnt);
     b->tile_pre = reinterpret_cast<int32_t*>(w + o.tile_pre);
     b->tile_tok = reinterpret_cast<int32_t*>(w + o.tile_tok);
+    b->tile_tok_pre = reinterpret_cast<int32_t*>(w + o.tile_tok_pre);
+    b->tok_pos = reinterpret_cast<int32_t*>(w + o.tok_pos);
+    b->tok_src = reinterpret_cast<int32_t*>(w + o.tok_src);
     b->err = reinterpret_cast<uint32_t*>(w + o.err);
 
     const int impl = cfg->permute_impl == EP_PERMUTE_DEFAULT ? EP_PERMUTE_BULK : cfg->permute_impl;
@@ -496,6 +508,75 @@ ep_status ep_dispatch_backward(ep_buffer* buf, const void* grad_recv_x,
     if (ep::launch_combine(a, buf->combine_grid, opts(buf, as_stream(stream))) != cudaSuccess)
         return EP_ERR_CUDA;
     return EP_OK;
+}
+
+ep::DedupArgs dedup_args(ep_buffer* b, const void* x, const float* scores, const int32_t* ids,
+                         int64_t T, int64_t N)
+{
+    ep::DedupArgs a;
+    a.x = x;
+    a.scores = scores;
+    a.ids = ids;
+    a.T = T;
+    a.K = b->cfg.topk;
+    a.E = b->cfg.num_experts;
+    a.R = b->cfg.num_ranks;
+    a.P = pad4(N);
+    a.row_bytes = b->row_bytes;
+    a.recv_x = b->recv_x;
+    a.recv_tok_src = b->tok_src;
+    a.recv_topk_idx = b->recv_src;     // the per-expert sources' region holds R*P*K ints
+    a.recv_topk_w = b->recv_scores;    // and the scores' region R*P*K floats
+    a.tok_pos = b->tok_pos;
+    a.err = b->err;
+    return a;
+}
+
+ep_status ep_dispatch_dedup(ep_buffer* buf, const void* x, const float* scores, const int32_t* ids,
+                            int64_t T, int64_t N, ep_stream_t stream, ep_dedup_out* out)
+{
+    ep_status st = check_call(buf, ids, T, N);
+    if (st != EP_OK) return st;
+    if (T > 0 && (!x || !scores)) return EP_ERR_INVALID_ARG;
+    if (!is_aligned(x, 16) || !is_aligned(scores, 4)) return EP_ERR_ALIGNMENT;
+    cudaStream_t s = as_stream(stream);
+    ep::LayoutArgs la = layout_args(buf, ids, T, N);
+    la.tile_tok_pre = buf->tile_tok_pre;
+    const ep::LaunchOpts o = opts(buf, s);
+    if (ep::launch_layout(la, o) != cudaSuccess) return EP_ERR_CUDA;
+    remember_layout(buf, T, N);
+    if (ep::launch_dedup(la, dedup_args(buf, x, scores, ids, T, N), o) != cudaSuccess)
+        return EP_ERR_CUDA;
+    buf->last_dedup = true;
+    if (out) {
+        out->recv_x = buf->recv_x;
+        out->recv_tok_src = buf->tok_src;
+        out->recv_topk_idx = buf->recv_src;
+        out->recv_topk_w = buf->recv_scores;
+        out->tok_pos = buf->tok_pos;
+        out->rows_per_rank_stride = pad4(N);
+        fill_layout(buf, &out->layout);
+    }
+    return EP_OK;
+}
+
+ep_status ep_dedup_expand(ep_buffer* buf, const int32_t* ids, void* y_recv, ep_stream_t stream)
+{
+    if (!buf) return EP_ERR_INVALID_ARG;
+    if (!buf->has_layout || !buf->last_dedup) return EP_ERR_NO_LAYOUT;
+    if (buf->last_T > 0 && (!ids || !y_recv)) return EP_ERR_INVALID_ARG;
+    if (!is_aligned(ids, 4) || !is_aligned(y_recv, 16)) return EP_ERR_ALIGNMENT;
+    // y_recv must not overlap the workspace that holds the dedupe rows.
+    const uint8_t* y0 = static_cast<const uint8_t*>(y_recv);
+    const uint8_t* w0 = buf->recv_x;
+    const uint8_t* w1 = reinterpret_cast<const uint8_t*>(buf->err) + 4;
+    const size_t ybytes = (size_t)buf->cfg.num_ranks * (size_t)buf->last_S * (size_t)buf->row_bytes;
+    if (y0 && y0 < w1 && w0 < y0 + ybytes) return EP_ERR_INVALID_ARG;
+    const ep::DedupArgs a = dedup_args(buf, nullptr, nullptr, ids, buf->last_T, buf->last_N);
+    return ep::launch_dedup_expand(a, buf->pos, y_recv, opts(buf, as_stream(stream))) ==
+                   cudaSuccess
+               ? EP_OK
+               : EP_ERR_CUDA;
 }
 
 ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights, int64_t din,

@@ -63,6 +63,7 @@ struct LayoutArgs {
     int32_t* tile_cnt;         // [tiles][Ep] per-tile expert counts (scratch)
     int32_t* tile_pre;         // [tiles][Ep] exclusive prefix over tiles (scratch)
     int32_t* tile_tok;         // [tiles][R] per-tile distinct-token counts (scratch)
+    int32_t* tile_tok_pre;     // [tiles][R] their exclusive prefix over tiles, or null
     int32_t* cnt;              // [E]
     int32_t* expert_offset;    // [E]
     int32_t* rows_per_rank;    // [R]
@@ -162,6 +163,28 @@ struct CombineBwdArgs {
     bool packed;
 };
 cudaError_t launch_combine_backward(const CombineBwdArgs& a, int grid, const LaunchOpts& o);
+
+// Per-rank dedupe (dedup.cu): one receive row per distinct (token, rank).
+struct DedupArgs {
+    const void* x;             // [T][row_bytes]
+    const float* scores;       // [T][K]
+    const int32_t* ids;        // [T][K]
+    int64_t T;
+    int K, E, R;
+    int64_t P;                 // rows reserved per rank
+    int64_t row_bytes;
+    void* recv_x;              // [R*P][row_bytes]
+    int32_t* recv_tok_src;     // [R*P]
+    int32_t* recv_topk_idx;    // [R*P][K]
+    float* recv_topk_w;        // [R*P][K]
+    int32_t* tok_pos;          // [T][R]
+    uint32_t* err;
+};
+// positions (per layout tile, after launch_layout_counts) + copies.
+cudaError_t launch_dedup(const LayoutArgs& l, const DedupArgs& a, const LaunchOpts& o);
+// y[pos[t][k]] = recv_x[tok_pos[t][r(e)]] for every routed pair.
+cudaError_t launch_dedup_expand(const DedupArgs& a, const int32_t* pos, void* y,
+                                const LaunchOpts& o);
 
 // Expert consumer: grouped GEMM y[p] = x[p] * W_e^T over each expert's rows,
 // driven by the device counts and offsets (expert_gemm.cu).

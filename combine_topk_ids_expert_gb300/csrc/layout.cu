@@ -137,13 +137,16 @@ layout_scan_kernel(LayoutArgs a)
         s_grp[g * Ep + 4 * q + 2] = acc.z;
         s_grp[g * Ep + 4 * q + 3] = acc.w;
     }
-    // Distinct tokens per rank: thread (g2, r) sums rows g2, g2 + NG2, ...
+    // Distinct tokens per rank: thread (g2, r) sums the contiguous rows of row
+    // group g2 of column r.
     const int NG2 = 1024 / a.R;
+    const int RG2 = (G + NG2 - 1) / NG2;
+    const int g2 = tid / a.R, rr = tid % a.R;
+    const int q0 = min(G, g2 * RG2), q1 = min(G, q0 + RG2);
     if (tid < NG2 * a.R) {
-        const int g2 = tid / a.R, r = tid % a.R;
         int s = 0;
 #pragma unroll 4
-        for (int row = g2; row < G; row += NG2) s += __ldcg(a.tile_tok + (int64_t)row * a.R + r);
+        for (int row = q0; row < q1; ++row) s += __ldcg(a.tile_tok + (int64_t)row * a.R + rr);
         s_tok[tid] = s;
     }
     __syncthreads();
@@ -158,12 +161,24 @@ layout_scan_kernel(LayoutArgs a)
             total += v;
         }
     }
-    if (tid < a.R) {
+    if (tid < a.R) {   // exclusive scan of the group sums down column tid
         int s = 0;
-        for (int g2 = 0; g2 < NG2; ++g2) s += s_tok[g2 * a.R + tid];
+        for (int gg = 0; gg < NG2; ++gg) {
+            const int v = s_tok[gg * a.R + tid];
+            s_tok[gg * a.R + tid] = s;
+            s += v;
+        }
         a.tokens_in_rank[tid] = s;
     }
     __syncthreads();
+    if (a.tile_tok_pre && tid < NG2 * a.R) {   // each tile's exclusive prefix per rank
+        int run = s_tok[tid];
+        for (int row = q0; row < q1; ++row) {
+            const int v = __ldcg(a.tile_tok + (int64_t)row * a.R + rr);
+            a.tile_tok_pre[(int64_t)row * a.R + rr] = run;
+            run += v;
+        }
+    }
 
     // Exclusive prefix of every tile row: the group's base plus its earlier rows
     // (from registers when the group fits one chunk, else reloaded).

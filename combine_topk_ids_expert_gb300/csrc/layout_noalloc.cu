@@ -118,6 +118,7 @@ extern "C" ep_status ep_dispatch_layout_noalloc(
     a.tile_pre = reinterpret_cast<int32_t*>(p);
     p += seg(tiles * (size_t)a.Ep * 4);
     a.tile_tok = reinterpret_cast<int32_t*>(p);
+    a.tile_tok_pre = nullptr;
     p += seg(tiles * (size_t)R * 4);
     a.cnt = tokens_per_expert;
     a.expert_offset = expert_offset;

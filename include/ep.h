@@ -149,6 +149,24 @@ typedef struct {
     ep_layout layout;
 } ep_dispatch_out;
 
+/* Result of a per-rank dedupe dispatch: views into the workspace. Rank r owns
+ * rows [r*rows_per_rank_stride, r*rows_per_rank_stride + tokens_in_rank[r]) of
+ * recv_x ([R*P][D], configured dtype), in ascending token order, one row per
+ * distinct (token, rank). recv_tok_src [R*P] is the row's token, recv_topk_idx
+ * [R*P][K] its local expert index on that rank per k (or -1), recv_topk_w
+ * [R*P][K] the score of those pairs (or 0). tok_pos [T][R] is the row of
+ * (t, r) or -1. layout is the same call's per-expert layout. The dedupe rows
+ * share the per-expert receive rows' storage: a later dispatch overwrites them. */
+typedef struct {
+    void* recv_x;
+    int32_t* recv_tok_src;
+    int32_t* recv_topk_idx;
+    float* recv_topk_w;
+    int32_t* tok_pos;
+    int64_t rows_per_rank_stride;   /* P = roundup4(N) */
+    ep_layout layout;
+} ep_dedup_out;
+
 /* Read-only facts about a buffer (for tuning and for counting launches). */
 typedef struct {
     int64_t workspace_bytes;    /* bytes the buffer uses from the workspace */
@@ -255,6 +273,29 @@ EP_API ep_status ep_dispatch_backward(ep_buffer* buf, const void* grad_recv_x,
                                       const float* grad_recv_scores, int64_t num_tokens,
                                       void* grad_x_TD, int32_t grad_x_dtype,
                                       float* grad_scores_TK, ep_stream_t stream);
+
+/* Per-rank dedupe dispatch: each token is sent to each destination rank
+ * once, however many of that rank's experts it selected ([titan] "Backend
+ * behavior": DeepEP's per-rank layout stride; [graph] "Internode": per-rank
+ * token counts on the device), then expanded to experts at the receiver
+ * (ep_dedup_expand). Arguments as ep_dispatch; results in *out (see
+ * ep_dedup_out). Also computes the per-expert layout (counts, offsets,
+ * positions) of the call. On DeepSeek-style routing it writes about 40% of
+ * the rows ep_dispatch writes. */
+EP_API ep_status ep_dispatch_dedup(ep_buffer* buf, const void* x_TD, const float* topk_scores_TK,
+                                   const int32_t* topk_expert_ids_TK, int64_t num_tokens,
+                                   int64_t num_tokens_per_rank, ep_stream_t stream,
+                                   ep_dedup_out* out);
+
+/* The receiver's expansion of the last ep_dispatch_dedup on this buffer into
+ * the per-expert layout: y_recv[pos[t][k]] = dedupe row of (t, rank of
+ * topk_expert_ids_TK[t][k]) for every routed pair; y_recv is [R*S][D] of the
+ * configured dtype, caller-owned, outside the workspace, and then feeds
+ * ep_combine like recv_x. topk_expert_ids_TK must be the dedupe call's ids
+ * (a pair whose rank row is missing raises EP_DEVERR_ROW_OOB and is skipped).
+ * EP_ERR_NO_LAYOUT unless the buffer's last dispatch was ep_dispatch_dedup. */
+EP_API ep_status ep_dedup_expand(ep_buffer* buf, const int32_t* topk_expert_ids_TK, void* y_recv,
+                                 ep_stream_t stream);
 
 /* The expert consumer between dispatch and combine: a grouped GEMM driven by
  * the per-expert counts and offsets that the last layout on this buffer left
