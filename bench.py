@@ -58,6 +58,9 @@ def parse_args():
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
     ap.add_argument("--gemm", type=int, default=0, metavar="DOUT",
                     help="instead: time the expert grouped GEMM (D -> DOUT) on the receive rows")
+    ap.add_argument("--mode", choices=["step", "dedup", "backward"], default="step",
+                    help="step: layout+dispatch+combine (the benchmark); dedup: the per-rank "
+                         "dedupe dispatch alone; backward: combine and dispatch backward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -597,10 +600,97 @@ def run_gemm(args) -> None:
     print(json.dumps(line))
 
 
+def run_aux(args) -> None:
+    """Times a NEXT-row operation (dedupe dispatch, or the backward pass) on the
+    workload's first call, L2 flushed between steps, and prints one JSON line."""
+    import torch
+
+    import combine_topk_ids_expert_gb300 as ep
+    from combine_topk_ids_expert_gb300.build import build as build_lib
+    build_lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = W.WORKLOADS[args.workload]
+    inps, N = step_calls(args, w)
+    inp = inps[0]
+    T, D, K, b = inp["T"], w.D, w.K, w.elem_bytes
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    x = torch.from_numpy(inp["x"].view(np.int16) if w.dtype == "bf16" else inp["x"]).to(dev)
+    x = x.view(tdt)
+    ids = torch.from_numpy(inp["ids"]).to(dev)
+    sc = torch.from_numpy(inp["scores"]).to(dev)
+    n_max = args.tokens if args.tokens > 0 else w.N_max
+    buf = ep.Buffer(n_max, D, w.E, w.R, K, dtype=tdt, device=dev)
+    h = buf.handle
+    row = D * b
+    if args.mode == "dedup":
+        d = buf.dispatch_dedup(x, sc, ids, N)
+        torch.cuda.synchronize(dev)
+        rows = int(d.layout.tokens_in_rank.sum().item())
+        nbytes = T * row + rows * row + T * K * 8 + rows * (4 + 8 * K) + T * w.R * 4
+        metric = "per-rank dedupe dispatch tokens/s (layout + one row per distinct (token, rank))"
+
+        def op():
+            ep.ep_dispatch_dedup(h, x, sc, ids, T, N)
+        extra = {"dedupe_rows": rows, "per_expert_rows": T * K}
+    else:
+        d = buf.dispatch(x, sc, ids, N)
+        g = torch.randn((T, D), device=dev, dtype=torch.float32).to(tdt)
+        gy = torch.empty_like(d.recv_x)
+        gx = torch.empty((T, D), dtype=tdt, device=dev)
+        gs = torch.empty((T, K), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize(dev)
+        pairs = int(d.layout.tokens_per_expert.sum().item())
+        nbytes = (T * row + 2 * pairs * row + T * K * 12) + (pairs * row + T * row + T * K * 4)
+        metric = "combine + dispatch backward tokens/s (grad_y, grad_scores, grad_x)"
+        code = ep.EP_BF16 if tdt == torch.bfloat16 else ep.EP_F32
+
+        def op():
+            ep.ep_combine_backward(h, g, d.recv_x, sc, T, gy, gs)
+            ep.ep_dispatch_backward(h, gy, None, T, gx, code)
+        extra = {"pairs": pairs}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        op()
+    torch.cuda.synchronize(dev)
+    Ks = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(Ks)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    launches0 = buf.info()["kernel_launches"]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record()
+        op()
+        e1.record()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    assert buf.device_error() == 0
+    avg = sum(a.elapsed_time(c) for a, c in ev) / Ks
+    peak, src = measured_peak_hbm()
+    gbs = nbytes / (avg / 1e3) / 1e9
+    line = {"metric": metric, "value": T / (avg / 1e3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": Ks, "warmup": args.warmup, "ms_per_step": avg, "higher_is_better": True,
+            "dtype": w.dtype, "data": "synthetic", "config": workload_desc(w, T, N),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_source": src,
+                         "algorithmic_bytes_per_launch": nbytes},
+            "gpu_launches": buf.info()["kernel_launches"] - launches0, "clocks": clk}
+    line.update(extra)
+    buf.close()
+    print(json.dumps(line))
+
+
 def main():
     args = parse_args()
     if args.gemm and args.impl == "gb300":
         run_gemm(args)
+        return
+    if args.mode != "step" and args.impl == "gb300":
+        run_aux(args)
         return
     world, rank, _ = dist_env()
     w = W.WORKLOADS[args.workload]
