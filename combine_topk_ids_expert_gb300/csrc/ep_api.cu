@@ -26,6 +26,7 @@ struct ep_buffer {
     int64_t max_tiles;      // layout tiles the tables hold
     int ep_stride;          // row stride of the tile tables: roundup4(E)
     bool pdl;               // launch with programmatic dependent launch
+    int tiles_per_sm;       // layout tiles (fused-dispatch CTAs) per SM
     int64_t test_skip_load; // test hook (EP_TEST_SKIP_LOAD), -1 = off
     size_t ws_bytes;
     // carved device pointers
@@ -187,7 +188,7 @@ ep::LayoutArgs layout_args(ep_buffer* b, const int32_t* ids, int64_t T, int64_t 
     a.ids = ids;
     a.T = T;
     a.S = pad4(N) * b->cfg.topk;
-    a.tpt = ep::tokens_per_tile(T, b->cfg.topk, b->num_sms);
+    a.tpt = ep::tokens_per_tile(T, b->cfg.topk, b->num_sms * b->tiles_per_sm);
     a.ntiles = (int)ep::tile_count(T, a.tpt);
     a.K = b->cfg.topk;
     a.E = b->cfg.num_experts;
@@ -323,6 +324,9 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     {
         const char* v = std::getenv("EP_PDL");
         b->pdl = !(v && std::strcmp(v, "0") == 0);
+        // Tuning knob: fused-dispatch CTAs per SM (1 or 2).
+        const char* tps = std::getenv("EP_TILES_PER_SM");
+        b->tiles_per_sm = (tps && std::strcmp(tps, "2") == 0) ? 2 : 1;
         // Test hook: make one bounded wait of the bulk permute run out.
         const char* t = std::getenv("EP_TEST_SKIP_LOAD");
         b->test_skip_load = (t && *t) ? std::strtoll(t, nullptr, 10) : -1;
@@ -347,8 +351,8 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     b->err = reinterpret_cast<uint32_t*>(w + o.err);
 
     const int impl = cfg->permute_impl == EP_PERMUTE_DEFAULT ? EP_PERMUTE_BULK : cfg->permute_impl;
-    if (ep::plan_permute(impl, rb, cfg->topk, cfg->num_experts, b->num_sms, &b->permute) !=
-            cudaSuccess ||
+    if (ep::plan_permute(impl, rb, cfg->topk, cfg->num_experts, b->num_sms, b->tiles_per_sm,
+                         &b->permute) != cudaSuccess ||
         ep::plan_combine(cfg->dtype == EP_BF16 ? 0 : 1, b->num_sms, &b->combine_grid) !=
             cudaSuccess ||
         cudaMemset(b->err, 0, sizeof(uint32_t)) != cudaSuccess ||

@@ -19,7 +19,7 @@ constexpr int kMaxTopk = 64;        // per-token positions staged in shared memo
 constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
 constexpr int kMaxTilePairs = 8192;   // pairs one tile may hold (fused kernel's shared table)
-constexpr int kTileBaseCap = 256;     // tiles per call before large calls add more
+constexpr int kTileBaseCap = 1024;    // tiles per call before large calls add more
 
 inline int round_up4(int e) { return (e + 3) / 4 * 4; }
 
@@ -114,7 +114,9 @@ struct PermutePlan {
     int fused_smem_cap;        // fused layout+permute: max dynamic shared memory per CTA
 };
 // Chooses grids and staging for a row size on the current device.
-cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms,
+// tiles_per_sm: fused-dispatch CTAs sharing an SM (each gets that share of
+// shared memory for its ring).
+cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms, int tiles_per_sm,
                          PermutePlan* plan);
 cudaError_t launch_permute(const PermuteArgs& a, const PermutePlan& plan, const LaunchOpts& o);
 

@@ -285,7 +285,7 @@ int vec_unroll(int64_t row_bytes)
 
 }  // namespace
 
-cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms,
+cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms, int tiles_per_sm,
                          PermutePlan* plan)
 {
     (void)E;
@@ -309,7 +309,9 @@ cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms,
             e = cudaFuncSetAttribute(dispatch_fused_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemCap);
             if (e != cudaSuccess) return e;
-            plan->fused_smem_cap = kFusedSmemCap;
+            // Each fused CTA on an SM gets its share (minus the per-CTA reserve).
+            plan->fused_smem_cap =
+                tiles_per_sm <= 1 ? kFusedSmemCap : (kFusedSmemCap + 1024) / tiles_per_sm - 1536;
             plan->grid = num_sms;
             return cudaSuccess;
         }
