@@ -587,15 +587,34 @@ def run_gemm(args) -> None:
     flops = 2.0 * pairs * w.D * dout
     tf = flops / (avg / 1e3) / 1e12
     peak, src = measured_peak_bf16(sustained=False)
+    # Algorithmic HBM bytes: the weights of every expert that has rows (read at
+    # least once), the routed rows in and their outputs out.
+    used = int((d.layout.tokens_per_expert > 0).sum().item())
+    nbytes = 2 * (used * dout * w.D + pairs * w.D + pairs * dout)
+    bw_peak, bw_src = measured_peak_hbm()
+    floor_tensor = flops / (peak * 1e12) * 1e3
+    floor_hbm = nbytes / (bw_peak * 1e9) * 1e3
+    if floor_tensor >= floor_hbm:
+        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(tf / peak, 4), "peak_source": src}
+    else:
+        gbs = nbytes / (avg / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": bw_peak, "unit": "GB/s",
+                "frac": round(gbs / bw_peak, 4), "peak_source": bw_src,
+                "algorithmic_bytes_per_launch": nbytes}
+    roof["floors_ms"] = {"tensor": round(floor_tensor, 4), "hbm": round(floor_hbm, 4)}
+    info = buf.info()
     line = {"metric": "expert grouped GEMM TFLOP/s (bf16 in, fp32 accumulate, tcgen05)",
             "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
             "ms_per_step": avg, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"{w.name} receive rows ({pairs} routed pairs) x "
                                    f"W[{w.E}, {dout}, {w.D}]",
-                       "rows": pairs, "din": w.D, "dout": dout, "experts": w.E},
-            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_source": src},
-            "gpu_launches": buf.info()["kernel_launches"] - launches0, "clocks": clk}
+                       "rows": pairs, "din": w.D, "dout": dout, "experts": w.E,
+                       "l2": "inputs larger than L2 (weights + rows), no flush"},
+            "roofline": roof,
+            "kernel": {1: "single-CTA tiles", 2: "two-CTA clusters"}.get(info["gemm_kernel"]),
+            "grid": info["gemm_grid"],
+            "gpu_launches": info["kernel_launches"] - launches0, "clocks": clk}
     buf.close()
     print(json.dumps(line))
 

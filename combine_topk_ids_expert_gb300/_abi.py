@@ -96,6 +96,8 @@ class EpBufferInfo(C.Structure):
         ("permute_grid", C.c_int32),
         ("combine_grid", C.c_int32),
         ("bulk_stages", C.c_int32),
+        ("gemm_kernel", C.c_int32),
+        ("gemm_grid", C.c_int32),
     ]
 
 

@@ -27,6 +27,10 @@ struct ep_buffer {
     int ep_stride;          // row stride of the tile tables: roundup4(E)
     bool pdl;               // launch with programmatic dependent launch
     int tiles_per_sm;       // layout tiles (fused-dispatch CTAs) per SM
+    bool gemm_pair;         // expert GEMM may use the 2-CTA cluster kernel
+    int gemm_bk;            // expert GEMM K slice per ring stage (64 or 32)
+    int gemm_kernel;        // last expert GEMM: 0 none, 1 single-CTA, 2 cluster pairs
+    int gemm_grid;
     int64_t test_skip_load; // test hook (EP_TEST_SKIP_LOAD), -1 = off
     size_t ws_bytes;
     // carved device pointers
@@ -327,6 +331,12 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         // Tuning knob: fused-dispatch CTAs per SM (1 or 2).
         const char* tps = std::getenv("EP_TILES_PER_SM");
         b->tiles_per_sm = (tps && std::strcmp(tps, "2") == 0) ? 2 : 1;
+        // Tuning knob: EP_GEMM_PAIR=0 keeps the expert GEMM on single-CTA tiles.
+        const char* gp = std::getenv("EP_GEMM_PAIR");
+        b->gemm_pair = !(gp && std::strcmp(gp, "0") == 0);
+        // Tuning knob: EP_GEMM_BK=32 or 64, the expert GEMM's K slice per stage.
+        const char* bk = std::getenv("EP_GEMM_BK");
+        b->gemm_bk = (bk && std::strcmp(bk, "32") == 0) ? 32 : 64;
         // Test hook: make one bounded wait of the bulk permute run out.
         const char* t = std::getenv("EP_TEST_SKIP_LOAD");
         b->test_skip_load = (t && *t) ? std::strtoll(t, nullptr, 10) : -1;
@@ -596,6 +606,8 @@ ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights
     const int64_t rows = (int64_t)buf->cfg.num_ranks * buf->last_S;
     if (rows <= 0) return EP_OK;
     if ((int64_t)buf->cfg.num_experts * dout > INT32_MAX) return EP_ERR_CAPACITY;
+    // Row tiles times column blocks (and work units) are counted in int32.
+    if ((rows / 128 + buf->cfg.num_experts) * (dout / 128) > INT32_MAX) return EP_ERR_CAPACITY;
     ep::GemmArgs a;
     a.cnt = buf->cnt;
     a.expert_offset = buf->expert_offset;
@@ -603,9 +615,16 @@ ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights
     a.din = din;
     a.dout = dout;
     a.E = buf->cfg.num_experts;
+    a.pair = buf->gemm_pair ? 1 : 0;
+    a.bk = buf->gemm_bk;
     a.err = buf->err;
-    const cudaError_t e =
-        ep::launch_expert_gemm(a, x_recv, rows, weights, buf->num_sms, opts(buf, as_stream(stream)));
+    int kernel = 0, grid = 0;
+    const cudaError_t e = ep::launch_expert_gemm(a, x_recv, rows, weights, buf->num_sms,
+                                                 opts(buf, as_stream(stream)), &kernel, &grid);
+    if (e == cudaSuccess) {
+        buf->gemm_kernel = kernel;
+        buf->gemm_grid = grid;
+    }
     if (e == cudaErrorInvalidValue) return EP_ERR_INVALID_ARG;
     return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
@@ -636,6 +655,8 @@ ep_status ep_buffer_query(const ep_buffer* buf, ep_buffer_info* info)
     info->permute_grid = buf->permute.grid;
     info->combine_grid = buf->combine_grid;
     info->bulk_stages = buf->permute.stages;
+    info->gemm_kernel = buf->gemm_kernel;
+    info->gemm_grid = buf->gemm_grid;
     return EP_OK;
 }
 

@@ -196,11 +196,14 @@ struct GemmArgs {
     void* y;                       // [rows][dout] bf16
     int64_t din, dout;             // din % 64 == 0, dout % 128 == 0
     int E;
+    int pair;                      // allow the 2-CTA cluster kernel (dout % 512 == 0)
+    int bk;                        // K per ring stage: 64 or 32
     uint32_t* err;
 };
 // x: [rows][din] bf16 receive rows; w: [E][dout][din] bf16.
+// kernel_used: 1 single-CTA tiles, 2 two-CTA clusters; grid_used: its CTAs.
 cudaError_t launch_expert_gemm(const GemmArgs& a, const void* x, int64_t rows, const void* w,
-                               int grid, const LaunchOpts& o);
+                               int grid, const LaunchOpts& o, int* kernel_used, int* grid_used);
 
 // Launches kernel with an optional programmatic-dependent-launch attribute.
 template <typename... KArgs, typename... Args>

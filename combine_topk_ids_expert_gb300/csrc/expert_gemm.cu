@@ -7,12 +7,13 @@
 // tile list is derived on the device from the counts.
 //
 // sm_103a tensor cores, written directly:
-//   - one CTA per SM, persistent over tiles of 128 rows x BN output columns
-//     of one expert (tile order: the BN-wide column blocks of one row block
-//     first, so the row block is reused from L2);
-//   - warp 0 (one thread) streams 64-wide K slices of the row block and of
-//     the expert's weights into a 4-stage shared-memory ring with TMA tensor
-//     copies (128-byte swizzle), completion on mbarriers;
+//   - one CTA per SM, persistent over output tiles of 128 rows x BN columns
+//     of one expert (tile order: the column blocks of one row block first,
+//     so the row block is reused from L2);
+//   - warp 0 (one thread) streams BK-wide K slices of the row block and of
+//     the expert's weights into a shared-memory ring with TMA tensor copies
+//     (128-byte swizzle for BK = 64, 64-byte for BK = 32), completion on
+//     mbarriers;
 //   - warp 1 owns two BN-column fp32 accumulators in tensor memory (TMEM)
 //     and one thread issues tcgen05.mma (M=128, N=BN, K=16, bf16 inputs, fp32
 //     accumulate) from shared-memory descriptors, committing each stage back
@@ -20,8 +21,27 @@
 //     between the accumulators so the epilogue overlaps the next tile;
 //   - warps 2-5 read the accumulator with tcgen05.ld (each warp its 32-lane
 //     quarter), round to bf16 and store the rows that belong to the expert.
+//
+// The copies of a stage are issued when the MMAs release its slot and are
+// needed STAGES-1 stages later, so the ring's depth in MMA time must cover
+// the copies' latency. The same shared memory holds 4 stages of BK = 64 or 9
+// of BK = 32: the finer slices buy a third more lookahead.
+//
+// Two-CTA cluster variant (PAIR): the two CTAs of a cluster share one operand
+// tile per slice through TMA multicast, each still computing its own
+// 128 x 256 tile:
+//   - shared weights: row tiles 2i and 2i+1 of one expert, same column block;
+//     each CTA loads its own rows and one half of W's tile, multicast to both;
+//   - shared rows: the last row tile of an expert with an odd count, column
+//     blocks 2j and 2j+1; each CTA loads one half of the row tile, multicast
+//     to both, and its own rows of W.
+// That moves 32 or 40 KB from L2 per SM per 64-wide slice instead of 48. A
+// stage is free again only when both CTAs' MMAs have read it, so each MMA
+// commit arrives on the stage's empty barrier in both CTAs.
+//
 // Every wait is bounded; on a timeout the CTA reports EP_DEVERR_TIMEOUT,
-// waits for its copies and MMAs in flight, frees its TMEM and returns.
+// waits (bounded) for its copies and MMAs in flight, frees its TMEM and
+// returns.
 #include <cuda.h>
 
 #include <mutex>
@@ -32,34 +52,53 @@ namespace ep {
 namespace {
 
 constexpr int kBM = 128;            // rows per tile = TMEM lanes = UMMA M
-constexpr int kBK = 64;             // K per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;          // K per tcgen05.mma for 16-bit inputs
-constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kEpilogueThreads = 128;
+constexpr int kPairBN = 256;
+constexpr uint16_t kBothCtas = 0x3;
+constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_103
 
-template <int BN>
-struct Tile {
-    static constexpr uint32_t kBytesA = kBM * kBK * 2;
-    static constexpr uint32_t kBytesB = BN * kBK * 2;
+// Bytes after the ring: barriers, TMEM address, abort flag and the two
+// per-expert prefix arrays (sized for the largest expert count).
+template <int STAGES>
+constexpr int tail_bytes()
+{
+    return 8 * (2 * STAGES + 5) + 8 + 8 * (kMaxExperts + 1);
+}
+
+template <int BN_, int BK_, int STAGES_, bool PAIR_>
+struct Cfg {
+    static constexpr int BN = BN_, BK = BK_, STAGES = STAGES_;
+    static constexpr bool PAIR = PAIR_;
+    static constexpr uint32_t kBytesA = kBM * BK * 2;
+    static constexpr uint32_t kBytesB = BN * BK * 2;
     static constexpr uint32_t kStageBytes = kBytesA + kBytesB;
     // Instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1), A and
     // B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
     // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                        ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-    // Two accumulators, so the epilogue of one tile overlaps the MMAs of the next.
     static constexpr uint32_t kTmemCols = 2 * BN;
+    // One K slice of a row is one swizzle span: 128 bytes (BK = 64) or 64 (BK = 32).
+    static constexpr uint32_t kSpan = BK * 2;
+    static constexpr uint64_t kSwizzleMode = (BK == 64) ? 2 : 4;   // descriptor: 128B = 2, 64B = 4
+    static constexpr uint32_t kSbo = 8 * kSpan;                     // bytes between 8-row groups
+    static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStageBytes + tail_bytes<STAGES>();
+    static_assert(BK == 64 || BK == 32, "K slice is one 128- or 64-byte swizzle span");
+    static_assert(!PAIR || BN == kPairBN, "pairs use 256-column tiles");
+    static_assert(kSmem <= (size_t)kSmemLimit, "ring does not fit in shared memory");
 };
 
 // Shared-memory matrix descriptor for a K-major tile written by TMA with the
-// 128-byte swizzle: start address >> 4 (bits 0-13), leading offset 16 B
-// (unused for this layout), stride 1024 B between 8-row groups (bits 32-45),
-// descriptor version 1 (bits 46-47), swizzle mode 128B = 2 (bits 61-63).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+// 128- or 64-byte swizzle: start address >> 4 (bits 0-13), leading offset 16 B
+// (unused for these layouts), stride between 8-row groups >> 4 (bits 32-45),
+// descriptor version 1 (bits 46-47), swizzle mode (bits 61-63).
+template <class C>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr)
 {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
-           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+           ((uint64_t)(C::kSbo >> 4) << 32) | ((uint64_t)1 << 46) | (C::kSwizzleMode << 61);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
@@ -69,6 +108,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Multicast: the data and the completion go to the same CTA-relative offsets
+// in every CTA of mask.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                               uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
         : "memory");
 }
 
@@ -123,6 +174,15 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
                  : "memory");
 }
 
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
     asm volatile(
@@ -140,6 +200,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 __device__ __forceinline__ void tmem_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ int cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return (int)r;
+}
+
+__device__ __forceinline__ int cluster_index()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return (int)r;
+}
+
+__device__ __forceinline__ int cluster_count()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return (int)r;
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -165,48 +253,102 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi)
     return r;
 }
 
-// Expert of m-tile number mt: the e with s_mtile[e] <= mt < s_mtile[e+1].
-__device__ __forceinline__ int expert_of(const int* s_mtile, int E, int mt)
+// Index e with pre[e] <= i < pre[e+1] of a non-decreasing prefix (i < pre[E]).
+__device__ __forceinline__ int expert_of(const int* pre, int E, int i)
 {
-    int lo = 0, hi = E;   // invariant: s_mtile[lo] <= mt < s_mtile[hi]
+    int lo = 0, hi = E;   // invariant: pre[lo] <= i < pre[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (s_mtile[mid] <= mt) lo = mid;
+        if (pre[mid] <= i) lo = mid;
         else hi = mid;
     }
     return lo;
 }
 
-template <int BN>
+// Work units of an expert with m row tiles and nbk 256-column blocks (nbk even).
+__host__ __device__ __forceinline__ int pair_units(int m, int nbk)
+{
+    return (m >> 1) * nbk + (m & 1) * (nbk >> 1);
+}
+
+struct TileRef {
+    int e;          // expert
+    int mt;         // row tile within the expert
+    int nb;         // column block
+    bool share_w;   // pairs: W's tile is shared (else the row tile is)
+};
+
+// Tile of work unit u for this CTA. Single CTAs: unit = (global row tile,
+// column block), column blocks fastest. Pairs: see the file comment; r is
+// the CTA's rank in its cluster.
+template <bool PAIR>
+__device__ __forceinline__ TileRef tile_of(const int* s_mtile, const int* s_unit, int E, int nbk,
+                                           int u, int r)
+{
+    TileRef p;
+    if (!PAIR) {
+        const int mt = u / nbk;
+        p.nb = u % nbk;
+        p.e = expert_of(s_mtile, E, mt);
+        p.mt = mt - s_mtile[p.e];
+        p.share_w = false;
+        return p;
+    }
+    p.e = expert_of(s_unit, E, u);
+    const int m = s_mtile[p.e + 1] - s_mtile[p.e];
+    const int v = u - s_unit[p.e];
+    const int w_units = (m >> 1) * nbk;
+    p.share_w = v < w_units;
+    if (p.share_w) {
+        p.mt = 2 * (v / nbk) + r;
+        p.nb = v % nbk;
+    } else {
+        p.mt = m - 1;
+        p.nb = 2 * (v - w_units) + r;
+    }
+    return p;
+}
+
+// tm_a / tm_b: boxes of [128 rows][BK] and [BN rows][BK]; tm_a_half /
+// tm_b_half: the same with half the rows (pairs only).
+template <class C>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_half,
+                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b_half,
                    GemmArgs a)
 {
-    using C = Tile<BN>;
+    constexpr int STAGES = C::STAGES, BN = C::BN, BK = C::BK;
+    constexpr bool PAIR = C::PAIR;
     extern __shared__ uint8_t smem_raw[];
-    // Swizzled tiles want 1024-byte alignment.
+    // Swizzled tiles want 1024-byte alignment; the offset is the same in both
+    // CTAs of a pair (multicast copies and remote arrivals address the peer by
+    // CTA-relative offset).
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     const uint32_t tiles_u32 = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
-    const uint32_t full0 = smem_u32(bars);                 // kStages
-    const uint32_t empty0 = full0 + 8u * kStages;          // kStages
-    const uint32_t accum_full0 = empty0 + 8u * kStages;    // 2: one per accumulator
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+    const uint32_t full0 = smem_u32(bars);                 // STAGES
+    const uint32_t empty0 = full0 + 8u * STAGES;           // STAGES
+    const uint32_t accum_full0 = empty0 + 8u * STAGES;     // 2: one per accumulator
     const uint32_t accum_empty0 = accum_full0 + 16u;       // 2
     const uint32_t drain = accum_empty0 + 16u;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    const int E = a.E;
     int* s_mtile = const_cast<int*>(reinterpret_cast<volatile int*>(s_abort + 1));   // [E + 1]
+    int* s_unit = s_mtile + (E + 1);                                                // [E + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int E = a.E;
-    const int k_iters = (int)(a.din / kBK);
-    const int n_blocks = (int)(a.dout / BN);
+    const int r = PAIR ? cluster_rank() : 0;
+    const int first = PAIR ? cluster_index() : (int)blockIdx.x;
+    const int step = PAIR ? cluster_count() : (int)gridDim.x;
+    const int k_iters = (int)(a.din / BK);
+    const int nbk = (int)(a.dout / BN);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8u * s, 1u);
-            mbar_init(empty0 + 8u * s, 1u);
+            mbar_init(empty0 + 8u * s, PAIR ? 2u : 1u);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accum_full0 + 8u * b, 1u);
@@ -223,76 +365,107 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
 
     griddep_wait();   // counts, offsets and the receive rows come from earlier kernels
 
-    // Prefix over experts of their 128-row tiles (warp 0, 32 experts at a time).
+    // Prefixes over experts of their 128-row tiles and (pairs) work units.
     if (warp == 0) {
-        int carry = 0;
-        if (lane == 0) s_mtile[0] = 0;
+        int carry_m = 0, carry_u = 0;
+        if (lane == 0) {
+            s_mtile[0] = 0;
+            s_unit[0] = 0;
+        }
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
             int m = (e < E) ? (__ldcg(a.cnt + e) + kBM - 1) / kBM : 0;
+            int u = PAIR ? pair_units(m, nbk) : 0;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, m, d);
-                if (lane >= d) m += n;
+                const int nm = __shfl_up_sync(0xffffffffu, m, d);
+                const int nu = __shfl_up_sync(0xffffffffu, u, d);
+                if (lane >= d) {
+                    m += nm;
+                    u += nu;
+                }
             }
-            if (e < E) s_mtile[e + 1] = carry + m;
-            carry += __shfl_sync(0xffffffffu, m, 31);
+            if (e < E) {
+                s_mtile[e + 1] = carry_m + m;
+                s_unit[e + 1] = carry_u + u;
+            }
+            carry_m += __shfl_sync(0xffffffffu, m, 31);
+            carry_u += __shfl_sync(0xffffffffu, u, 31);
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast or remote arrival
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const int total_tiles = s_mtile[E] * n_blocks;
+    const int total = PAIR ? s_unit[E] : s_mtile[E] * nbk;
 
     if (warp == 0 && lane == 0) {
         // ---- TMA producer --------------------------------------------------
         int g = 0;   // k-slices issued
-        for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x) {
-            const int mt = t / n_blocks, nb = t % n_blocks;
-            const int e = expert_of(s_mtile, E, mt);
-            const int row0 = __ldcg(a.expert_offset + e) + (mt - s_mtile[e]) * kBM;
-            const int wrow0 = e * (int)a.dout + nb * BN;
+        for (int u = first; u < total && !*s_abort; u += step) {
+            const TileRef p = tile_of<PAIR>(s_mtile, s_unit, E, nbk, u, r);
+            const int row0 = __ldcg(a.expert_offset + p.e) + p.mt * kBM;
+            const int wrow0 = p.e * (int)a.dout + p.nb * BN;
             for (int k = 0; k < k_iters; ++k, ++g) {
-                const int s = g % kStages;
-                const uint32_t ph = (uint32_t)((g / kStages) & 1);
+                const int s = g % STAGES;
+                const uint32_t ph = (uint32_t)((g / STAGES) & 1);
                 if (!wait_or_abort(empty0 + 8u * s, ph ^ 1u, s_abort)) break;
-                mbar_expect_tx(full0 + 8u * s, C::kStageBytes);
+                const uint32_t fb = full0 + 8u * s;
+                mbar_expect_tx(fb, C::kStageBytes);   // pairs: own copies plus the peer's half
                 const uint32_t sa = tiles_u32 + (uint32_t)s * C::kStageBytes;
-                tma_load_2d(sa, &tm_x, k * kBK, row0, full0 + 8u * s);
-                tma_load_2d(sa + C::kBytesA, &tm_w, k * kBK, wrow0, full0 + 8u * s);
+                const uint32_t sb = sa + C::kBytesA;
+                const int kc = k * BK;
+                if (!PAIR) {
+                    tma_load_2d(sa, &tm_a, kc, row0, fb);
+                    tma_load_2d(sb, &tm_b, kc, wrow0, fb);
+                } else if (p.share_w) {
+                    tma_load_2d(sa, &tm_a, kc, row0, fb);
+                    tma_load_2d_mc(sb + (uint32_t)r * (C::kBytesB / 2), &tm_b_half, kc,
+                                   wrow0 + r * (BN / 2), fb, kBothCtas);
+                } else {
+                    tma_load_2d_mc(sa + (uint32_t)r * (C::kBytesA / 2), &tm_a_half, kc,
+                                   row0 + r * (kBM / 2), fb, kBothCtas);
+                    tma_load_2d(sb, &tm_b, kc, wrow0, fb);
+                }
             }
         }
-        // Let the copies this thread issued land before shared memory goes away.
+        // The copies this thread issued land before shared memory goes away;
+        // for pairs, both CTAs also release those stages, so no multicast copy
+        // or remote arrival is still headed for either CTA.
         const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
-        for (int i = (g > kStages ? g - kStages : 0); i < g; ++i)
-            mbar_wait_until(full0 + 8u * (uint32_t)(i % kStages), (uint32_t)((i / kStages) & 1),
-                            deadline);
+        for (int i = (g > STAGES ? g - STAGES : 0); i < g; ++i) {
+            const uint32_t s = (uint32_t)(i % STAGES), par = (uint32_t)((i / STAGES) & 1);
+            mbar_wait_until(full0 + 8u * s, par, deadline);
+            if (PAIR) mbar_wait_until(empty0 + 8u * s, par, deadline);
+        }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer ----------------------------------------------------
         int g = 0, tl = 0;
         bool issued = false;
-        for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x, ++tl) {
+        for (int u = first; u < total && !*s_abort; u += step, ++tl) {
             const int acc = tl & 1, use = tl >> 1;      // accumulator and its use count
             if (!wait_or_abort(accum_empty0 + 8u * acc, (uint32_t)((use & 1) ^ 1), s_abort)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
             bool ok = true;
             for (int k = 0; k < k_iters; ++k, ++g) {
-                const int s = g % kStages;
-                if (!wait_or_abort(full0 + 8u * s, (uint32_t)((g / kStages) & 1), s_abort)) {
+                const int s = g % STAGES;
+                if (!wait_or_abort(full0 + 8u * s, (uint32_t)((g / STAGES) & 1), s_abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t sa = tiles_u32 + (uint32_t)s * C::kStageBytes;
 #pragma unroll
-                for (int j = 0; j < kBK / kUmmaK; ++j)
-                    umma_bf16(d_tmem, sw128_desc(sa + j * kUmmaK * 2),
-                              sw128_desc(sa + C::kBytesA + j * kUmmaK * 2), C::kIdesc,
+                for (int j = 0; j < BK / kUmmaK; ++j)
+                    umma_bf16(d_tmem, smem_desc<C>(sa + j * kUmmaK * 2),
+                              smem_desc<C>(sa + C::kBytesA + j * kUmmaK * 2), C::kIdesc,
                               (k | j) != 0 ? 1u : 0u);
                 issued = true;
-                umma_commit(empty0 + 8u * s);   // frees the stage once these MMAs finish
+                // Frees the stage once these MMAs finish (in both CTAs of a pair).
+                if (PAIR) umma_commit_mc(empty0 + 8u * s, kBothCtas);
+                else umma_commit(empty0 + 8u * s);
             }
             if (!ok) break;
             umma_commit(accum_full0 + 8u * acc);   // the tile's accumulator is complete
@@ -308,23 +481,22 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         uint16_t* y = static_cast<uint16_t*>(a.y);
         int tl = 0;
-        for (int t = blockIdx.x; t < total_tiles && !*s_abort; t += gridDim.x, ++tl) {
+        for (int u = first; u < total && !*s_abort; u += step, ++tl) {
             const int acc = tl & 1, use = tl >> 1;
             if (!wait_or_abort(accum_full0 + 8u * acc, (uint32_t)(use & 1), s_abort)) break;
             tc_fence_after();
             const uint32_t t_acc = t_lane + (uint32_t)(acc * BN);
-            const int mt = t / n_blocks, nb = t % n_blocks;
-            const int e = expert_of(s_mtile, E, mt);
-            const int m_in = (mt - s_mtile[e]) * kBM;
-            const int rows = min(kBM, __ldcg(a.cnt + e) - m_in);
-            const int64_t row = (int64_t)__ldcg(a.expert_offset + e) + m_in + r_in;
+            const TileRef p = tile_of<PAIR>(s_mtile, s_unit, E, nbk, u, r);
+            const int m_in = p.mt * kBM;
+            const int rows = min(kBM, __ldcg(a.cnt + p.e) - m_in);
+            const int64_t row = (int64_t)__ldcg(a.expert_offset + p.e) + m_in + r_in;
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 uint32_t v[32];
                 tmem_ld32(t_acc + (uint32_t)c, v);
                 tmem_wait_ld();
                 if (r_in < rows) {
-                    int4* dst = reinterpret_cast<int4*>(y + row * a.dout + nb * BN + c);
+                    int4* dst = reinterpret_cast<int4*>(y + row * a.dout + p.nb * BN + c);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         int4 w;
@@ -348,8 +520,20 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+    if (PAIR) cluster_sync();   // neither CTA exits while the other may still address its shared memory
     griddep_launch_dependents();
 }
+
+// Ring depths: as many stages as fit next to the tail (at most 12).
+template <int BN, int BK>
+constexpr int stages_for()
+{
+    const int fit = (kSmemLimit - 1024 - tail_bytes<12>()) / (int)((kBM + BN) * BK * 2);
+    return fit > 12 ? 12 : fit;
+}
+
+template <int BN, int BK, bool PAIR>
+using CfgOf = Cfg<BN, BK, stages_for<BN, BK>(), PAIR>;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -371,52 +555,130 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D bf16 tensor map over [rows][inner] with a box of [box_rows][64] and the
-// 128-byte swizzle the UMMA descriptors expect.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows)
+// 2-D bf16 tensor map over [rows][inner] with a box of [box_rows][bk] and the
+// swizzle the UMMA descriptors expect (one swizzle span per box row).
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+              int bk)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {inner, rows};
     const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)bk, box_rows};
     const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
-size_t gemm_smem_bytes(int E)
+void set_attrs(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, bool pair, bool pdl)
 {
-    return 1024 + (size_t)kStages * Tile<BN>::kStageBytes + 8 * (2 * kStages + 5) + 8 +
-           4 * (size_t)(E + 1);
+    int n = 0;
+    if (pair) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg->attrs = attr;
+    cfg->numAttrs = n;
 }
 
-template <int BN>
-cudaError_t launch_bn(const GemmArgs& a, const void* x, int64_t rows, const void* w, int grid,
-                      const LaunchOpts& o)
+// CTAs of the persistent cluster grid: twice the clusters that fit at once
+// (one CTA per SM), within the SM budget; 0 if no cluster fits.
+template <class C>
+int pair_grid(int num_sms)
 {
-    CUtensorMap tx, tw;
-    if (!make_map(&tx, x, (uint64_t)a.din, (uint64_t)rows, kBM) ||
-        !make_map(&tw, w, (uint64_t)a.din, (uint64_t)a.E * (uint64_t)a.dout, BN))
-        return cudaErrorInvalidValue;
-    const size_t smem = gemm_smem_bytes<BN>(a.E);
-    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::mutex mu;
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int fit = (dev >= 0 && dev < 64) ? cached[dev] : 0;
+    if (fit == 0) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[2];
+        cfg.gridDim = dim3((unsigned)(sms & ~1));
+        cfg.blockDim = dim3(kGemmThreads);
+        cfg.dynamicSmemBytes = C::kSmem;
+        set_attrs(&cfg, attr, true, false);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_kernel<C>, &cfg) != cudaSuccess ||
+            n < 1) {
+            cudaGetLastError();
+            return 0;
+        }
+        fit = 2 * n;
+        if (dev >= 0 && dev < 64) cached[dev] = fit;
+    }
+    const int budget = num_sms & ~1;
+    return fit < budget ? fit : budget;
+}
+
+template <class C>
+cudaError_t launch_cfg(const GemmArgs& a, const void* x, int64_t rows, const void* w, int num_sms,
+                       const LaunchOpts& o, int* grid_used)
+{
+    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(expert_gemm_kernel<BN>, dim3(grid), dim3(kGemmThreads), smem, o, tx, tw, a);
+    int grid = num_sms;
+    if (C::PAIR) {
+        grid = pair_grid<C>(num_sms);
+        if (grid < 2) return cudaErrorNotSupported;
+    }
+    CUtensorMap ta, ta_half, tb, tb_half;
+    const uint64_t wrows = (uint64_t)a.E * (uint64_t)a.dout;
+    if (!make_map(&ta, x, (uint64_t)a.din, (uint64_t)rows, kBM, C::BK) ||
+        !make_map(&ta_half, x, (uint64_t)a.din, (uint64_t)rows, kBM / 2, C::BK) ||
+        !make_map(&tb, w, (uint64_t)a.din, wrows, C::BN, C::BK) ||
+        !make_map(&tb_half, w, (uint64_t)a.din, wrows, C::BN / 2, C::BK))
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = o.stream;
+    set_attrs(&cfg, attr, C::PAIR, o.pdl);
+    e = cudaLaunchKernelEx(&cfg, expert_gemm_kernel<C>, ta, ta_half, tb, tb_half, a);
+    if (e == cudaSuccess && o.launches) ++*o.launches;
+    *grid_used = grid;
+    return e;
+}
+
+template <int BK>
+cudaError_t launch_bk(const GemmArgs& a, const void* x, int64_t rows, const void* w, int grid,
+                      const LaunchOpts& o, int* kernel_used, int* grid_used)
+{
+    if (a.pair && a.dout % (2 * kPairBN) == 0) {
+        *kernel_used = 2;
+        const cudaError_t e = launch_cfg<CfgOf<kPairBN, BK, true>>(a, x, rows, w, grid, o, grid_used);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    *kernel_used = 1;
+    if (a.dout % 256 == 0)
+        return launch_cfg<CfgOf<256, BK, false>>(a, x, rows, w, grid, o, grid_used);
+    return launch_cfg<CfgOf<128, BK, false>>(a, x, rows, w, grid, o, grid_used);
 }
 
 }  // namespace
 
 cudaError_t launch_expert_gemm(const GemmArgs& a, const void* x, int64_t rows, const void* w,
-                               int grid, const LaunchOpts& o)
+                               int grid, const LaunchOpts& o, int* kernel_used, int* grid_used)
 {
-    if (a.din % kBK != 0 || a.dout % 128 != 0) return cudaErrorInvalidValue;
-    if (a.dout % 256 == 0) return launch_bn<256>(a, x, rows, w, grid, o);
-    return launch_bn<128>(a, x, rows, w, grid, o);
+    if (a.din % 64 != 0 || a.dout % 128 != 0) return cudaErrorInvalidValue;
+    if (a.bk == 32) return launch_bk<32>(a, x, rows, w, grid, o, kernel_used, grid_used);
+    return launch_bk<64>(a, x, rows, w, grid, o, kernel_used, grid_used);
 }
 
 }  // namespace ep

@@ -178,6 +178,9 @@ typedef struct {
     int32_t permute_grid;       /* CTAs of the permute kernel */
     int32_t combine_grid;       /* CTAs of the combine kernel */
     int32_t bulk_stages;        /* shared-memory row slots per CTA of the bulk permute */
+    int32_t gemm_kernel;        /* last ep_expert_gemm launch: 0 none, 1 single-CTA tiles,
+                                   2 two-CTA clusters sharing operand tiles by multicast */
+    int32_t gemm_grid;          /* CTAs of that launch */
 } ep_buffer_info;
 
 /* Bytes of device workspace ep_buffer_init needs for this configuration, or 0

@@ -53,11 +53,21 @@ CASES = {
     "packed":       (73, 300, 301, 256, 256, 16, 4, 4, "zipf", "packed"),
     "ds_like":      (74, 1000, 1003, 1024, 512, 32, 8, 8, "zipf", "strided"),
     "many_empty":   (75, 37, 40, 128, 256, 256, 8, 8, "uniform", "strided"),
+    # dout a multiple of 512: two-CTA clusters sharing W's tile (row-tile pairs of
+    # one expert) or the row tile (an expert's odd last row tile)
+    "pair_zipf":    (76, 600, 600, 256, 512, 16, 4, 4, "zipf", "strided"),
+    "pair_packed":  (77, 500, 503, 128, 1024, 8, 2, 2, "uniform", "packed"),
+    "pair_empty":   (78, 37, 40, 64, 512, 256, 8, 8, "uniform", "strided"),
+    "pair_e1024":   (79, 300, 300, 64, 512, 1024, 8, 64, "uniform", "strided"),
+    "pair_big":     (82, 2000, 2000, 512, 2048, 8, 2, 2, "zipf", "strided"),
 }
 
 
+@pytest.mark.parametrize("bk", ["64", "32"])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_expert_gemm_parity(orc, case):
+def test_expert_gemm_parity(orc, monkeypatch, case, bk):
+    # bk: K per ring stage (128-byte swizzle at 64, 64-byte at 32)
+    monkeypatch.setenv("EP_GEMM_BK", bk)
     seed, T, N, din, dout, E, K, R, ik, layout = CASES[case]
     x = W.hidden(seed, T, din, "bf16")
     ids, sc = W.routing(seed, T, E, K, ik, "sigmoid_norm")
@@ -69,9 +79,65 @@ def test_expert_gemm_parity(orc, case):
     buf.expert_gemm(d.recv_x.reshape(R * S, din), to_dev(w), y_recv=y)
     torch.cuda.synchronize()
     assert buf.device_error() == 0
+    assert buf.info()["gemm_kernel"] == (2 if dout % 512 == 0 else 1)
     ref = orc.dispatch(x, sc, ids, N, E, R, packed=(layout == "packed"))
     check_gemm(orc, to_np(y), ref["recv_x"], w, ref["cnt"], ref["expert_offset"])
     buf.close()
+
+
+@pytest.mark.parametrize("name", ["deepseek", "mixtral"])
+def test_gemm_variants_fullsize(orc, monkeypatch, name):
+    # Full workload shape, D -> 2048: single-CTA and two-CTA cluster kernels at
+    # 64- and 32-wide K slices all issue the same MMA sequence per output tile,
+    # so the four agree bit for bit; sampled rows of a few experts are checked
+    # against the oracle.
+    w_ = W.WORKLOADS[name]
+    inp = W.make(name)
+    D, E, dout = w_.D, w_.E, 2048
+    xd, idd, scd = to_dev(inp["x"]), to_dev(inp["ids"]), to_dev(inp["scores"])
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    wd = (torch.randn((E * dout, D), generator=gen, device="cuda") * 0.03).to(torch.bfloat16)
+    bufs, ys = [], []
+    for pair, bk in (("1", "64"), ("0", "64"), ("1", "32"), ("0", "32")):
+        monkeypatch.setenv("EP_GEMM_PAIR", pair)
+        monkeypatch.setenv("EP_GEMM_BK", bk)
+        buf = ep.Buffer(w_.N_max, D, E, w_.R, w_.K, dtype=torch.bfloat16)
+        d = buf.dispatch(xd, scd, idd, w_.N)
+        rows = w_.R * d.layout.rank_stride
+        y = torch.full((rows, dout), SENTINEL, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        buf.expert_gemm(d.recv_x.reshape(rows, D), wd.reshape(E, dout, D), y_recv=y)
+        torch.cuda.synchronize()
+        assert buf.device_error() == 0
+        assert buf.info()["gemm_kernel"] == (2 if pair == "1" else 1)
+        if bufs:
+            buf.close()
+            assert torch.equal(ys[0].view(torch.int16), y.view(torch.int16)), (pair, bk)
+            del d, y
+        else:
+            bufs.append((buf, d))
+            ys.append(y)
+    buf, d = bufs[0]
+    cnt = to_np(d.layout.tokens_per_expert)
+    off = to_np(d.layout.expert_offset)
+    order = np.argsort(-cnt, kind="stable")
+    experts = [int(e) for e in (order[0], order[len(order) // 2], order[-1]) if cnt[e] > 0]
+    xs, ws, cs, y_rows = [], [], [], []
+    for e in experts:
+        n = int(cnt[e])
+        pick = sorted({0, n // 2, n - 1, min(n - 1, 127), min(n - 1, 128)})
+        rows = torch.tensor([int(off[e]) + i for i in pick], device="cuda")
+        xs.append(to_np(d.recv_x.reshape(-1, D)[rows]))
+        y_rows.append(to_np(ys[0][rows]))
+        ws.append(to_np(wd.reshape(E, dout, D)[e]))
+        cs.append(len(pick))
+    cnt_s = np.array(cs, np.int32)
+    off_s = np.concatenate([[0], np.cumsum(cnt_s)[:-1]]).astype(np.int32)
+    check_gemm(orc, np.concatenate(y_rows), np.concatenate(xs), np.stack(ws), cnt_s, off_s)
+    for b, _ in bufs:
+        b.close()
+    del bufs, ys, wd
+    torch.cuda.empty_cache()
 
 
 def test_gemm_output_feeds_combine(orc):
@@ -96,17 +162,20 @@ def test_gemm_output_feeds_combine(orc):
     buf.close()
 
 
-def test_gemm_graph_replay_fresh_routing(orc):
-    # Captured once; each replay's tile list follows that replay's counts.
+@pytest.mark.parametrize("dout,bk", [(128, "64"), (512, "64"), (512, "32")])
+def test_gemm_graph_replay_fresh_routing(orc, monkeypatch, dout, bk):
+    # Captured once; each replay's tile list follows that replay's counts
+    # (dout 512: the two-CTA cluster kernel).
+    monkeypatch.setenv("EP_GEMM_BK", bk)
     T, N, D, E, K, R = 256, 256, 128, 8, 2, 2
     buf = ep.Buffer(N, D, E, R, K, dtype=torch.bfloat16)
     x = W.hidden(90, T, D, "bf16")
-    w = W.hidden(91, E * 128, D, "bf16").reshape(E, 128, D)
+    w = W.hidden(91, E * dout, D, "bf16").reshape(E, dout, D)
     xd, wd = to_dev(x), to_dev(w)
     ids_d = torch.empty((T, K), dtype=torch.int32, device="cuda")
     sc_d = torch.empty((T, K), dtype=torch.float32, device="cuda")
     S = ep.ep_pad_tokens(N) * K
-    y = torch.empty((R * S, 128), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((R * S, dout), dtype=torch.bfloat16, device="cuda")
     ids0, sc0 = W.routing(92, T, E, K, "zipf", "sigmoid_norm")
     ids_d.copy_(torch.from_numpy(ids0))
     sc_d.copy_(torch.from_numpy(sc0))
