@@ -612,7 +612,8 @@ def run_gemm(args) -> None:
                        "rows": pairs, "din": w.D, "dout": dout, "experts": w.E,
                        "l2": "inputs larger than L2 (weights + rows), no flush"},
             "roofline": roof,
-            "kernel": {1: "single-CTA tiles", 2: "two-CTA clusters"}.get(info["gemm_kernel"]),
+            "kernel": {1: "single-CTA 128-row tiles", 2: "two-SM 256-row tiles"}.get(
+                info["gemm_kernel"]),
             "grid": info["gemm_grid"],
             "gpu_launches": info["kernel_launches"] - launches0, "clocks": clk}
     buf.close()

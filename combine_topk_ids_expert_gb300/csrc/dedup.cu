@@ -18,6 +18,7 @@
 //   dedup_expand : a CTA per token; copies each pair's dedupe row to its
 //                  per-expert receive row (the receiver's expansion).
 #include "ep_device.cuh"
+#include "ep_next.cuh"
 
 namespace ep {
 namespace {

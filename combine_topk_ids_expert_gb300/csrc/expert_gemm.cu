@@ -22,22 +22,22 @@
 //   - warps 2-5 read the accumulator with tcgen05.ld (each warp its 32-lane
 //     quarter), round to bf16 and store the rows that belong to the expert.
 //
-// The copies of a stage are issued when the MMAs release its slot and are
-// needed STAGES-1 stages later, so the ring's depth in MMA time must cover
-// the copies' latency. The same shared memory holds 4 stages of BK = 64 or 9
-// of BK = 32: the finer slices buy a third more lookahead.
+// A single-CTA 128 x 256 MMA reads 12 KB of operands from shared memory per
+// K=16 step, and at that rate the MMAs alone run well below the tensor
+// cores' peak (measured: 1.46 PFLOP/s with the copies switched off).
 //
-// Two-CTA cluster variant (PAIR): the two CTAs of a cluster share one operand
-// tile per slice through TMA multicast, each still computing its own
-// 128 x 256 tile:
-//   - shared weights: row tiles 2i and 2i+1 of one expert, same column block;
-//     each CTA loads its own rows and one half of W's tile, multicast to both;
-//   - shared rows: the last row tile of an expert with an odd count, column
-//     blocks 2j and 2j+1; each CTA loads one half of the row tile, multicast
-//     to both, and its own rows of W.
-// That moves 32 or 40 KB from L2 per SM per 64-wide slice instead of 48. A
-// stage is free again only when both CTAs' MMAs have read it, so each MMA
-// commit arrives on the stage's empty barrier in both CTAs.
+// Two-SM variant (PAIR, the default where dout % 256 == 0): a cluster of two
+// CTAs computes 256 x 256 tiles with tcgen05.mma.cta_group::2 (M = 256):
+//   - CTA r holds rows [128r, 128r + 128) of the tile and the W rows
+//     [128r, 128r + 128) of the column block, so each SM reads 8 KB per K=16
+//     step and takes 32 KB per 64-wide slice into shared memory instead of 48;
+//   - both CTAs' TMA copies complete on the leader's (rank 0) full barrier;
+//     the leader's one MMA thread issues for both SMs, and its commits arrive
+//     on both CTAs' barriers (stage release, accumulator ready);
+//   - each CTA's epilogue drains its own TMEM (its 128 rows x 256 columns) and
+//     tells the leader, which reuses an accumulator only after both have.
+// Tiles cover 256 rows of one expert, so an expert's last tile is padded to
+// 256 rows instead of 128.
 //
 // Every wait is bounded; on a timeout the CTA reports EP_DEVERR_TIMEOUT,
 // waits (bounded) for its copies and MMAs in flight, frees its TMEM and
@@ -47,6 +47,7 @@
 #include <mutex>
 
 #include "ep_device.cuh"
+#include "ep_next.cuh"
 
 namespace ep {
 namespace {
@@ -54,32 +55,36 @@ namespace {
 constexpr int kBM = 128;            // rows per tile = TMEM lanes = UMMA M
 constexpr int kUmmaK = 16;          // K per tcgen05.mma for 16-bit inputs
 constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr int kEpilogueThreads = 128;
 constexpr int kPairBN = 256;
 constexpr uint16_t kBothCtas = 0x3;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_103
 
-// Bytes after the ring: barriers, TMEM address, abort flag and the two
-// per-expert prefix arrays (sized for the largest expert count).
+// Bytes after the ring: barriers, TMEM address, abort flag and the
+// per-expert tile prefix (sized for the largest expert count).
 template <int STAGES>
 constexpr int tail_bytes()
 {
-    return 8 * (2 * STAGES + 5) + 8 + 8 * (kMaxExperts + 1);
+    return 8 * (2 * STAGES + 5) + 8 + 4 * (kMaxExperts + 1);
 }
 
 template <int BN_, int BK_, int STAGES_, bool PAIR_>
 struct Cfg {
     static constexpr int BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr bool PAIR = PAIR_;
+    static constexpr int kTileRows = PAIR ? 2 * kBM : kBM;          // rows of one work unit
+    static constexpr int kRowsB = PAIR ? BN / 2 : BN;               // W rows this CTA holds
     static constexpr uint32_t kBytesA = kBM * BK * 2;
-    static constexpr uint32_t kBytesB = BN * BK * 2;
-    static constexpr uint32_t kStageBytes = kBytesA + kBytesB;
+    static constexpr uint32_t kBytesB = kRowsB * BK * 2;
+    static constexpr uint32_t kStageBytes = kBytesA + kBytesB;      // per CTA
     // Instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1), A and
     // B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
-    // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+    // N >> 3 at bits 17-22, M >> 4 at bits 24-28 (M = 256 across a pair).
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                       ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-    static constexpr uint32_t kTmemCols = 2 * BN;
+                                       ((uint32_t)(BN >> 3) << 17) |
+                                       ((uint32_t)(kTileRows >> 4) << 24);
+    static constexpr uint32_t kTmemCols = 2 * BN;                   // two accumulators per CTA
+    // Epilogue warps that release an accumulator (both CTAs for a pair).
+    static constexpr uint32_t kReleaseCount = PAIR ? 8u : 4u;
     // One K slice of a row is one swizzle span: 128 bytes (BK = 64) or 64 (BK = 32).
     static constexpr uint32_t kSpan = BK * 2;
     static constexpr uint64_t kSwizzleMode = (BK == 64) ? 2 : 4;   // descriptor: 128B = 2, 64B = 4
@@ -111,16 +116,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         : "memory");
 }
 
-// Multicast: the data and the completion go to the same CTA-relative offsets
-// in every CTA of mask.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
-                                               uint32_t bar, uint16_t mask)
+// Pair form: the data lands in this CTA's shared memory, the completion on an
+// mbarrier that may be the peer's (bar: a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, int c0,
+                                                 int c1, uint32_t bar)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2 "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
+}
+
+// shared::cluster address of the same offset in CTA rank of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, int rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
@@ -138,49 +158,91 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// tcgen05 allocation, MMA and commit; a kernel uses one CTA group throughout
+// (PAIR: cta_group::2, issued for both CTAs of the pair).
+template <bool PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
+    if (PAIR)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         dst_smem),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         dst_smem),
+                     "r"(ncols)
+                     : "memory");
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void tmem_relinquish()
 {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (PAIR) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                     "r"(ncols)
+                     : "memory");
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
+// Arrives on bar once the MMAs issued so far finish; PAIR: on bar in both CTAs.
+template <bool PAIR>
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
+    if (PAIR)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+            "[%0], %1;" ::"r"(bar),
+            "h"(kBothCtas)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
 }
 
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask)
+// Arrives on this CTA's bar only.
+template <bool PAIR>
+__device__ __forceinline__ void umma_commit_local(uint32_t bar)
 {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-        "[%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
+    if (PAIR)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
@@ -265,182 +327,144 @@ __device__ __forceinline__ int expert_of(const int* pre, int E, int i)
     return lo;
 }
 
-// Work units of an expert with m row tiles and nbk 256-column blocks (nbk even).
-__host__ __device__ __forceinline__ int pair_units(int m, int nbk)
-{
-    return (m >> 1) * nbk + (m & 1) * (nbk >> 1);
-}
-
 struct TileRef {
-    int e;          // expert
-    int mt;         // row tile within the expert
-    int nb;         // column block
-    bool share_w;   // pairs: W's tile is shared (else the row tile is)
+    int e;    // expert
+    int mt;   // row tile (of kTileRows rows) within the expert
+    int nb;   // column block
 };
 
-// Tile of work unit u for this CTA. Single CTAs: unit = (global row tile,
-// column block), column blocks fastest. Pairs: see the file comment; r is
-// the CTA's rank in its cluster.
-template <bool PAIR>
-__device__ __forceinline__ TileRef tile_of(const int* s_mtile, const int* s_unit, int E, int nbk,
-                                           int u, int r)
+// Work unit u = (global row tile, column block), column blocks fastest.
+__device__ __forceinline__ TileRef tile_of(const int* s_mtile, int E, int nbk, int u)
 {
     TileRef p;
-    if (!PAIR) {
-        const int mt = u / nbk;
-        p.nb = u % nbk;
-        p.e = expert_of(s_mtile, E, mt);
-        p.mt = mt - s_mtile[p.e];
-        p.share_w = false;
-        return p;
-    }
-    p.e = expert_of(s_unit, E, u);
-    const int m = s_mtile[p.e + 1] - s_mtile[p.e];
-    const int v = u - s_unit[p.e];
-    const int w_units = (m >> 1) * nbk;
-    p.share_w = v < w_units;
-    if (p.share_w) {
-        p.mt = 2 * (v / nbk) + r;
-        p.nb = v % nbk;
-    } else {
-        p.mt = m - 1;
-        p.nb = 2 * (v - w_units) + r;
-    }
+    const int mt = u / nbk;
+    p.nb = u % nbk;
+    p.e = expert_of(s_mtile, E, mt);
+    p.mt = mt - s_mtile[p.e];
     return p;
 }
 
-// tm_a / tm_b: boxes of [128 rows][BK] and [BN rows][BK]; tm_a_half /
-// tm_b_half: the same with half the rows (pairs only).
+// tm_a: box of [128 rows][BK] over the receive rows; tm_b: box of
+// [kRowsB rows][BK] over the weights (half a column block per CTA for pairs).
 template <class C>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_half,
-                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b_half,
+expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    GemmArgs a)
 {
     constexpr int STAGES = C::STAGES, BN = C::BN, BK = C::BK;
     constexpr bool PAIR = C::PAIR;
     extern __shared__ uint8_t smem_raw[];
     // Swizzled tiles want 1024-byte alignment; the offset is the same in both
-    // CTAs of a pair (multicast copies and remote arrivals address the peer by
-    // CTA-relative offset).
+    // CTAs of a pair (the MMA reads the peer's tiles, and copies and arrivals
+    // reach the peer, at the same CTA-relative offsets).
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     const uint32_t tiles_u32 = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
-    const uint32_t full0 = smem_u32(bars);                 // STAGES
+    const uint32_t full0 = smem_u32(bars);                 // STAGES (pairs: the leader's count)
     const uint32_t empty0 = full0 + 8u * STAGES;           // STAGES
     const uint32_t accum_full0 = empty0 + 8u * STAGES;     // 2: one per accumulator
-    const uint32_t accum_empty0 = accum_full0 + 16u;       // 2
+    const uint32_t accum_empty0 = accum_full0 + 16u;       // 2 (pairs: the leader's count)
     const uint32_t drain = accum_empty0 + 16u;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-    const int E = a.E;
     int* s_mtile = const_cast<int*>(reinterpret_cast<volatile int*>(s_abort + 1));   // [E + 1]
-    int* s_unit = s_mtile + (E + 1);                                                // [E + 1]
+    const int E = a.E;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = PAIR ? cluster_rank() : 0;
+    const bool leader = r == 0;
     const int first = PAIR ? cluster_index() : (int)blockIdx.x;
     const int step = PAIR ? cluster_count() : (int)gridDim.x;
     const int k_iters = (int)(a.din / BK);
     const int nbk = (int)(a.dout / BN);
+    // The barriers the MMA thread waits on live in the leader (rank 0).
+    const uint32_t lead_full0 = PAIR ? map_to_rank(full0, 0) : full0;
+    const uint32_t lead_accum_empty0 = PAIR ? map_to_rank(accum_empty0, 0) : accum_empty0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8u * s, 1u);
-            mbar_init(empty0 + 8u * s, PAIR ? 2u : 1u);
+            mbar_init(empty0 + 8u * s, 1u);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accum_full0 + 8u * b, 1u);
-            mbar_init(accum_empty0 + 8u * b, (uint32_t)kEpilogueThreads);
+            mbar_init(accum_empty0 + 8u * b, C::kReleaseCount);
         }
         mbar_init(drain, 1u);
         *s_abort = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<PAIR>(smem_u32(s_tmem), C::kTmemCols);
+        tmem_relinquish<PAIR>();
     }
 
     griddep_wait();   // counts, offsets and the receive rows come from earlier kernels
 
-    // Prefixes over experts of their 128-row tiles and (pairs) work units.
+    // Prefix over experts of their row tiles (kTileRows rows each).
     if (warp == 0) {
-        int carry_m = 0, carry_u = 0;
-        if (lane == 0) {
-            s_mtile[0] = 0;
-            s_unit[0] = 0;
-        }
+        int carry = 0;
+        if (lane == 0) s_mtile[0] = 0;
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
-            int m = (e < E) ? (__ldcg(a.cnt + e) + kBM - 1) / kBM : 0;
-            int u = PAIR ? pair_units(m, nbk) : 0;
+            int m = (e < E) ? (__ldcg(a.cnt + e) + C::kTileRows - 1) / C::kTileRows : 0;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                const int nm = __shfl_up_sync(0xffffffffu, m, d);
-                const int nu = __shfl_up_sync(0xffffffffu, u, d);
-                if (lane >= d) {
-                    m += nm;
-                    u += nu;
-                }
+                const int n = __shfl_up_sync(0xffffffffu, m, d);
+                if (lane >= d) m += n;
             }
-            if (e < E) {
-                s_mtile[e + 1] = carry_m + m;
-                s_unit[e + 1] = carry_u + u;
-            }
-            carry_m += __shfl_sync(0xffffffffu, m, 31);
-            carry_u += __shfl_sync(0xffffffffu, u, 31);
+            if (e < E) s_mtile[e + 1] = carry + m;
+            carry += __shfl_sync(0xffffffffu, m, 31);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast or remote arrival
+    if (PAIR) cluster_sync();   // the peer's barriers exist before any copy or arrival reaches them
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const int total = PAIR ? s_unit[E] : s_mtile[E] * nbk;
+    const int total = s_mtile[E] * nbk;
 
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer --------------------------------------------------
+        // ---- TMA producer (each CTA fills its own ring) --------------------
         int g = 0;   // k-slices issued
         for (int u = first; u < total && !*s_abort; u += step) {
-            const TileRef p = tile_of<PAIR>(s_mtile, s_unit, E, nbk, u, r);
-            const int row0 = __ldcg(a.expert_offset + p.e) + p.mt * kBM;
-            const int wrow0 = p.e * (int)a.dout + p.nb * BN;
+            const TileRef p = tile_of(s_mtile, E, nbk, u);
+            const int row0 = __ldcg(a.expert_offset + p.e) + p.mt * C::kTileRows + r * kBM;
+            const int wrow0 = p.e * (int)a.dout + p.nb * BN + r * C::kRowsB;
             for (int k = 0; k < k_iters; ++k, ++g) {
                 const int s = g % STAGES;
                 const uint32_t ph = (uint32_t)((g / STAGES) & 1);
                 if (!wait_or_abort(empty0 + 8u * s, ph ^ 1u, s_abort)) break;
-                const uint32_t fb = full0 + 8u * s;
-                mbar_expect_tx(fb, C::kStageBytes);   // pairs: own copies plus the peer's half
                 const uint32_t sa = tiles_u32 + (uint32_t)s * C::kStageBytes;
                 const uint32_t sb = sa + C::kBytesA;
                 const int kc = k * BK;
                 if (!PAIR) {
+                    const uint32_t fb = full0 + 8u * s;
+                    mbar_expect_tx(fb, C::kStageBytes);
                     tma_load_2d(sa, &tm_a, kc, row0, fb);
                     tma_load_2d(sb, &tm_b, kc, wrow0, fb);
-                } else if (p.share_w) {
-                    tma_load_2d(sa, &tm_a, kc, row0, fb);
-                    tma_load_2d_mc(sb + (uint32_t)r * (C::kBytesB / 2), &tm_b_half, kc,
-                                   wrow0 + r * (BN / 2), fb, kBothCtas);
                 } else {
-                    tma_load_2d_mc(sa + (uint32_t)r * (C::kBytesA / 2), &tm_a_half, kc,
-                                   row0 + r * (kBM / 2), fb, kBothCtas);
-                    tma_load_2d(sb, &tm_b, kc, wrow0, fb);
+                    // Both CTAs' copies complete on the leader's barrier, which
+                    // expects the bytes of both.
+                    if (leader) mbar_expect_tx(full0 + 8u * s, 2u * C::kStageBytes);
+                    const uint32_t fb = lead_full0 + 8u * s;
+                    tma_load_2d_pair(sa, &tm_a, kc, row0, fb);
+                    tma_load_2d_pair(sb, &tm_b, kc, wrow0, fb);
                 }
             }
         }
-        // The copies this thread issued land before shared memory goes away;
-        // for pairs, both CTAs also release those stages, so no multicast copy
-        // or remote arrival is still headed for either CTA.
+        // The copies this thread issued land before shared memory goes away
+        // (a pair's copies are tracked by the leader's barrier: wait for the
+        // MMAs to release the stages instead).
         const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
         for (int i = (g > STAGES ? g - STAGES : 0); i < g; ++i) {
             const uint32_t s = (uint32_t)(i % STAGES), par = (uint32_t)((i / STAGES) & 1);
-            mbar_wait_until(full0 + 8u * s, par, deadline);
             if (PAIR) mbar_wait_until(empty0 + 8u * s, par, deadline);
+            else mbar_wait_until(full0 + 8u * s, par, deadline);
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer ----------------------------------------------------
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ---- MMA issuer (pairs: the leader's, for both SMs) ----------------
         int g = 0, tl = 0;
         bool issued = false;
         for (int u = first; u < total && !*s_abort; u += step, ++tl) {
@@ -459,25 +483,23 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
                 const uint32_t sa = tiles_u32 + (uint32_t)s * C::kStageBytes;
 #pragma unroll
                 for (int j = 0; j < BK / kUmmaK; ++j)
-                    umma_bf16(d_tmem, smem_desc<C>(sa + j * kUmmaK * 2),
-                              smem_desc<C>(sa + C::kBytesA + j * kUmmaK * 2), C::kIdesc,
-                              (k | j) != 0 ? 1u : 0u);
+                    umma_bf16<PAIR>(d_tmem, smem_desc<C>(sa + j * kUmmaK * 2),
+                                    smem_desc<C>(sa + C::kBytesA + j * kUmmaK * 2), C::kIdesc,
+                                    (k | j) != 0 ? 1u : 0u);
                 issued = true;
-                // Frees the stage once these MMAs finish (in both CTAs of a pair).
-                if (PAIR) umma_commit_mc(empty0 + 8u * s, kBothCtas);
-                else umma_commit(empty0 + 8u * s);
+                umma_commit<PAIR>(empty0 + 8u * s);   // frees the stage (in both CTAs of a pair)
             }
             if (!ok) break;
-            umma_commit(accum_full0 + 8u * acc);   // the tile's accumulator is complete
+            umma_commit<PAIR>(accum_full0 + 8u * acc);   // the tile's accumulator is complete
         }
         if (issued) {   // every MMA this thread issued has finished before TMEM is freed
-            umma_commit(drain);
+            umma_commit_local<PAIR>(drain);
             mbar_wait(drain, 0u);
         }
     } else if (warp >= 2) {
         // ---- epilogue: TMEM -> bf16 -> global ------------------------------
         const int quarter = warp & 3;                  // TMEM lanes this warp may read
-        const int r_in = quarter * 32 + lane;          // accumulator row = tile row
+        const int r_in = quarter * 32 + lane;          // accumulator row = tile row (of this CTA)
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         uint16_t* y = static_cast<uint16_t*>(a.y);
         int tl = 0;
@@ -486,8 +508,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
             if (!wait_or_abort(accum_full0 + 8u * acc, (uint32_t)(use & 1), s_abort)) break;
             tc_fence_after();
             const uint32_t t_acc = t_lane + (uint32_t)(acc * BN);
-            const TileRef p = tile_of<PAIR>(s_mtile, s_unit, E, nbk, u, r);
-            const int m_in = p.mt * kBM;
+            const TileRef p = tile_of(s_mtile, E, nbk, u);
+            const int m_in = p.mt * C::kTileRows + r * kBM;
             const int rows = min(kBM, __ldcg(a.cnt + p.e) - m_in);
             const int64_t row = (int64_t)__ldcg(a.expert_offset + p.e) + m_in + r_in;
 #pragma unroll 1
@@ -508,32 +530,42 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
                     }
                 }
             }
+            // This warp's reads of the accumulator are done: one arrival per
+            // warp on the leader's barrier.
             tc_fence_before();
-            mbar_arrive(accum_empty0 + 8u * acc);
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR) mbar_arrive_cluster(lead_accum_empty0 + 8u * acc);
+                else mbar_arrive(accum_empty0 + 8u * acc);
+            }
         }
     }
 
     if (threadIdx.x == 0 && *s_abort) atomicOr(a.err, kErrTimeout);
     tc_fence_before();
     __syncthreads();
+    // Pairs: the leader's MMAs (which read the peer's shared memory and write
+    // its TMEM) and its arrivals on the peer are done before either CTA frees
+    // TMEM or exits.
+    if (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::kTmemCols);
+        tmem_dealloc<PAIR>(tmem, C::kTmemCols);
     }
-    if (PAIR) cluster_sync();   // neither CTA exits while the other may still address its shared memory
     griddep_launch_dependents();
 }
 
-// Ring depths: as many stages as fit next to the tail (at most 12).
-template <int BN, int BK>
+// Ring depths: as many stages as fit next to the tail (at most 12); a stage
+// holds 128 rows and the CTA's rows_b rows of W.
+template <int ROWS_B, int BK>
 constexpr int stages_for()
 {
-    const int fit = (kSmemLimit - 1024 - tail_bytes<12>()) / (int)((kBM + BN) * BK * 2);
+    const int fit = (kSmemLimit - 1024 - tail_bytes<12>()) / (int)((kBM + ROWS_B) * BK * 2);
     return fit > 12 ? 12 : fit;
 }
 
 template <int BN, int BK, bool PAIR>
-using CfgOf = Cfg<BN, BK, stages_for<BN, BK>(), PAIR>;
+using CfgOf = Cfg<BN, BK, stages_for<(PAIR ? BN / 2 : BN), BK>(), PAIR>;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -636,12 +668,10 @@ cudaError_t launch_cfg(const GemmArgs& a, const void* x, int64_t rows, const voi
         grid = pair_grid<C>(num_sms);
         if (grid < 2) return cudaErrorNotSupported;
     }
-    CUtensorMap ta, ta_half, tb, tb_half;
+    CUtensorMap ta, tb;
     const uint64_t wrows = (uint64_t)a.E * (uint64_t)a.dout;
     if (!make_map(&ta, x, (uint64_t)a.din, (uint64_t)rows, kBM, C::BK) ||
-        !make_map(&ta_half, x, (uint64_t)a.din, (uint64_t)rows, kBM / 2, C::BK) ||
-        !make_map(&tb, w, (uint64_t)a.din, wrows, C::BN, C::BK) ||
-        !make_map(&tb_half, w, (uint64_t)a.din, wrows, C::BN / 2, C::BK))
+        !make_map(&tb, w, (uint64_t)a.din, wrows, C::kRowsB, C::BK))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -650,7 +680,7 @@ cudaError_t launch_cfg(const GemmArgs& a, const void* x, int64_t rows, const voi
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = o.stream;
     set_attrs(&cfg, attr, C::PAIR, o.pdl);
-    e = cudaLaunchKernelEx(&cfg, expert_gemm_kernel<C>, ta, ta_half, tb, tb_half, a);
+    e = cudaLaunchKernelEx(&cfg, expert_gemm_kernel<C>, ta, tb, a);
     if (e == cudaSuccess && o.launches) ++*o.launches;
     *grid_used = grid;
     return e;
@@ -660,7 +690,7 @@ template <int BK>
 cudaError_t launch_bk(const GemmArgs& a, const void* x, int64_t rows, const void* w, int grid,
                       const LaunchOpts& o, int* kernel_used, int* grid_used)
 {
-    if (a.pair && a.dout % (2 * kPairBN) == 0) {
+    if (a.pair && a.dout % kPairBN == 0) {
         *kernel_used = 2;
         const cudaError_t e = launch_cfg<CfgOf<kPairBN, BK, true>>(a, x, rows, w, grid, o, grid_used);
         if (e != cudaErrorNotSupported) return e;

@@ -178,8 +178,8 @@ typedef struct {
     int32_t permute_grid;       /* CTAs of the permute kernel */
     int32_t combine_grid;       /* CTAs of the combine kernel */
     int32_t bulk_stages;        /* shared-memory row slots per CTA of the bulk permute */
-    int32_t gemm_kernel;        /* last ep_expert_gemm launch: 0 none, 1 single-CTA tiles,
-                                   2 two-CTA clusters sharing operand tiles by multicast */
+    int32_t gemm_kernel;        /* last ep_expert_gemm launch: 0 none, 1 single-CTA
+                                   128-row tiles, 2 two-SM 256-row tiles (CTA pairs) */
     int32_t gemm_grid;          /* CTAs of that launch */
 } ep_buffer_info;
 
@@ -314,7 +314,12 @@ EP_API ep_status ep_dedup_expand(ep_buffer* buf, const int32_t* topk_expert_ids_
  * dout % 128 == 0; bf16 buffers only (EP_ERR_INVALID_ARG otherwise). Rows of
  * y_recv that belong to no expert are not written. Summation order inside the
  * tensor cores is the hardware's: results are within the fp32 summation bound
- * of the exact product, not bitwise fixed across GPU models. */
+ * of the exact product, not bitwise fixed across GPU models. Tiles: 256 rows
+ * on an SM pair (tcgen05 cta_group::2) when dout % 256 == 0 and the last call
+ * routed at least 512 rows per expert on average (T * K >= 512 * E), else
+ * 128 rows per SM; both issue the same K order, so they agree bit for bit.
+ * The environment variable EP_GEMM_PAIR=0 or 1, read at ep_buffer_init,
+ * forces one of them. */
 EP_API ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights,
                                 int64_t din, int64_t dout, void* y_recv, ep_stream_t stream);
 

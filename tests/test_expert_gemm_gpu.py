@@ -53,8 +53,8 @@ CASES = {
     "packed":       (73, 300, 301, 256, 256, 16, 4, 4, "zipf", "packed"),
     "ds_like":      (74, 1000, 1003, 1024, 512, 32, 8, 8, "zipf", "strided"),
     "many_empty":   (75, 37, 40, 128, 256, 256, 8, 8, "uniform", "strided"),
-    # dout a multiple of 512: two-CTA clusters sharing W's tile (row-tile pairs of
-    # one expert) or the row tile (an expert's odd last row tile)
+    # more cases on the 2-SM kernel (dout % 256 == 0): 256-row tiles, odd and
+    # even tile counts per expert, empty experts, the packed layout
     "pair_zipf":    (76, 600, 600, 256, 512, 16, 4, 4, "zipf", "strided"),
     "pair_packed":  (77, 500, 503, 128, 1024, 8, 2, 2, "uniform", "packed"),
     "pair_empty":   (78, 37, 40, 64, 512, 256, 8, 8, "uniform", "strided"),
@@ -63,10 +63,12 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("bk", ["64", "32"])
+@pytest.mark.parametrize("pair,bk", [("1", "64"), ("0", "64"), ("1", "32")])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_expert_gemm_parity(orc, monkeypatch, case, bk):
-    # bk: K per ring stage (128-byte swizzle at 64, 64-byte at 32)
+def test_expert_gemm_parity(orc, monkeypatch, case, pair, bk):
+    # pair: 2-SM 256-row tiles (where dout % 256 == 0) or single-CTA 128-row
+    # tiles; bk: K per ring stage (128-byte swizzle at 64, 64-byte at 32)
+    monkeypatch.setenv("EP_GEMM_PAIR", pair)
     monkeypatch.setenv("EP_GEMM_BK", bk)
     seed, T, N, din, dout, E, K, R, ik, layout = CASES[case]
     x = W.hidden(seed, T, din, "bf16")
@@ -79,7 +81,7 @@ def test_expert_gemm_parity(orc, monkeypatch, case, bk):
     buf.expert_gemm(d.recv_x.reshape(R * S, din), to_dev(w), y_recv=y)
     torch.cuda.synchronize()
     assert buf.device_error() == 0
-    assert buf.info()["gemm_kernel"] == (2 if dout % 512 == 0 else 1)
+    assert buf.info()["gemm_kernel"] == (2 if pair == "1" and dout % 256 == 0 else 1)
     ref = orc.dispatch(x, sc, ids, N, E, R, packed=(layout == "packed"))
     check_gemm(orc, to_np(y), ref["recv_x"], w, ref["cnt"], ref["expert_offset"])
     buf.close()
@@ -87,10 +89,10 @@ def test_expert_gemm_parity(orc, monkeypatch, case, bk):
 
 @pytest.mark.parametrize("name", ["deepseek", "mixtral"])
 def test_gemm_variants_fullsize(orc, monkeypatch, name):
-    # Full workload shape, D -> 2048: single-CTA and two-CTA cluster kernels at
-    # 64- and 32-wide K slices all issue the same MMA sequence per output tile,
-    # so the four agree bit for bit; sampled rows of a few experts are checked
-    # against the oracle.
+    # Full workload shape, D -> 2048: the 2-SM kernel (M = 256 across a pair)
+    # and the single-CTA kernel (M = 128), at 64- and 32-wide K slices, issue the
+    # same K=16 steps in the same order for every output, so the four agree bit
+    # for bit; sampled rows of a few experts are checked against the oracle.
     w_ = W.WORKLOADS[name]
     inp = W.make(name)
     D, E, dout = w_.D, w_.E, 2048
@@ -140,6 +142,23 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
     torch.cuda.empty_cache()
 
 
+def test_gemm_tile_choice_follows_rows_per_expert(monkeypatch):
+    # Unforced, 2-SM tiles are used when the last call routed >= 512 rows per
+    # expert on average (T * K >= 512 * E), single-CTA tiles otherwise.
+    monkeypatch.delenv("EP_GEMM_PAIR", raising=False)
+    D, E, K, R = 128, 4, 2, 1
+    w = to_dev(W.hidden(84, E * 256, D, "bf16").reshape(E, 256, D))
+    buf = ep.Buffer(1024, D, E, R, K, dtype=torch.bfloat16)
+    for T, want in ((1024, 2), (1023, 1)):
+        ids, sc = W.routing(85, T, E, K, "uniform", "sigmoid_norm")
+        d = buf.dispatch(to_dev(W.hidden(86, T, D, "bf16")), to_dev(sc), to_dev(ids), T)
+        buf.expert_gemm(d.recv_x, w)
+        torch.cuda.synchronize()
+        assert buf.info()["gemm_kernel"] == want, T
+    assert buf.device_error() == 0
+    buf.close()
+
+
 def test_gemm_output_feeds_combine(orc):
     # layout -> dispatch -> expert GEMM (D -> D) -> combine on the device, as the
     # worst-token page's graph test chains them; combine of the GEMM's output is
@@ -165,7 +184,7 @@ def test_gemm_output_feeds_combine(orc):
 @pytest.mark.parametrize("dout,bk", [(128, "64"), (512, "64"), (512, "32")])
 def test_gemm_graph_replay_fresh_routing(orc, monkeypatch, dout, bk):
     # Captured once; each replay's tile list follows that replay's counts
-    # (dout 512: the two-CTA cluster kernel).
+    # (dout 512: the 2-SM kernel).
     monkeypatch.setenv("EP_GEMM_BK", bk)
     T, N, D, E, K, R = 256, 256, 128, 8, 2, 2
     buf = ep.Buffer(N, D, E, R, K, dtype=torch.bfloat16)
