@@ -62,6 +62,8 @@ def parse_args():
                     help="step: layout+dispatch+combine (the benchmark); dedup: the per-rank "
                          "dedupe dispatch alone; backward: combine and dispatch backward")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph-leg", action="store_true",
+                    help="skip the extra captured-graph timing of the same step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU time spent timing the oracle")
@@ -102,6 +104,17 @@ def algorithmic_bytes(T: int, K: int, D: int, b: int, pairs: int) -> dict:
     #          rows read    out written  pos+score read
     return {"layout": layout, "permute": permute, "combine": combine,
             "step": layout + permute + combine}
+
+
+def quantile(xs, q: float) -> float:
+    """q-quantile of xs by linear interpolation between order statistics."""
+    v = sorted(xs)
+    if not v:
+        return float("nan")
+    f = q * (len(v) - 1)
+    i = int(f)
+    j = min(i + 1, len(v) - 1)
+    return v[i] + (v[j] - v[i]) * (f - i)
 
 
 def measured_peak_hbm() -> tuple[float, str]:
@@ -355,18 +368,20 @@ def run_gb300(args) -> dict | None:
             ep.ep_dispatch(h, xs[i], scs[i], idss[i], Ts[i], N, stream_ptr)
             ep.ep_combine(h, recv_x, scs[i], Ts[i], outs[i], out_code, stream_ptr)
 
-    graph = None
-    if args.graph:
+    def capture():
         step_kernels(sptr)
         torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
+        g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(dev)
         s.wait_stream(stream)
         with torch.cuda.stream(s):
-            with torch.cuda.graph(graph, stream=s):
+            with torch.cuda.graph(g, stream=s):
                 step_kernels(s.cuda_stream)
         stream.wait_stream(s)
         torch.cuda.synchronize(dev)
+        return g
+
+    graph = capture() if args.graph else None
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -421,6 +436,7 @@ def run_gb300(args) -> dict | None:
     peak, peak_src = measured_peak_hbm()
     res = {"ms_per_step": ms_per_step, "value": tok_s,
            "step_ms_median": statistics.median(step_ms),
+           "step_ms_p10": quantile(step_ms, 0.10), "step_ms_p90": quantile(step_ms, 0.90),
            "hbm_gbs_step": nbytes["step"] / (ms_per_step / 1e3) / 1e9,
            "wall_s": wall, "launches": launches, "clocks": clk, "T_step": T_step,
            "calls_per_step": n_calls}
@@ -454,6 +470,35 @@ def run_gb300(args) -> dict | None:
     res["bytes"] = nbytes
     res["pairs"] = sum(pairs)
     res["info"] = buf.info()
+
+    # The same step replayed from a captured CUDA graph (events around each
+    # replay, L2 flushed before each), reported beside the eager timing.
+    if graph is None and not args.no_graph_leg:
+        g = capture()
+        for _ in range(3):
+            flush.zero_()
+            g.replay()
+        Kg = max(3, min(K, 300))
+        evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(Kg)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for a, c in evg:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            c.record(stream)
+        torch.cuda.synchronize(dev)
+        assert buf.device_error() == 0
+        for o, r in zip(outs, ref_outs):
+            assert torch.equal(o.view(raw), r.view(raw)), "graph replays changed the output"
+        gms = [a.elapsed_time(c) for a, c in evg]
+        g_ms = max_over_ranks(sum(gms), world) / Kg
+        res["graph_replay"] = {"steps": Kg, "ms_per_step": g_ms,
+                               "value": replica_throughput(T_step, Kg, sum(gms), world),
+                               "unit": "tokens/s", "median_ms": statistics.median(gms),
+                               "p10_ms": quantile(gms, 0.10), "p90_ms": quantile(gms, 0.90)}
+        del g
 
     # End to end through the public API with host buffers: every call copies its
     # inputs from pinned host memory and its output back, inside the timed region.
@@ -761,12 +806,16 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic", "config": cfg,
             "achieved_hbm_gbs": round(res["hbm_gbs_step"], 1),
-            "hbm_frac_step": round(res["hbm_gbs_step"] / measured_peak_hbm()[0], 4)}
+            "hbm_frac_step": round(res["hbm_gbs_step"] / measured_peak_hbm()[0], 4),
+            "step_ms": {"median": res["step_ms_median"], "p10": res["step_ms_p10"],
+                        "p90": res["step_ms_p90"]}}
     if "roofline" in res:
         line["roofline"] = res["roofline"]
         line["kernels"] = res["kernels"]
     if "e2e" in res:
         line["e2e"] = res["e2e"]
+    if "graph_replay" in res:
+        line["graph_replay"] = res["graph_replay"]
     line["gpu_launches"] = res["launches"]
     line["clocks"] = res["clocks"]
     if not args.no_cpu_baseline:

@@ -11,10 +11,18 @@
 //
 // Kernels (after the layout's count and scan, which also leave each tile's
 // exclusive prefix of distinct tokens per rank):
-//   dedup_pos    : one CTA per layout tile; warp ballots rank each token among
-//                  the tile's tokens that hit rank r, in token order.
-//   dedup_copy   : a CTA per token (grid-stride); the row is loaded once in
-//                  16-byte vectors and stored to each destination rank's row.
+//   dedup_fused  : the default. One CTA (8 warps) per layout tile. Thread 0
+//                  starts bulk async loads of the tile's rows into a shared-
+//                  memory ring before waiting for the scan; then all warps
+//                  compute the tile's per-expert positions (kept for the
+//                  expansion) and each token's dedupe row per rank (warp
+//                  ballots rank the tile's tokens that hit rank r, in token
+//                  order) into shared memory; then warp 0 streams the rows out
+//                  (lane r issues the bulk store for rank r, r + 32) while
+//                  warps 1-7 write sources, local expert indices and scores.
+//   dedup_pos + dedup_copy : the same in two kernels (after the layout's
+//                  positions), for tiles whose tables do not fit in shared
+//                  memory: a CTA per token copies the row in 16-byte vectors.
 //   dedup_expand : a CTA per token; copies each pair's dedupe row to its
 //                  per-expert receive row (the receiver's expansion).
 #include "ep_device.cuh"
@@ -24,6 +32,11 @@ namespace ep {
 namespace {
 
 constexpr int kCopyThreads = 128;
+constexpr int kLag = 4;                            // store groups in flight before a slot is reused
+constexpr int kMaxStages = 32;
+constexpr int kFusedSmemCap = 227 * 1024 - 1024;   // dynamic shared memory of the fused kernel
+
+int slot_bytes_of(int64_t row_bytes) { return (int)((row_bytes + 127) / 128 * 128); }
 
 __device__ __forceinline__ unsigned long long rank_mask(const int32_t* ids, int64_t t, int K,
                                                         int E, int eloc)
@@ -37,13 +50,13 @@ __device__ __forceinline__ unsigned long long rank_mask(const int32_t* ids, int6
     return m;
 }
 
-__global__ void __launch_bounds__(kLayoutThreads)
-dedup_pos_kernel(LayoutArgs l, DedupArgs a)
+// Dedupe row of each (token, rank) of layout tile `tile`: written to
+// a.tok_pos[t][r] and, if s_tok is given, to s_tok[i * R + r] (i = token in the
+// tile); -1 where the token selects none of rank r's experts. s_rbase holds
+// kLayoutWarps * kMaxRanks ints. Ends with __syncthreads.
+__device__ __forceinline__ void tile_dedup_rows(const LayoutArgs& l, const DedupArgs& a, int tile,
+                                                int (*s_rbase)[kMaxRanks], int* s_tok)
 {
-    __shared__ int s_base[kLayoutWarps][kMaxRanks];
-    griddep_wait();
-    griddep_launch_dependents();
-    const int tile = blockIdx.x;
     const int64_t t0 = (int64_t)tile * l.tpt;
     const int64_t t1 = min(l.T, t0 + l.tpt);
     const int n = (int)(t1 - t0);
@@ -54,7 +67,7 @@ dedup_pos_kernel(LayoutArgs l, DedupArgs a)
     const int w_end = min(n, w_begin + seg);
 
     for (int i = threadIdx.x; i < kLayoutWarps * kMaxRanks; i += blockDim.x)
-        s_base[i / kMaxRanks][i % kMaxRanks] = 0;
+        s_rbase[i / kMaxRanks][i % kMaxRanks] = 0;
     __syncthreads();
 
     // Pass 1: tokens of this warp's segment that hit each rank.
@@ -63,7 +76,7 @@ dedup_pos_kernel(LayoutArgs l, DedupArgs a)
         const unsigned long long m = (i < w_end) ? rank_mask(a.ids, t0 + i, a.K, a.E, eloc) : 0ull;
         for (int r = 0; r < R; ++r) {
             const unsigned b = __ballot_sync(0xffffffffu, (m >> r) & 1ull);
-            if (lane == 0) s_base[warp][r] += __popc(b);
+            if (lane == 0) s_rbase[warp][r] += __popc(b);
         }
         __syncwarp();
     }
@@ -75,8 +88,8 @@ dedup_pos_kernel(LayoutArgs l, DedupArgs a)
         const int r = threadIdx.x;
         int base = (int)((int64_t)r * a.P) + __ldcg(l.tile_tok_pre + (int64_t)tile * R + r);
         for (int w = 0; w < kLayoutWarps; ++w) {
-            const int c = s_base[w][r];
-            s_base[w][r] = base;
+            const int c = s_rbase[w][r];
+            s_rbase[w][r] = base;
             base += c;
         }
     }
@@ -90,13 +103,27 @@ dedup_pos_kernel(LayoutArgs l, DedupArgs a)
         for (int r = 0; r < R; ++r) {
             const bool bit = (m >> r) & 1ull;
             const unsigned b = __ballot_sync(0xffffffffu, bit);
-            const int base = s_base[warp][r];
-            if (in) a.tok_pos[(t0 + i) * R + r] = bit ? base + __popc(b & lanemask_lt(lane)) : -1;
+            const int base = s_rbase[warp][r];
+            if (in) {
+                const int q = bit ? base + __popc(b & lanemask_lt(lane)) : -1;
+                a.tok_pos[(t0 + i) * R + r] = q;
+                if (s_tok) s_tok[i * R + r] = q;
+            }
             __syncwarp();
-            if (lane == 0) s_base[warp][r] = base + __popc(b);
+            if (lane == 0) s_rbase[warp][r] = base + __popc(b);
             __syncwarp();
         }
     }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+dedup_pos_kernel(LayoutArgs l, DedupArgs a)
+{
+    __shared__ int s_rbase[kLayoutWarps][kMaxRanks];
+    griddep_wait();
+    griddep_launch_dependents();
+    tile_dedup_rows(l, a, blockIdx.x, s_rbase, nullptr);
 }
 
 template <int U>
@@ -155,6 +182,104 @@ dedup_copy_kernel(DedupArgs a)
             }
         }
         __syncthreads();
+    }
+    griddep_launch_dependents();
+}
+
+// Loads this CTA issued for tokens [from, to) land before its shared memory is
+// released (after a timed-out wait), under one deadline.
+__device__ void drain_ring(uint32_t bar0, int stages, int from, int to)
+{
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    for (int m = from; m < to; ++m)
+        mbar_wait_until(bar0 + 8u * (uint32_t)(m % stages), (uint32_t)((m / stages) & 1), deadline);
+}
+
+// Positions + dedupe rows + copies of one layout tile per CTA (file comment).
+// Shared memory: [stages slots][kLayoutWarps * Ep ints][kLayoutWarps * kMaxRanks
+// ints][tile tokens * R ints].
+__global__ void __launch_bounds__(kLayoutThreads, 1)
+dedup_fused_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kMaxStages];
+    int* s_base = reinterpret_cast<int*>(smem + (size_t)stages * slot_bytes);
+    int (*s_rbase)[kMaxRanks] = reinterpret_cast<int (*)[kMaxRanks]>(s_base + kLayoutWarps * L.Ep);
+    int* s_tok = s_base + kLayoutWarps * L.Ep + kLayoutWarps * kMaxRanks;
+    const int tile = blockIdx.x;
+    const int64_t t0 = (int64_t)tile * L.tpt;
+    const int64_t t1 = min(L.T, t0 + L.tpt);
+    const int n_my = (int)(t1 - t0);
+    const int R = a.R, K = a.K, eloc = a.E / a.R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bytes = static_cast<uint32_t>(a.row_bytes);
+    const uint32_t slot0 = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
+    uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
+    const int n_pro = n_my < stages ? n_my : stages;
+
+    auto issue_load = [&](int i) {
+        const int s = i % stages;
+        const uint32_t bar = bar0 + 8u * s;
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(slot0 + (uint32_t)s * (uint32_t)slot_bytes, x + (t0 + i) * a.row_bytes, bytes, bar);
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(bar0 + 8u * s, 1u);
+        fence_mbar_init();
+        // The rows do not depend on the layout: start them before waiting for it.
+        for (int i = 0; i < n_pro; ++i) issue_load(i);
+    }
+
+    griddep_wait();                                   // counts and offsets are ready
+    tile_positions(L, tile, s_base, L.pos, nullptr);  // per-expert rows, for the expansion
+    tile_dedup_rows(L, a, tile, s_rbase, s_tok);      // ends with __syncthreads
+
+    if (warp == 0) {
+        bool ok = true;
+        int i = 0;
+        for (; i < n_my; ++i) {
+            const int s = i % stages;
+            if (!mbar_wait(bar0 + 8u * s, (uint32_t)((i / stages) & 1))) {
+                ok = false;
+                break;
+            }
+            for (int r = lane; r < R; r += 32) {
+                const int q = s_tok[i * R + r];
+                if (q >= 0)
+                    bulk_s2g(rx + (int64_t)q * a.row_bytes, slot0 + (uint32_t)s * (uint32_t)slot_bytes,
+                             bytes);
+            }
+            bulk_commit();
+            const int j = i - kLag;
+            if (j >= 0 && j + stages < n_my) {
+                bulk_wait_read<kLag>();
+                __syncwarp();
+                if (lane == 0) issue_load(j + stages);
+            }
+        }
+        bulk_wait_all();
+        if (!ok && lane == 0) {
+            atomicOr(a.err, kErrTimeout);
+            int issued_hi = (i - kLag) + stages;   // loads issued for tokens < issued_hi
+            if (issued_hi < n_pro) issued_hi = n_pro;
+            drain_ring(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my);
+        }
+    } else {
+        // Per dedupe row: source token, and per k the local expert index and score.
+        const int per_tok = R * K;
+        for (int j = threadIdx.x - 32; j < n_my * per_tok; j += kLayoutThreads - 32) {
+            const int i = j / per_tok, r = (j / K) % R, k = j % K;
+            const int q = s_tok[i * R + r];
+            if (q < 0) continue;
+            const int64_t t = t0 + i;
+            const int e = valid_id(__ldcg(a.ids + t * K + k), a.E);
+            const bool mine = e >= 0 && e / eloc == r;
+            a.recv_topk_idx[(int64_t)q * K + k] = mine ? e - r * eloc : -1;
+            a.recv_topk_w[(int64_t)q * K + k] = mine ? __ldcg(a.scores + t * K + k) : 0.0f;
+            if (k == 0) a.recv_tok_src[q] = (int32_t)t;
+        }
     }
     griddep_launch_dependents();
 }
@@ -228,6 +353,27 @@ cudaError_t launch_dedup(const LayoutArgs& l, const DedupArgs& a, const LaunchOp
         default:
             return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_dedup_fused(const LayoutArgs& l, const DedupArgs& a, const LaunchOpts& o)
+{
+    if (l.ntiles <= 0 || a.T <= 0) return cudaSuccess;
+    static bool attr_set = false;
+    if (!attr_set) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            dedup_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemCap);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int slot = slot_bytes_of(a.row_bytes);
+    const int64_t fixed =
+        ((int64_t)kLayoutWarps * l.Ep + (int64_t)kLayoutWarps * kMaxRanks + l.tpt * a.R) * 4;
+    int64_t stages = (kFusedSmemCap - fixed) / slot;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (a.row_bytes > (1 << 20) || stages < kLag + 2) return cudaErrorNotSupported;
+    const size_t smem = (size_t)(stages * slot + fixed);
+    return launch_kernel(dedup_fused_kernel, dim3(l.ntiles), dim3(kLayoutThreads), smem, o, l, a,
+                         (int)stages, slot);
 }
 
 cudaError_t launch_dedup_expand(const DedupArgs& a, const int32_t* pos, void* y,

@@ -30,6 +30,7 @@ struct ep_buffer {
     int tiles_per_sm;       // layout tiles (fused-dispatch CTAs) per SM
     int gemm_pair;          // expert GEMM tiles: -1 by routed rows per expert, 0 single, 1 2-SM
     int gemm_bk;            // expert GEMM K slice per ring stage (64 or 32)
+    bool dedup_fused;       // dedupe dispatch in one kernel after the counts
     int gemm_kernel;        // last expert GEMM: 0 none, 1 single-CTA, 2 two-SM
     int gemm_grid;
     int64_t test_skip_load; // test hook (EP_TEST_SKIP_LOAD), -1 = off
@@ -338,6 +339,9 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         // Tuning knob: EP_GEMM_BK=32 or 64, the expert GEMM's K slice per stage.
         const char* bk = std::getenv("EP_GEMM_BK");
         b->gemm_bk = (bk && std::strcmp(bk, "32") == 0) ? 32 : 64;
+        // Tuning knob: EP_DEDUP_FUSED=0 runs the dedupe dispatch as positions + copy kernels.
+        const char* df = std::getenv("EP_DEDUP_FUSED");
+        b->dedup_fused = !(df && std::strcmp(df, "0") == 0);
         // Test hook: make one bounded wait of the bulk permute run out.
         const char* t = std::getenv("EP_TEST_SKIP_LOAD");
         b->test_skip_load = (t && *t) ? std::strtoll(t, nullptr, 10) : -1;
@@ -558,10 +562,18 @@ ep_status ep_dispatch_dedup(ep_buffer* buf, const void* x, const float* scores, 
     ep::LayoutArgs la = layout_args(buf, ids, T, N);
     la.tile_tok_pre = buf->tile_tok_pre;
     const ep::LaunchOpts o = opts(buf, s);
-    if (ep::launch_layout(la, o) != cudaSuccess) return EP_ERR_CUDA;
+    const ep::DedupArgs da = dedup_args(buf, x, scores, ids, T, N);
+    if (ep::launch_layout_counts(la, o) != cudaSuccess) return EP_ERR_CUDA;
     remember_layout(buf, T, N);
-    if (ep::launch_dedup(la, dedup_args(buf, x, scores, ids, T, N), o) != cudaSuccess)
+    const cudaError_t e =
+        buf->dedup_fused ? ep::launch_dedup_fused(la, da, o) : cudaErrorNotSupported;
+    if (e == cudaErrorNotSupported) {
+        if (ep::launch_layout_positions(la, o) != cudaSuccess ||
+            ep::launch_dedup(la, da, o) != cudaSuccess)
+            return EP_ERR_CUDA;
+    } else if (e != cudaSuccess) {
         return EP_ERR_CUDA;
+    }
     buf->last_dedup = true;
     if (out) {
         out->recv_x = buf->recv_x;

@@ -24,8 +24,11 @@ struct DedupArgs {
     int32_t* tok_pos;          // [T][R]
     uint32_t* err;
 };
-// positions (per layout tile, after launch_layout_counts) + copies.
+// positions (per layout tile, after launch_layout) + copies.
 cudaError_t launch_dedup(const LayoutArgs& l, const DedupArgs& a, const LaunchOpts& o);
+// per-expert positions + dedupe rows + copies in one kernel (after
+// launch_layout_counts); cudaErrorNotSupported if a tile's tables do not fit.
+cudaError_t launch_dedup_fused(const LayoutArgs& l, const DedupArgs& a, const LaunchOpts& o);
 // y[pos[t][k]] = recv_x[tok_pos[t][r(e)]] for every routed pair.
 cudaError_t launch_dedup_expand(const DedupArgs& a, const int32_t* pos, void* y,
                                 const LaunchOpts& o);

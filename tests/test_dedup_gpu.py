@@ -22,11 +22,17 @@ CASES = {
     "k1_r1":        (122, 300, 300, 300, 64, "f32", 8, 1, 1, "uniform"),
     "e1024_r64":    (123, 500, 502, 502, 32, "bf16", 1024, 8, 64, "uniform"),
     "tiny_T13":     (124, 13, 16, 32, 64, "f32", 8, 2, 2, "uniform"),
+    "k16_r64_odd":  (125, 3001, 3001, 3100, 40, "bf16", 256, 16, 64, "zipf"),
+    "prefill_like": (126, 32768, 32768, 32768, 64, "bf16", 256, 8, 8, "zipf"),
 }
 
 
+@pytest.mark.parametrize("fused", ["1", "0"])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_dedup_parity_and_expand(orc, case):
+def test_dedup_parity_and_expand(orc, monkeypatch, case, fused):
+    # fused: one kernel after the counts (positions, dedupe rows, bulk copies);
+    # "0": positions, dedupe rows and vector copies as separate kernels
+    monkeypatch.setenv("EP_DEDUP_FUSED", fused)
     seed, T, N, N_max, D, dtype, E, K, R, ik = CASES[case]
     x = W.hidden(seed, T, D, dtype)
     ids, sc = W.routing(seed, T, E, K, ik, "sigmoid_norm")
