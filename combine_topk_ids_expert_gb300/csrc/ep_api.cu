@@ -31,6 +31,9 @@ struct ep_buffer {
     int gemm_pair;          // expert GEMM tiles: -1 by routed rows per expert, 0 single, 1 2-SM
     int gemm_bk;            // expert GEMM K slice per ring stage (64 or 32)
     bool dedup_fused;       // dedupe dispatch in one kernel after the counts
+    bool onepass;           // dispatch as one cooperative kernel where it fits
+    bool coop_pdl;          // cooperative launches take programmatic serialization
+    uint32_t* gbar;         // [2] the one-pass dispatch's grid barrier
     int gemm_kernel;        // last expert GEMM: 0 none, 1 single-CTA, 2 two-SM
     int gemm_grid;
     int64_t test_skip_load; // test hook (EP_TEST_SKIP_LOAD), -1 = off
@@ -111,7 +114,8 @@ struct Carve {
 
 struct Offsets {
     size_t recv_x, recv_scores, recv_src, pos, cnt, expert_offset, rows_per_rank, rank_prefix,
-        tokens_in_rank, tile_cnt, tile_pre, tile_tok, tile_tok_pre, tok_pos, tok_src, err, total;
+        tokens_in_rank, tile_cnt, tile_pre, tile_tok, tile_tok_pre, tok_pos, tok_src, gbar, err,
+        total;
 };
 
 Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, int64_t max_tiles)
@@ -136,7 +140,8 @@ Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, i
     o.tile_tok_pre = cv.take((size_t)max_tiles * R * 4);
     o.tok_pos = cv.take((size_t)c->num_max_tokens_per_rank * R * 4);
     o.tok_src = cv.take(R * (size_t)pad4(c->num_max_tokens_per_rank) * 4);
-    o.err = cv.take(4);
+    o.gbar = cv.take(8);
+    o.err = cv.take(4);   // last: the workspace ends after the error word
     o.total = cv.off;
     return o;
 }
@@ -211,6 +216,7 @@ ep::LayoutArgs layout_args(ep_buffer* b, const int32_t* ids, int64_t T, int64_t 
     a.tokens_in_rank = b->tokens_in_rank;
     a.pos = b->pos;
     a.err = b->err;
+    a.gbar = b->gbar;
     a.packed = b->cfg.layout_mode == EP_LAYOUT_PACKED;
     return a;
 }
@@ -263,6 +269,15 @@ ep_status enqueue_dispatch(ep_buffer* b, const void* x, const float* scores, con
     const ep::LayoutArgs la = layout_args(b, ids, T, N);
     const ep::LaunchOpts o = opts(b, s);
     if (b->permute.impl == EP_PERMUTE_BULK) {
+        if (b->onepass) {
+            const cudaError_t e1 = ep::launch_dispatch_onepass(la, permute_args(b, x, scores),
+                                                               b->permute, o, b->coop_pdl);
+            if (e1 == cudaSuccess) {
+                remember_layout(b, T, N);
+                return EP_OK;
+            }
+            if (e1 != cudaErrorNotSupported) return EP_ERR_CUDA;
+        }
         if (ep::launch_layout_counts(la, o) != cudaSuccess) return EP_ERR_CUDA;
         remember_layout(b, T, N);
         const cudaError_t e = ep::launch_dispatch_fused(la, permute_args(b, x, scores), b->permute, o);
@@ -342,6 +357,9 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         // Tuning knob: EP_DEDUP_FUSED=0 runs the dedupe dispatch as positions + copy kernels.
         const char* df = std::getenv("EP_DEDUP_FUSED");
         b->dedup_fused = !(df && std::strcmp(df, "0") == 0);
+        // Tuning knob: EP_DISPATCH_ONEPASS=0 keeps the dispatch as count + scan + fused.
+        const char* op = std::getenv("EP_DISPATCH_ONEPASS");
+        b->onepass = !(op && std::strcmp(op, "0") == 0);
         // Test hook: make one bounded wait of the bulk permute run out.
         const char* t = std::getenv("EP_TEST_SKIP_LOAD");
         b->test_skip_load = (t && *t) ? std::strtoll(t, nullptr, 10) : -1;
@@ -364,6 +382,8 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     b->tok_pos = reinterpret_cast<int32_t*>(w + o.tok_pos);
     b->tok_src = reinterpret_cast<int32_t*>(w + o.tok_src);
     b->err = reinterpret_cast<uint32_t*>(w + o.err);
+    b->gbar = reinterpret_cast<uint32_t*>(w + o.gbar);
+    b->coop_pdl = ep::probe_cooperative_pdl();
 
     const int impl = cfg->permute_impl == EP_PERMUTE_DEFAULT ? EP_PERMUTE_BULK : cfg->permute_impl;
     if (ep::plan_permute(impl, rb, cfg->topk, cfg->num_experts, b->num_sms, b->tiles_per_sm,
@@ -371,6 +391,7 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         ep::plan_combine(cfg->dtype == EP_BF16 ? 0 : 1, b->num_sms, &b->combine_grid) !=
             cudaSuccess ||
         cudaMemset(b->err, 0, sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(b->gbar, 0, 2 * sizeof(uint32_t)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         delete b;
         return EP_ERR_CUDA;
@@ -656,6 +677,11 @@ ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flag
     if (cudaMemcpyAsync(&v, buf->err, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaMemsetAsync(buf->err, 0, sizeof v, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
+        return EP_ERR_CUDA;
+    // A timed-out grid barrier leaves its arrival count behind: start it over.
+    if ((v & EP_DEVERR_TIMEOUT) &&
+        (cudaMemsetAsync(buf->gbar, 0, 2 * sizeof(uint32_t), s) != cudaSuccess ||
+         cudaStreamSynchronize(s) != cudaSuccess))
         return EP_ERR_CUDA;
     *flags = v;
     return EP_OK;

@@ -163,9 +163,11 @@ __device__ __forceinline__ void bulk_wait_all()
 // 32-pair chunk). Warp w owns the flat pairs [w*seg, w*seg + seg) of the tile,
 // so the order is the flat pair order t*K + k. Called by all kLayoutThreads
 // threads of the block; s_base holds kLayoutWarps * Ep ints. Writes the rows
-// to pos_out (global) and, if s_pos is given, to s_pos[i] (shared).
+// to pos_out (global) and, if s_pos is given, to s_pos[i] (shared). If s_seed
+// is given, s_seed[e] replaces expert_offset[e] + tile_pre[tile][e].
 __device__ __forceinline__ void tile_positions(const LayoutArgs& a, int tile, int* s_base,
-                                               int32_t* pos_out, int* s_pos)
+                                               int32_t* pos_out, int* s_pos,
+                                               const int* s_seed = nullptr)
 {
     const int64_t t0 = (int64_t)tile * a.tpt;
     const int64_t t1 = min(a.T, t0 + a.tpt);
@@ -192,9 +194,10 @@ __device__ __forceinline__ void tile_positions(const LayoutArgs& a, int tile, in
     __syncthreads();
 
     // Exclusive prefix over warps, seeded with the expert's first row and the
-    // counts of all earlier tiles.
+    // counts of all earlier tiles (from s_seed when the caller has them).
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int base = __ldcg(a.expert_offset + e) + __ldcg(a.tile_pre + (int64_t)tile * Ep + e);
+        int base = s_seed ? s_seed[e]
+                          : __ldcg(a.expert_offset + e) + __ldcg(a.tile_pre + (int64_t)tile * Ep + e);
 #pragma unroll
         for (int w = 0; w < kLayoutWarps; ++w) {
             const int c = s_base[w * Ep + e];
@@ -221,6 +224,97 @@ __device__ __forceinline__ void tile_positions(const LayoutArgs& a, int tile, in
         __syncwarp();
     }
     __syncthreads();
+}
+
+// ---- per-tile expert histogram -----------------------------------------------
+//
+// s_hist[e] = pairs of tile `tile` with expert e (e < Ep; zeroed here), s_tok[r]
+// = tokens of the tile with at least one expert on rank r. Full warps walk the
+// tile so every lane takes part in __match_any_sync (equal ids are grouped and
+// one lane per group adds the group size); each thread loads kHistUnroll ids
+// before matching them. Invalid ids count as none and set kErrBadId. Ends
+// with __syncthreads.
+constexpr int kHistUnroll = 4;
+
+__device__ __forceinline__ void tile_histogram(const LayoutArgs& a, int tile, int* s_hist,
+                                               int* s_tok)
+{
+    const int64_t t0 = (int64_t)tile * a.tpt;
+    const int64_t t1 = min(a.T, t0 + a.tpt);
+    const int64_t p0 = t0 * a.K;
+    const int np = (int)((t1 - t0) * a.K);
+    const int lane = threadIdx.x & 31;
+    const int nthr = (int)blockDim.x;
+
+    for (int i = threadIdx.x; i < a.Ep; i += nthr) s_hist[i] = 0;
+    if (threadIdx.x < a.R) s_tok[threadIdx.x] = 0;
+    __syncthreads();
+
+    const int np32 = (np + 31) & ~31;
+    bool bad = false;
+    for (int base = 0; base < np32; base += kHistUnroll * nthr) {
+        int e[kHistUnroll];
+#pragma unroll
+        for (int j = 0; j < kHistUnroll; ++j) {
+            const int i = base + j * nthr + (int)threadIdx.x;
+            const int raw = (i < np) ? __ldcg(a.ids + p0 + i) : -1;
+            e[j] = valid_id(raw, a.E);
+            bad |= (e[j] != raw);
+        }
+#pragma unroll
+        for (int j = 0; j < kHistUnroll; ++j) {
+            const int warp_first = base + j * nthr + ((int)threadIdx.x & ~31);
+            if (warp_first < np32) {
+                const unsigned peers = __match_any_sync(0xffffffffu, e[j]);
+                if (e[j] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[e[j]], __popc(peers));
+            }
+        }
+    }
+    if (bad) atomicOr(a.err, kErrBadId);
+
+    // Distinct tokens per logical rank: one 64-bit rank set per token.
+    const int eloc = a.E / a.R;
+    for (int64_t t = t0 + threadIdx.x; t < t1; t += nthr) {
+        unsigned long long mask = 0ull;
+#pragma unroll 8
+        for (int k = 0; k < a.K; ++k) {
+            const int e = valid_id(__ldcg(a.ids + t * a.K + k), a.E);
+            if (e >= 0) mask |= 1ull << (e / eloc);
+        }
+        while (mask) {
+            atomicAdd(&s_tok[__ffsll((long long)mask) - 1], 1);
+            mask &= mask - 1ull;
+        }
+    }
+    __syncthreads();
+}
+
+// ---- grid barrier ----------------------------------------------------------
+//
+// For a cooperative launch (every CTA resident). bar[0] counts arrivals,
+// bar[1] is the generation; the last arrival resets the count and advances
+// the generation. Called by one thread per CTA after the CTA's writes are
+// fenced; false if the others have not arrived within the wait limit (the
+// count is then left inconsistent: the host resets both words when it reads
+// the timeout bit).
+__device__ __forceinline__ bool grid_barrier(uint32_t* bar, uint32_t n)
+{
+    uint32_t gen, old;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(bar + 1) : "memory");
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(bar) : "memory");
+    if (old == n - 1) {
+        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(bar) : "memory");
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar + 1) : "memory");
+        return true;
+    }
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    while (true) {
+        uint32_t g;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(bar + 1) : "memory");
+        if (g != gen) return true;
+        if (globaltimer_ns() > deadline) return false;
+        __nanosleep(64);
+    }
 }
 
 }  // namespace ep

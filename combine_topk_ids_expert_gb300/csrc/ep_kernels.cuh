@@ -71,6 +71,7 @@ struct LayoutArgs {
     int32_t* tokens_in_rank;   // [R]
     int32_t* pos;              // [T][K]
     uint32_t* err;
+    uint32_t* gbar;            // [2] grid barrier of the one-pass dispatch, or null
     bool packed;               // ranks back to back instead of r*S
 };
 
@@ -125,6 +126,14 @@ cudaError_t launch_permute(const PermuteArgs& a, const PermutePlan& plan, const 
 // fit the fused kernel (then the caller runs positions + permute separately).
 cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
                                   const PermutePlan& plan, const LaunchOpts& o);
+// Layout + positions + permute in one cooperative kernel (count, grid
+// barrier, prefix, positions, copies); cudaErrorNotSupported where a tile does
+// not fit or the tiles cannot all be resident. pdl_ok: cooperative launches
+// accept the programmatic-serialization attribute (probe_cooperative_pdl).
+cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
+                                    const PermutePlan& plan, const LaunchOpts& o, bool pdl_ok);
+// Synchronous: whether a cooperative launch with programmatic serialization runs.
+bool probe_cooperative_pdl();
 
 struct CombineArgs {
     const void* y;             // [R*S][D] of in_dtype

@@ -24,7 +24,6 @@
 namespace ep {
 namespace {
 
-constexpr int kCountUnroll = 4;
 constexpr int kScanRows = 10;   // tile rows a scan thread holds in registers
 
 __global__ void __launch_bounds__(kLayoutThreads)
@@ -35,56 +34,7 @@ layout_count_kernel(LayoutArgs a)
     griddep_wait();
     griddep_launch_dependents();
     const int tile = blockIdx.x;
-    const int64_t t0 = (int64_t)tile * a.tpt;
-    const int64_t t1 = min(a.T, t0 + a.tpt);
-    const int64_t p0 = t0 * a.K;
-    const int np = (int)((t1 - t0) * a.K);
-    const int lane = threadIdx.x & 31;
-
-    for (int i = threadIdx.x; i < a.Ep; i += blockDim.x) s_hist[i] = 0;
-    if (threadIdx.x < a.R) s_tok[threadIdx.x] = 0;
-    __syncthreads();
-
-    // Full warps walk the tile so every lane takes part in __match_any_sync;
-    // each thread loads kCountUnroll ids before matching them.
-    const int np32 = (np + 31) & ~31;
-    bool bad = false;
-    for (int base = 0; base < np32; base += kCountUnroll * kLayoutThreads) {
-        int e[kCountUnroll];
-#pragma unroll
-        for (int j = 0; j < kCountUnroll; ++j) {
-            const int i = base + j * kLayoutThreads + (int)threadIdx.x;
-            const int raw = (i < np) ? __ldcg(a.ids + p0 + i) : -1;
-            e[j] = valid_id(raw, a.E);
-            bad |= (e[j] != raw);
-        }
-#pragma unroll
-        for (int j = 0; j < kCountUnroll; ++j) {
-            const int warp_first = base + j * kLayoutThreads + ((int)threadIdx.x & ~31);
-            if (warp_first < np32) {
-                const unsigned peers = __match_any_sync(0xffffffffu, e[j]);
-                if (e[j] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[e[j]], __popc(peers));
-            }
-        }
-    }
-    if (bad) atomicOr(a.err, kErrBadId);
-
-    // Distinct tokens per logical rank: one 64-bit rank set per token.
-    const int eloc = a.E / a.R;
-    for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
-        unsigned long long mask = 0ull;
-#pragma unroll 8
-        for (int k = 0; k < a.K; ++k) {
-            const int e = valid_id(__ldcg(a.ids + t * a.K + k), a.E);
-            if (e >= 0) mask |= 1ull << (e / eloc);
-        }
-        while (mask) {
-            atomicAdd(&s_tok[__ffsll((long long)mask) - 1], 1);
-            mask &= mask - 1ull;
-        }
-    }
-    __syncthreads();
-
+    tile_histogram(a, tile, s_hist, s_tok);
     for (int e = threadIdx.x; e < a.Ep; e += blockDim.x)
         a.tile_cnt[(int64_t)tile * a.Ep + e] = s_hist[e];
     if (threadIdx.x < a.R) a.tile_tok[(int64_t)tile * a.R + threadIdx.x] = s_tok[threadIdx.x];

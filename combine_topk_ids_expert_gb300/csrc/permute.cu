@@ -34,6 +34,7 @@ constexpr int kBulkLag = 4;            // store groups in flight before a slot i
 constexpr int kBulkMaxStages = 32;
 constexpr int kBulkSmemBudget = 200 * 1024;
 constexpr int kFusedSmemCap = 227 * 1024 - 1024;   // dynamic shared memory of the fused kernel
+constexpr int kOnepassStaticReserve = 2048;         // the one-pass kernel's extra static arrays
 
 int slot_bytes_of(int64_t row_bytes) { return (int)((row_bytes + 127) / 128 * 128); }
 
@@ -189,10 +190,147 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
     griddep_launch_dependents();
 }
 
+// One-pass layout of tile `tile` (dispatch_onepass): this tile's counts, a
+// grid barrier, then every tile's counts summed per expert (before this tile,
+// and in all) and scanned over experts. Leaves s_seed[e] = this tile's first
+// receive row of expert e, s_tot[e] = cnt[e], s_off[e] = expert_offset[e],
+// s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r],
+// s_rank[2][r] = tokens_in_rank[r]. Global writes: this tile's rows of the
+// count tables and the barrier words only, which no earlier kernel in the
+// stream reads. False if the barrier timed out. s_work: kLayoutWarps * Ep ints.
+__device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* s_seed, int* s_tot,
+                               int* s_off, int (*s_rank)[kMaxRanks], int* s_tok, int* s_wsum,
+                               int* s_flag)
+{
+    const int Ep = L.Ep, E = L.E, R = L.R, G = (int)gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    tile_histogram(L, tile, s_tot, s_tok);   // ends with __syncthreads
+    for (int e = threadIdx.x; e < Ep; e += blockDim.x) L.tile_cnt[(int64_t)tile * Ep + e] = s_tot[e];
+    if (threadIdx.x < R) L.tile_tok[(int64_t)tile * R + threadIdx.x] = s_tok[threadIdx.x];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *s_flag = grid_barrier(L.gbar, (uint32_t)G) ? 1 : 0;
+    __syncthreads();
+    if (!*s_flag) return false;
+
+    // Column sums of all tiles' counts: thread (g, q) adds the 4-expert column
+    // q over tiles g, g + NG, ... into s_work[2g][.] (tiles before this one)
+    // and s_work[2g + 1][.] (all tiles).
+    const int Q = Ep / 4;
+    int NG = kLayoutThreads / Q;
+    if (NG > kLayoutWarps / 2) NG = kLayoutWarps / 2;
+    if (NG < 1) NG = 1;
+    const int g = threadIdx.x / Q, q = threadIdx.x % Q;
+    if (g < NG && q < Q) {
+        const int4* tc = reinterpret_cast<const int4*>(L.tile_cnt);
+        int4 bef = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+#pragma unroll 8
+        for (int t = g; t < G; t += NG) {
+            const int4 v = ld_cg_v4(tc + (int64_t)t * Q + q);
+            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+            if (t < tile) {
+                bef.x += v.x; bef.y += v.y; bef.z += v.z; bef.w += v.w;
+            }
+        }
+        int* b = s_work + (2 * g) * Ep + 4 * q;
+        int* a = s_work + (2 * g + 1) * Ep + 4 * q;
+        b[0] = bef.x; b[1] = bef.y; b[2] = bef.z; b[3] = bef.w;
+        a[0] = tot.x; a[1] = tot.y; a[2] = tot.z; a[3] = tot.w;
+    }
+    // Distinct tokens per rank over all tiles: thread (g2, r) adds rows g2, g2 + NG2, ...
+    const int NG2 = kLayoutThreads / R;
+    const int g2 = threadIdx.x / R, r2 = threadIdx.x % R;
+    int tsum = 0;
+    if (g2 < NG2)
+        for (int t = g2; t < G; t += NG2) tsum += __ldcg(L.tile_tok + (int64_t)t * R + r2);
+    __syncthreads();
+    for (int e = threadIdx.x; e < Ep; e += blockDim.x) {
+        int b = 0, a = 0;
+        for (int gg = 0; gg < NG; ++gg) {
+            b += s_work[(2 * gg) * Ep + e];
+            a += s_work[(2 * gg + 1) * Ep + e];
+        }
+        s_seed[e] = b;
+        s_tot[e] = a;
+    }
+    if (threadIdx.x < R) s_rank[2][threadIdx.x] = 0;
+    __syncthreads();
+    if (g2 < NG2 && tsum) atomicAdd(&s_rank[2][r2], tsum);
+
+    // Inclusive prefix of the totals over experts (C consecutive experts per
+    // thread, then warps, then the block) into s_off.
+    const int C = (Ep + kLayoutThreads - 1) / kLayoutThreads;
+    const int e0 = threadIdx.x * C;
+    int run = 0;
+    for (int j = 0; j < C; ++j) {
+        const int e = e0 + j;
+        if (e < E) run += s_tot[e];
+    }
+    int v = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += n;
+    }
+    if (lane == 31) s_wsum[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int c = s_wsum[w];
+            s_wsum[w] = acc;
+            acc += c;
+        }
+    }
+    __syncthreads();
+    int incl = v - run + s_wsum[warp];   // exclusive prefix of this thread's first expert
+    for (int j = 0; j < C; ++j) {
+        const int e = e0 + j;
+        if (e < E) {
+            incl += s_tot[e];
+            s_off[e] = incl;
+        }
+    }
+    __syncthreads();
+
+    // Offsets: ranks own contiguous expert blocks (packed: back to back).
+    const int eloc = E / R;
+    if (threadIdx.x < R) {
+        const int r = threadIdx.x;
+        const int hi = s_off[(r + 1) * eloc - 1];
+        const int lo = (r > 0) ? s_off[r * eloc - 1] : 0;
+        s_rank[0][r] = hi - lo;
+        s_rank[1][r] = hi;
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int excl = s_off[e] - s_tot[e];
+        int off;
+        if (L.packed) {
+            off = excl;
+        } else {
+            const int r = e / eloc;
+            const int lo = (r > 0) ? s_off[r * eloc - 1] : 0;
+            off = (int)((int64_t)r * L.S + (excl - lo));
+        }
+        s_work[e] = off;   // s_off still holds the inclusive prefix other threads read
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        s_off[e] = s_work[e];
+        s_seed[e] += s_work[e];
+    }
+    __syncthreads();
+    return true;
+}
+
 // Positions + permute of one layout tile per CTA (see the file comment).
-// Shared memory: [stages slots of slot_bytes][kLayoutWarps * Ep ints][tile pairs ints].
+// ONEPASS: the layout is computed here too (onepass_layout; launched
+// cooperatively, so every tile's CTA is resident for the grid barrier).
+// Shared memory: [stages slots of slot_bytes][kLayoutWarps * Ep ints][tile pairs
+// ints] (+ ONEPASS: [3 * Ep ints]).
+template <bool ONEPASS>
 __global__ void __launch_bounds__(kLayoutThreads, 1)
-dispatch_fused_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
+dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kBulkMaxStages];
@@ -228,8 +366,42 @@ dispatch_fused_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
         for (int i = 0; i < n_pro; ++i) issue_load(i);
     }
 
-    griddep_wait();                                   // counts and offsets are ready
-    tile_positions(L, tile, s_base, L.pos, s_pos);    // ends with __syncthreads
+    if constexpr (ONEPASS) {
+        __shared__ int s_rank[3][kMaxRanks];
+        __shared__ int s_tok[kMaxRanks];
+        __shared__ int s_wsum[kLayoutWarps];
+        __shared__ int s_flag;
+        const int tile_pairs = (int)(L.tpt * L.K);
+        int* s_seed = s_pos + tile_pairs;
+        int* s_tot = s_seed + L.Ep;
+        int* s_off = s_tot + L.Ep;
+        const bool ok = onepass_layout(L, tile, s_base, s_seed, s_tot, s_off, s_rank, s_tok, s_wsum,
+                                       &s_flag);
+        if (!ok) {   // barrier timed out: report, let this CTA's loads land, leave
+            if (threadIdx.x == 0) {
+                atomicOr(a.err, kErrTimeout);
+                drain_loads(bar0, stages, 0, n_pro, skipped);
+            }
+            griddep_launch_dependents();
+            return;
+        }
+        griddep_wait();   // the previous kernel in the stream may read what follows
+        if (tile == 0) {
+            for (int e = threadIdx.x; e < L.E; e += blockDim.x) {
+                L.cnt[e] = s_tot[e];
+                L.expert_offset[e] = s_off[e];
+            }
+            if (threadIdx.x < L.R) {
+                L.rows_per_rank[threadIdx.x] = s_rank[0][threadIdx.x];
+                L.rank_prefix[threadIdx.x] = s_rank[1][threadIdx.x];
+                L.tokens_in_rank[threadIdx.x] = s_rank[2][threadIdx.x];
+            }
+        }
+        tile_positions(L, tile, s_base, L.pos, s_pos, s_seed);   // ends with __syncthreads
+    } else {
+        griddep_wait();                                   // counts and offsets are ready
+        tile_positions(L, tile, s_base, L.pos, s_pos);    // ends with __syncthreads
+    }
 
     if (warp == 0) {
         bool ok = true;
@@ -306,8 +478,12 @@ cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  plan->smem_bytes);
             if (e != cudaSuccess) return e;
-            e = cudaFuncSetAttribute(dispatch_fused_kernel,
+            e = cudaFuncSetAttribute(dispatch_tile_kernel<false>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemCap);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(dispatch_tile_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kFusedSmemCap - kOnepassStaticReserve);
             if (e != cudaSuccess) return e;
             // Each fused CTA on an SM gets its share (minus the per-CTA reserve).
             plan->fused_smem_cap =
@@ -366,8 +542,79 @@ cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
     if (stages > kBulkMaxStages) stages = kBulkMaxStages;
     if (stages < kBulkLag + 2) return cudaErrorNotSupported;
     const size_t smem = (size_t)(stages * slot + fixed);
-    return launch_kernel(dispatch_fused_kernel, dim3(l.ntiles), dim3(kLayoutThreads), smem, o, l,
-                         p, (int)stages, slot);
+    return launch_kernel(dispatch_tile_kernel<false>, dim3(l.ntiles), dim3(kLayoutThreads), smem, o,
+                         l, p, (int)stages, slot);
+}
+
+cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
+                                    const PermutePlan& plan, const LaunchOpts& o, bool pdl_ok)
+{
+    if (plan.impl != 2 || plan.fused_smem_cap <= 0 || l.K > 32 || !l.gbar || l.ntiles <= 0)
+        return cudaErrorNotSupported;
+    const int64_t tile_pairs = l.tpt * l.K;
+    if (tile_pairs > kMaxTilePairs) return cudaErrorNotSupported;
+    const int slot = slot_bytes_of(p.row_bytes);
+    const int64_t fixed = ((int64_t)kLayoutWarps * l.Ep + tile_pairs + 3 * (int64_t)l.Ep) * 4;
+    int64_t stages = (plan.fused_smem_cap - kOnepassStaticReserve - fixed) / slot;
+    if (stages > kBulkMaxStages) stages = kBulkMaxStages;
+    if (stages < kBulkLag + 2) return cudaErrorNotSupported;
+    const size_t smem = (size_t)(stages * slot + fixed);
+    // Every CTA must be resident at once for the grid barrier.
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_tile_kernel<true>,
+                                                      kLayoutThreads, smem) != cudaSuccess)
+        return cudaErrorNotSupported;
+    if ((int64_t)per_sm * sms < l.ntiles) return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(l.ntiles);
+    cfg.blockDim = dim3(kLayoutThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = o.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (o.pdl && pdl_ok) ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, dispatch_tile_kernel<true>, l, p, (int)stages, slot);
+    if (e == cudaSuccess && o.launches) ++*o.launches;
+    return e;
+}
+
+namespace {
+__global__ void coop_probe_kernel(int* out)
+{
+    if (threadIdx.x == 0 && blockIdx.x == 0 && out) *out = 1;
+}
+}  // namespace
+
+bool probe_cooperative_pdl()
+{
+    int* d = nullptr;
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return false;
+    bool ok = false;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, coop_probe_kernel, d) == cudaSuccess &&
+        cudaLaunchKernelEx(&cfg, coop_probe_kernel, d) == cudaSuccess &&
+        cudaStreamSynchronize(s) == cudaSuccess)
+        ok = true;
+    cudaGetLastError();
+    cudaStreamDestroy(s);
+    return ok;
 }
 
 }  // namespace ep

@@ -192,3 +192,33 @@ def test_bounded_wait_runs_out_and_reports(orc, monkeypatch):
     want, _ = orc.combine(ref["recv_x"], sc, ref["pos"], ref["rank_prefix"], ref["S"], R)
     assert_combine_equal(to_np(out), want)
     good.close()
+
+
+def test_grid_barrier_runs_out_and_recovers(orc):
+    # The one-pass dispatch meets all its CTAs at a grid barrier (two words at
+    # the end of the workspace: arrivals, generation) with a 2 s limit. Seeding
+    # the arrival count past the grid size means no CTA is ever the last to
+    # arrive, so every CTA's wait runs out: the kernel must report
+    # EP_DEVERR_TIMEOUT and return; reading the flag starts the barrier over,
+    # and the next dispatch on the same buffer is oracle-exact.
+    buf = ep.Buffer(64, D, E, R, K, dtype=torch.bfloat16, permute_impl=ep.EP_PERMUTE_BULK)
+    x, ids, sc = small(T=40, seed=9)
+    xd, idd, scd = to_dev(x), to_dev(ids), to_dev(sc)
+    ws = buf.workspace
+    align = 256                      # workspace carve granularity
+    gbar = ws.numel() - 2 * align    # [arrivals, generation], then the error word
+    ws[gbar:gbar + 4].view(torch.int32).fill_(1 << 20)
+    n0 = buf.info()["kernel_launches"]
+    buf.dispatch(xd, scd, idd, 40)
+    torch.cuda.synchronize()
+    assert buf.info()["kernel_launches"] - n0 == 1, "expected the one-pass dispatch"
+    assert buf.device_error() & ep.EP_DEVERR_TIMEOUT
+    assert int(ws[gbar:gbar + 8].view(torch.int32).abs().sum().item()) == 0
+    d = buf.dispatch(xd, scd, idd, 40)
+    out = buf.combine(d.recv_x, scd)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, 40, E, R)
+    want, _ = orc.combine(ref["recv_x"], sc, ref["pos"], ref["rank_prefix"], ref["S"], R)
+    assert_combine_equal(to_np(out), want)
+    buf.close()

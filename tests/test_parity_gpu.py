@@ -18,8 +18,18 @@ from gpu_util import (assert_combine_equal, assert_layout_equal, assert_recv_equ
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = [ep.EP_PERMUTE_VEC, ep.EP_PERMUTE_BULK]
-IMPL_IDS = ["vec", "bulk"]
+# vec: 16-byte vector permute; bulk: the default bulk dispatch (one cooperative
+# kernel: counts, grid barrier, prefix, positions, copies); fused: the bulk
+# dispatch as count + scan + fused positions/copy kernels (EP_DISPATCH_ONEPASS=0)
+IMPLS = ["vec", "bulk", "fused"]
+IMPL_IDS = IMPLS
+
+
+@pytest.fixture
+def impl(request, monkeypatch):
+    if request.param == "fused":
+        monkeypatch.setenv("EP_DISPATCH_ONEPASS", "0")
+    return ep.EP_PERMUTE_VEC if request.param == "vec" else ep.EP_PERMUTE_BULK
 
 # id: (seed, T, N, N_max, D, dtype, E, K, R, ids, scores)
 CASES = {
@@ -63,7 +73,7 @@ def run_and_check(orc, x, ids, sc, N, N_max, D, dtype, E, K, R, impl):
     buf.close()
 
 
-@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS, indirect=True)
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_parity(orc, case, impl):
     seed, T, N, N_max, D, dtype, E, K, R, ik, sk = CASES[case]
@@ -71,7 +81,7 @@ def test_parity(orc, case, impl):
     run_and_check(orc, x, ids, sc, N, N_max, D, dtype, E, K, R, impl)
 
 
-@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS, indirect=True)
 def test_empty_calls(orc, impl):
     D, E, K, R = 64, 8, 2, 2
     buf = ep.Buffer(32, D, E, R, K, dtype=torch.float32, permute_impl=impl)
@@ -88,7 +98,7 @@ def test_empty_calls(orc, impl):
     assert buf.device_error() == 0
 
 
-@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS, indirect=True)
 def test_bad_and_duplicate_ids(orc, impl):
     # -1 routes nowhere; ids outside [-1, E) are treated as -1 and reported;
     # a repeated id gets one row per occurrence.
@@ -116,7 +126,7 @@ def test_bad_and_duplicate_ids(orc, impl):
     assert not got[36].any()                 # a token with no expert combines to +0
 
 
-@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS, indirect=True)
 def test_scaled_experts(orc, impl):
     # Expert stand-in y = 2^((e mod 4) - 1) * recv_x (exact in bf16) between
     # dispatch and combine: a wrong row or k in the gather changes the result.
@@ -162,7 +172,7 @@ def test_unequal_count_runs_match(orc):
             assert np.array_equal(outs[0], outs[1])
 
 
-@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS)
+@pytest.mark.parametrize("impl", IMPLS, ids=IMPL_IDS, indirect=True)
 @pytest.mark.parametrize("case", ["tiny_T13_N16", "ds_small_tiles", "k3_e48_r4_f32",
                                   "k40_e64_r8", "e1024_r64"])
 def test_parity_packed_layout(orc, case, impl):
@@ -197,4 +207,32 @@ def test_parity_packed_layout(orc, case, impl):
     gx_ref, _, _ = orc.dispatch_backward(gy_ref, None, ref["pos"], ref["rank_prefix"], ref["S"],
                                          R, packed=True)
     assert np.array_equal(bits(to_np(grad_x)), bits(gx_ref))
+    buf.close()
+
+
+@pytest.mark.parametrize("onepass,launches", [("1", 1), ("0", 3)])
+def test_bulk_dispatch_launch_count(orc, monkeypatch, onepass, launches):
+    # The default bulk dispatch is one cooperative kernel; without it, count,
+    # scan and the fused positions/copy kernel. Both match the oracle.
+    monkeypatch.setenv("EP_DISPATCH_ONEPASS", onepass)
+    seed, T, N, N_max, D, dtype, E, K, R, ik, sk = CASES["ds_small_tiles"]
+    x, ids, sc = case_inputs(seed, T, D, dtype, E, K, ik, sk)
+    buf = ep.Buffer(N_max, D, E, R, K, dtype=torch_dtype(dtype))
+    n0 = buf.info()["kernel_launches"]
+    d = buf.dispatch(to_dev(x), to_dev(sc), to_dev(ids), N)
+    torch.cuda.synchronize()
+    assert buf.info()["kernel_launches"] - n0 == launches
+    assert buf.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, N, E, R)
+    assert_layout_equal(d.layout, ref)
+    assert_recv_equal(d, ref, R)
+    # back-to-back calls reuse the grid barrier; a later call still matches
+    ids2, sc2 = W.routing(seed + 1, T, E, K, "uniform", sk)
+    for _ in range(3):
+        d = buf.dispatch(to_dev(x), to_dev(sc2), to_dev(ids2), N)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref2 = orc.dispatch(x, sc2, ids2, N, E, R)
+    assert_layout_equal(d.layout, ref2)
+    assert_recv_equal(d, ref2, R)
     buf.close()
