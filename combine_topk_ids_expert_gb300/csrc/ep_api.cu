@@ -28,7 +28,7 @@ struct ep_buffer {
     int ep_stride;          // row stride of the tile tables: roundup4(E)
     bool pdl;               // launch with programmatic dependent launch
     int tiles_per_sm;       // layout tiles (fused-dispatch CTAs) per SM
-    int gemm_pair;          // expert GEMM tiles: -1 by routed rows per expert, 0 single, 1 2-SM
+    int gemm_kind;          // expert GEMM kernel (GemmArgs::kind), 0: chosen per call
     int gemm_bk;            // expert GEMM K slice per ring stage (64 or 32)
     bool dedup_fused;       // dedupe dispatch in one kernel after the counts
     bool onepass;           // dispatch as one cooperative kernel where it fits
@@ -348,9 +348,10 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         // Tuning knob: fused-dispatch CTAs per SM (1 or 2).
         const char* tps = std::getenv("EP_TILES_PER_SM");
         b->tiles_per_sm = (tps && std::strcmp(tps, "2") == 0) ? 2 : 1;
-        // Tuning knob: EP_GEMM_PAIR=0 / 1 forces single-CTA / 2-SM expert GEMM tiles.
-        const char* gp = std::getenv("EP_GEMM_PAIR");
-        b->gemm_pair = (gp && std::strcmp(gp, "0") == 0) ? 0 : (gp && std::strcmp(gp, "1") == 0) ? 1 : -1;
+        // Tuning knob: EP_GEMM_KERNEL=1 / 2 forces the expert GEMM's kernel
+        // (single-CTA 128-row tiles, 2-SM 256-row tiles).
+        const char* gk = std::getenv("EP_GEMM_KERNEL");
+        b->gemm_kind = (gk && gk[0] >= '1' && gk[0] <= '2' && gk[1] == 0) ? gk[0] - '0' : 0;
         // Tuning knob: EP_GEMM_BK=32 or 64, the expert GEMM's K slice per stage.
         const char* bk = std::getenv("EP_GEMM_BK");
         b->gemm_bk = (bk && std::strcmp(bk, "32") == 0) ? 32 : 64;
@@ -649,12 +650,12 @@ ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights
     a.din = din;
     a.dout = dout;
     a.E = buf->cfg.num_experts;
-    // 2-SM tiles cover 256 rows of one expert: worth it when experts hold at
-    // least 512 routed rows on average (the last call's T * K / E), else the
-    // padding of each expert's last tile costs more than the pair saves.
-    a.pair = buf->gemm_pair >= 0
-                 ? buf->gemm_pair
-                 : (buf->last_T * buf->cfg.topk >= (int64_t)512 * buf->cfg.num_experts ? 1 : 0);
+    // 2-SM row tiles cover 256 rows of one expert: worth it when experts hold
+    // at least 512 routed rows on average (the last call's T * K / E), else
+    // the padding of each expert's last tile costs more than the pair saves.
+    a.kind = buf->gemm_kind > 0
+                 ? buf->gemm_kind
+                 : (buf->last_T * buf->cfg.topk >= (int64_t)512 * buf->cfg.num_experts ? 2 : 1);
     a.bk = buf->gemm_bk;
     a.err = buf->err;
     int kernel = 0, grid = 0;

@@ -41,12 +41,13 @@ struct GemmArgs {
     void* y;                       // [rows][dout] bf16
     int64_t din, dout;             // din % 64 == 0, dout % 128 == 0
     int E;
-    int pair;                      // allow the 2-SM kernel (dout % 256 == 0)
+    int kind;                      // 1 single-CTA 128-row tiles, 2 two-SM 256-row tiles
+                                   // (needs dout % 256 == 0, else falls back to 1)
     int bk;                        // K per ring stage: 64 or 32
     uint32_t* err;
 };
 // x: [rows][din] bf16 receive rows; w: [E][dout][din] bf16.
-// kernel_used: 1 single-CTA tiles, 2 two-SM tiles; grid_used: its CTAs.
+// kernel_used: the kind that ran (see GemmArgs::kind); grid_used: its CTAs.
 cudaError_t launch_expert_gemm(const GemmArgs& a, const void* x, int64_t rows, const void* w,
                                int grid, const LaunchOpts& o, int* kernel_used, int* grid_used);
 

@@ -623,10 +623,11 @@ void set_attrs(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, bool pair, bo
     cfg->numAttrs = n;
 }
 
-// CTAs of the persistent cluster grid: twice the clusters that fit at once
-// (one CTA per SM), within the SM budget; 0 if no cluster fits.
-template <class C>
-int pair_grid(int num_sms)
+// CTAs of the persistent cluster grid of `kernel` (its dynamic shared memory
+// attribute already set): twice the clusters that fit at once (one CTA per SM),
+// within the SM budget; 0 if no cluster fits. Cached per kernel and device.
+template <typename Kernel>
+int cluster_grid(Kernel kernel, size_t smem, int num_sms)
 {
     static std::mutex mu;
     static int cached[64] = {};
@@ -641,11 +642,10 @@ int pair_grid(int num_sms)
         cudaLaunchAttribute attr[2];
         cfg.gridDim = dim3((unsigned)(sms & ~1));
         cfg.blockDim = dim3(kGemmThreads);
-        cfg.dynamicSmemBytes = C::kSmem;
+        cfg.dynamicSmemBytes = smem;
         set_attrs(&cfg, attr, true, false);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_kernel<C>, &cfg) != cudaSuccess ||
-            n < 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
             cudaGetLastError();
             return 0;
         }
@@ -665,7 +665,7 @@ cudaError_t launch_cfg(const GemmArgs& a, const void* x, int64_t rows, const voi
     if (e != cudaSuccess) return e;
     int grid = num_sms;
     if (C::PAIR) {
-        grid = pair_grid<C>(num_sms);
+        grid = cluster_grid(expert_gemm_kernel<C>, C::kSmem, num_sms);
         if (grid < 2) return cudaErrorNotSupported;
     }
     CUtensorMap ta, tb;
@@ -690,7 +690,7 @@ template <int BK>
 cudaError_t launch_bk(const GemmArgs& a, const void* x, int64_t rows, const void* w, int grid,
                       const LaunchOpts& o, int* kernel_used, int* grid_used)
 {
-    if (a.pair && a.dout % kPairBN == 0) {
+    if (a.kind >= 2 && a.dout % kPairBN == 0) {
         *kernel_used = 2;
         const cudaError_t e = launch_cfg<CfgOf<kPairBN, BK, true>>(a, x, rows, w, grid, o, grid_used);
         if (e != cudaErrorNotSupported) return e;

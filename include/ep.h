@@ -318,8 +318,8 @@ EP_API ep_status ep_dedup_expand(ep_buffer* buf, const int32_t* topk_expert_ids_
  * on an SM pair (tcgen05 cta_group::2) when dout % 256 == 0 and the last call
  * routed at least 512 rows per expert on average (T * K >= 512 * E), else
  * 128 rows per SM; both issue the same K order, so they agree bit for bit.
- * The environment variable EP_GEMM_PAIR=0 or 1, read at ep_buffer_init,
- * forces one of them. */
+ * The environment variable EP_GEMM_KERNEL=1 (128-row) or 2 (256-row), read at
+ * ep_buffer_init, forces one of them. */
 EP_API ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights,
                                 int64_t din, int64_t dout, void* y_recv, ep_stream_t stream);
 

@@ -63,12 +63,17 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("pair,bk", [("1", "64"), ("0", "64"), ("1", "32")])
+def expected_kind(kind: str, dout: int) -> int:
+    return int(kind) if dout % 256 == 0 else 1
+
+
+@pytest.mark.parametrize("kind,bk", [("2", "64"), ("1", "64"), ("2", "32")])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_expert_gemm_parity(orc, monkeypatch, case, pair, bk):
-    # pair: 2-SM 256-row tiles (where dout % 256 == 0) or single-CTA 128-row
-    # tiles; bk: K per ring stage (128-byte swizzle at 64, 64-byte at 32)
-    monkeypatch.setenv("EP_GEMM_PAIR", pair)
+def test_expert_gemm_parity(orc, monkeypatch, case, kind, bk):
+    # kind: 1 single-CTA 128-row tiles, 2 two-SM 256-row tiles (falls back to 1
+    # where dout % 256 != 0); bk: K per ring stage (128-byte swizzle at 64,
+    # 64-byte at 32)
+    monkeypatch.setenv("EP_GEMM_KERNEL", kind)
     monkeypatch.setenv("EP_GEMM_BK", bk)
     seed, T, N, din, dout, E, K, R, ik, layout = CASES[case]
     x = W.hidden(seed, T, din, "bf16")
@@ -81,7 +86,7 @@ def test_expert_gemm_parity(orc, monkeypatch, case, pair, bk):
     buf.expert_gemm(d.recv_x.reshape(R * S, din), to_dev(w), y_recv=y)
     torch.cuda.synchronize()
     assert buf.device_error() == 0
-    assert buf.info()["gemm_kernel"] == (2 if pair == "1" and dout % 256 == 0 else 1)
+    assert buf.info()["gemm_kernel"] == expected_kind(kind, dout)
     ref = orc.dispatch(x, sc, ids, N, E, R, packed=(layout == "packed"))
     check_gemm(orc, to_np(y), ref["recv_x"], w, ref["cnt"], ref["expert_offset"])
     buf.close()
@@ -91,8 +96,8 @@ def test_expert_gemm_parity(orc, monkeypatch, case, pair, bk):
 def test_gemm_variants_fullsize(orc, monkeypatch, name):
     # Full workload shape, D -> 2048: the 2-SM kernel (M = 256 across a pair)
     # and the single-CTA kernel (M = 128), at 64- and 32-wide K slices, issue the
-    # same K=16 steps in the same order for every output, so the four agree bit
-    # for bit; sampled rows of a few experts are checked against the oracle.
+    # same K=16 steps in the same order for every output, so all agree bit for
+    # bit; sampled rows of a few experts are checked against the oracle.
     w_ = W.WORKLOADS[name]
     inp = W.make(name)
     D, E, dout = w_.D, w_.E, 2048
@@ -101,8 +106,8 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
     gen.manual_seed(1234)
     wd = (torch.randn((E * dout, D), generator=gen, device="cuda") * 0.03).to(torch.bfloat16)
     bufs, ys = [], []
-    for pair, bk in (("1", "64"), ("0", "64"), ("1", "32"), ("0", "32")):
-        monkeypatch.setenv("EP_GEMM_PAIR", pair)
+    for kind, bk in (("2", "64"), ("1", "64"), ("2", "32"), ("1", "32")):
+        monkeypatch.setenv("EP_GEMM_KERNEL", kind)
         monkeypatch.setenv("EP_GEMM_BK", bk)
         buf = ep.Buffer(w_.N_max, D, E, w_.R, w_.K, dtype=torch.bfloat16)
         d = buf.dispatch(xd, scd, idd, w_.N)
@@ -111,10 +116,10 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
         buf.expert_gemm(d.recv_x.reshape(rows, D), wd.reshape(E, dout, D), y_recv=y)
         torch.cuda.synchronize()
         assert buf.device_error() == 0
-        assert buf.info()["gemm_kernel"] == (2 if pair == "1" else 1)
+        assert buf.info()["gemm_kernel"] == int(kind)
         if bufs:
             buf.close()
-            assert torch.equal(ys[0].view(torch.int16), y.view(torch.int16)), (pair, bk)
+            assert torch.equal(ys[0].view(torch.int16), y.view(torch.int16)), (kind, bk)
             del d, y
         else:
             bufs.append((buf, d))
@@ -145,7 +150,7 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
 def test_gemm_tile_choice_follows_rows_per_expert(monkeypatch):
     # Unforced, 2-SM tiles are used when the last call routed >= 512 rows per
     # expert on average (T * K >= 512 * E), single-CTA tiles otherwise.
-    monkeypatch.delenv("EP_GEMM_PAIR", raising=False)
+    monkeypatch.delenv("EP_GEMM_KERNEL", raising=False)
     D, E, K, R = 128, 4, 2, 1
     w = to_dev(W.hidden(84, E * 256, D, "bf16").reshape(E, 256, D))
     buf = ep.Buffer(1024, D, E, R, K, dtype=torch.bfloat16)
@@ -181,11 +186,10 @@ def test_gemm_output_feeds_combine(orc):
     buf.close()
 
 
-@pytest.mark.parametrize("dout,bk", [(128, "64"), (512, "64"), (512, "32")])
-def test_gemm_graph_replay_fresh_routing(orc, monkeypatch, dout, bk):
-    # Captured once; each replay's tile list follows that replay's counts
-    # (dout 512: the 2-SM kernel).
-    monkeypatch.setenv("EP_GEMM_BK", bk)
+@pytest.mark.parametrize("dout,kind", [(128, "1"), (512, "2"), (512, "1")])
+def test_gemm_graph_replay_fresh_routing(orc, monkeypatch, dout, kind):
+    # Captured once; each replay's tile list follows that replay's counts.
+    monkeypatch.setenv("EP_GEMM_KERNEL", kind)
     T, N, D, E, K, R = 256, 256, 128, 8, 2, 2
     buf = ep.Buffer(N, D, E, R, K, dtype=torch.bfloat16)
     x = W.hidden(90, T, D, "bf16")
