@@ -580,6 +580,10 @@ cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
     cfg.attrs = attr;
     cfg.numAttrs = (o.pdl && pdl_ok) ? 2 : 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, dispatch_tile_kernel<true>, l, p, (int)stages, slot);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {   // fewer SMs than the device reports (MPS)
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
     if (e == cudaSuccess && o.launches) ++*o.launches;
     return e;
 }
