@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--mode", choices=["step", "dedup", "backward"], default="step",
                     help="step: layout+dispatch+combine (the benchmark); dedup: the per-rank "
                          "dedupe dispatch alone; backward: combine and dispatch backward")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="routing and hidden-state seed (default: the workload's own)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph-leg", action="store_true",
                     help="skip the extra captured-graph timing of the same step")
@@ -295,9 +297,9 @@ def step_calls(args, w: W.Workload) -> tuple[list[dict], int]:
     one per source rank of the ragged workload (padded to the group max)."""
     if args.tokens > 0 or w.T is not None:
         T, N = workload_tokens(args, w)
-        return [W.make(args.workload, rank=0, T=T)], N
+        return [W.make(args.workload, rank=0, T=T, seed=args.seed)], N
     counts = W.ragged_counts(w)
-    return [W.make(args.workload, rank=r) for r in range(w.ragged_ranks)], max(counts)
+    return [W.make(args.workload, rank=r, seed=args.seed) for r in range(w.ragged_ranks)], max(counts)
 
 
 def run_gb300(args) -> dict | None:
@@ -764,7 +766,7 @@ def main():
         if rank != 0:
             return
         T, N = workload_tokens(args, w)
-        inp = W.make(args.workload, rank=0, T=T)
+        inp = W.make(args.workload, rank=0, T=T, seed=args.seed)
         tpc = oracle_tokens_per_call(w)
         budget = max(1.0, min(args.cpu_seconds, 20.0)) / max(1, args.steps + args.warmup)
         for _ in range(args.warmup):
@@ -819,7 +821,7 @@ def main():
     line["gpu_launches"] = res["launches"]
     line["clocks"] = res["clocks"]
     if not args.no_cpu_baseline:
-        inp = W.make(args.workload, rank=0, T=T)
+        inp = W.make(args.workload, rank=0, T=T, seed=args.seed)
         tpc = oracle_tokens_per_call(w)
         r = oracle_sample_run(w, inp, args.cpu_seconds, tpc)
         line["cpu_baseline"] = {

@@ -23,7 +23,8 @@ from dataclasses import dataclass
 import torch
 
 from . import _abi
-from ._abi import (EP_BF16, EP_DEVERR_BAD_ID, EP_DEVERR_ROW_OOB, EP_DEVERR_TIMEOUT, EP_F32,
+from ._abi import (EP_BF16, EP_DEVERR_BAD_ID, EP_DEVERR_DEBUG_STRAY, EP_DEVERR_DEBUG_UNWRITTEN,
+                   EP_DEVERR_ROW_OOB, EP_DEVERR_TIMEOUT, EP_F32,
                    EP_LAYOUT_PACKED, EP_LAYOUT_STRIDED, EP_PERMUTE_BULK, EP_PERMUTE_DEFAULT,
                    EP_PERMUTE_VEC, EpBufferInfo, EpConfig, EpDedupOut, EpDispatchOut, EpError,
                    EpLayout, check)
@@ -38,7 +39,8 @@ __all__ = [
     "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
     "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
     "EP_LAYOUT_STRIDED", "EP_LAYOUT_PACKED",
-    "EP_DEVERR_BAD_ID", "EP_DEVERR_ROW_OOB", "EP_DEVERR_TIMEOUT", "library_path",
+    "EP_DEVERR_BAD_ID", "EP_DEVERR_ROW_OOB", "EP_DEVERR_TIMEOUT", "EP_DEVERR_DEBUG_UNWRITTEN",
+    "EP_DEVERR_DEBUG_STRAY", "library_path",
 ]
 
 _TORCH_TO_EP = {torch.bfloat16: EP_BF16, torch.float32: EP_F32}

@@ -33,6 +33,8 @@ EP_LAYOUT_PACKED = 1
 EP_DEVERR_BAD_ID = 0x1
 EP_DEVERR_ROW_OOB = 0x2
 EP_DEVERR_TIMEOUT = 0x4
+EP_DEVERR_DEBUG_UNWRITTEN = 0x8   # EP_DEBUG=1 only
+EP_DEVERR_DEBUG_STRAY = 0x10      # EP_DEBUG=1 only
 
 
 class EpConfig(C.Structure):

@@ -14,6 +14,8 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ep.h"
 #include "ep_kernels.cuh"
 #include "ep_next.cuh"
@@ -32,6 +34,8 @@ struct ep_buffer {
     int gemm_bk;            // expert GEMM K slice per ring stage (64 or 32)
     bool dedup_fused;       // dedupe dispatch in one kernel after the counts
     bool onepass;           // dispatch as one cooperative kernel where it fits
+    bool debug;             // EP_DEBUG: sentinel fill and checks of the receive rows
+    bool nvtx;              // EP_NVTX: an NVTX range around every call
     bool coop_pdl;          // cooperative launches take programmatic serialization
     uint32_t* gbar;         // [2] the one-pass dispatch's grid barrier
     int gemm_kernel;        // last expert GEMM: 0 none, 1 single-CTA, 2 two-SM
@@ -193,6 +197,43 @@ void fill_dispatch(const ep_buffer* b, ep_dispatch_out* out)
 
 ep::LaunchOpts opts(ep_buffer* b, cudaStream_t s) { return ep::LaunchOpts{s, b->pdl, &b->launches}; }
 
+// An NVTX range for the lifetime of a call when EP_NVTX=1.
+struct Range {
+    bool on;
+    Range(const ep_buffer* b, const char* name) : on(b && b->nvtx)
+    {
+        if (on) nvtxRangePushA(name);
+    }
+    ~Range()
+    {
+        if (on) nvtxRangePop();
+    }
+};
+
+// EP_DEBUG: the call's receive rows (R * S) get the 0xFF sentinel before a permute.
+bool debug_fill(ep_buffer* b, int64_t S, cudaStream_t s)
+{
+    return !b->debug || cudaMemsetAsync(b->recv_x, 0xFF,
+                                        (size_t)b->cfg.num_ranks * (size_t)S * (size_t)b->row_bytes,
+                                        s) == cudaSuccess;
+}
+
+// EP_DEBUG: rows inside each rank's true total written, the rest untouched.
+bool debug_check(ep_buffer* b, const void* rows, cudaStream_t s)
+{
+    if (!b->debug) return true;
+    ep::SentinelArgs a;
+    a.recv_x = static_cast<const uint8_t*>(rows);
+    a.S = b->last_S;
+    a.row_bytes = b->row_bytes;
+    a.R = b->cfg.num_ranks;
+    a.packed = b->cfg.layout_mode == EP_LAYOUT_PACKED;
+    a.rows_per_rank = b->rows_per_rank;
+    a.rank_prefix = b->rank_prefix;
+    a.err = b->err;
+    return ep::launch_sentinel_check(a, b->num_sms, opts(b, s)) == cudaSuccess;
+}
+
 ep::LayoutArgs layout_args(ep_buffer* b, const int32_t* ids, int64_t T, int64_t N)
 {
     ep::LayoutArgs a;
@@ -337,7 +378,13 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     if (!b) return EP_ERR_INVALID_ARG;
     b->cfg = *cfg;
     b->device = dev;
-    b->num_sms = (cfg->num_sms > 0 && cfg->num_sms < sms) ? cfg->num_sms : sms;
+    // SM budget: the config's, else EP_NUM_SMS, else every SM.
+    int budget = cfg->num_sms;
+    if (budget <= 0) {
+        const char* ns = std::getenv("EP_NUM_SMS");
+        budget = ns ? std::atoi(ns) : 0;
+    }
+    b->num_sms = (budget > 0 && budget < sms) ? budget : sms;
     b->row_bytes = rb;
     b->s_max = s_max;
     b->max_tiles = tiles;
@@ -361,6 +408,11 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         // Tuning knob: EP_DISPATCH_ONEPASS=0 keeps the dispatch as count + scan + fused.
         const char* op = std::getenv("EP_DISPATCH_ONEPASS");
         b->onepass = !(op && std::strcmp(op, "0") == 0);
+        // Debugging: EP_DEBUG=1 (sentinel checks), EP_NVTX=1 (NVTX ranges).
+        const char* dbg = std::getenv("EP_DEBUG");
+        b->debug = dbg && std::strcmp(dbg, "1") == 0;
+        const char* nv = std::getenv("EP_NVTX");
+        b->nvtx = nv && std::strcmp(nv, "1") == 0;
         // Test hook: make one bounded wait of the bulk permute run out.
         const char* t = std::getenv("EP_TEST_SKIP_LOAD");
         b->test_skip_load = (t && *t) ? std::strtoll(t, nullptr, 10) : -1;
@@ -410,6 +462,7 @@ ep_status ep_buffer_destroy(ep_buffer* buf)
 ep_status ep_dispatch_layout(ep_buffer* buf, const int32_t* ids, int64_t T, int64_t N,
                              ep_stream_t stream, ep_layout* out, int32_t* host_counts)
 {
+    const Range range(buf, "ep_dispatch_layout");
     ep_status st = check_call(buf, ids, T, N);
     if (st != EP_OK) return st;
     cudaStream_t s = as_stream(stream);
@@ -429,12 +482,15 @@ ep_status ep_dispatch_layout(ep_buffer* buf, const int32_t* ids, int64_t T, int6
 ep_status ep_dispatch(ep_buffer* buf, const void* x, const float* scores, const int32_t* ids,
                       int64_t T, int64_t N, ep_stream_t stream, ep_dispatch_out* out)
 {
+    const Range range(buf, "ep_dispatch");
     ep_status st = check_call(buf, ids, T, N);
     if (st != EP_OK) return st;
     if (T > 0 && (!x || !scores)) return EP_ERR_INVALID_ARG;
     if (!is_aligned(x, 16) || !is_aligned(scores, 4)) return EP_ERR_ALIGNMENT;
+    if (!debug_fill(buf, pad4(N) * buf->cfg.topk, as_stream(stream))) return EP_ERR_CUDA;
     st = enqueue_dispatch(buf, x, scores, ids, T, N, as_stream(stream));
     if (st != EP_OK) return st;
+    if (!debug_check(buf, buf->recv_x, as_stream(stream))) return EP_ERR_CUDA;
     fill_dispatch(buf, out);
     return EP_OK;
 }
@@ -442,12 +498,15 @@ ep_status ep_dispatch(ep_buffer* buf, const void* x, const float* scores, const 
 ep_status ep_dispatch_permute(ep_buffer* buf, const void* x, const float* scores,
                               ep_stream_t stream, ep_dispatch_out* out)
 {
+    const Range range(buf, "ep_dispatch_permute");
     if (!buf) return EP_ERR_INVALID_ARG;
     if (!buf->has_layout) return EP_ERR_NO_LAYOUT;
     ep_status st = check_rows(buf, x, scores);
     if (st != EP_OK) return st;
+    if (!debug_fill(buf, buf->last_S, as_stream(stream))) return EP_ERR_CUDA;
     st = enqueue_permute(buf, x, scores, as_stream(stream));
     if (st != EP_OK) return st;
+    if (!debug_check(buf, buf->recv_x, as_stream(stream))) return EP_ERR_CUDA;
     fill_dispatch(buf, out);
     return EP_OK;
 }
@@ -455,6 +514,7 @@ ep_status ep_dispatch_permute(ep_buffer* buf, const void* x, const float* scores
 ep_status ep_combine(ep_buffer* buf, const void* y, const float* scores, int64_t T, void* out,
                      int32_t out_dtype, ep_stream_t stream)
 {
+    const Range range(buf, "ep_combine");
     if (!buf) return EP_ERR_INVALID_ARG;
     if (!buf->has_layout || T != buf->last_T) return EP_ERR_NO_LAYOUT;
     if (out_dtype != EP_BF16 && out_dtype != EP_F32) return EP_ERR_INVALID_ARG;
@@ -479,6 +539,7 @@ ep_status ep_combine(ep_buffer* buf, const void* y, const float* scores, int64_t
     a.unit_weights = false;
     a.gather_in = nullptr;
     a.gather_out = nullptr;
+    if (y == buf->recv_x && !debug_check(buf, y, as_stream(stream))) return EP_ERR_CUDA;
     if (ep::launch_combine(a, buf->combine_grid, opts(buf, as_stream(stream))) != cudaSuccess)
         return EP_ERR_CUDA;
     return EP_OK;
@@ -488,6 +549,7 @@ ep_status ep_combine_backward(ep_buffer* buf, const void* grad_out, const void* 
                               const float* scores, int64_t T, void* grad_y, float* grad_scores,
                               ep_stream_t stream)
 {
+    const Range range(buf, "ep_combine_backward");
     if (!buf) return EP_ERR_INVALID_ARG;
     if (!buf->has_layout || T != buf->last_T) return EP_ERR_NO_LAYOUT;
     if (T > 0 && (!grad_out || !scores || !grad_y || (grad_scores && !y)))
@@ -521,6 +583,7 @@ ep_status ep_dispatch_backward(ep_buffer* buf, const void* grad_recv_x,
                                const float* grad_recv_scores, int64_t T, void* grad_x,
                                int32_t grad_x_dtype, float* grad_scores, ep_stream_t stream)
 {
+    const Range range(buf, "ep_dispatch_backward");
     if (!buf) return EP_ERR_INVALID_ARG;
     if (!buf->has_layout || T != buf->last_T) return EP_ERR_NO_LAYOUT;
     if (grad_x_dtype != EP_BF16 && grad_x_dtype != EP_F32) return EP_ERR_INVALID_ARG;
@@ -576,6 +639,7 @@ ep::DedupArgs dedup_args(ep_buffer* b, const void* x, const float* scores, const
 ep_status ep_dispatch_dedup(ep_buffer* buf, const void* x, const float* scores, const int32_t* ids,
                             int64_t T, int64_t N, ep_stream_t stream, ep_dedup_out* out)
 {
+    const Range range(buf, "ep_dispatch_dedup");
     ep_status st = check_call(buf, ids, T, N);
     if (st != EP_OK) return st;
     if (T > 0 && (!x || !scores)) return EP_ERR_INVALID_ARG;
@@ -611,6 +675,7 @@ ep_status ep_dispatch_dedup(ep_buffer* buf, const void* x, const float* scores, 
 
 ep_status ep_dedup_expand(ep_buffer* buf, const int32_t* ids, void* y_recv, ep_stream_t stream)
 {
+    const Range range(buf, "ep_dedup_expand");
     if (!buf) return EP_ERR_INVALID_ARG;
     if (!buf->has_layout || !buf->last_dedup) return EP_ERR_NO_LAYOUT;
     if (buf->last_T > 0 && (!ids || !y_recv)) return EP_ERR_INVALID_ARG;
@@ -631,6 +696,7 @@ ep_status ep_dedup_expand(ep_buffer* buf, const int32_t* ids, void* y_recv, ep_s
 ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights, int64_t din,
                          int64_t dout, void* y_recv, ep_stream_t stream)
 {
+    const Range range(buf, "ep_expert_gemm");
     if (!buf) return EP_ERR_INVALID_ARG;
     if (!buf->has_layout) return EP_ERR_NO_LAYOUT;
     if (buf->cfg.dtype != EP_BF16) return EP_ERR_INVALID_ARG;

@@ -51,4 +51,18 @@ struct GemmArgs {
 cudaError_t launch_expert_gemm(const GemmArgs& a, const void* x, int64_t rows, const void* w,
                                int grid, const LaunchOpts& o, int* kernel_used, int* grid_used);
 
+// Sentinel checks of the receive buffer (debug.cu, EP_DEBUG=1).
+constexpr uint32_t kErrDebugUnwritten = 0x8u;   // a row inside a rank's total kept the sentinel
+constexpr uint32_t kErrDebugStray = 0x10u;      // a row past a rank's total was written
+struct SentinelArgs {
+    const uint8_t* recv_x;          // [R*S][row_bytes]
+    int64_t S, row_bytes;
+    int R;
+    bool packed;
+    const int32_t* rows_per_rank;   // [R]
+    const int32_t* rank_prefix;     // [R]
+    uint32_t* err;
+};
+cudaError_t launch_sentinel_check(const SentinelArgs& a, int num_sms, const LaunchOpts& o);
+
 }  // namespace ep

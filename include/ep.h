@@ -90,6 +90,11 @@ typedef enum {
 #define EP_DEVERR_BAD_ID 0x1u     /* an id outside [-1, E) was seen; treated as -1 */
 #define EP_DEVERR_ROW_OOB 0x2u    /* combine met a row outside its rank's true total; skipped */
 #define EP_DEVERR_TIMEOUT 0x4u    /* a bounded device-side wait gave up; outputs invalid */
+/* Only with EP_DEBUG=1 (read at ep_buffer_init): the dispatch fills its receive
+ * rows with 0xFF before the permute and checks them after it; the combine
+ * repeats the check when it reads the receive buffer itself. */
+#define EP_DEVERR_DEBUG_UNWRITTEN 0x8u  /* a row inside a rank's true total kept the 0xFF fill */
+#define EP_DEVERR_DEBUG_STRAY 0x10u     /* a row past a rank's true total was written */
 
 /* Lifetime configuration ([titan] "API design": the dispatcher configuration
  * carries the lifetime maximum num_max_tokens_per_rank; persistent storage is
