@@ -1,6 +1,7 @@
 // ep_kernels.cuh - internal interface between the C ABI (ep_api.cu,
-// layout_noalloc.cu) and the sm_103a kernels (layout.cu, permute.cu,
-// combine.cu). Not installed.
+// layout_noalloc.cu) and the sm_103a kernels of the dispatch + combine step
+// (layout.cu, permute.cu, combine.cu); ep_next.cuh extends it for the dedupe,
+// the expert GEMM and the debug checks. Not installed.
 #pragma once
 
 #include <cuda_runtime.h>

@@ -17,8 +17,10 @@
 //           as 16-byte vectors by row groups, per-expert totals, expert offsets
 //           within each rank, per-rank totals and their inclusive prefix.
 //   pos   : one CTA per tile; stable rank of each pair among the pairs of the
-//           same expert in flat order t*K+k (tile_positions). The bulk
-//           dispatch fuses this pass into its permute kernel instead.
+//           same expert in flat order t*K+k (tile_positions).
+// The default bulk dispatch does all three inside its one-pass kernel
+// (permute.cu); these kernels serve the layout-only call, the vector permute,
+// the dedupe dispatch and the bulk dispatch where a tile does not fit.
 #include "ep_device.cuh"
 
 namespace ep {

@@ -6,15 +6,19 @@
 // the current capacity; DeepEP: the current capacity is the per-rank layout
 // stride).
 //
-// HBM-bound: reads T rows and writes up to T*K rows. Three kernels:
-//   dispatch_fused : the default. One CTA (8 warps) per layout tile, about one
-//                    per SM. Thread 0 starts bulk async loads of the tile's
-//                    rows into a shared-memory ring *before* waiting for the
-//                    layout scan (the rows do not depend on it), then all
-//                    warps compute the tile's positions into shared memory,
-//                    then warp 0 streams the rows out: lane k issues the bulk
-//                    store of destination k; warps 1-7 write scores and
-//                    sources. Completion of loads is tracked by mbarriers
+// HBM-bound: reads T rows and writes up to T*K rows. Kernels:
+//   dispatch_tile<ONEPASS> : one CTA (8 warps) per layout tile, about one per
+//                    SM. Thread 0 starts bulk async loads of the tile's rows
+//                    into a shared-memory ring before the layout is known
+//                    (the rows do not depend on it). The one-pass form (the
+//                    default, a cooperative launch) then counts its tile,
+//                    meets every other CTA at a grid barrier and derives its
+//                    prefixes from all tiles' counts; the fused form waits
+//                    for the separate count and scan kernels instead. Then
+//                    all warps compute the tile's positions into shared
+//                    memory, and warp 0 streams the rows out: lane k issues
+//                    the bulk store of destination k; warps 1-7 write scores
+//                    and sources. Completion of loads is tracked by mbarriers
 //                    (bounded waits); a slot is reused only after its stores
 //                    have read it (cp.async.bulk.wait_group.read).
 //   permute_bulk   : the same ring for a standalone permute (positions from
