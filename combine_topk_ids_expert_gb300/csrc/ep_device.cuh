@@ -1,7 +1,8 @@
-// ep_device.cuh - device helpers shared by the layout, permute and combine
-// kernels: programmatic-dependent-launch controls, id checks, mbarrier and
-// bulk-async-copy wrappers (hand-written PTX), and the stable per-tile
-// position pass.
+// ep_device.cuh - device helpers shared by the layout, permute, combine,
+// dedupe and GEMM kernels: programmatic-dependent-launch controls, id checks,
+// mbarrier and bulk-async-copy wrappers (hand-written PTX), the per-tile
+// expert histogram, the stable per-tile position pass and the grid barrier
+// of the one-pass dispatch.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -12,10 +13,12 @@
 namespace ep {
 
 // ---- programmatic dependent launch -----------------------------------------
-// Every kernel is launched so that it may start while its predecessor in the
-// stream finishes. It must call griddep_wait() before touching memory the
-// predecessor may write or read; it calls griddep_launch_dependents() once its
-// own successor may start its prologue. Both are no-ops for a normal launch.
+// Kernels are launched so that they may start while their predecessor in the
+// stream finishes (the combine is the exception: in captured graphs an early
+// combine measured slower). A kernel calls griddep_wait() before touching
+// memory its predecessor may write or read, and griddep_launch_dependents()
+// once its own successor may start its prologue. Both are no-ops for a normal
+// launch.
 
 __device__ __forceinline__ void griddep_wait()
 {
