@@ -106,7 +106,8 @@ typedef struct {
     int32_t num_ranks;               /* R, 1 <= R <= 64 logical ranks */
     int32_t topk;                    /* K, 1 <= K <= min(E, 64) */
     int32_t dtype;                   /* ep_dtype of x_TD and the receive buffer */
-    int32_t num_sms;                 /* SMs the copy kernels may use; 0 = all ([flex]) */
+    int32_t num_sms;                 /* SMs the copy kernels may use; 0 = the environment
+                                        variable EP_NUM_SMS if set, else all ([flex]) */
     int32_t permute_impl;            /* ep_permute_impl */
     int32_t layout_mode;             /* ep_layout_mode: where each rank's rows start.
                                         STRIDED ([titan] "Backend behavior": the current
