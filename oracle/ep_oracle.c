@@ -266,8 +266,13 @@ int oracle_layout(const int32_t* ids, int64_t T, int64_t N, int32_t K, int32_t E
         }
     int32_t run = 0;
     for (int32_t r = 0; r < R; ++r) {
+#if ORACLE_MUTANT == 18
+        rank_prefix_R[r] = run;                     /* mutant: exclusive prefix */
+        run += rows_per_rank_R[r];
+#else
         run += rows_per_rank_R[r];
         rank_prefix_R[r] = run;
+#endif
     }
 
     /* Step 3: first row of each expert: inside its rank's block of S rows
@@ -350,7 +355,11 @@ int oracle_dispatch(const void* x, int64_t row_bytes, const float* scores, const
             if (p < 0) continue;
             memcpy(rb + p * row_bytes, xb + t * row_bytes, (size_t)row_bytes);
             recv_scores[p] = scores[t * K + k];
+#if ORACLE_MUTANT == 19
+            recv_src[p] = (int32_t)t;                   /* mutant: token, not pair index */
+#else
             recv_src[p] = (int32_t)(t * K + k);
+#endif
         }
     return ORC_OK;
 }
@@ -441,6 +450,8 @@ int oracle_combine(const void* y, int y_kind, int64_t D, const float* scores,
             float acc = 0.0f;
 #if ORACLE_MUTANT == 1
             for (int32_t k = 0; k < K - 1; ++k) {   /* mutant: drops the last term */
+#elif ORACLE_MUTANT == 17
+            for (int32_t k = K - 1; k >= 0; --k) {  /* mutant: descending k */
 #else
             for (int32_t k = 0; k < K; ++k) {
 #endif
@@ -502,7 +513,11 @@ int oracle_combine_backward(const void* grad_out, int g_kind, const void* y, int
     for (int64_t t = 0; t < T; ++t)
         for (int32_t k = 0; k < K; ++k) {
             int64_t p = pos_TK[t * K + k];
+#if ORACLE_MUTANT == 23
+            float dot = 0.0f;                           /* mutant: fp32 dot */
+#else
             double dot = 0.0;
+#endif
             if (p >= 0 && !row_ok(p, rank_prefix_R, S, R, packed)) {
                 *err |= ORC_ERR_ROW_OOB;
                 p = -1;
@@ -622,7 +637,11 @@ int oracle_dispatch_dedup(const void* x, int64_t row_bytes, const float* scores,
             for (int32_t k = 0; k < K; ++k) {
                 int32_t e = ids[t * K + k];
                 int mine = e >= 0 && e < E && rank_of(e, E, R) == r;
+#if ORACLE_MUTANT == 21
+                recv_topk_idx[q * K + k] = mine ? e : -1;  /* mutant: global expert id */
+#else
                 recv_topk_idx[q * K + k] = mine ? e - r * eloc : -1;
+#endif
                 recv_topk_w[q * K + k] = mine ? scores[t * K + k] : 0.0f;
             }
             ++q;
@@ -649,8 +668,13 @@ int oracle_dedup_expand(const void* recv_tok_x, int64_t row_bytes, const int32_t
             const int64_t p = pos_TK[t * K + k];
             const int32_t e = ids[t * K + k];
             if (p < 0 || e < 0 || e >= E) continue;
+#if ORACLE_MUTANT == 22
+            const int64_t q = tok_pos_TR[t * R + (rank_of(e, E, R) + 1) % R];   /* mutant */
+            if (q < 0) continue;
+#else
             const int64_t q = tok_pos_TR[t * R + rank_of(e, E, R)];
             if (q < 0) return ORC_EINVAL;
+#endif
             memcpy((uint8_t*)y + p * row_bytes, (const uint8_t*)recv_tok_x + q * row_bytes,
                    (size_t)row_bytes);
         }
@@ -685,7 +709,11 @@ int oracle_expert_gemm(const uint16_t* x, const uint16_t* w, const int32_t* cnt_
         for (int64_t j = 0; j < cnt_E[e]; ++j) {
             int64_t p = (int64_t)expert_offset_E[e] + j;
             for (int64_t o = 0; o < dout; ++o) {
+#if ORACLE_MUTANT == 20
+                float acc = 0.0f;                       /* mutant: fp32 sum */
+#else
                 double acc = 0.0;
+#endif
                 for (int64_t i = 0; i < din; ++i)
                     acc += (double)oracle_f32_from_bf16(x[p * din + i]) *
                            (double)oracle_f32_from_bf16(we[o * din + i]);

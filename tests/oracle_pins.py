@@ -596,4 +596,50 @@ def pin_dedup_expand_reproduces_dispatch(o):
     assert int(dd["tokens_in_rank"].sum()) < T * K           # duplicates were folded
 
 
+# ---------------------------------------------------------------------------
+# Summation order and precision, by inputs where they change the exact result
+# ---------------------------------------------------------------------------
+
+def pin_combine_ascending_k_fma_chain(o):
+    # One token, K = 3, y rows of ones, scores (1, 2^-24, -1). The fp32 chain in
+    # ascending k: fma(1,1,0) = 1; fma(2^-24,1,1) = 1 + 2^-24, a tie that rounds
+    # to even, 1; fma(-1,1,1) = 0. Descending k would give 2^-24 instead.
+    T, N, E, K, R, D = 1, 1, 4, 3, 1, 4
+    for ids in (np.array([[0, 1, 2]], np.int32), np.array([[2, 0, 1]], np.int32)):
+        x = np.ones((T, D), np.float32)
+        sc = np.array([[1.0, 2.0 ** -24, -1.0]], np.float32)
+        d = o.dispatch(x, sc, ids, N, E, R)
+        out, err = o.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R, "f32")
+        assert err == 0
+        assert np.array_equal(out.view(np.uint32), np.zeros((T, D), np.uint32))
+
+
+def pin_expert_gemm_exact_cancellation(o):
+    # x row (2^24, thirty-two ones, -2^24) against a weight row of ones: the exact
+    # dot product is 32, which bf16 holds; a running fp32 sum loses every 1
+    # against 2^24 (its spacing there is 2) and would return 0.
+    din, dout, E = 34, 2, 1
+    row = np.concatenate([[2.0 ** 24], np.ones(32), [-(2.0 ** 24)]]).astype(np.float32)
+    x = _bf16_bits(row[None, :])
+    w = _bf16_bits(np.ones((E * dout, din), np.float32)).reshape(E, dout, din)
+    y = o.expert_gemm(x, w, np.array([1], np.int32), np.array([0], np.int32))
+    assert np.array_equal(_f32_from_bits(y), np.full((1, dout), 32.0, np.float32))
+
+
+def pin_combine_backward_score_gradient_exact(o):
+    # grad_scores[t][k] = <grad_out[t], y[pos[t][k]]>, summed exactly and rounded
+    # once: grad_out (2^24, thirty-two ones, -2^24) against a row of ones is 32;
+    # a running fp32 sum would give 0.
+    T, N, E, K, R = 1, 1, 2, 1, 1
+    D = 34
+    x = np.ones((T, D), np.float32)
+    ids = np.array([[1]], np.int32)
+    sc = np.array([[0.5]], np.float32)
+    g = np.concatenate([[2.0 ** 24], np.ones(32), [-(2.0 ** 24)]]).astype(np.float32)[None, :]
+    d = o.dispatch(x, sc, ids, N, E, R)
+    _, gs, err = o.combine_backward(g, d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R)
+    assert err == 0
+    assert gs[0, 0] == np.float32(32.0)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

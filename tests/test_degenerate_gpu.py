@@ -72,3 +72,15 @@ def test_tiny_call_in_a_large_buffer(orc, path):
     ids, sc = W.routing(153, 1, 32, 4, "uniform", "sigmoid_norm")
     ref, _ = check(orc, x, ids, sc, 1, 100_000, 64, "bf16", 32, 4, 8, path)
     assert ref["S"] == 4 * 4
+
+
+def test_combine_follows_ascending_k(orc, path):
+    # Scores (1, 2^-24, -1) on rows of ones: the fp32 fma chain in ascending k
+    # gives exactly +0 (1, then a tie rounded to even, then 0); any other order
+    # gives 2^-24. Checked for two orders of the same experts.
+    for order in ([0, 1, 2], [2, 0, 1]):
+        x = np.ones((1, 4), np.float32)
+        ids = np.array([order], np.int32)
+        sc = np.array([[1.0, 2.0 ** -24, -1.0]], np.float32)
+        _, out = check(orc, x, ids, sc, 1, 1, 4, "f32", 4, 3, 1, path)
+        assert np.array_equal(out.view(np.uint32), np.zeros((1, 4), np.uint32))

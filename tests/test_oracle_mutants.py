@@ -29,6 +29,13 @@ MUTANTS = {
     14: "packed layout placed like the strided one",
     15: "expert GEMM uses the next expert's weights",
     16: "dedupe writes one row per pair instead of per rank",
+    17: "combine accumulates in descending k",
+    18: "rank prefix exclusive instead of inclusive",
+    19: "receive source records the token, not the pair",
+    20: "expert GEMM sums in fp32",
+    21: "dedupe records global expert ids",
+    22: "dedupe expansion reads another rank's row",
+    23: "combine backward score gradient summed in fp32",
 }
 
 
