@@ -32,6 +32,7 @@ struct ep_buffer {
     int tiles_per_sm;       // layout tiles (fused-dispatch CTAs) per SM
     int gemm_kind;          // expert GEMM kernel (GemmArgs::kind), 0: chosen per call
     int gemm_bk;            // expert GEMM K slice per ring stage (64 or 32)
+    int gemm_light_rows;    // expert GEMM: experts with at most this many rows are light
     bool dedup_fused;       // dedupe dispatch in one kernel after the counts
     bool onepass;           // dispatch as one cooperative kernel where it fits
     bool debug;             // EP_DEBUG: sentinel fill and checks of the receive rows
@@ -72,6 +73,9 @@ struct ep_buffer {
 namespace {
 
 constexpr size_t kAlign = 256;
+// Expert GEMM schedule: experts with at most this many rows are light (their
+// weights feed one or two 128-row tiles, so those tiles wait on HBM).
+constexpr int kGemmLightRows = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -402,6 +406,10 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         // Tuning knob: EP_GEMM_BK=32 or 64, the expert GEMM's K slice per stage.
         const char* bk = std::getenv("EP_GEMM_BK");
         b->gemm_bk = (bk && std::strcmp(bk, "32") == 0) ? 32 : 64;
+        // Tuning knob: EP_GEMM_LIGHT_ROWS=n, experts with at most n rows are
+        // scheduled as light (0: one sequence in expert order).
+        const char* lr = std::getenv("EP_GEMM_LIGHT_ROWS");
+        b->gemm_light_rows = lr ? (std::atoi(lr) > 0 ? std::atoi(lr) : 0) : kGemmLightRows;
         // Tuning knob: EP_DEDUP_FUSED=0 runs the dedupe dispatch as positions + copy kernels.
         const char* df = std::getenv("EP_DEDUP_FUSED");
         b->dedup_fused = !(df && std::strcmp(df, "0") == 0);
@@ -723,6 +731,7 @@ ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights
                  ? buf->gemm_kind
                  : (buf->last_T * buf->cfg.topk >= (int64_t)512 * buf->cfg.num_experts ? 2 : 1);
     a.bk = buf->gemm_bk;
+    a.light_rows = buf->gemm_light_rows;
     a.err = buf->err;
     int kernel = 0, grid = 0;
     const cudaError_t e = ep::launch_expert_gemm(a, x_recv, rows, weights, buf->num_sms,

@@ -44,6 +44,8 @@ struct GemmArgs {
     int kind;                      // 1 single-CTA 128-row tiles, 2 two-SM 256-row tiles
                                    // (needs dout % 256 == 0, else falls back to 1)
     int bk;                        // K per ring stage: 64 or 32
+    int light_rows;                // experts with at most this many rows are scheduled as
+                                   // light (interleaved with the rest); 0: none is
     uint32_t* err;
 };
 // x: [rows][din] bf16 receive rows; w: [E][dout][din] bf16.

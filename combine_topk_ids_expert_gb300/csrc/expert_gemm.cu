@@ -10,6 +10,13 @@
 //   - one CTA per SM, persistent over output tiles of 128 rows x BN columns
 //     of one expert (tile order: the column blocks of one row block first,
 //     so the row block is reused from L2);
+//   - light experts (at most light_rows rows: their weights are read from
+//     HBM for one or two row tiles, so their tiles wait on memory) and heavy
+//     ones (weights reused from L2 by many row tiles, so their tiles wait on
+//     the tensor cores) form two tile sequences, each in expert order, that
+//     are interleaved in proportion to their lengths: at every point of the
+//     schedule both kinds run side by side, instead of a tensor-bound phase
+//     followed by a memory-bound one when the routing is skewed;
 //   - warp 0 (one thread) streams BK-wide K slices of the row block and of
 //     the expert's weights into a shared-memory ring with TMA tensor copies
 //     (128-byte swizzle for BK = 64, 64-byte for BK = 32), completion on
@@ -59,12 +66,12 @@ constexpr int kPairBN = 256;
 constexpr uint16_t kBothCtas = 0x3;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_103
 
-// Bytes after the ring: barriers, TMEM address, abort flag and the
-// per-expert tile prefix (sized for the largest expert count).
+// Bytes after the ring: barriers, TMEM address, abort flag and the two
+// per-expert tile prefixes (heavy, light; sized for the largest expert count).
 template <int STAGES>
 constexpr int tail_bytes()
 {
-    return 8 * (2 * STAGES + 5) + 8 + 4 * (kMaxExperts + 1);
+    return 8 * (2 * STAGES + 5) + 8 + 8 * (kMaxExperts + 1);
 }
 
 template <int BN_, int BK_, int STAGES_, bool PAIR_>
@@ -333,14 +340,30 @@ struct TileRef {
     int nb;   // column block
 };
 
-// Work unit u = (global row tile, column block), column blocks fastest.
-__device__ __forceinline__ TileRef tile_of(const int* s_mtile, int E, int nbk, int u)
+// The schedule: uh heavy units then, interleaved with them in proportion,
+// total - uh light ones. Within a class, unit v = (row tile of the class's
+// prefix, column block), column blocks fastest.
+struct Schedule {
+    const int* heavy;   // [E + 1] prefix of the heavy experts' row tiles (light: 0)
+    const int* light;   // [E + 1] prefix of the light experts' row tiles (heavy: 0)
+    int uh, total;      // heavy units, all units
+};
+
+// Unit u is the h-th heavy unit when floor((u + 1) uh / total) steps past
+// h = floor(u uh / total), else the (u - h)-th light one: the heavy units
+// before u are exactly floor(u uh / total), so every unit of both classes
+// appears once.
+__device__ __forceinline__ TileRef tile_of(const Schedule& q, int E, int nbk, int u)
 {
+    const int h = (int)(((int64_t)u * q.uh) / q.total);
+    const bool heavy = (int)(((int64_t)(u + 1) * q.uh) / q.total) > h;
+    const int* pre = heavy ? q.heavy : q.light;
+    const int v = heavy ? h : u - h;
     TileRef p;
-    const int mt = u / nbk;
-    p.nb = u % nbk;
-    p.e = expert_of(s_mtile, E, mt);
-    p.mt = mt - s_mtile[p.e];
+    const int mt = v / nbk;
+    p.nb = v % nbk;
+    p.e = expert_of(pre, E, mt);
+    p.mt = mt - pre[p.e];
     return p;
 }
 
@@ -368,7 +391,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
     const uint32_t drain = accum_empty0 + 16u;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-    int* s_mtile = const_cast<int*>(reinterpret_cast<volatile int*>(s_abort + 1));   // [E + 1]
+    int* s_heavy = const_cast<int*>(reinterpret_cast<volatile int*>(s_abort + 1));   // [E + 1]
+    int* s_light = s_heavy + (kMaxExperts + 1);                                        // [E + 1]
     const int E = a.E;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -402,20 +426,32 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
 
     griddep_wait();   // counts, offsets and the receive rows come from earlier kernels
 
-    // Prefix over experts of their row tiles (kTileRows rows each).
+    // Prefixes over experts of their row tiles (kTileRows rows each), one per
+    // class: experts with at most light_rows rows are light.
     if (warp == 0) {
-        int carry = 0;
-        if (lane == 0) s_mtile[0] = 0;
+        int carry_h = 0, carry_l = 0;
+        if (lane == 0) s_heavy[0] = s_light[0] = 0;
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
-            int m = (e < E) ? (__ldcg(a.cnt + e) + C::kTileRows - 1) / C::kTileRows : 0;
+            const int c = (e < E) ? __ldcg(a.cnt + e) : 0;
+            const int m = (c + C::kTileRows - 1) / C::kTileRows;
+            const bool is_light = c <= a.light_rows;
+            int mh = is_light ? 0 : m, ml = is_light ? m : 0;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, m, d);
-                if (lane >= d) m += n;
+                const int nh = __shfl_up_sync(0xffffffffu, mh, d);
+                const int nl = __shfl_up_sync(0xffffffffu, ml, d);
+                if (lane >= d) {
+                    mh += nh;
+                    ml += nl;
+                }
             }
-            if (e < E) s_mtile[e + 1] = carry + m;
-            carry += __shfl_sync(0xffffffffu, m, 31);
+            if (e < E) {
+                s_heavy[e + 1] = carry_h + mh;
+                s_light[e + 1] = carry_l + ml;
+            }
+            carry_h += __shfl_sync(0xffffffffu, mh, 31);
+            carry_l += __shfl_sync(0xffffffffu, ml, 31);
         }
     }
     tc_fence_before();
@@ -423,13 +459,18 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
     if (PAIR) cluster_sync();   // the peer's barriers exist before any copy or arrival reaches them
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const int total = s_mtile[E] * nbk;
+    Schedule q;
+    q.heavy = s_heavy;
+    q.light = s_light;
+    q.uh = s_heavy[E] * nbk;
+    q.total = q.uh + s_light[E] * nbk;
+    const int total = q.total;
 
     if (warp == 0 && lane == 0) {
         // ---- TMA producer (each CTA fills its own ring) --------------------
         int g = 0;   // k-slices issued
         for (int u = first; u < total && !*s_abort; u += step) {
-            const TileRef p = tile_of(s_mtile, E, nbk, u);
+            const TileRef p = tile_of(q, E, nbk, u);
             const int row0 = __ldcg(a.expert_offset + p.e) + p.mt * C::kTileRows + r * kBM;
             const int wrow0 = p.e * (int)a.dout + p.nb * BN + r * C::kRowsB;
             for (int k = 0; k < k_iters; ++k, ++g) {
@@ -508,7 +549,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
             if (!wait_or_abort(accum_full0 + 8u * acc, (uint32_t)(use & 1), s_abort)) break;
             tc_fence_after();
             const uint32_t t_acc = t_lane + (uint32_t)(acc * BN);
-            const TileRef p = tile_of(s_mtile, E, nbk, u);
+            const TileRef p = tile_of(q, E, nbk, u);
             const int m_in = p.mt * C::kTileRows + r * kBM;
             const int rows = min(kBM, __ldcg(a.cnt + p.e) - m_in);
             const int64_t row = (int64_t)__ldcg(a.expert_offset + p.e) + m_in + r_in;

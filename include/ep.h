@@ -325,7 +325,12 @@ EP_API ep_status ep_dedup_expand(ep_buffer* buf, const int32_t* topk_expert_ids_
  * routed at least 512 rows per expert on average (T * K >= 512 * E), else
  * 128 rows per SM; both issue the same K order, so they agree bit for bit.
  * The environment variable EP_GEMM_KERNEL=1 (128-row) or 2 (256-row), read at
- * ep_buffer_init, forces one of them. */
+ * ep_buffer_init, forces one of them. Schedule: the tiles of experts with at
+ * most 256 rows (memory-bound: their weights serve one or two tiles) are
+ * interleaved in proportion with the others' (tensor-bound: weights reused
+ * from L2), so skewed routing keeps both HBM and the tensor cores busy;
+ * EP_GEMM_LIGHT_ROWS=n sets the threshold (0: all tiles in expert order).
+ * The schedule changes which SM computes a tile, never its K order. */
 EP_API ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* weights,
                                 int64_t din, int64_t dout, void* y_recv, ep_stream_t stream);
 

@@ -67,14 +67,21 @@ def expected_kind(kind: str, dout: int) -> int:
     return int(kind) if dout % 256 == 0 else 1
 
 
-@pytest.mark.parametrize("kind,bk", [("2", "64"), ("1", "64"), ("2", "32")])
+@pytest.mark.parametrize("kind,bk,light", [("2", "64", None), ("1", "64", None), ("2", "32", None),
+                                           ("1", "64", "0"), ("2", "64", "0")])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_expert_gemm_parity(orc, monkeypatch, case, kind, bk):
+def test_expert_gemm_parity(orc, monkeypatch, case, kind, bk, light):
     # kind: 1 single-CTA 128-row tiles, 2 two-SM 256-row tiles (falls back to 1
     # where dout % 256 != 0); bk: K per ring stage (128-byte swizzle at 64,
-    # 64-byte at 32)
+    # 64-byte at 32); light: the schedule's light-expert threshold in rows
+    # (None: the default, light experts interleaved with heavy ones; "0": one
+    # sequence in expert order)
     monkeypatch.setenv("EP_GEMM_KERNEL", kind)
     monkeypatch.setenv("EP_GEMM_BK", bk)
+    if light is None:
+        monkeypatch.delenv("EP_GEMM_LIGHT_ROWS", raising=False)
+    else:
+        monkeypatch.setenv("EP_GEMM_LIGHT_ROWS", light)
     seed, T, N, din, dout, E, K, R, ik, layout = CASES[case]
     x = W.hidden(seed, T, din, "bf16")
     ids, sc = W.routing(seed, T, E, K, ik, "sigmoid_norm")
@@ -97,7 +104,10 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
     # Full workload shape, D -> 2048: the 2-SM kernel (M = 256 across a pair)
     # and the single-CTA kernel (M = 128), at 64- and 32-wide K slices, issue the
     # same K=16 steps in the same order for every output, so all agree bit for
-    # bit; sampled rows of a few experts are checked against the oracle.
+    # bit; so do the schedules (light experts interleaved with heavy ones at the
+    # default threshold, none light, all light), which change only which SM
+    # computes a tile and when. Sampled rows of a few experts are checked
+    # against the oracle.
     w_ = W.WORKLOADS[name]
     inp = W.make(name)
     D, E, dout = w_.D, w_.E, 2048
@@ -106,9 +116,15 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
     gen.manual_seed(1234)
     wd = (torch.randn((E * dout, D), generator=gen, device="cuda") * 0.03).to(torch.bfloat16)
     bufs, ys = [], []
-    for kind, bk in (("2", "64"), ("1", "64"), ("2", "32"), ("1", "32")):
+    for kind, bk, light in (("2", "64", None), ("1", "64", None), ("2", "32", None),
+                            ("1", "32", None), ("1", "64", "0"), ("2", "64", "0"),
+                            ("1", "64", "1000000"), ("2", "64", "1000000")):
         monkeypatch.setenv("EP_GEMM_KERNEL", kind)
         monkeypatch.setenv("EP_GEMM_BK", bk)
+        if light is None:
+            monkeypatch.delenv("EP_GEMM_LIGHT_ROWS", raising=False)
+        else:
+            monkeypatch.setenv("EP_GEMM_LIGHT_ROWS", light)
         buf = ep.Buffer(w_.N_max, D, E, w_.R, w_.K, dtype=torch.bfloat16)
         d = buf.dispatch(xd, scd, idd, w_.N)
         rows = w_.R * d.layout.rank_stride
@@ -119,7 +135,7 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
         assert buf.info()["gemm_kernel"] == int(kind)
         if bufs:
             buf.close()
-            assert torch.equal(ys[0].view(torch.int16), y.view(torch.int16)), (kind, bk)
+            assert torch.equal(ys[0].view(torch.int16), y.view(torch.int16)), (kind, bk, light)
             del d, y
         else:
             bufs.append((buf, d))
