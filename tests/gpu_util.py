@@ -40,14 +40,15 @@ def assert_layout_equal(lay: ep.Layout, ref: dict) -> None:
 
 
 def assert_recv_equal(d: ep.DispatchResult, ref: dict, R: int) -> None:
-    """Every defined receive row (inside each rank's true total) equals the oracle's."""
+    """Every defined receive row (inside each rank's true total) equals the oracle's,
+    bit for bit (NaN payloads and signed zeros included: the rows are copies)."""
     S = ref["S"]
     rx = to_np(d.recv_x.reshape(R * S, -1))
     rs = to_np(d.recv_scores.reshape(-1))
     rsrc = to_np(d.recv_src.reshape(-1))
     for r in range(R):
         lo, hi = r * S, r * S + int(ref["rows_per_rank"][r])
-        assert np.array_equal(rx[lo:hi], ref["recv_x"][lo:hi]), f"recv_x rank {r}"
+        assert np.array_equal(bits(rx[lo:hi]), bits(ref["recv_x"][lo:hi])), f"recv_x rank {r}"
         assert np.array_equal(rs[lo:hi].view(np.uint32),
                               ref["recv_scores"][lo:hi].view(np.uint32)), f"recv_scores rank {r}"
         assert np.array_equal(rsrc[lo:hi], ref["recv_src"][lo:hi]), f"recv_src rank {r}"

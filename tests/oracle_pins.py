@@ -642,4 +642,85 @@ def pin_combine_backward_score_gradient_exact(o):
     assert gs[0, 0] == np.float32(32.0)
 
 
+# ---------------------------------------------------------------------------
+# IEEE special values: overflow, signed zero, infinities, NaN, subnormals
+# ---------------------------------------------------------------------------
+
+def pin_bf16_nan_stays_nan(o):
+    # A NaN must round to a NaN of the same sign, even when all of its payload
+    # sits in the dropped low half (truncation would turn 7f800001 into +inf).
+    for f_hex in ("7fc00000", "7f800001", "ff800001", "7fffffff", "ffc00000", "7f80ffff"):
+        f = np.array([int(f_hex, 16)], dtype=np.uint32).view(np.float32)
+        h = int(o.bf16_from_f32(f)[0])
+        assert (h & 0x7F80) == 0x7F80 and (h & 0x007F) != 0, (f_hex, hex(h))
+        assert (h >> 15) == (int(f_hex, 16) >> 31), (f_hex, hex(h))
+
+
+BF16_MAX, BF16_MIN_SUB = 0x7F7F, 0x0001
+
+
+def special_value_case():
+    """Six tokens, two experts each (ids [0, 1], one rank), and the two rows
+    each token gathers, every element of a row the same bf16 value. Returns
+    (ids, scores, rows [T, 2] of bf16 patterns, expected bf16 output per
+    token, None where the result is NaN). The expected values follow from the
+    fma chain acc = fma(s1, y1, fma(s0, y0, +0)) and round-to-nearest-even:
+      0: max + 2^119 = (2 - 2^-8) 2^127 exactly, a tie above the largest
+         finite bf16 with an odd kept bit: +inf;
+      1: max + 2^118 = (2 - 2^-7 + 2^-9) 2^127, below the tie: max;
+      2: -0 + -0 from an accumulator of +0: fma(1, -0, +0) = +0, so +0;
+      3: +inf + -inf: NaN;
+      4: 0.75 * 2^-133 = 3 * 2^-135, an fp32 subnormal (0x0000c000), above
+         the bf16 tie: the smallest bf16 subnormal, 0x0001 (a flush to zero
+         would give 0);
+      5: 0 * inf: NaN."""
+    ids = np.tile(np.array([[0, 1]], np.int32), (6, 1))
+    sc = np.array([[1, 1], [1, 1], [1, 1], [1, 1], [0.75, 0], [0, 1]], np.float32)
+    rows = np.array([[BF16_MAX, 0x7B00],        # max, 2^119
+                     [BF16_MAX, 0x7A80],        # max, 2^118
+                     [0x8000, 0x8000],          # -0, -0
+                     [0x7F80, 0xFF80],          # +inf, -inf
+                     [BF16_MIN_SUB, 0x3F80],    # 2^-133, 1 (weight 0)
+                     [0x7F80, 0x3F80]],         # +inf (weight 0), 1
+                    np.uint16)
+    want = [0x7F80, BF16_MAX, 0x0000, None, BF16_MIN_SUB, None]
+    return ids, sc, rows, want
+
+
+def special_value_y(d, rows, D):
+    """The receive buffer of dispatch result d with each token's two gathered
+    rows replaced by the case's constant rows."""
+    y = np.array(d["recv_x"], copy=True)
+    for t in range(rows.shape[0]):
+        for k in range(2):
+            y[int(d["pos"][t, k])] = np.full(D, rows[t, k], np.uint16)
+    return y
+
+
+def bf16_is_nan(h):
+    h = np.asarray(h, np.uint16)
+    return ((h & 0x7F80) == 0x7F80) & ((h & 0x007F) != 0)
+
+
+def pin_combine_ieee_special_values(o):
+    ids, sc, rows, want = special_value_case()
+    T, D, E, R = ids.shape[0], 8, 2, 1
+    x = np.zeros((T, D), np.uint16)
+    d = o.dispatch(x, sc, ids, T, E, R)
+    y = special_value_y(d, rows, D)
+    out, err = o.combine(y, sc, d["pos"], d["rank_prefix"], d["S"], R)
+    assert err == 0
+    for t, w in enumerate(want):
+        if w is None:
+            assert np.all(bf16_is_nan(out[t])), (t, out[t])
+        else:
+            assert np.all(out[t] == w), (t, hex(int(out[t, 0])), hex(w))
+    # fp32 output: token 0 keeps the exact sum (2 - 2^-8) 2^127 = 0x7f7f8000,
+    # token 4 the subnormal 0x0000c000.
+    out32, _ = o.combine(y, sc, d["pos"], d["rank_prefix"], d["S"], R, "f32")
+    assert np.all(out32[0].view(np.uint32) == 0x7F7F8000)
+    assert np.all(out32[4].view(np.uint32) == 0x0000C000)
+    assert np.all(out32[2].view(np.uint32) == 0)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

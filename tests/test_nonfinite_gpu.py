@@ -1,0 +1,115 @@
+"""Extreme and non-finite values through dispatch and combine, on every dispatch path.
+
+- x drawn as uniformly random bit patterns: NaNs, infinities, subnormals,
+  signed zeros and values near the overflow threshold all occur. The dispatch
+  copies bytes, so every receive row equals the oracle's bit for bit, NaN
+  payloads included.
+- The combine equals the oracle bit for bit wherever the oracle's result is not
+  a NaN, and is a NaN wherever it is (which NaN the bf16 rounding or the fma
+  returns is not fixed by the pages: payloads are left unpinned).
+- Rows made by hand for the bf16 overflow tie, a sum just below it, -0 + -0,
+  inf - inf, a subnormal product (a flush to zero would show) and 0 * inf are
+  checked against the values IEEE-754 arithmetic fixes, and against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_topk_ids_expert_gb300 as ep
+import workloads as W
+from gpu_util import assert_layout_equal, assert_recv_equal, bits, to_dev, to_np, torch_dtype
+from oracle_pins import bf16_is_nan, special_value_case, special_value_y
+
+pytestmark = pytest.mark.gpu
+
+TAG_BITS = 31
+
+
+@pytest.fixture(params=["onepass", "fused", "vec"])
+def path(request, monkeypatch):
+    if request.param == "fused":
+        monkeypatch.setenv("EP_DISPATCH_ONEPASS", "0")
+    return ep.EP_PERMUTE_VEC if request.param == "vec" else ep.EP_PERMUTE_BULK
+
+
+def is_nan(a: np.ndarray) -> np.ndarray:
+    return bf16_is_nan(a) if a.dtype == np.uint16 else np.isnan(a)
+
+
+def assert_equal_nan_as_class(got: np.ndarray, want: np.ndarray) -> None:
+    assert got.shape == want.shape and got.dtype == want.dtype
+    nw, ng = is_nan(want), is_nan(got)
+    assert np.array_equal(nw, ng), f"{int((nw != ng).sum())} outputs differ in NaN-ness"
+    assert np.array_equal(bits(got)[~nw], bits(want)[~nw]), "combine differs from the oracle"
+
+
+def random_bits(seed: int, T: int, D: int, dtype: str) -> np.ndarray:
+    v = W.u64(seed, TAG_BITS, T * D).reshape(T, D)
+    if dtype == "bf16":
+        return (v & np.uint64(0xFFFF)).astype(np.uint16)
+    return (v & np.uint64(0xFFFFFFFF)).astype(np.uint32).view(np.float32)
+
+
+CASES = {
+    # name: (seed, T, N, D, dtype, E, K, R)
+    "bf16": (160, 300, 302, 128, "bf16", 16, 4, 4),
+    "f32": (161, 200, 200, 64, "f32", 8, 3, 2),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_random_bit_patterns(orc, path, case):
+    seed, T, N, D, dtype, E, K, R = CASES[case]
+    x = random_bits(seed, T, D, dtype)
+    ids, sc = W.routing(seed, T, E, K, "zipf", "sigmoid_norm")
+    sc[::7, 0] = 0.0          # 0 * inf and 0 * NaN occur too
+    buf = ep.Buffer(N, D, E, R, K, dtype=torch_dtype(dtype), permute_impl=path)
+    scd = to_dev(sc)
+    d = buf.dispatch(to_dev(x), scd, to_dev(ids), N)
+    outs = {"same": buf.combine(d.recv_x, scd)}
+    if dtype == "bf16":
+        outs["f32"] = buf.combine(d.recv_x, scd, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, N, E, R)
+    assert_layout_equal(d.layout, ref)
+    assert_recv_equal(d, ref, R)
+    n_nan = 0
+    for kind, out in outs.items():
+        want, err = orc.combine(ref["recv_x"], sc, ref["pos"], ref["rank_prefix"], ref["S"], R,
+                                kind)
+        assert err == 0
+        assert_equal_nan_as_class(to_np(out), want)
+        n_nan += int(is_nan(want).sum())
+    assert n_nan > 0, "the inputs produced no NaN: the case tests nothing it claims"
+    buf.close()
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_ieee_special_values(orc, path, out_dtype):
+    ids, sc, rows, want = special_value_case()
+    T, D, E, R, K = ids.shape[0], 8, 2, 1, 2
+    x = np.zeros((T, D), np.uint16)
+    buf = ep.Buffer(T, D, E, R, K, dtype=torch.bfloat16, permute_impl=path)
+    scd = to_dev(sc)
+    d = buf.dispatch(to_dev(x), scd, to_dev(ids), T)
+    ref = orc.dispatch(x, sc, ids, T, E, R)
+    assert_layout_equal(d.layout, ref)
+    y = special_value_y(ref, rows, D)
+    od = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+    out = to_np(buf.combine(to_dev(y), scd, out_dtype=od))
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    oracle_out, err = orc.combine(y, sc, ref["pos"], ref["rank_prefix"], ref["S"], R, out_dtype)
+    assert err == 0
+    assert_equal_nan_as_class(out, oracle_out)
+    if out_dtype == "bf16":
+        for t, w in enumerate(want):
+            if w is None:
+                assert np.all(bf16_is_nan(out[t])), t
+            else:
+                assert np.all(out[t] == w), (t, hex(int(out[t, 0])), hex(w))
+    else:
+        u = out.view(np.uint32)
+        assert np.all(u[0] == 0x7F7F8000) and np.all(u[2] == 0) and np.all(u[4] == 0x0000C000)
+    buf.close()

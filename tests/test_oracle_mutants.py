@@ -36,6 +36,8 @@ MUTANTS = {
     21: "dedupe records global expert ids",
     22: "dedupe expansion reads another rank's row",
     23: "combine backward score gradient summed in fp32",
+    24: "combine flushes subnormal results to zero",
+    25: "bf16 cast rounds NaNs like numbers",
 }
 
 
