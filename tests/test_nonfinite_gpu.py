@@ -113,3 +113,64 @@ def test_ieee_special_values(orc, path, out_dtype):
         u = out.view(np.uint32)
         assert np.all(u[0] == 0x7F7F8000) and np.all(u[2] == 0) and np.all(u[4] == 0x0000C000)
     buf.close()
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_backward_random_bit_patterns(orc, case):
+    # grad_y = s * grad_out (one product, one rounding) and grad_x (the fma chain
+    # with unit weights) against the oracle, NaN as a class. The score gradients
+    # (length-D dot products in a free fp32 order) are left out here: with
+    # magnitudes up to the format's maximum, a partial fp32 sum can overflow where
+    # the oracle's exact sum does not.
+    seed, T, N, D, dtype, E, K, R = CASES[case]
+    x = random_bits(seed, T, D, dtype)
+    g = random_bits(seed + 1, T, D, dtype)
+    ids, sc = W.routing(seed, T, E, K, "uniform", "sigmoid_norm")
+    sc[::5, -1] = 0.0
+    buf = ep.Buffer(N, D, E, R, K, dtype=torch_dtype(dtype))
+    scd = to_dev(sc)
+    d = buf.dispatch(to_dev(x), scd, to_dev(ids), N)
+    grad_y, _ = buf.combine_backward(to_dev(g), d.recv_x, scd, want_scores=False)
+    grad_x, _ = buf.dispatch_backward(grad_y, T)
+    grad_x32, _ = buf.dispatch_backward(grad_y, T, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, N, E, R)
+    S = ref["S"]
+    gy_ref, _, err = orc.combine_backward(g, ref["recv_x"], sc, ref["pos"], ref["rank_prefix"],
+                                          S, R)
+    assert err == 0
+    pos = ref["pos"]
+    valid = pos[pos >= 0]
+    assert_equal_nan_as_class(to_np(grad_y.reshape(R * S, D))[valid], gy_ref[valid])
+    for out, kind in ((grad_x, "same"), (grad_x32, "f32")):
+        want, _, _ = orc.dispatch_backward(gy_ref, None, pos, ref["rank_prefix"], S, R, kind)
+        assert_equal_nan_as_class(to_np(out), want)
+    buf.close()
+
+
+def test_dedup_random_bit_patterns(orc):
+    # The dedupe rows and their expansion are copies: bit for bit, NaN payloads
+    # included; the combine on the expanded rows as above.
+    seed, T, N, D, dtype, E, K, R = CASES["bf16"]
+    x = random_bits(seed + 7, T, D, dtype)
+    ids, sc = W.routing(seed + 7, T, E, K, "zipf", "sigmoid_norm")
+    buf = ep.Buffer(N, D, E, R, K, dtype=torch.bfloat16)
+    scd, idd = to_dev(sc), to_dev(ids)
+    dd = buf.dispatch_dedup(to_dev(x), scd, idd, N)
+    y = buf.dedup_expand(idd)
+    out = buf.combine(y, scd)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch_dedup(x, sc, ids, N, E, R)
+    P, tir = ref["P"], ref["tokens_in_rank"]
+    rx = to_np(dd.recv_x.reshape(R * P, D))
+    for r in range(R):
+        rows = slice(r * P, r * P + int(tir[r]))
+        assert np.array_equal(bits(rx[rows]), bits(ref["recv_tok_x"][rows]))
+    d = orc.dispatch(x, sc, ids, N, E, R)
+    valid = d["pos"][d["pos"] >= 0]
+    assert np.array_equal(bits(to_np(y.reshape(-1, D))[valid]), bits(d["recv_x"][valid]))
+    want, _ = orc.combine(d["recv_x"], sc, d["pos"], d["rank_prefix"], d["S"], R)
+    assert_equal_nan_as_class(to_np(out), want)
+    buf.close()
