@@ -40,14 +40,18 @@ def assert_layout_equal(lay: ep.Layout, ref: dict) -> None:
 
 
 def assert_recv_equal(d: ep.DispatchResult, ref: dict, R: int) -> None:
-    """Every defined receive row (inside each rank's true total) equals the oracle's,
-    bit for bit (NaN payloads and signed zeros included: the rows are copies)."""
+    """Every defined receive row (inside each rank's true total; for the packed
+    layout, every row below the true total) equals the oracle's, bit for bit (NaN
+    payloads and signed zeros included: the rows are copies)."""
     S = ref["S"]
     rx = to_np(d.recv_x.reshape(R * S, -1))
     rs = to_np(d.recv_scores.reshape(-1))
     rsrc = to_np(d.recv_src.reshape(-1))
-    for r in range(R):
-        lo, hi = r * S, r * S + int(ref["rows_per_rank"][r])
+    if d.layout.packed:     # ranks back to back: rows [0, true total)
+        ranges = [(0, int(ref["rank_prefix"][-1]))]
+    else:                   # rank r: rows [r*S, r*S + rows_per_rank[r])
+        ranges = [(r * S, r * S + int(ref["rows_per_rank"][r])) for r in range(R)]
+    for r, (lo, hi) in enumerate(ranges):
         assert np.array_equal(bits(rx[lo:hi]), bits(ref["recv_x"][lo:hi])), f"recv_x rank {r}"
         assert np.array_equal(rs[lo:hi].view(np.uint32),
                               ref["recv_scores"][lo:hi].view(np.uint32)), f"recv_scores rank {r}"
