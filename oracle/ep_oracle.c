@@ -24,7 +24,8 @@
  *
  * Conventions: ids are int32, -1 means "no expert"; scores are fp32; hidden
  * rows are either fp32 or bf16 stored as uint16 bit patterns. Return value 0 =
- * success, 1 = invalid argument, 2 = out of memory (host scratch).
+ * success, 1 = invalid argument, 2 = out of memory (host scratch), 3 = a
+ * computed receive row outside the receive buffer (refused, never written).
  */
 #include <math.h>
 #include <stdint.h>
@@ -34,6 +35,7 @@
 #define ORC_OK 0
 #define ORC_EINVAL 1
 #define ORC_ENOMEM 2
+#define ORC_EBOUNDS 3   /* a computed receive row outside the receive buffer */
 
 /* Element kinds of hidden rows, as the Python wrapper passes them. */
 #define ORC_BF16 0
@@ -334,7 +336,9 @@ int oracle_layout(const int32_t* ids, int64_t T, int64_t N, int32_t K, int32_t E
  * entries, where S = oracle_rank_stride(N, K). For each pair with a row p:
  *   recv_x[p] = x[t], recv_scores[p] = scores[t][k], recv_src[p] = t*K + k.
  * Receive rows past a rank's true total are left as the caller filled them.
- * The layout outputs are written as oracle_layout writes them.
+ * The layout outputs are written as oracle_layout writes them. A position
+ * outside the R * S receive rows returns ORC_EBOUNDS before anything is
+ * written there.
  */
 int oracle_dispatch(const void* x, int64_t row_bytes, const float* scores, const int32_t* ids,
                     int64_t T, int64_t N, int32_t K, int32_t E, int32_t R, int32_t packed,
@@ -349,10 +353,14 @@ int oracle_dispatch(const void* x, int64_t row_bytes, const float* scores, const
     if (rc != ORC_OK) return rc;
     const uint8_t* xb = (const uint8_t*)x;
     uint8_t* rb = (uint8_t*)recv_x;
+    /* The receive buffer holds R * S rows; a position outside it cannot come
+     * from a correct layout, and is refused instead of written. */
+    const int64_t rows = (int64_t)R * *S_out;
     for (int64_t t = 0; t < T; ++t)
         for (int32_t k = 0; k < K; ++k) {
             int64_t p = pos_TK[t * K + k];
             if (p < 0) continue;
+            if (p >= rows) return ORC_EBOUNDS;
             memcpy(rb + p * row_bytes, xb + t * row_bytes, (size_t)row_bytes);
             recv_scores[p] = scores[t * K + k];
 #if ORACLE_MUTANT == 19
