@@ -39,9 +39,9 @@ def _kind(a: np.ndarray) -> int:
 class Oracle:
     """One loaded build of the oracle (mutant=0 is the real one)."""
 
-    def __init__(self, mutant: int = 0):
+    def __init__(self, mutant: int = 0, sanitize: bool = False):
         self.mutant = mutant
-        self.lib = C.CDLL(build_oracle(mutant))
+        self.lib = C.CDLL(build_oracle(mutant, sanitize=sanitize))
         L = self.lib
         i64, i32 = C.c_int64, C.c_int32
         for name, args in {

@@ -16,19 +16,25 @@ SRC = os.path.join(HERE, "ep_oracle.c")
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-Wall", "-Wextra"]
 
 
-def lib_path(mutant: int = 0) -> str:
-    name = "libep_oracle.so" if mutant == 0 else f"libep_oracle_mutant{mutant}.so"
+# AddressSanitizer build (used by the CPU tests with libasan preloaded).
+ASAN_FLAGS = ["-fsanitize=address", "-fno-omit-frame-pointer", "-g"]
+
+
+def lib_path(mutant: int = 0, sanitize: bool = False) -> str:
+    name = "libep_oracle" + ("" if mutant == 0 else f"_mutant{mutant}")
+    name += "_asan.so" if sanitize else ".so"
     return os.path.join(HERE, "_build", name)
 
 
-def build_oracle(mutant: int = 0, force: bool = False) -> str:
-    out = lib_path(mutant)
+def build_oracle(mutant: int = 0, force: bool = False, sanitize: bool = False) -> str:
+    out = lib_path(mutant, sanitize)
     if (not force and os.path.exists(out)
             and os.path.getmtime(out) >= os.path.getmtime(SRC)):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
-    cmd = ["gcc", *CFLAGS, f"-DORACLE_MUTANT={mutant}", SRC, "-o", tmp, "-lm"]
+    extra = ASAN_FLAGS if sanitize else []
+    cmd = ["gcc", *CFLAGS, *extra, f"-DORACLE_MUTANT={mutant}", SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
