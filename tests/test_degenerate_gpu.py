@@ -4,7 +4,9 @@
 - no routing at all (every id is -1): empty layout, zero output rows;
 - K = E: every token selects every expert;
 - a tiny call in a large buffer (T = 1 with N_max = 100,000: the per-rank
-  stride follows the call's N, not N_max).
+  stride follows the call's N, not N_max);
+- the combine follows ascending k (an order-sensitive fma chain);
+- an empty call (T = 0) after a full one: the layout describes the empty call.
 """
 import numpy as np
 import pytest
@@ -84,3 +86,28 @@ def test_combine_follows_ascending_k(orc, path):
         sc = np.array([[1.0, 2.0 ** -24, -1.0]], np.float32)
         _, out = check(orc, x, ids, sc, 1, 1, 4, "f32", 4, 3, 1, path)
         assert np.array_equal(out.view(np.uint32), np.zeros((1, 4), np.uint32))
+
+
+def test_empty_call_after_a_full_one(orc, path):
+    # T = 0 (with N = 0 and with N = 6) after a call that filled the layout: the
+    # layout must describe the empty call (every count and prefix zero, S = P*K),
+    # not the previous one; the combine of zero tokens is a no-op; the next full
+    # call is exact again.
+    D, E, K, R = 64, 16, 4, 4
+    buf = ep.Buffer(300, D, E, R, K, dtype=torch.bfloat16, permute_impl=path)
+    x = W.hidden(154, 200, D, "bf16")
+    ids, sc = W.routing(154, 200, E, K, "zipf", "sigmoid_norm")
+    buf.dispatch(to_dev(x), to_dev(sc), to_dev(ids), 200)
+    for N in (0, 6):
+        x0 = np.zeros((0, D), np.uint16)
+        ids0 = np.zeros((0, K), np.int32)
+        sc0 = np.zeros((0, K), np.float32)
+        d = buf.dispatch(to_dev(x0), to_dev(sc0), to_dev(ids0), N)
+        out = buf.combine(d.recv_x, to_dev(sc0))
+        torch.cuda.synchronize()
+        assert buf.device_error() == 0
+        assert out.shape == (0, D)
+        ref = orc.dispatch(x0, sc0, ids0, N, E, R)
+        assert_layout_equal(d.layout, ref)
+        assert ref["S"] == ((N + 3) // 4 * 4) * K
+    check(orc, x, ids, sc, 200, 300, D, "bf16", E, K, R, path)
