@@ -3,7 +3,8 @@
  *
  * One process drives one GPU. "Ranks" are R logical partitions of this GPU's
  * receive buffer: experts are split into R contiguous blocks of E/R experts,
- * and rank r owns receive rows [r*S, (r+1)*S). Everything here follows the
+ * and rank r owns receive rows [r*S, (r+1)*S) (the default strided layout;
+ * EP_LAYOUT_PACKED puts the ranks' rows back to back). Everything here follows the
  * token-dispatcher pages:
  *   [titan] "Unify expert parallel token dispatcher API" (pytorch/torchtitan
  *           pull 3970): sections "API design", "Backend behavior",
