@@ -35,7 +35,8 @@ __all__ = [
     "ep_dispatch", "ep_dispatch_permute", "ep_combine", "ep_combine_backward",
     "ep_dispatch_backward", "ep_dispatch_dedup", "ep_dedup_expand", "ep_expert_gemm",
     "ep_get_device_error", "DedupResult",
-    "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_pad_tokens", "ep_derive_max_tokens_pretrain",
+    "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_pad_tokens", "group_num_tokens_per_rank",
+    "ep_derive_max_tokens_pretrain",
     "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
     "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
     "EP_LAYOUT_STRIDED", "EP_LAYOUT_PACKED",
@@ -228,6 +229,27 @@ def ep_dispatch_layout_noalloc(topk_expert_ids_TK: torch.Tensor, num_tokens: int
 
 def ep_pad_tokens(n: int) -> int:
     return int(_abi.lib().ep_pad_tokens(n))
+
+
+def group_num_tokens_per_rank(num_local_tokens: int, group=None) -> int:
+    """num_tokens_per_rank for one expert-parallel group: the largest token count
+    of its ranks ("fix(moe): equalize and align per-rank token counts for HybridEP
+    dispatch", section "Fix": every rank pads to the EP-group max; dispatch then
+    rounds it up to a multiple of 4, as ep_pad_tokens shows). One all-reduce (MAX)
+    over the torch.distributed `group`, on a CUDA tensor under NCCL and a host
+    tensor otherwise; without an initialised process group, the local count.
+    Host logic on host integers: nothing here reads device memory."""
+    import torch.distributed as dist
+    n = int(num_local_tokens)
+    if n < 0:
+        raise ValueError(f"num_local_tokens must be >= 0, got {n}")
+    if not (dist.is_available() and dist.is_initialized()):
+        return n
+    nccl = dist.get_backend(group) == "nccl"
+    dev = torch.device("cuda", torch.cuda.current_device()) if nccl else torch.device("cpu")
+    t = torch.tensor([n], dtype=torch.int64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return int(t.item())
 
 
 def ep_derive_max_tokens_pretrain(local_batch_size: int, seq_len: int, cp: int, tp: int) -> int:
