@@ -20,13 +20,6 @@ from gpu_util import (assert_combine_equal, assert_layout_equal, assert_recv_equ
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["onepass", "fused", "vec"])
-def path(request, monkeypatch):
-    if request.param == "fused":
-        monkeypatch.setenv("EP_DISPATCH_ONEPASS", "0")
-    return ep.EP_PERMUTE_VEC if request.param == "vec" else ep.EP_PERMUTE_BULK
-
-
 def check(orc, x, ids, sc, N, N_max, D, dtype, E, K, R, impl):
     buf = ep.Buffer(N_max, D, E, R, K, dtype=torch_dtype(dtype), permute_impl=impl)
     scd = to_dev(sc)

@@ -25,13 +25,6 @@ pytestmark = pytest.mark.gpu
 TAG_BITS = 31
 
 
-@pytest.fixture(params=["onepass", "fused", "vec"])
-def path(request, monkeypatch):
-    if request.param == "fused":
-        monkeypatch.setenv("EP_DISPATCH_ONEPASS", "0")
-    return ep.EP_PERMUTE_VEC if request.param == "vec" else ep.EP_PERMUTE_BULK
-
-
 def is_nan(a: np.ndarray) -> np.ndarray:
     return bf16_is_nan(a) if a.dtype == np.uint16 else np.isnan(a)
 

@@ -26,13 +26,6 @@ CASES = {
 BULK_STAGES = {"bf16_32k_rows": 6, "bf16_40k_rows": 0, "f32_256k_rows": 0}
 
 
-@pytest.fixture(params=["onepass", "fused", "vec"])
-def path(request, monkeypatch):
-    if request.param == "fused":
-        monkeypatch.setenv("EP_DISPATCH_ONEPASS", "0")
-    return ep.EP_PERMUTE_VEC if request.param == "vec" else ep.EP_PERMUTE_BULK
-
-
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_wide_rows_dispatch_combine(orc, path, case):
     seed, T, N, D, dtype, E, K, R = CASES[case]
