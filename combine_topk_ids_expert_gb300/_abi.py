@@ -19,6 +19,7 @@ EP_ERR_WORKSPACE = 4
 EP_ERR_CAPTURE_HOST_SYNC = 5
 EP_ERR_CUDA = 6
 EP_ERR_NO_LAYOUT = 7
+EP_ERR_HOST_ALLOC = 8
 
 EP_BF16 = 0
 EP_F32 = 1

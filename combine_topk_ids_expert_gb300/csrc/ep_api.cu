@@ -10,6 +10,7 @@
 // no host handshake, no host-mapped counters, counts stay on the device.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -343,6 +344,45 @@ ep_status check_rows(const ep_buffer* b, const void* x, const float* scores)
     return EP_OK;
 }
 
+// ---- environment knobs, read once at ep_buffer_init ------------------------
+
+bool env_is(const char* name, const char* value)
+{
+    const char* v = std::getenv(name);
+    return v && std::strcmp(v, value) == 0;
+}
+
+int64_t env_int(const char* name, int64_t fallback)
+{
+    const char* v = std::getenv(name);
+    return (v && *v) ? std::strtoll(v, nullptr, 10) : fallback;
+}
+
+void read_knobs(ep_buffer* b)
+{
+    b->pdl = !env_is("EP_PDL", "0");
+    // Fused-dispatch CTAs per SM (1 or 2).
+    b->tiles_per_sm = env_is("EP_TILES_PER_SM", "2") ? 2 : 1;
+    // EP_GEMM_KERNEL=1 / 2 forces the expert GEMM's kernel (single-CTA
+    // 128-row tiles, 2-SM 256-row tiles); 0 chooses per call.
+    b->gemm_kind = env_is("EP_GEMM_KERNEL", "1") ? 1 : env_is("EP_GEMM_KERNEL", "2") ? 2 : 0;
+    // EP_GEMM_BK=32 or 64: the expert GEMM's K slice per ring stage.
+    b->gemm_bk = env_is("EP_GEMM_BK", "32") ? 32 : 64;
+    // EP_GEMM_LIGHT_ROWS=n: experts with at most n rows are scheduled as light
+    // (0: one sequence in expert order).
+    const int64_t lr = env_int("EP_GEMM_LIGHT_ROWS", kGemmLightRows);
+    b->gemm_light_rows = lr > 0 ? (int)std::min<int64_t>(lr, INT32_MAX) : 0;
+    // EP_DEDUP_FUSED=0 runs the dedupe dispatch as positions + copy kernels.
+    b->dedup_fused = !env_is("EP_DEDUP_FUSED", "0");
+    // EP_DISPATCH_ONEPASS=0 keeps the dispatch as count + scan + fused.
+    b->onepass = !env_is("EP_DISPATCH_ONEPASS", "0");
+    // Debugging: EP_DEBUG=1 (sentinel checks), EP_NVTX=1 (NVTX ranges).
+    b->debug = env_is("EP_DEBUG", "1");
+    b->nvtx = env_is("EP_NVTX", "1");
+    // Test hook: make one bounded wait of the bulk permute run out.
+    b->test_skip_load = env_int("EP_TEST_SKIP_LOAD", -1);
+}
+
 }  // namespace
 
 extern "C" {
@@ -379,52 +419,17 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         return EP_ERR_CUDA;
 
     ep_buffer* b = new (std::nothrow) ep_buffer();
-    if (!b) return EP_ERR_INVALID_ARG;
+    if (!b) return EP_ERR_HOST_ALLOC;
     b->cfg = *cfg;
     b->device = dev;
     // SM budget: the config's, else EP_NUM_SMS, else every SM.
-    int budget = cfg->num_sms;
-    if (budget <= 0) {
-        const char* ns = std::getenv("EP_NUM_SMS");
-        budget = ns ? std::atoi(ns) : 0;
-    }
+    const int budget = cfg->num_sms > 0 ? cfg->num_sms : (int)env_int("EP_NUM_SMS", 0);
     b->num_sms = (budget > 0 && budget < sms) ? budget : sms;
     b->row_bytes = rb;
     b->s_max = s_max;
     b->max_tiles = tiles;
     b->ep_stride = ep::round_up4(cfg->num_experts);
-    {
-        const char* v = std::getenv("EP_PDL");
-        b->pdl = !(v && std::strcmp(v, "0") == 0);
-        // Tuning knob: fused-dispatch CTAs per SM (1 or 2).
-        const char* tps = std::getenv("EP_TILES_PER_SM");
-        b->tiles_per_sm = (tps && std::strcmp(tps, "2") == 0) ? 2 : 1;
-        // Tuning knob: EP_GEMM_KERNEL=1 / 2 forces the expert GEMM's kernel
-        // (single-CTA 128-row tiles, 2-SM 256-row tiles).
-        const char* gk = std::getenv("EP_GEMM_KERNEL");
-        b->gemm_kind = (gk && gk[0] >= '1' && gk[0] <= '2' && gk[1] == 0) ? gk[0] - '0' : 0;
-        // Tuning knob: EP_GEMM_BK=32 or 64, the expert GEMM's K slice per stage.
-        const char* bk = std::getenv("EP_GEMM_BK");
-        b->gemm_bk = (bk && std::strcmp(bk, "32") == 0) ? 32 : 64;
-        // Tuning knob: EP_GEMM_LIGHT_ROWS=n, experts with at most n rows are
-        // scheduled as light (0: one sequence in expert order).
-        const char* lr = std::getenv("EP_GEMM_LIGHT_ROWS");
-        b->gemm_light_rows = lr ? (std::atoi(lr) > 0 ? std::atoi(lr) : 0) : kGemmLightRows;
-        // Tuning knob: EP_DEDUP_FUSED=0 runs the dedupe dispatch as positions + copy kernels.
-        const char* df = std::getenv("EP_DEDUP_FUSED");
-        b->dedup_fused = !(df && std::strcmp(df, "0") == 0);
-        // Tuning knob: EP_DISPATCH_ONEPASS=0 keeps the dispatch as count + scan + fused.
-        const char* op = std::getenv("EP_DISPATCH_ONEPASS");
-        b->onepass = !(op && std::strcmp(op, "0") == 0);
-        // Debugging: EP_DEBUG=1 (sentinel checks), EP_NVTX=1 (NVTX ranges).
-        const char* dbg = std::getenv("EP_DEBUG");
-        b->debug = dbg && std::strcmp(dbg, "1") == 0;
-        const char* nv = std::getenv("EP_NVTX");
-        b->nvtx = nv && std::strcmp(nv, "1") == 0;
-        // Test hook: make one bounded wait of the bulk permute run out.
-        const char* t = std::getenv("EP_TEST_SKIP_LOAD");
-        b->test_skip_load = (t && *t) ? std::strtoll(t, nullptr, 10) : -1;
-    }
+    read_knobs(b);
     b->ws_bytes = o.total;
     uint8_t* w = static_cast<uint8_t*>(workspace);
     b->recv_x = w + o.recv_x;
@@ -815,6 +820,7 @@ const char* ep_status_string(ep_status s)
         case EP_ERR_CAPTURE_HOST_SYNC: return "synchronous call on a capturing stream";
         case EP_ERR_CUDA: return "CUDA runtime error";
         case EP_ERR_NO_LAYOUT: return "no layout for this call on the buffer";
+        case EP_ERR_HOST_ALLOC: return "host-side buffer handle could not be allocated";
     }
     return "unknown status";
 }

@@ -71,7 +71,8 @@ typedef enum {
     EP_ERR_WORKSPACE = 4,         /* workspace too small, misaligned or not device memory */
     EP_ERR_CAPTURE_HOST_SYNC = 5, /* a synchronous call was made on a capturing stream */
     EP_ERR_CUDA = 6,              /* a CUDA runtime call or launch failed */
-    EP_ERR_NO_LAYOUT = 7          /* combine/permute before any layout on this buffer, or T differs */
+    EP_ERR_NO_LAYOUT = 7,         /* combine/permute before any layout on this buffer, or T differs */
+    EP_ERR_HOST_ALLOC = 8         /* the host-side buffer handle could not be allocated */
 } ep_status;
 
 typedef enum { EP_BF16 = 0, EP_F32 = 1 } ep_dtype;
@@ -203,7 +204,8 @@ EP_API size_t ep_buffer_required_bytes(const ep_config* cfg);
  * ep_buffer_required_bytes(cfg) bytes, and must outlive the buffer. The
  * current device at this call is the buffer's device. Synchronous (clears
  * the device error word). Returns EP_ERR_INVALID_ARG for a bad cfg,
- * EP_ERR_WORKSPACE for an unusable workspace, EP_ERR_CUDA if no device. */
+ * EP_ERR_WORKSPACE for an unusable workspace, EP_ERR_CUDA if no device,
+ * EP_ERR_HOST_ALLOC if the host-side handle cannot be allocated. */
 EP_API ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace_bytes,
                          ep_buffer** out);
 

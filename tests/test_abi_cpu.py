@@ -73,11 +73,11 @@ def test_capacity_golden():
 
 def test_status_strings():
     seen = set()
-    for s in range(8):
+    for s in range(9):
         msg = ep.ep_status_string(s)
         assert msg and msg != "unknown status"
         seen.add(msg)
-    assert len(seen) == 8
+    assert len(seen) == 9
     assert ep.ep_status_string(99) == "unknown status"
 
 
