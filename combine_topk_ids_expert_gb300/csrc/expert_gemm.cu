@@ -42,9 +42,14 @@
 //     the leader's one MMA thread issues for both SMs, and its commits arrive
 //     on both CTAs' barriers (stage release, accumulator ready);
 //   - each CTA's epilogue drains its own TMEM (its 128 rows x 256 columns) and
-//     tells the leader, which reuses an accumulator only after both have.
+//     tells the leader, which reuses an accumulator only after both have;
+//   - an expert's last rows, when at most 128 remain, run as one M = 128 tile
+//     across the pair (64 rows per CTA, loaded with a 64-row box). Its
+//     accumulator holds the CTA's 64 rows twice in 128 columns: lanes 0-63
+//     with output columns [0, 128), lanes 64-127 with [128, 256), so every
+//     epilogue warp drains 32 rows x 128 columns.
 // Tiles cover 256 rows of one expert, so an expert's last tile is padded to
-// 256 rows instead of 128.
+// 256 rows when more than 128 remain (to 128 otherwise).
 //
 // Every wait is bounded; on a timeout the CTA reports EP_DEVERR_TIMEOUT,
 // waits (bounded) for its copies and MMAs in flight, frees its TMEM and
@@ -66,12 +71,13 @@ constexpr int kPairBN = 256;
 constexpr uint16_t kBothCtas = 0x3;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_103
 
-// Bytes after the ring: barriers, TMEM address, abort flag and the two
-// per-expert tile prefixes (heavy, light; sized for the largest expert count).
+// Bytes after the ring: barriers, TMEM address, abort flag, the two
+// per-expert tile prefixes (heavy, light) and the per-expert row counts (all
+// sized for the largest expert count).
 template <int STAGES>
 constexpr int tail_bytes()
 {
-    return 8 * (2 * STAGES + 5) + 8 + 8 * (kMaxExperts + 1);
+    return 8 * (2 * STAGES + 5) + 8 + 8 * (kMaxExperts + 1) + 4 * kMaxExperts;
 }
 
 template <int BN_, int BK_, int STAGES_, bool PAIR_>
@@ -89,6 +95,11 @@ struct Cfg {
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                        ((uint32_t)(BN >> 3) << 17) |
                                        ((uint32_t)(kTileRows >> 4) << 24);
+    // Pairs: an expert's last rows, when at most 128 are left, run as M = 128
+    // across the pair (64 rows per CTA; same N).
+    static constexpr uint32_t kIdescHalf = (kIdesc & ~(0x1Fu << 24)) |
+                                           ((uint32_t)((kTileRows / 2) >> 4) << 24);
+    static constexpr uint32_t kBytesAHalf = kBytesA / 2;
     static constexpr uint32_t kTmemCols = 2 * BN;                   // two accumulators per CTA
     // Epilogue warps that release an accumulator (both CTAs for a pair).
     static constexpr uint32_t kReleaseCount = PAIR ? 8u : 4u;
@@ -335,9 +346,10 @@ __device__ __forceinline__ int expert_of(const int* pre, int E, int i)
 }
 
 struct TileRef {
-    int e;    // expert
-    int mt;   // row tile (of kTileRows rows) within the expert
-    int nb;   // column block
+    int e;       // expert
+    int mt;      // row tile (of kTileRows rows) within the expert
+    int nb;      // column block
+    bool half;   // pairs: the expert's last rows, at most kTileRows / 2 of them (M = 128)
 };
 
 // The schedule: uh heavy units then, interleaved with them in proportion,
@@ -346,7 +358,10 @@ struct TileRef {
 struct Schedule {
     const int* heavy;   // [E + 1] prefix of the heavy experts' row tiles (light: 0)
     const int* light;   // [E + 1] prefix of the light experts' row tiles (heavy: 0)
+    const int* cnt;     // [E] rows of each expert
     int uh, total;      // heavy units, all units
+    int tile_rows;      // rows of a full row tile
+    bool halves;        // pairs: last row tiles of at most tile_rows / 2 rows run as M = 128
 };
 
 // Unit u is the h-th heavy unit when floor((u + 1) uh / total) steps past
@@ -364,15 +379,18 @@ __device__ __forceinline__ TileRef tile_of(const Schedule& q, int E, int nbk, in
     p.nb = v % nbk;
     p.e = expert_of(pre, E, mt);
     p.mt = mt - pre[p.e];
+    p.half = q.halves && q.cnt[p.e] - p.mt * q.tile_rows <= q.tile_rows / 2;
     return p;
 }
 
-// tm_a: box of [128 rows][BK] over the receive rows; tm_b: box of
-// [kRowsB rows][BK] over the weights (half a column block per CTA for pairs).
+// tm_a: box of [128 rows][BK] over the receive rows; tm_a_half: [64 rows][BK]
+// (pairs' M = 128 tiles); tm_b: box of [kRowsB rows][BK] over the weights
+// (half a column block per CTA for pairs).
 template <class C>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   GemmArgs a)
+expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                   const __grid_constant__ CUtensorMap tm_a_half,
+                   const __grid_constant__ CUtensorMap tm_b, GemmArgs a)
 {
     constexpr int STAGES = C::STAGES, BN = C::BN, BK = C::BK;
     constexpr bool PAIR = C::PAIR;
@@ -393,6 +411,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     int* s_heavy = const_cast<int*>(reinterpret_cast<volatile int*>(s_abort + 1));   // [E + 1]
     int* s_light = s_heavy + (kMaxExperts + 1);                                        // [E + 1]
+    int* s_cnt = s_light + (kMaxExperts + 1);                                          // [E]
     const int E = a.E;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -434,6 +453,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
             const int c = (e < E) ? __ldcg(a.cnt + e) : 0;
+            if (e < E) s_cnt[e] = c;
             const int m = (c + C::kTileRows - 1) / C::kTileRows;
             const bool is_light = c <= a.light_rows;
             int mh = is_light ? 0 : m, ml = is_light ? m : 0;
@@ -462,6 +482,9 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
     Schedule q;
     q.heavy = s_heavy;
     q.light = s_light;
+    q.cnt = s_cnt;
+    q.tile_rows = C::kTileRows;
+    q.halves = PAIR;
     q.uh = s_heavy[E] * nbk;
     q.total = q.uh + s_light[E] * nbk;
     const int total = q.total;
@@ -471,7 +494,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
         int g = 0;   // k-slices issued
         for (int u = first; u < total && !*s_abort; u += step) {
             const TileRef p = tile_of(q, E, nbk, u);
-            const int row0 = __ldcg(a.expert_offset + p.e) + p.mt * C::kTileRows + r * kBM;
+            const int row0 = __ldcg(a.expert_offset + p.e) + p.mt * C::kTileRows +
+                             r * (p.half ? kBM / 2 : kBM);
             const int wrow0 = p.e * (int)a.dout + p.nb * BN + r * C::kRowsB;
             for (int k = 0; k < k_iters; ++k, ++g) {
                 const int s = g % STAGES;
@@ -487,10 +511,12 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
                     tma_load_2d(sb, &tm_b, kc, wrow0, fb);
                 } else {
                     // Both CTAs' copies complete on the leader's barrier, which
-                    // expects the bytes of both.
-                    if (leader) mbar_expect_tx(full0 + 8u * s, 2u * C::kStageBytes);
+                    // expects the bytes of both (an M = 128 tile: 64 rows of x per CTA).
+                    if (leader)
+                        mbar_expect_tx(full0 + 8u * s,
+                                       2u * (p.half ? C::kBytesAHalf + C::kBytesB : C::kStageBytes));
                     const uint32_t fb = lead_full0 + 8u * s;
-                    tma_load_2d_pair(sa, &tm_a, kc, row0, fb);
+                    tma_load_2d_pair(sa, p.half ? &tm_a_half : &tm_a, kc, row0, fb);
                     tma_load_2d_pair(sb, &tm_b, kc, wrow0, fb);
                 }
             }
@@ -513,6 +539,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
             if (!wait_or_abort(accum_empty0 + 8u * acc, (uint32_t)((use & 1) ^ 1), s_abort)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+            const uint32_t idesc = tile_of(q, E, nbk, u).half ? C::kIdescHalf : C::kIdesc;
             bool ok = true;
             for (int k = 0; k < k_iters; ++k, ++g) {
                 const int s = g % STAGES;
@@ -525,7 +552,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
 #pragma unroll
                 for (int j = 0; j < BK / kUmmaK; ++j)
                     umma_bf16<PAIR>(d_tmem, smem_desc<C>(sa + j * kUmmaK * 2),
-                                    smem_desc<C>(sa + C::kBytesA + j * kUmmaK * 2), C::kIdesc,
+                                    smem_desc<C>(sa + C::kBytesA + j * kUmmaK * 2), idesc,
                                     (k | j) != 0 ? 1u : 0u);
                 issued = true;
                 umma_commit<PAIR>(empty0 + 8u * s);   // frees the stage (in both CTAs of a pair)
@@ -550,24 +577,33 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_consta
             tc_fence_after();
             const uint32_t t_acc = t_lane + (uint32_t)(acc * BN);
             const TileRef p = tile_of(q, E, nbk, u);
-            const int m_in = p.mt * C::kTileRows + r * kBM;
-            const int rows = min(kBM, __ldcg(a.cnt + p.e) - m_in);
-            const int64_t row = (int64_t)__ldcg(a.expert_offset + p.e) + m_in + r_in;
+            // The rows this warp drains and the output columns they cover. A full
+            // tile: lane quarter w holds this CTA's tile rows 32w..32w+31, every
+            // column. A pair's M = 128 tile: the CTA's 64 rows appear twice, lanes
+            // 0-63 with output columns [0, BN/2) and lanes 64-127 with
+            // [BN/2, BN), both in accumulator columns [0, BN/2).
+            const int sub = p.half ? 32 * (quarter & 1) + lane : r_in;
+            const int col0 = p.half ? (BN / 2) * (quarter >> 1) : 0;
+            const int ncols = p.half ? BN / 2 : BN;
+            const int part = p.half ? kBM / 2 : kBM;       // rows of this CTA's part
+            const int m_in = p.mt * C::kTileRows + r * part;
+            const int rows = min(part, q.cnt[p.e] - m_in);
+            const int64_t row = (int64_t)__ldcg(a.expert_offset + p.e) + m_in + sub;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < ncols; c += 32) {
                 uint32_t v[32];
                 tmem_ld32(t_acc + (uint32_t)c, v);
                 tmem_wait_ld();
-                if (r_in < rows) {
-                    int4* dst = reinterpret_cast<int4*>(y + row * a.dout + p.nb * BN + c);
+                if (sub < rows) {
+                    int4* dst = reinterpret_cast<int4*>(y + row * a.dout + p.nb * BN + col0 + c);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int g = 0; g < 4; ++g) {
                         int4 w;
-                        w.x = (int)pack_bf16x2_rn(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-                        w.y = (int)pack_bf16x2_rn(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-                        w.z = (int)pack_bf16x2_rn(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-                        w.w = (int)pack_bf16x2_rn(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-                        dst[q] = w;
+                        w.x = (int)pack_bf16x2_rn(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
+                        w.y = (int)pack_bf16x2_rn(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+                        w.z = (int)pack_bf16x2_rn(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
+                        w.w = (int)pack_bf16x2_rn(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+                        dst[g] = w;
                     }
                 }
             }
@@ -709,9 +745,10 @@ cudaError_t launch_cfg(const GemmArgs& a, const void* x, int64_t rows, const voi
         grid = cluster_grid(expert_gemm_kernel<C>, C::kSmem, num_sms);
         if (grid < 2) return cudaErrorNotSupported;
     }
-    CUtensorMap ta, tb;
+    CUtensorMap ta, ta_half, tb;
     const uint64_t wrows = (uint64_t)a.E * (uint64_t)a.dout;
     if (!make_map(&ta, x, (uint64_t)a.din, (uint64_t)rows, kBM, C::BK) ||
+        !make_map(&ta_half, x, (uint64_t)a.din, (uint64_t)rows, kBM / 2, C::BK) ||
         !make_map(&tb, w, (uint64_t)a.din, wrows, C::kRowsB, C::BK))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -721,7 +758,7 @@ cudaError_t launch_cfg(const GemmArgs& a, const void* x, int64_t rows, const voi
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = o.stream;
     set_attrs(&cfg, attr, C::PAIR, o.pdl);
-    e = cudaLaunchKernelEx(&cfg, expert_gemm_kernel<C>, ta, tb, a);
+    e = cudaLaunchKernelEx(&cfg, expert_gemm_kernel<C>, ta, ta_half, tb, a);
     if (e == cudaSuccess && o.launches) ++*o.launches;
     *grid_used = grid;
     return e;

@@ -324,9 +324,10 @@ EP_API ep_status ep_dedup_expand(ep_buffer* buf, const int32_t* topk_expert_ids_
  * y_recv that belong to no expert are not written. Summation order inside the
  * tensor cores is the hardware's: results are within the fp32 summation bound
  * of the exact product, not bitwise fixed across GPU models. Tiles: 256 rows
- * on an SM pair (tcgen05 cta_group::2) when dout % 256 == 0 and the last call
- * routed at least 512 rows per expert on average (T * K >= 512 * E), else
- * 128 rows per SM; both issue the same K order, so they agree bit for bit.
+ * on an SM pair (tcgen05 cta_group::2; an expert's last 128 rows or fewer as
+ * one 128-row pair tile) when dout % 256 == 0 and the last call routed at
+ * least 512 rows per expert on average (T * K >= 512 * E), else 128 rows per
+ * SM; all issue the same K order, so they agree bit for bit.
  * The environment variable EP_GEMM_KERNEL=1 (128-row) or 2 (256-row), read at
  * ep_buffer_init, forces one of them. Schedule: the tiles of experts with at
  * most 256 rows (memory-bound: their weights serve one or two tiles) are
