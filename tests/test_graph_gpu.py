@@ -161,3 +161,110 @@ def test_prefill32k_graph_100_replays(orc):
     buf.close()
     eager.close()
     torch.cuda.empty_cache()
+
+
+def _capture(seq):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        seq(s)                                     # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        res = seq(s)
+    torch.cuda.synchronize()
+    return g, res
+
+
+def test_graph_dedupe_path_fresh_routing(orc):
+    # The per-rank dedupe dispatch, the receiver's expansion and the combine,
+    # captured once and replayed with fresh routing: every replay matches the
+    # oracle (dedupe rows, expansion, combine).
+    T, N, D, E, K, R = 700, 702, 128, 64, 8, 8
+    buf = ep.Buffer(704, D, E, R, K, dtype=torch.bfloat16)
+    x = W.hidden(60, T, D, "bf16")
+    xd = to_dev(x)
+    ids_d = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    sc_d = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    S = ep.ep_pad_tokens(N) * K
+    y = torch.empty((R, S, D), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+
+    def seq(stream):
+        dd = buf.dispatch_dedup(xd, sc_d, ids_d, N, stream=stream)
+        buf.dedup_expand(ids_d, y_recv=y, stream=stream)
+        buf.combine(y, sc_d, out=out, stream=stream)
+        return dd
+
+    ids0, sc0 = W.routing(61, T, E, K, "zipf", "sigmoid_norm")
+    ids_d.copy_(torch.from_numpy(ids0))
+    sc_d.copy_(torch.from_numpy(sc0))
+    g, dd = _capture(seq)
+    for i in range(6):
+        ids_i, sc_i = W.routing(62 + i, T, E, K, "zipf" if i % 2 else "uniform", "sigmoid_norm")
+        ids_d.copy_(torch.from_numpy(ids_i))
+        sc_d.copy_(torch.from_numpy(sc_i))
+        g.replay()
+        torch.cuda.synchronize()
+        assert buf.device_error() == 0
+        ref = orc.dispatch_dedup(x, sc_i, ids_i, N, E, R)
+        P, tir = ref["P"], ref["tokens_in_rank"]
+        rx = to_np(dd.recv_x.reshape(R * P, D))
+        for r in range(R):
+            rows = slice(r * P, r * P + int(tir[r]))
+            assert np.array_equal(rx[rows], ref["recv_tok_x"][rows]), (i, r)
+        d = orc.dispatch(x, sc_i, ids_i, N, E, R)
+        valid = d["pos"][d["pos"] >= 0]
+        assert np.array_equal(to_np(y.reshape(-1, D))[valid], d["recv_x"][valid])
+        want, _ = orc.combine(d["recv_x"], sc_i, d["pos"], d["rank_prefix"], d["S"], R)
+        assert_combine_equal(to_np(out), want)
+    buf.close()
+
+
+def test_graph_backward_fresh_routing(orc):
+    # Dispatch, combine backward and dispatch backward captured once and
+    # replayed with fresh routing and a fresh upstream gradient.
+    T, N, D, E, K, R = 600, 600, 256, 32, 4, 4
+    buf = ep.Buffer(N, D, E, R, K, dtype=torch.bfloat16)
+    x = W.hidden(70, T, D, "bf16")
+    xd = to_dev(x)
+    ids_d = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    sc_d = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    g_d = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    S = ep.ep_pad_tokens(N) * K
+    grad_y = torch.empty((R, S, D), dtype=torch.bfloat16, device="cuda")
+    state = {}
+
+    def seq(stream):
+        d = buf.dispatch(xd, sc_d, ids_d, N, stream=stream)
+        buf.combine_backward(g_d, d.recv_x, sc_d, grad_y=grad_y, want_scores=False,
+                             stream=stream)
+        gx, _ = buf.dispatch_backward(grad_y, T, stream=stream)
+        state["gx"] = gx
+        return d
+
+    ids0, sc0 = W.routing(71, T, E, K, "uniform", "sigmoid_norm")
+    ids_d.copy_(torch.from_numpy(ids0))
+    sc_d.copy_(torch.from_numpy(sc0))
+    g_d.copy_(to_dev(W.hidden(72, T, D, "bf16")))
+    g, _ = _capture(seq)
+    gx = state["gx"]
+    for i in range(5):
+        ids_i, sc_i = W.routing(73 + i, T, E, K, "zipf", "sigmoid_norm")
+        gi = W.hidden(80 + i, T, D, "bf16")
+        ids_d.copy_(torch.from_numpy(ids_i))
+        sc_d.copy_(torch.from_numpy(sc_i))
+        g_d.copy_(to_dev(gi))
+        g.replay()
+        torch.cuda.synchronize()
+        assert buf.device_error() == 0
+        ref = orc.dispatch(x, sc_i, ids_i, N, E, R)
+        gy_ref, _, _ = orc.combine_backward(gi, ref["recv_x"], sc_i, ref["pos"],
+                                            ref["rank_prefix"], ref["S"], R)
+        valid = ref["pos"][ref["pos"] >= 0]
+        assert np.array_equal(to_np(grad_y.reshape(-1, D))[valid], gy_ref[valid]), i
+        gx_ref, _, _ = orc.dispatch_backward(gy_ref, None, ref["pos"], ref["rank_prefix"],
+                                             ref["S"], R)
+        assert np.array_equal(to_np(gx), gx_ref), i
+    buf.close()
