@@ -233,9 +233,15 @@ int oracle_layout(const int32_t* ids, int64_t T, int64_t N, int32_t K, int32_t E
                   int32_t* pos_TK, int64_t* S_out, uint32_t* err)
 {
     if (check_shape(T, N, K, E, R) != ORC_OK) return ORC_EINVAL;
+#if ORACLE_MUTANT == 26
+    int64_t P = oracle_pad_tokens(T);               /* mutant: capacity from T, not N */
+    int64_t S = oracle_rank_stride(T, K);
+    if (P < T || S < P * K) return ORC_EINVAL;
+#else
     int64_t P = oracle_pad_tokens(N);
     int64_t S = oracle_rank_stride(N, K);
     if (P < N || S < P * K) return ORC_EINVAL;      /* the padded block covers every token */
+#endif
     int32_t* ip = padded_ids(ids, T, P, K, E, err);
     if (!ip) return ORC_ENOMEM;
 
@@ -395,7 +401,11 @@ uint16_t oracle_bf16_from_f32(float f)
 #else
     uint32_t low = u & 0xffffu;
     uint32_t kept = u >> 16;
+#if ORACLE_MUTANT == 28
+    if (low >= 0x8000u) kept += 1u;                 /* mutant: ties away from zero */
+#else
     if (low > 0x8000u || (low == 0x8000u && (kept & 1u))) kept += 1u;
+#endif
     return (uint16_t)kept;
 #endif
 }
@@ -729,7 +739,11 @@ int oracle_expert_gemm(const uint16_t* x, const uint16_t* w, const int32_t* cnt_
 #endif
                 for (int64_t i = 0; i < din; ++i)
                     acc += (double)oracle_f32_from_bf16(x[p * din + i]) *
+#if ORACLE_MUTANT == 27
+                           (double)oracle_f32_from_bf16(we[i * dout + o]);   /* mutant: W^T */
+#else
                            (double)oracle_f32_from_bf16(we[o * din + i]);
+#endif
                 y[p * dout + o] = oracle_bf16_from_f32((float)acc);
             }
         }

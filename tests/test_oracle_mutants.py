@@ -38,6 +38,9 @@ MUTANTS = {
     23: "combine backward score gradient summed in fp32",
     24: "combine flushes subnormal results to zero",
     25: "bf16 cast rounds NaNs like numbers",
+    26: "capacity from the call's T instead of num_tokens_per_rank",
+    27: "expert GEMM reads the weights transposed",
+    28: "bf16 ties round away from zero",
 }
 
 
