@@ -1,0 +1,39 @@
+"""bench.py's reference arm runs on the host cores alone (the oracle, no GPU):
+one JSON line with the contract's keys, the same metric and workload
+description as the GPU arm, and no GPU launches. Under torchrun only rank 0
+prints; the others exit 0 without work."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(env_extra, *args):
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        *args], capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_reference_arm_prints_one_contract_line():
+    lines = _run({}, "--steps", "2", "--warmup", "1", "--cpu-seconds", "1")
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    import bench
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["gpu_launches"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("deepseek: T=8192 D=7168 bf16 E=256 K=8 R=8")
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    lines = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"},
+                 "--steps", "1", "--warmup", "0", "--cpu-seconds", "1")
+    assert lines == []
