@@ -37,3 +37,18 @@ def test_reference_arm_other_ranks_print_nothing():
     lines = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"},
                  "--steps", "1", "--warmup", "0", "--cpu-seconds", "1")
     assert lines == []
+
+
+def test_algorithmic_bytes_match_the_row_traffic_formula():
+    # Rows: x read once, T*K rows written, T*K rows read, T rows written:
+    # T*D*b*(2 + 2K) bytes per call (201.3 MB Mixtral-shaped, 2.114 GB
+    # DeepSeek-shaped, 8.456 GB for the 32k prefill); metadata: ids and scores
+    # read, positions written and read, receive scores and sources written,
+    # 32 bytes per routed pair.
+    import bench
+    for T, K, D, b, rows_mb in [(4096, 2, 4096, 2, 201.3), (8192, 8, 7168, 2, 2113.9),
+                                (32768, 8, 7168, 2, 8455.7)]:
+        ab = bench.algorithmic_bytes(T, K, D, b, T * K)
+        assert ab["step"] == ab["layout"] + ab["permute"] + ab["combine"]
+        assert ab["step"] - 32 * T * K == T * D * b * (2 + 2 * K)
+        assert round(T * D * b * (2 + 2 * K) / 1e6, 1) == rows_mb
