@@ -782,7 +782,8 @@ def main():
                 "ms_per_step": secs / len(runs) * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
                 "config": workload_desc(w, T, N),
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1,
+                                 "host_cores": os.cpu_count(), "kind": "oracle",
                                  "sample": sample},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0},
@@ -826,7 +827,7 @@ def main():
         r = oracle_sample_run(w, inp, args.cpu_seconds, tpc)
         line["cpu_baseline"] = {
             "value": r["tokens"] / r["seconds"], "unit": "tokens/s", "cores": 1,
-            "kind": "oracle",
+            "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": (f"{r['calls']} oracle dispatch+combine calls over consecutive "
                        f"{tpc}-token slices of the same workload ({r['tokens']} tokens, "
                        f"{r['seconds']:.1f} s, single thread)")}

@@ -27,6 +27,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["steps"] == 2 and d["warmup"] == 1 and d["gpu_launches"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["host_cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
