@@ -131,3 +131,44 @@ def test_calls_reject_null_buffer():
     assert L.ep_combine(None, None, None, 0, None, 0, None) == _abi.EP_ERR_INVALID_ARG
     assert L.ep_dispatch_permute(None, None, None, None, None) == _abi.EP_ERR_INVALID_ARG
     assert L.ep_buffer_destroy(None) == _abi.EP_OK
+
+
+def test_ctypes_mirror_matches_the_header():
+    # The ctypes structures and constants of _abi.py against include/ep.h as a C
+    # compiler lays them out: every struct's size, every field's offset and size,
+    # every EP_* constant's value (a C program generated from the mirror, built by
+    # gcc).
+    import shutil
+    import subprocess
+    import tempfile
+
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    structs = {"ep_config": _abi.EpConfig, "ep_layout": _abi.EpLayout,
+               "ep_dispatch_out": _abi.EpDispatchOut, "ep_dedup_out": _abi.EpDedupOut,
+               "ep_buffer_info": _abi.EpBufferInfo}
+    consts = sorted(n for n in dir(_abi) if re.fullmatch(r"EP_[A-Z0-9_]+", n))
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ep.h"', "int main(void) {"]
+    for cname, st in structs.items():
+        lines.append(f'printf("size {cname} %zu\\n", sizeof({cname}));')
+        for f, _ in st._fields_:
+            lines.append(f'printf("off {cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+            lines.append(f'printf("fsz {cname}.{f} %zu\\n", sizeof((({cname}*)0)->{f}));')
+    for c in consts:
+        lines.append(f'printf("const {c} %lld\\n", (long long)({c}));')
+    lines += ["return 0;", "}"]
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "m.c"), os.path.join(d, "m")
+        with open(src, "w") as f:
+            f.write("\n".join(lines))
+        subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), src, "-o", exe],
+                       check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(line.rsplit(" ", 1) for line in out if line)
+    for cname, st in structs.items():
+        assert int(got[f"size {cname}"]) == C.sizeof(st), cname
+        for f, _ in st._fields_:
+            assert int(got[f"off {cname}.{f}"]) == getattr(st, f).offset, (cname, f)
+            assert int(got[f"fsz {cname}.{f}"]) == getattr(st, f).size, (cname, f)
+    for c in consts:
+        assert int(got[f"const {c}"]) == getattr(_abi, c), c
