@@ -199,7 +199,9 @@ typedef struct {
  * layout arrays. */
 EP_API size_t ep_buffer_required_bytes(const ep_config* cfg);
 
-/* Create a buffer over caller-owned device workspace. workspace must be
+/* Create a buffer over caller-owned device workspace ([titan] "API design": the
+ * lifetime maximum num_max_tokens_per_rank sizes persistent storage once;
+ * "Backend behavior": DeepEP and HybridEP preallocate). workspace must be
  * device memory on the current device, 256-byte aligned, at least
  * ep_buffer_required_bytes(cfg) bytes, and must outlive the buffer. The
  * current device at this call is the buffer's device. Synchronous (clears
@@ -209,7 +211,8 @@ EP_API size_t ep_buffer_required_bytes(const ep_config* cfg);
 EP_API ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace_bytes,
                          ep_buffer** out);
 
-/* Release the host-side handle. Does not free the workspace. NULL is a no-op. */
+/* Release the host-side handle. Does not free the workspace. NULL is a no-op.
+ * (Plumbing: no page passage defines it.) */
 EP_API ep_status ep_buffer_destroy(ep_buffer* buf);
 
 /* Dispatch layout ([titan] "API design"; [graph] "Internode" items 2-3):
@@ -237,7 +240,9 @@ EP_API ep_status ep_dispatch(ep_buffer* buf, const void* x_TD, const float* topk
                       const int32_t* topk_expert_ids_TK, int64_t num_tokens,
                       int64_t num_tokens_per_rank, ep_stream_t stream, ep_dispatch_out* out);
 
-/* The permute half of ep_dispatch alone, using the layout of the last
+/* The permute half of ep_dispatch alone ([titan] "Backend behavior": rows go to
+ * the receive buffer with the current capacity as the per-rank stride), using
+ * the layout of the last
  * ep_dispatch_layout / ep_dispatch on this buffer (same T; x_TD and
  * topk_scores_TK have that T). EP_ERR_NO_LAYOUT if there is none. */
 EP_API ep_status ep_dispatch_permute(ep_buffer* buf, const void* x_TD, const float* topk_scores_TK,
@@ -274,7 +279,8 @@ EP_API ep_status ep_combine_backward(ep_buffer* buf, const void* grad_out_TD, co
                                      const float* topk_scores_TK, int64_t num_tokens,
                                      void* grad_y_recv, float* grad_scores_TK, ep_stream_t stream);
 
-/* Backward of ep_dispatch (same source as ep_combine_backward). grad_recv_x is
+/* Backward of ep_dispatch, its adjoint ([align] "Testing": forward and backward
+ * of unequal-count runs reproduce the equal-count run bitwise). grad_recv_x is
  * [R*S][D] of the configured dtype; grad_x_TD [T][D] of grad_x_dtype:
  *   grad_x_TD[t][d] = sum over valid k (ascending, fp32 from +0) of
  *                     grad_recv_x[pos[t][k]][d], rounded to grad_x_dtype;
@@ -300,7 +306,8 @@ EP_API ep_status ep_dispatch_dedup(ep_buffer* buf, const void* x_TD, const float
                                    ep_dedup_out* out);
 
 /* The receiver's expansion of the last ep_dispatch_dedup on this buffer into
- * the per-expert layout: y_recv[pos[t][k]] = dedupe row of (t, rank of
+ * the per-expert layout ([titan] "Backend behavior": DeepEP's per-rank layout,
+ * each token sent once per rank and spread over that rank's experts there): y_recv[pos[t][k]] = dedupe row of (t, rank of
  * topk_expert_ids_TK[t][k]) for every routed pair; y_recv is [R*S][D] of the
  * configured dtype, caller-owned, outside the workspace, and then feeds
  * ep_combine like recv_x. topk_expert_ids_TK must be the dedupe call's ids
@@ -339,16 +346,20 @@ EP_API ep_status ep_expert_gemm(ep_buffer* buf, const void* x_recv, const void* 
                                 int64_t din, int64_t dout, void* y_recv, ep_stream_t stream);
 
 /* Synchronously read and clear the device error word (EP_DEVERR_* bits).
- * Refused with EP_ERR_CAPTURE_HOST_SYNC while the stream is capturing. */
+ * Refused with EP_ERR_CAPTURE_HOST_SYNC while the stream is capturing. Status
+ * stays on the device and is read only here ([graph] "Internode" item 1: no
+ * host handshake on the dispatch path). */
 EP_API ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flags);
 
-/* Read-only facts about buf. */
+/* Read-only facts about buf. (Plumbing: no page passage defines it.) */
 EP_API ep_status ep_buffer_query(const ep_buffer* buf, ep_buffer_info* info);
 
 /* The dispatch layout of ep_dispatch_layout, for callers that cannot allocate
  * device memory or keep a workspace (for example an op inside a host framework
  * that owns every device allocation and only hands it input and output
- * tensors). The source pages have no counterpart: it exists for such callers.
+ * tensors). The layout is ep_dispatch_layout's ([titan] "API design";
+ * [graph] "Internode" item 2: counts stay on the device); the pages have no
+ * variant without a workspace: it exists for such callers.
  * No buffer is involved and nothing is allocated: the caller passes
  * topk_expert_ids_TK [T][K] and the outputs (device pointers, 4-byte aligned):
  * tokens_per_expert [E], expert_offset [E], rows_per_rank [R], rank_prefix [R],
@@ -388,7 +399,7 @@ EP_API int64_t ep_derive_max_tokens_inference(int64_t max_num_batched_tokens, in
  * EP_ERR_INVALID_ARG (not positive) or EP_ERR_CAPACITY (too small). */
 EP_API ep_status ep_validate_max_tokens(int64_t configured, int64_t derived);
 
-/* Static description of a status code. */
+/* Static description of a status code. (Plumbing: no page passage defines it.) */
 EP_API const char* ep_status_string(ep_status s);
 
 #ifdef __cplusplus
