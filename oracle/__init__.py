@@ -55,6 +55,7 @@ class Oracle:
             f.argtypes, f.restype = args, i64
         L.oracle_bf16_from_f32.argtypes, L.oracle_bf16_from_f32.restype = [C.c_float], C.c_uint16
         L.oracle_f32_from_bf16.argtypes, L.oracle_f32_from_bf16.restype = [C.c_uint16], C.c_float
+        L.oracle_bf16_from_f64.argtypes, L.oracle_bf16_from_f64.restype = [C.c_double], C.c_uint16
         u32p = C.POINTER(C.c_uint32)
         L.oracle_routing_map.argtypes = [_i32p, _f32p, i64, i64, i32, i32, _u8p, _f32p, u32p]
         L.oracle_layout.argtypes = [_i32p, i64, i64, i32, i32, i32, i32, _i32p, _i32p, _i32p,
@@ -97,6 +98,10 @@ class Oracle:
     def bf16_from_f32(self, a) -> np.ndarray:
         a = np.asarray(a, dtype=np.float32).ravel()
         return np.array([self.lib.oracle_bf16_from_f32(float(v)) for v in a], dtype=np.uint16)
+
+    def bf16_from_f64(self, a) -> np.ndarray:
+        a = np.asarray(a, dtype=np.float64).ravel()
+        return np.array([self.lib.oracle_bf16_from_f64(float(v)) for v in a], dtype=np.uint16)
 
     def f32_from_bf16(self, h) -> np.ndarray:
         h = np.asarray(h, dtype=np.uint16).ravel()

@@ -19,8 +19,17 @@
  * Where the pages leave a step open, the reading taken is stated at the step.
  * Every function here is pinned by the CPU tests (worked values printed on the
  * pages, closed forms, library-routine cross-checks, brute force on tiny
- * inputs), except the payload of the NaN that bf16 rounding returns: parity
- * unpinned (that a NaN stays a NaN of the same sign is pinned).
+ * inputs, hand-worked IEEE-754 encodings, NaN results included).
+ *
+ * NaN results. The pages say nothing about NaNs. IEEE 754-2008 section 6.2
+ * asks an arithmetic operation with a NaN result for a quiet NaN but leaves
+ * its payload to a recommendation (6.2.3), says nothing about which of
+ * several NaN operands propagates, and gives a NaN's sign no meaning (6.3);
+ * hosts differ (the default NaN is ffc00000 on x86, 7fc00000 on Arm). So a
+ * NaN produced by the arithmetic here (combine's fma chain, the backward's
+ * products and sums) is delivered as THE canonical quiet NaN, 7fc00000 (bf16
+ * 7fc0), and only a format conversion of a given NaN keeps its sign and
+ * leading payload bits (6.2.3). Copies (dispatch, dedupe) keep every bit.
  *
  * Conventions: ids are int32, -1 means "no expert"; scores are fp32; hidden
  * rows are either fp32 or bf16 stored as uint16 bit patterns. Return value 0 =
@@ -386,13 +395,18 @@ int oracle_dispatch(const void* x, int64_t row_bytes, const float* scores, const
  * bf16 keeps the top 16 bits of the fp32 encoding; the dropped low 16 bits
  * round up when above half an ulp, or exactly half with an odd kept bit.
  * A carry out of the mantissa correctly bumps the exponent (and overflows the
- * largest finite values to infinity). NaN inputs return a quiet NaN with the
- * same sign (payload: parity unpinned). */
+ * largest finite values to infinity). A NaN converts as IEEE 754-2008 6.2.3
+ * recommends for a narrowing conversion: a quiet NaN of the same sign that
+ * keeps the leading payload bits which fit (fp32 significand bits 21..16
+ * become bf16 bits 5..0; the quiet bit 6 is set). */
 uint16_t oracle_bf16_from_f32(float f)
 {
     uint32_t u;
     memcpy(&u, &f, sizeof u);
-#if ORACLE_MUTANT != 25
+#if ORACLE_MUTANT == 30
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+        return (uint16_t)0x7fc0u;                   /* mutant: drops sign and payload */
+#elif ORACLE_MUTANT != 25
     if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
         return (uint16_t)((u >> 16) | 0x0040u);
 #endif
@@ -417,6 +431,23 @@ float oracle_f32_from_bf16(uint16_t h)
     float f;
     memcpy(&f, &u, sizeof f);
     return f;
+}
+
+/* The canonical quiet NaN (positive, quiet bit set, zero payload) in place of
+ * whatever NaN the host's arithmetic produced; other values pass unchanged.
+ * Every NaN result of the arithmetic below goes through this (see the NaN
+ * reading at the top of the file). */
+static float canonical_nan(float v)
+{
+#if ORACLE_MUTANT == 29
+    return v;                                       /* mutant: the host's own NaN */
+#else
+    if (isnan(v)) {
+        const uint32_t q = 0x7fc00000u;
+        memcpy(&v, &q, sizeof v);
+    }
+    return v;
+#endif
 }
 
 static float load_elem(const void* base, int kind, int64_t i)
@@ -450,9 +481,12 @@ static int row_ok(int64_t p, const int32_t* rank_prefix_R, int64_t S, int32_t R,
  * kind y_kind. For every token t < T and element d:
  *     acc = +0.0f
  *     for k = 0 .. K-1 with pos[t][k] >= 0:  acc = fmaf(scores[t][k], y[pos][d], acc)
- *     out[t][d] = acc (fp32) or its bf16 rounding (round to nearest even).
+ *     out[t][d] = acc (fp32) or its bf16 rounding (round to nearest even),
+ *                 the canonical quiet NaN where acc is a NaN.
  * The accumulation is fp32 in ascending k, one fused multiply-add per term
- * (reading: the pages fix no order; this is the fixed top-k order). A row p
+ * (reading: the pages fix no order; this is the fixed top-k order). A NaN
+ * stays a NaN through the rest of the chain, so replacing the final value is
+ * the same as replacing every NaN along the way. A row p
  * of rank r = p / S is used only when p - r*S < rank_prefix[r] -
  * rank_prefix[r-1] (the rank's true total); any other row raises
  * ORC_ERR_ROW_OOB and contributes nothing. Only rows t < T are written: the
@@ -491,6 +525,7 @@ int oracle_combine(const void* y, int y_kind, int64_t D, const float* scores,
 #if ORACLE_MUTANT == 24
             if (fabsf(acc) < 1.17549435e-38f) acc = 0.0f;   /* mutant: flushes subnormals */
 #endif
+            acc = canonical_nan(acc);
             if (out_kind == ORC_F32)
                 ((float*)out)[t * D + d] = acc;
             else
@@ -521,6 +556,7 @@ static void store_elem(void* base, int kind, int64_t i, float v)
  *   grad_scores[t][k]    = sum_d grad_out[t][d] * y[pos[t][k]][d], summed in
  *                          fp64 in ascending d and rounded once to fp32
  *                          (0 for a pair without a valid row).
+ * A NaN product or sum is the canonical quiet NaN.
  * Rows of grad_y that no valid pair references are left as the caller filled
  * them. A pair whose row lies outside its rank's true total raises
  * ORC_ERR_ROW_OOB and contributes nothing. grad_scores may be NULL. */
@@ -553,11 +589,11 @@ int oracle_combine_backward(const void* grad_out, int g_kind, const void* y, int
 #endif
                 for (int64_t d = 0; d < D; ++d) {
                     float g = load_elem(grad_out, g_kind, t * D + d);
-                    store_elem(grad_y, y_kind, p * D + d, s * g);
+                    store_elem(grad_y, y_kind, p * D + d, canonical_nan(s * g));
                     dot += (double)g * (double)load_elem(y, y_kind, p * D + d);
                 }
             }
-            if (grad_scores) grad_scores[t * K + k] = (float)dot;
+            if (grad_scores) grad_scores[t * K + k] = canonical_nan((float)dot);
         }
     return ORC_OK;
 }
@@ -566,7 +602,8 @@ int oracle_combine_backward(const void* grad_out, int g_kind, const void* y, int
  * recv_scores[pos[t][k]] = s[t][k]:
  *   grad_x[t][d]      = sum over valid k (ascending) of grad_recv[pos[t][k]][d],
  *                       accumulated in fp32 from +0 (the same chain as
- *                       combine with unit weights) and rounded to grad_x's kind;
+ *                       combine with unit weights, a NaN sum canonical) and
+ *                       rounded to grad_x's kind;
  *   grad_scores[t][k] = grad_recv_scores[pos[t][k]] (0 without a valid row).
  * grad_recv_scores and grad_scores may be NULL (then that part is skipped). */
 int oracle_dispatch_backward(const void* grad_recv, int g_kind, int64_t D,
@@ -590,7 +627,7 @@ int oracle_dispatch_backward(const void* grad_recv, int g_kind, int64_t D,
                 if (!row_ok(p, rank_prefix_R, S, R, packed)) continue;
                 acc = fmaf(1.0f, load_elem(grad_recv, g_kind, p * D + d), acc);
             }
-            store_elem(grad_x, x_kind, t * D + d, acc);
+            store_elem(grad_x, x_kind, t * D + d, canonical_nan(acc));
         }
         for (int32_t k = 0; k < K; ++k) {
             int64_t p = pos_TK[t * K + k];
@@ -714,10 +751,39 @@ int oracle_dedup_expand(const void* recv_tok_x, int64_t row_bytes, const int32_t
  * dispatch -> expert -> combine). For every expert e and each of its rows
  * p = expert_offset[e] + j, j < cnt[e]:
  *     y[p][o] = sum_i x[p][i] * w[e][o][i]      (o < dout, i < din)
- * summed exactly in fp64 (products of bf16 values are exact) in ascending i
- * and rounded once to bf16. x and y are in the receive layout (rows of
+ * summed in fp64 in ascending i (each product of two bf16 values is exact in
+ * fp64) and rounded once, from fp64 straight to bf16 (oracle_bf16_from_f64: no
+ * intermediate fp32 rounding). x and y are in the receive layout (rows of
  * din / dout bf16 values), w is [E][dout][din] bf16. Rows of y that belong to
  * no expert are left as the caller filled them. */
+/* fp64 -> bf16 in one rounding, to nearest with ties to even. bf16 has 8
+ * significant bits, fp32's exponent range and subnormals spaced 2^-133 apart.
+ * With v = m * 2^e, 0.5 <= |m| < 1 (frexp), the bf16 values near v are spaced
+ * 2^(e-8), but never closer than 2^-133; v over that spacing, rounded to an
+ * integer with ties to even (nearbyint in the default rounding mode), times
+ * the spacing is the result: it has at most 8 significant bits and fits fp32
+ * exactly, except at 2^128 and beyond, which is infinity. A NaN gives the
+ * canonical quiet NaN (the sum is arithmetic, see the NaN reading above). */
+uint16_t oracle_bf16_from_f64(double v)
+{
+    if (isnan(v)) return (uint16_t)0x7fc0u;
+#if ORACLE_MUTANT == 31
+    return oracle_bf16_from_f32((float)v);          /* mutant: rounds twice, via fp32 */
+#endif
+    if (v != 0.0 && !isinf(v)) {
+        int e;
+        (void)frexp(v, &e);
+        int q = e - 8;
+        if (q < -133) q = -133;
+        v = ldexp(nearbyint(ldexp(v, -q)), q);
+        if (fabs(v) >= 0x1p128) v = v > 0 ? INFINITY : -INFINITY;
+    }
+    float f = (float)v;                 /* exact: v is a bf16 value (or 0, inf) */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
 int oracle_expert_gemm(const uint16_t* x, const uint16_t* w, const int32_t* cnt_E,
                        const int32_t* expert_offset_E, int32_t E, int64_t din, int64_t dout,
                        uint16_t* y)
@@ -744,7 +810,7 @@ int oracle_expert_gemm(const uint16_t* x, const uint16_t* w, const int32_t* cnt_
 #else
                            (double)oracle_f32_from_bf16(we[o * din + i]);
 #endif
-                y[p * dout + o] = oracle_bf16_from_f32((float)acc);
+                y[p * dout + o] = oracle_bf16_from_f64((double)acc);
             }
         }
     }

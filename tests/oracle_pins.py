@@ -95,6 +95,24 @@ def pin_bf16_golden(o):
         assert got == int(h_hex, 16), (f_hex, h_hex, hex(got), why)
 
 
+def pin_bf16_nan_golden(o):
+    # NaN conversions worked by hand from IEEE 754-2008 6.2.3 (sign and leading
+    # payload bits kept, quiet bit set).
+    for f_hex, h_hex, why in _golden("bf16_nan.json")["cases"]:
+        f = np.array([int(f_hex, 16)], dtype=np.uint32).view(np.float32)
+        got = int(o.bf16_from_f32(f)[0])
+        assert got == int(h_hex, 16), (f_hex, h_hex, hex(got), why)
+
+
+def pin_bf16_from_f64_golden(o):
+    # One rounding from fp64, worked by hand; several cases differ from rounding
+    # through fp32 first.
+    for expr, h_hex, why in _golden("bf16_from_f64.json")["cases"]:
+        v = float(eval(expr, {"__builtins__": {}}))
+        got = int(o.bf16_from_f64(np.array([v]))[0])
+        assert got == int(h_hex, 16), (expr, h_hex, hex(got), why)
+
+
 def pin_bf16_vs_torch(o):
     import torch
     rng_bits = W.u64(5, 21, 4000).astype(np.uint32)
@@ -518,10 +536,21 @@ def _gemm_case(seed=60, T=29, N=32, E=8, K=2, R=2, din=32, dout=24):
     return ids, sc, x, N, E, K, R, din, dout
 
 
+def _bf16_once(a64):
+    """fp64 values rounded once to bf16 (8 significant bits, nearest, ties to
+    even) by mpmath's correctly rounded conversion; the values here are normal
+    in bf16, so its unbounded exponent does not matter."""
+    import mpmath.libmp as L
+    out = np.empty(a64.size, np.uint16)
+    for i, v in enumerate(np.asarray(a64, np.float64).ravel()):
+        r = np.float32(L.to_float(L.from_float(float(v), 8, "n")))
+        out[i] = int(np.array([r]).view(np.uint32)[0]) >> 16
+    return out.reshape(np.shape(a64))
+
+
 def pin_expert_gemm_vs_numpy(o):
     # Each expert's rows times its weights, against numpy's fp64 matmul of the
-    # same bf16 values, rounded once by torch's bf16 cast.
-    import torch
+    # same bf16 values, rounded once to bf16 by mpmath.
     ids, sc, x, N, E, K, R, din, dout = _gemm_case()
     d = o.dispatch(x, sc, ids, N, E, R)
     w = W.hidden(61, E * dout, din, "bf16").reshape(E, dout, din)
@@ -532,10 +561,25 @@ def pin_expert_gemm_vs_numpy(o):
     for e in range(E):
         lo, n = int(d["expert_offset"][e]), int(d["cnt"][e])
         ref = xf[lo:lo + n] @ wf[e].T
-        want = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16)
-        assert np.array_equal(y[lo:lo + n].view(np.int16), want.view(torch.int16).numpy())
+        assert np.array_equal(y[lo:lo + n], _bf16_once(ref))
         covered[lo:lo + n] = True
     assert np.all(y[~covered] == 0xFFFF)              # rows of no expert untouched
+
+
+def pin_expert_gemm_single_rounding(o):
+    # x = (1, 2^-8, 2^-30, 0...) against unit weights: the exact sum 1 + 2^-8 +
+    # 2^-30 lies just above the bf16 tie at 1 + 2^-8, so one rounding gives
+    # 1 + 2^-7 (3f81); rounding through fp32 first loses the 2^-30 and the tie
+    # goes to even (3f80).
+    E, K, R, din, dout, T = 2, 1, 1, 16, 16, 4
+    ids = np.zeros((T, K), np.int32)
+    sc = np.ones((T, K), np.float32)
+    x = np.zeros((T, din), np.float32)
+    x[:, 0], x[:, 1], x[:, 2] = 1.0, 2.0 ** -8, 2.0 ** -30
+    d = o.dispatch(_bf16_bits(x), sc, ids, T, E, R)
+    w = np.broadcast_to(_bf16_bits(np.ones((dout, din), np.float32)), (E, dout, din)).copy()
+    y = o.expert_gemm(d["recv_x"], w, d["cnt"], d["expert_offset"])
+    assert np.all(y[d["pos"].ravel()] == 0x3F81), hex(int(y[0, 0]))
 
 
 def pin_expert_gemm_identity_weights(o):
@@ -657,6 +701,7 @@ def pin_bf16_nan_stays_nan(o):
 
 
 BF16_MAX, BF16_MIN_SUB = 0x7F7F, 0x0001
+NAN_BF16, NAN_F32 = 0x7FC0, 0x7FC00000      # the canonical quiet NaN
 
 
 def special_value_case():
@@ -673,17 +718,26 @@ def special_value_case():
       4: 0.75 * 2^-133 = 3 * 2^-135, an fp32 subnormal (0x0000c000), above
          the bf16 tie: the smallest bf16 subnormal, 0x0001 (a flush to zero
          would give 0);
-      5: 0 * inf: NaN."""
-    ids = np.tile(np.array([[0, 1]], np.int32), (6, 1))
-    sc = np.array([[1, 1], [1, 1], [1, 1], [1, 1], [0.75, 0], [0, 1]], np.float32)
+      5: 0 * inf: NaN;
+      6: a negative quiet NaN with a payload (ffd5) plus 1: NaN;
+      7: a signalling NaN (7f81) plus 1: NaN.
+    Every NaN result of the arithmetic is the canonical quiet NaN, 7fc0 in
+    bf16 (7fc00000 in fp32), whatever NaN the operands or the hardware carry:
+    IEEE 754-2008 6.2 fixes only that the result is a quiet NaN, so the one
+    encoding is the reading taken; NaN_BF16 marks those tokens."""
+    ids = np.tile(np.array([[0, 1]], np.int32), (8, 1))
+    sc = np.array([[1, 1], [1, 1], [1, 1], [1, 1], [0.75, 0], [0, 1], [1, 1], [1, 1]],
+                  np.float32)
     rows = np.array([[BF16_MAX, 0x7B00],        # max, 2^119
                      [BF16_MAX, 0x7A80],        # max, 2^118
                      [0x8000, 0x8000],          # -0, -0
                      [0x7F80, 0xFF80],          # +inf, -inf
                      [BF16_MIN_SUB, 0x3F80],    # 2^-133, 1 (weight 0)
-                     [0x7F80, 0x3F80]],         # +inf (weight 0), 1
+                     [0x7F80, 0x3F80],          # +inf (weight 0), 1
+                     [0xFFD5, 0x3F80],          # -NaN with payload, 1
+                     [0x7F81, 0x3F80]],         # signalling NaN, 1
                     np.uint16)
-    want = [0x7F80, BF16_MAX, 0x0000, None, BF16_MIN_SUB, None]
+    want = [0x7F80, BF16_MAX, 0x0000, NAN_BF16, BF16_MIN_SUB, NAN_BF16, NAN_BF16, NAN_BF16]
     return ids, sc, rows, want
 
 
@@ -711,16 +765,48 @@ def pin_combine_ieee_special_values(o):
     out, err = o.combine(y, sc, d["pos"], d["rank_prefix"], d["S"], R)
     assert err == 0
     for t, w in enumerate(want):
-        if w is None:
-            assert np.all(bf16_is_nan(out[t])), (t, out[t])
-        else:
-            assert np.all(out[t] == w), (t, hex(int(out[t, 0])), hex(w))
-    # fp32 output: token 0 keeps the exact sum (2 - 2^-8) 2^127 = 0x7f7f8000,
-    # token 4 the subnormal 0x0000c000.
+        assert np.all(out[t] == w), (t, hex(int(out[t, 0])), hex(w))
     out32, _ = o.combine(y, sc, d["pos"], d["rank_prefix"], d["S"], R, "f32")
-    assert np.all(out32[0].view(np.uint32) == 0x7F7F8000)
-    assert np.all(out32[4].view(np.uint32) == 0x0000C000)
-    assert np.all(out32[2].view(np.uint32) == 0)
+    assert np.array_equal(out32.view(np.uint32), special_value_f32(want, D))
+
+
+def special_value_f32(want, D):
+    """The fp32 combine outputs of special_value_case: token 0 keeps the exact
+    sum (2 - 2^-8) 2^127 = 0x7f7f8000, token 1 max + 2^118 = 0x7f7f4000, token 2
+    +0, token 4 the subnormal 0x0000c000, the NaN tokens 0x7fc00000."""
+    f32 = {0: 0x7F7F8000, 1: 0x7F7F4000, 2: 0x00000000, 4: 0x0000C000}
+    rows = [NAN_F32 if w == NAN_BF16 else f32[t] for t, w in enumerate(want)]
+    return np.repeat(np.array(rows, np.uint32)[:, None], D, axis=1)
+
+
+def pin_backward_nan_canonical(o):
+    # The backward's NaN results (s * NaN in grad_y, a NaN in grad_x's sum) are
+    # the canonical quiet NaN however the incoming NaN is encoded (negative,
+    # signalling, with a payload); finite entries are untouched.
+    T, N, E, K, R, D = 6, 8, 4, 2, 2, 8
+    ids = np.array([[0, 2], [1, 3], [0, 1], [2, 3], [3, 0], [1, 2]], np.int32)
+    sc = np.full((T, K), 0.5, np.float32)
+    x = _bf16_bits(np.ones((T, D), np.float32))
+    d = o.dispatch(x, sc, ids, N, E, R)
+    g = _bf16_bits(np.ones((T, D), np.float32))
+    g[0, :] = 0xFFD5        # negative quiet NaN with a payload
+    g[1, :4] = 0x7F81       # signalling NaN
+    g[2, 0] = 0x7FEA        # quiet NaN with a payload
+    for kind, nan in (("bf16", NAN_BF16), ("f32", NAN_F32)):
+        gk = g if kind == "bf16" else _f32_from_bits(g)
+        yk = d["recv_x"] if kind == "bf16" else _f32_from_bits(d["recv_x"])
+        gy, _, _ = o.combine_backward(gk, yk, sc, d["pos"], d["rank_prefix"], d["S"], R)
+        gy_bits = gy.view(np.uint16 if kind == "bf16" else np.uint32)
+        half = 0x3F00 if kind == "bf16" else 0x3F000000
+        gx, _, _ = o.dispatch_backward(gy, None, d["pos"], d["rank_prefix"], d["S"], R)
+        gx_bits = gx.view(np.uint16 if kind == "bf16" else np.uint32)
+        one = 0x3F80 if kind == "bf16" else 0x3F800000
+        nan_in = bf16_is_nan(g)
+        for t in range(T):
+            for k in range(K):
+                row = gy_bits[d["pos"][t, k]]
+                assert np.array_equal(row, np.where(nan_in[t], nan, half)), (kind, t, k)
+            assert np.array_equal(gx_bits[t], np.where(nan_in[t], nan, one)), (kind, t)
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -4,7 +4,8 @@ Each mutant plants one plausible mistake in the oracle's C source (a dropped
 term, a wrong sign, an inclusive instead of exclusive offset, a strided
 expert-to-rank map, a stride that ignores padding, an unstable order, bf16
 truncation, pairs counted instead of tokens, the wrong alignment, floor
-instead of ceiling division, padded rows that route somewhere). The pins are
+instead of ceiling division, padded rows that route somewhere, a NaN result
+other than the canonical one, a double rounding). The pins are
 only trusted if each of these is caught.
 """
 import pytest
@@ -41,6 +42,9 @@ MUTANTS = {
     26: "capacity from the call's T instead of num_tokens_per_rank",
     27: "expert GEMM reads the weights transposed",
     28: "bf16 ties round away from zero",
+    29: "arithmetic NaN results keep the host's NaN instead of the canonical one",
+    30: "bf16 cast of a NaN drops its sign and payload",
+    31: "expert GEMM rounds twice, through fp32",
 }
 
 
