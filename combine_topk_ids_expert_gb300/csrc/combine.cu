@@ -13,6 +13,12 @@
 // A gather: each output element is produced by exactly one thread, in a fixed
 // k order, with no atomics, so results are bitwise reproducible. HBM-bound:
 // reads up to T*K rows, writes T rows.
+//
+// NaN results: IEEE 754-2008 section 6.2 fixes only that an operation with a
+// NaN result returns a quiet NaN, not which one (the hardware's own is
+// 7fffffff). Every NaN this file's arithmetic produces is stored as the
+// canonical quiet NaN: 7fc00000 in fp32, 7fc0 in bf16 (positive, quiet bit,
+// empty payload), so results are the same bits on every machine.
 #include <cuda_bf16.h>
 
 #include "ep_device.cuh"
@@ -55,10 +61,24 @@ __device__ __forceinline__ void fma_vec<1>(float* acc, const int4& r, float w)
     acc[3] = __fmaf_rn(w, __int_as_float(r.w), acc[3]);
 }
 
+constexpr uint32_t kNanF32 = 0x7fc00000u;   // the canonical quiet NaN
+constexpr uint32_t kNanBf16 = 0x7fc0u;
+
+// v, or the canonical quiet NaN where v is a NaN.
+__device__ __forceinline__ float canonical_nan(float v)
+{
+    return v != v ? __uint_as_float(kNanF32) : v;
+}
+
+// Two fp32 values to bf16 (round to nearest even; a NaN to the canonical quiet
+// NaN), lo in the low half (the lower address).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x (low address) = lo
-    return *reinterpret_cast<uint32_t*>(&h);
+    uint32_t r = *reinterpret_cast<uint32_t*>(&h);
+    if (lo != lo) r = (r & 0xffff0000u) | kNanBf16;
+    if (hi != hi) r = (r & 0x0000ffffu) | (kNanBf16 << 16);
+    return r;
 }
 
 // Stores the N = InVec<IN>::kElems accumulators of vector v of token t.
@@ -87,7 +107,9 @@ __device__ __forceinline__ void store_out(void* out, int64_t t, int64_t D, int64
         float* o = static_cast<float*>(out) + e0;
 #pragma unroll
         for (int i = 0; i < N; i += 4)
-            *reinterpret_cast<float4*>(o + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+            *reinterpret_cast<float4*>(o + i) =
+                make_float4(canonical_nan(acc[i]), canonical_nan(acc[i + 1]),
+                            canonical_nan(acc[i + 2]), canonical_nan(acc[i + 3]));
     }
 }
 
@@ -162,7 +184,8 @@ __device__ __forceinline__ void unpack(const int4& r, float* f)
     }
 }
 
-// Packs N fp32 values to a 16-byte vector of the type (bf16: round to nearest even).
+// Packs N fp32 values to a 16-byte vector of the type (bf16: round to nearest
+// even); NaNs become the canonical quiet NaN.
 template <int IN>
 __device__ __forceinline__ int4 pack(const float* f)
 {
@@ -170,8 +193,8 @@ __device__ __forceinline__ int4 pack(const float* f)
         return make_int4((int)pack_bf16x2(f[0], f[1]), (int)pack_bf16x2(f[2], f[3]),
                          (int)pack_bf16x2(f[4], f[5]), (int)pack_bf16x2(f[6], f[7]));
     } else {
-        return make_int4(__float_as_int(f[0]), __float_as_int(f[1]), __float_as_int(f[2]),
-                         __float_as_int(f[3]));
+        return make_int4(__float_as_int(canonical_nan(f[0])), __float_as_int(canonical_nan(f[1])),
+                         __float_as_int(canonical_nan(f[2])), __float_as_int(canonical_nan(f[3])));
     }
 }
 
@@ -258,7 +281,7 @@ combine_backward_kernel(CombineBwdArgs a)
                     float sum = 0.0f;
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w) sum += s_red[w][threadIdx.x];
-                    a.grad_scores[t * a.K + k] = (s_pos[k] >= 0) ? sum : 0.0f;
+                    a.grad_scores[t * a.K + k] = (s_pos[k] >= 0) ? canonical_nan(sum) : 0.0f;
                 }
                 __syncthreads();
             }
