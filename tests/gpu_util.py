@@ -1,6 +1,9 @@
 """Helpers shared by the GPU parity tests: numpy <-> torch and oracle comparisons."""
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -104,3 +107,78 @@ def make_inputs(name: str, T: int | None = None, seed: int | None = None, rank: 
         base = w.seed if seed is None else seed
         inp["x"] = W.hidden(base + 7919 * rank, inp["T"], D, w.dtype)
     return inp
+
+
+# Host threads for full-size oracle runs: each thread runs the single-threaded
+# oracle on its own slice of tokens (ctypes releases the GIL during the call).
+ORACLE_THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+def pool_map(fn, items):
+    with ThreadPoolExecutor(ORACLE_THREADS) as ex:
+        return list(ex.map(fn, items))
+
+
+def identity_block(x: np.ndarray, pos: np.ndarray, a: int, b: int):
+    """Tokens [a, b) of a call under the identity expert, as a problem of its own:
+    the receive rows their valid pairs land on (y[pos[t, k]] = x[t]) packed in
+    flat pair order into one rank. Returns (rows, cpos, rank_prefix, S) for the
+    oracle; cpos[t - a, k] is the pair's row in the block or -1. Each token's
+    combine and backward depend only on its own pairs' rows, so the oracle run
+    on the block gives exactly its run on the whole call for these tokens."""
+    p = pos[a:b]
+    valid = p >= 0
+    n = int(valid.sum())
+    cpos = np.full(p.shape, -1, np.int32)
+    cpos[valid] = np.arange(n, dtype=np.int32)
+    tok = np.repeat(np.arange(a, b), p.shape[1]).reshape(p.shape)[valid]
+    rows = x[tok] if n else np.zeros((1, x.shape[1]), x.dtype)
+    return rows, cpos, np.array([n], np.int32), max(n, 1)
+
+
+def oracle_combine_all(o: oracle.Oracle, x: np.ndarray, scores: np.ndarray, pos: np.ndarray,
+                       out_dtype: str = "same", chunk: int = 1024) -> np.ndarray:
+    """The oracle's combine of EVERY token of a call whose expert is the identity
+    (pos: the oracle's own positions), run in token slices on host threads."""
+    T = pos.shape[0]
+
+    def run(a):
+        rows, cpos, prefix, S = identity_block(x, pos, a, min(T, a + chunk))
+        out, err = o.combine(rows, scores[a:a + chunk], cpos, prefix, S, 1, out_dtype)
+        assert err == 0
+        return out
+
+    parts = pool_map(run, range(0, T, chunk))
+    if parts:
+        return np.concatenate(parts)
+    kind = x.dtype if out_dtype == "same" else (np.uint16 if out_dtype == "bf16" else np.float32)
+    return np.zeros((0, x.shape[1]), kind)
+
+
+def oracle_backward_all(o: oracle.Oracle, x: np.ndarray, g: np.ndarray, scores: np.ndarray,
+                        pos: np.ndarray, chunk: int = 1024):
+    """The oracle's backward of EVERY token of an identity-expert call: grad_y of
+    the valid pairs in flat pair order [n_valid, D], grad_scores [T, K], grad_x
+    [T, D] (dispatch backward of the oracle's own grad_y)."""
+    T = pos.shape[0]
+
+    def run(a):
+        b = min(T, a + chunk)
+        rows, cpos, prefix, S = identity_block(x, pos, a, b)
+        gy, gs, err = o.combine_backward(g[a:b], rows, scores[a:b], cpos, prefix, S, 1)
+        assert err == 0
+        gx, _, err = o.dispatch_backward(gy, None, cpos, prefix, S, 1)
+        assert err == 0
+        return gy[:int(prefix[0])], gs, gx
+
+    parts = pool_map(run, range(0, T, chunk))
+    return (np.concatenate([q[0] for q in parts]), np.concatenate([q[1] for q in parts]),
+            np.concatenate([q[2] for q in parts]))
+
+
+def valid_rows(t: torch.Tensor, pos: np.ndarray) -> np.ndarray:
+    """Rows of a receive-layout tensor at every valid position, in flat pair
+    order, gathered on the device and copied to the host."""
+    D = t.shape[-1]
+    p = torch.from_numpy(pos.reshape(-1)[pos.reshape(-1) >= 0].astype(np.int64)).cuda()
+    return to_np(t.reshape(-1, D)[p])

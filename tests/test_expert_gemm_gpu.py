@@ -14,7 +14,7 @@ import torch
 
 import combine_topk_ids_expert_gb300 as ep
 import workloads as W
-from gpu_util import assert_combine_equal, to_dev, to_np
+from gpu_util import pool_map, assert_combine_equal, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -106,8 +106,8 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
     # same K=16 steps in the same order for every output, so all agree bit for
     # bit; so do the schedules (light experts interleaved with heavy ones at the
     # default threshold, none light, all light), which change only which SM
-    # computes a tile and when. Sampled rows of a few experts are checked
-    # against the oracle.
+    # computes a tile and when. Every row of the hottest, the median and the
+    # coldest expert is checked against the oracle.
     w_ = W.WORKLOADS[name]
     inp = W.make(name)
     D, E, dout = w_.D, w_.E, 2048
@@ -141,22 +141,31 @@ def test_gemm_variants_fullsize(orc, monkeypatch, name):
             bufs.append((buf, d))
             ys.append(y)
     buf, d = bufs[0]
-    cnt = to_np(d.layout.tokens_per_expert)
-    off = to_np(d.layout.expert_offset)
-    order = np.argsort(-cnt, kind="stable")
-    experts = [int(e) for e in (order[0], order[len(order) // 2], order[-1]) if cnt[e] > 0]
-    xs, ws, cs, y_rows = [], [], [], []
+    # Every row of the hottest, the median and the coldest used expert against
+    # the oracle, with each row's input taken from x through the oracle's own
+    # layout (receive row pos[t, k] holds x[t]).
+    ref = orc.layout(inp["ids"], w_.N, E, w_.R)
+    cnt, off = ref["cnt"], ref["expert_offset"]
+    T, K = inp["ids"].shape
+    src = np.full(w_.R * ref["S"], -1, np.int64)
+    valid = ref["pos"] >= 0
+    src[ref["pos"][valid]] = np.repeat(np.arange(T), K).reshape(T, K)[valid]
+    used = np.flatnonzero(cnt > 0)
+    order = used[np.argsort(-cnt[used], kind="stable")]
+    experts = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
+    w_np = to_np(wd.reshape(E, dout, D))
     for e in experts:
-        n = int(cnt[e])
-        pick = sorted({0, n // 2, n - 1, min(n - 1, 127), min(n - 1, 128)})
-        rows = torch.tensor([int(off[e]) + i for i in pick], device="cuda")
-        xs.append(to_np(d.recv_x.reshape(-1, D)[rows]))
-        y_rows.append(to_np(ys[0][rows]))
-        ws.append(to_np(wd.reshape(E, dout, D)[e]))
-        cs.append(len(pick))
-    cnt_s = np.array(cs, np.int32)
-    off_s = np.concatenate([[0], np.cumsum(cnt_s)[:-1]]).astype(np.int32)
-    check_gemm(orc, np.concatenate(y_rows), np.concatenate(xs), np.stack(ws), cnt_s, off_s)
+        rows = np.arange(int(off[e]), int(off[e]) + int(cnt[e]))
+        y_e = to_np(ys[0][torch.from_numpy(rows).cuda()])
+        x_e = inp["x"][src[rows]]
+        chunks = [(a, min(len(rows), a + 128)) for a in range(0, len(rows), 128)]
+
+        def run(c, e=e, x_e=x_e, y_e=y_e):
+            a, b = c
+            check_gemm(orc, y_e[a:b], x_e[a:b], w_np[e][None], np.array([b - a], np.int32),
+                       np.zeros(1, np.int32))
+
+        pool_map(run, chunks)
     for b, _ in bufs:
         b.close()
     del bufs, ys, wd

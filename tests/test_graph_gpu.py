@@ -14,7 +14,7 @@ import torch
 import combine_topk_ids_expert_gb300 as ep
 import workloads as W
 from gpu_util import (assert_combine_equal, assert_layout_equal, assert_recv_equal,
-                      sampled_combine_ref, to_dev, to_np)
+                      oracle_combine_all, to_dev, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -108,8 +108,9 @@ def test_graph_replay_fresh_routing_and_interleave(orc, impl):
 def test_prefill32k_graph_100_replays(orc):
     # 32k-token prefill in worst-token graph mode: one capture, 100 replays
     # with fresh Zipf(1.1) routing. Counts and positions are checked against
-    # the oracle on every replay; full receive rows and sampled combine on
-    # replays 0, 1, 49, 98, 99, where the replay also equals an eager run.
+    # the oracle on every replay; on replays 0, 1, 49, 98, 99 every receive row
+    # and the combine of every token, in bf16 and in fp32 before the cast, are
+    # checked against the oracle, and the replay equals an eager run.
     w = W.WORKLOADS["prefill32k"]
     T, N, D, E, K, R = w.T, w.N, w.D, w.E, w.K, w.R
     buf = ep.Buffer(w.N_max, D, E, R, K, dtype=torch.bfloat16)
@@ -118,20 +119,18 @@ def test_prefill32k_graph_100_replays(orc):
     ids_d = torch.empty((T, K), dtype=torch.int32, device="cuda")
     sc_d = torch.empty((T, K), dtype=torch.float32, device="cuda")
     out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    out32 = torch.empty((T, D), dtype=torch.float32, device="cuda")
     inp0 = W.make("prefill32k", replay=0, with_x=False)
     ids_d.copy_(torch.from_numpy(inp0["ids"]))
     sc_d.copy_(torch.from_numpy(inp0["scores"]))
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        d = buf.dispatch(xd, sc_d, ids_d, N, stream=s)
-        buf.combine(d.recv_x, sc_d, out=out, stream=s)
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        d = buf.dispatch(xd, sc_d, ids_d, N, stream=s)
-        buf.combine(d.recv_x, sc_d, out=out, stream=s)
+
+    def seq(stream):
+        d = buf.dispatch(xd, sc_d, ids_d, N, stream=stream)
+        buf.combine(d.recv_x, sc_d, out=out, stream=stream)
+        buf.combine(d.recv_x, sc_d, out=out32, out_dtype=torch.float32, stream=stream)
+        return d
+
+    g, d = _capture(seq)
     eager = ep.Buffer(w.N_max, D, E, R, K, dtype=torch.bfloat16)
     full = {0, 1, 49, 98, 99}
     for i in range(w.graph_replays):
@@ -147,16 +146,16 @@ def test_prefill32k_graph_100_replays(orc):
             rows = d.recv_x.reshape(-1, D)[pos].view(torch.int16)
             tok = torch.arange(T, device="cuda").repeat_interleave(K)
             assert torch.equal(rows, xd[tok].view(torch.int16))
-            rng = np.random.default_rng(i)
-            sample = np.unique(rng.integers(0, T, 96))
-            y = to_np(d.recv_x.reshape(-1, D))
-            want = sampled_combine_ref(orc, y, inp["scores"], ref["pos"], sample)
-            assert_combine_equal(to_np(out)[sample], want)
+            del rows, tok
+            for got, kind in ((out, "same"), (out32, "f32")):
+                want = oracle_combine_all(orc, x, inp["scores"], ref["pos"], kind)
+                assert_combine_equal(to_np(got), want)
+                del want
             de = eager.dispatch(xd, sc_d, ids_d, N)
             oe = eager.combine(de.recv_x, sc_d)
             torch.cuda.synchronize()
             assert torch.equal(oe.view(torch.int16), out.view(torch.int16))
-            del rows, tok, de, oe
+            del de, oe
     assert buf.device_error() == 0
     buf.close()
     eager.close()
