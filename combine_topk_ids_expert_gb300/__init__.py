@@ -24,7 +24,7 @@ import torch
 
 from . import _abi
 from ._abi import (EP_BF16, EP_DEVERR_BAD_ID, EP_DEVERR_DEBUG_STRAY, EP_DEVERR_DEBUG_UNWRITTEN,
-                   EP_DEVERR_ROW_OOB, EP_DEVERR_TIMEOUT, EP_F32,
+                   EP_DEVERR_ROW_OOB, EP_DEVERR_TIMEOUT, EP_F32, EP_NOALLOC_SCRATCH_BYTES,
                    EP_LAYOUT_PACKED, EP_LAYOUT_STRIDED, EP_PERMUTE_BULK, EP_PERMUTE_DEFAULT,
                    EP_PERMUTE_VEC, EpBufferInfo, EpConfig, EpDedupOut, EpDispatchOut, EpError,
                    EpLayout, check)
@@ -35,7 +35,8 @@ __all__ = [
     "ep_dispatch", "ep_dispatch_permute", "ep_combine", "ep_combine_backward",
     "ep_dispatch_backward", "ep_dispatch_dedup", "ep_dedup_expand", "ep_expert_gemm",
     "ep_get_device_error", "DedupResult",
-    "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_pad_tokens", "group_num_tokens_per_rank",
+    "ep_buffer_query", "ep_dispatch_layout_noalloc", "ep_dispatch_layout_noalloc_scratch_bytes",
+    "EP_NOALLOC_SCRATCH_BYTES", "ep_pattern_probe", "ep_pad_tokens", "group_num_tokens_per_rank",
     "ep_derive_max_tokens_pretrain",
     "ep_derive_max_tokens_inference", "ep_validate_max_tokens", "ep_status_string",
     "EP_BF16", "EP_F32", "EP_PERMUTE_DEFAULT", "EP_PERMUTE_VEC", "EP_PERMUTE_BULK",
@@ -213,18 +214,63 @@ def ep_dispatch_layout_noalloc(topk_expert_ids_TK: torch.Tensor, num_tokens: int
                                pos: torch.Tensor, error_flags: torch.Tensor | None = None,
                                stream=None) -> None:
     """The layout without a buffer, for callers that cannot allocate device
-    memory: the caller supplies every output tensor (int32, on the device);
-    the library uses its own fixed device scratch and allocates nothing."""
-    for name, t in (("topk_expert_ids_TK", topk_expert_ids_TK),
-                    ("tokens_per_expert", tokens_per_expert), ("expert_offset", expert_offset),
-                    ("rows_per_rank", rows_per_rank), ("rank_prefix", rank_prefix),
-                    ("tokens_in_rank", tokens_in_rank), ("pos", pos)):
-        _check_dtype(t, torch.int32, name)
-    check(_abi.lib().ep_dispatch_layout_noalloc(
-        _ptr(topk_expert_ids_TK), num_tokens, num_tokens_per_rank, topk, num_experts,
-        num_ranks, _ptr(tokens_per_expert), _ptr(expert_offset), _ptr(rows_per_rank),
-        _ptr(rank_prefix), _ptr(tokens_in_rank), _ptr(pos), _ptr(error_flags),
-        _stream(stream)), "ep_dispatch_layout_noalloc")
+    memory: the caller supplies every output tensor (int32, on one CUDA device);
+    the library uses its own fixed device scratch and allocates nothing. The
+    tensors' sizes are checked here, since the C call only sees pointers: ids
+    and pos hold num_tokens * topk entries, the per-expert outputs num_experts,
+    the per-rank outputs num_ranks, error_flags (optional) one word."""
+    T, K, E, R = int(num_tokens), int(topk), int(num_experts), int(num_ranks)
+    if T < 0 or int(num_tokens_per_rank) < T:
+        raise ValueError(f"need 0 <= num_tokens ({T}) <= num_tokens_per_rank "
+                         f"({num_tokens_per_rank})")
+    tensors = [("topk_expert_ids_TK", topk_expert_ids_TK, T * K),
+               ("tokens_per_expert", tokens_per_expert, E), ("expert_offset", expert_offset, E),
+               ("rows_per_rank", rows_per_rank, R), ("rank_prefix", rank_prefix, R),
+               ("tokens_in_rank", tokens_in_rank, R), ("pos", pos, T * K)]
+    if error_flags is not None:
+        tensors.append(("error_flags", error_flags, 1))
+    device = topk_expert_ids_TK.device
+    if not topk_expert_ids_TK.is_cuda:
+        raise ValueError("topk_expert_ids_TK must be a CUDA tensor")
+    for name, t, n in tensors:
+        if name != "error_flags":
+            _check_dtype(t, torch.int32, name)
+        elif t.dtype not in (torch.int32, torch.uint32) or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("error_flags must be a contiguous 4-byte integer CUDA tensor")
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, topk_expert_ids_TK on {device}")
+        if t.numel() < n:
+            raise ValueError(f"{name} has {t.numel()} elements, the call needs {n}")
+    with torch.cuda.device(device):     # the device whose scratch the call uses
+        check(_abi.lib().ep_dispatch_layout_noalloc(
+            _ptr(topk_expert_ids_TK), T, num_tokens_per_rank, K, E, R, _ptr(tokens_per_expert),
+            _ptr(expert_offset), _ptr(rows_per_rank), _ptr(rank_prefix), _ptr(tokens_in_rank),
+            _ptr(pos), _ptr(error_flags), _stream(stream)), "ep_dispatch_layout_noalloc")
+
+
+def ep_dispatch_layout_noalloc_scratch_bytes(num_tokens: int, topk: int, num_experts: int,
+                                             num_ranks: int) -> int:
+    """Bytes of the fixed device scratch that ep_dispatch_layout_noalloc needs for
+    these sizes (host arithmetic only); accepted when <= EP_NOALLOC_SCRATCH_BYTES."""
+    return int(_abi.lib().ep_dispatch_layout_noalloc_scratch_bytes(num_tokens, topk,
+                                                                   num_experts, num_ranks))
+
+
+def ep_pattern_probe(pattern: int, src: torch.Tensor | None, dst: torch.Tensor, rows: int,
+                     row_bytes: int, fan: int = 1, stream=None) -> None:
+    """Measurement aid: one of the hot path's HBM access patterns (EP_PATTERN_*)
+    on `rows` rows of row_bytes, alone in a kernel. Sizes are checked here:
+    FANOUT writes fan*rows rows, GATHER reads fan*rows rows, READ writes one
+    16-byte word per row."""
+    n_src = rows * row_bytes * (fan if pattern == _abi.EP_PATTERN_GATHER else 1)
+    n_dst = (rows * 16 if pattern == _abi.EP_PATTERN_READ
+             else rows * row_bytes * (fan if pattern == _abi.EP_PATTERN_FANOUT else 1))
+    if pattern != _abi.EP_PATTERN_WRITE and (src is None or src.numel() * src.element_size() < n_src):
+        raise ValueError(f"src must hold {n_src} bytes")
+    if dst.numel() * dst.element_size() < n_dst:
+        raise ValueError(f"dst must hold {n_dst} bytes")
+    check(_abi.lib().ep_pattern_probe(pattern, _ptr(src), _ptr(dst), rows, row_bytes, fan,
+                                      _stream(stream)), "ep_pattern_probe")
 
 
 def ep_pad_tokens(n: int) -> int:

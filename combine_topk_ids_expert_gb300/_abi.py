@@ -37,6 +37,14 @@ EP_DEVERR_TIMEOUT = 0x4
 EP_DEVERR_DEBUG_UNWRITTEN = 0x8   # EP_DEBUG=1 only
 EP_DEVERR_DEBUG_STRAY = 0x10      # EP_DEBUG=1 only
 
+EP_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+EP_PATTERN_READ = 0
+EP_PATTERN_WRITE = 1
+EP_PATTERN_COPY = 2
+EP_PATTERN_FANOUT = 3
+EP_PATTERN_GATHER = 4
+
 
 class EpConfig(C.Structure):
     _fields_ = [
@@ -133,10 +141,14 @@ SIGNATURES = {
                                              C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                                              C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                              C.c_void_p, C.c_void_p]),
+    "ep_dispatch_layout_noalloc_scratch_bytes": (C.c_size_t, [C.c_int64, C.c_int32, C.c_int32,
+                                                           C.c_int32]),
     "ep_pad_tokens": (C.c_int64, [C.c_int64]),
     "ep_derive_max_tokens_pretrain": (C.c_int64, [C.c_int64, C.c_int64, C.c_int64, C.c_int64]),
     "ep_derive_max_tokens_inference": (C.c_int64, [C.c_int64, C.c_int64, C.c_int64]),
     "ep_validate_max_tokens": (C.c_int, [C.c_int64, C.c_int64]),
+    "ep_pattern_probe": (C.c_int, [C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64,
+                                   C.c_int32, C.c_void_p]),
     "ep_status_string": (C.c_char_p, [C.c_int]),
 }
 

@@ -15,12 +15,16 @@
 // address: host code must never pass it to a kernel. The first call on each
 // device (with that device current) asks the runtime for the array's device
 // address with cudaGetSymbolAddress and caches it; kernels receive that
-// address. Make that first call before any stream capture.
+// address. Make that first call before any stream capture. The cache is keyed
+// by the device's current context as well (its driver context id), so after a
+// cudaDeviceReset, or under another context of the same device, the next call
+// looks the address up again instead of using one that is no longer mapped.
 //
 // Every call shares the one array, which keeps the last call's contents.
 // Nothing in it needs to start at zero (each word a call reads was written
 // earlier in the same call), but calls whose GPU work overlaps (two streams,
 // or two threads) race on it: serialize them.
+#include <cuda.h>            // driver types only: the entry points are looked up at run time
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -30,14 +34,47 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(4) << 20;   // 4 MiB per device
+constexpr size_t kScratchBytes = EP_NOALLOC_SCRATCH_BYTES;   // 4 MiB per device
 constexpr size_t kSegAlign = 256;
 constexpr int kCachedDevices = 64;
 
 static __device__ __align__(256) uint8_t g_layout_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kCachedDevices];   // device address of g_layout_scratch, per device
+struct ScratchSlot {
+    unsigned long long ctx;   // driver id of the context the address belongs to (0: unknown)
+    void* addr;               // device address of g_layout_scratch in that context
+};
+ScratchSlot g_scratch[kCachedDevices];   // per device
+
+// The current context's driver id, or 0 when there is none yet or the driver
+// entry points cannot be had (then the cache is keyed by device alone). The
+// entry points come from the runtime, so the library does not link libcuda.
+unsigned long long current_context_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+    if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 size_t seg(size_t bytes) { return (bytes + kSegAlign - 1) / kSegAlign * kSegAlign; }
 
@@ -53,21 +90,24 @@ size_t scratch_needed(int64_t T, int K, int E, int R)
     return 2 * seg(tiles * Ep * 4) + seg(tiles * (size_t)R * 4) + seg(4);
 }
 
-// Device address of g_layout_scratch on the current device, looked up once per device.
+// Device address of g_layout_scratch on the current device, looked up once per
+// device (and again when the device's current context has changed).
 cudaError_t scratch_address(void** out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < kCachedDevices;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (dev >= 0 && dev < kCachedDevices && g_scratch_addr[dev]) {
-        *out = g_scratch_addr[dev];
+    if (cached && g_scratch[dev].addr && g_scratch[dev].ctx == current_context_id()) {
+        *out = g_scratch[dev].addr;
         return cudaSuccess;
     }
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_layout_scratch);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kCachedDevices) g_scratch_addr[dev] = ptr;
+    // The lookup has made the runtime's context current: key the entry by it.
+    if (cached) g_scratch[dev] = ScratchSlot{current_context_id(), ptr};
     *out = ptr;
     return cudaSuccess;
 }
@@ -75,6 +115,13 @@ cudaError_t scratch_address(void** out)
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace
+
+extern "C" size_t ep_dispatch_layout_noalloc_scratch_bytes(int64_t num_tokens, int32_t topk,
+                                                          int32_t num_experts, int32_t num_ranks)
+{
+    if (num_tokens < 0 || topk < 1 || num_experts < 1 || num_ranks < 1) return 0;
+    return scratch_needed(num_tokens, topk, num_experts, num_ranks);
+}
 
 extern "C" ep_status ep_dispatch_layout_noalloc(
     const int32_t* topk_expert_ids_TK, int64_t num_tokens, int64_t num_tokens_per_rank,

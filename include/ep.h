@@ -370,10 +370,14 @@ EP_API ep_status ep_buffer_query(const ep_buffer* buf, ep_buffer_info* info);
  * process exits; a call whose tile tables need more,
  *   ceil(T / max(1, 2048/K)) * (2*roundup4(E) + R) * 4 bytes (plus alignment),
  * is rejected with EP_ERR_CAPACITY (about 516k tokens at E=256, R=8, K=8;
- * about 126k at E=1024, R=64, K=8). The first call on each device (with that
- * device current) looks up the array's device address; make it before any
- * stream capture. All calls share the array, so calls whose GPU work overlaps
- * (other streams or threads) race: serialize them. Asynchronous on stream. */
+ * about 126k at E=1024, R=64, K=8; ep_dispatch_layout_noalloc_scratch_bytes
+ * gives the exact figure). The first call on each device (with that device
+ * current) looks up the array's device address; make it before any stream
+ * capture. The address is kept per device and context: after a
+ * cudaDeviceReset, or in another context of the device, the next call looks
+ * it up again (so that call, too, must come before any capture). All calls
+ * share the array, so calls whose GPU work overlaps (other streams or
+ * threads) race: serialize them. Asynchronous on stream. */
 EP_API ep_status ep_dispatch_layout_noalloc(const int32_t* topk_expert_ids_TK, int64_t num_tokens,
                                             int64_t num_tokens_per_rank, int32_t topk,
                                             int32_t num_experts, int32_t num_ranks,
@@ -381,6 +385,17 @@ EP_API ep_status ep_dispatch_layout_noalloc(const int32_t* topk_expert_ids_TK, i
                                             int32_t* rows_per_rank, int32_t* rank_prefix,
                                             int32_t* tokens_in_rank, int32_t* pos,
                                             uint32_t* error_flags, ep_stream_t stream);
+
+/* Size of the fixed device array behind ep_dispatch_layout_noalloc (per GPU). */
+#define EP_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/* Bytes of that array a call of ep_dispatch_layout_noalloc with these sizes
+ * needs; the call is accepted when this is at most EP_NOALLOC_SCRATCH_BYTES.
+ * Host-only arithmetic: no device is touched. 0 for a non-positive topk,
+ * num_experts or num_ranks, or a negative num_tokens. (Plumbing: no page
+ * passage defines it.) */
+EP_API size_t ep_dispatch_layout_noalloc_scratch_bytes(int64_t num_tokens, int32_t topk,
+                                                       int32_t num_experts, int32_t num_ranks);
 
 /* roundup4(n): the padded per-rank token count ([align] "Problem" item 2, "Fix"). */
 EP_API int64_t ep_pad_tokens(int64_t n);
@@ -398,6 +413,28 @@ EP_API int64_t ep_derive_max_tokens_inference(int64_t max_num_batched_tokens, in
  * must be positive and at least the derived requirement. Returns EP_OK,
  * EP_ERR_INVALID_ARG (not positive) or EP_ERR_CAPACITY (too small). */
 EP_API ep_status ep_validate_max_tokens(int64_t configured, int64_t derived);
+
+/* Access patterns of the hot path, for ep_pattern_probe. */
+typedef enum {
+    EP_PATTERN_READ = 0,     /* dst[r] (16 bytes) = XOR of the words of src row r */
+    EP_PATTERN_WRITE = 1,    /* dst row r filled (src unused) */
+    EP_PATTERN_COPY = 2,     /* dst row r = src row r */
+    EP_PATTERN_FANOUT = 3,   /* dst row j*rows + r = src row r, j < fan (the dispatch's shape) */
+    EP_PATTERN_GATHER = 4    /* dst row r = XOR of src rows j*rows + r, j < fan (the combine's) */
+} ep_pattern;
+
+/* Measurement aid (plumbing: no page passage defines it). Moves `rows` rows of
+ * row_bytes (a multiple of 16) in one of the shapes above, with the combine's
+ * kernel structure (a 128-thread CTA per row, 16-byte vectors, as many CTAs
+ * per SM as fit) and nothing else in the kernel, so that a benchmark can time
+ * the HBM ceiling of the dispatch's 1:fan fan-out and the combine's fan:1
+ * gather on this GPU. src and dst are device pointers, 16-byte aligned, sized
+ * for the pattern (FANOUT: dst holds fan*rows rows; GATHER: src holds
+ * fan*rows rows; READ: dst holds rows 16-byte words); 1 <= fan <= 64.
+ * Asynchronous on stream; EP_ERR_INVALID_ARG / EP_ERR_ALIGNMENT on bad
+ * arguments, with nothing enqueued. */
+EP_API ep_status ep_pattern_probe(int32_t pattern, const void* src, void* dst, int64_t rows,
+                                  int64_t row_bytes, int32_t fan, ep_stream_t stream);
 
 /* Static description of a status code. (Plumbing: no page passage defines it.) */
 EP_API const char* ep_status_string(ep_status s);
