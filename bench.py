@@ -15,7 +15,14 @@ ranks are partitions of one GPU's buffer), the timed region is bracketed by a
 barrier and synchronisation, and the slowest rank's time is used.
 
 --impl reference times the CPU oracle (single-threaded C, the correctness
-reference) on the host cores, on a bounded sample of the same workload.
+reference) on one host core, on the same step: its dispatch and combine of the
+same call(s) with the same inputs (about 2 s per DeepSeek-shaped step; 5 steps
+by default). The GPU arm's `cpu_baseline` is the median of 3 such runs.
+
+Other modes: --mode ceilings (the HBM ceiling of each access pattern the step
+uses), --mode dedup / backward, --gemm DOUT (the expert grouped GEMM);
+--graph [--fresh-routing] replays each step from a CUDA graph (with a fresh
+routing copied into the captured inputs before every replay).
 """
 from __future__ import annotations
 
@@ -47,8 +54,10 @@ KERNEL_SOURCES = [os.path.join(ROOT, "combine_topk_ids_expert_gb300", "csrc", f)
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 2000 on the GPU, 5 for the oracle arm)")
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="untimed warm-up steps (default: 20 on the GPU, 1 for the oracle arm)")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="deepseek", choices=sorted(W.WORKLOADS))
     ap.add_argument("--permute", choices=["default", "vec", "bulk"], default="default")
@@ -56,20 +65,36 @@ def parse_args():
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (and N) of the workload: smaller cases for profiling")
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
+    ap.add_argument("--fresh-routing", action="store_true",
+                    help="with --graph: write a fresh routing (ids and scores) into the captured "
+                         "input buffers before every replay, outside the timed events")
+    ap.add_argument("--flush", choices=["read", "memset"], default="read",
+                    help="L2 flush between timed steps: read: a read-only sweep over 4x L2 (every "
+                         "dirty line is written back before the step starts); memset: a write of "
+                         "2x L2 (leaves ~L2-size dirty lines that the step then writes back)")
     ap.add_argument("--gemm", type=int, default=0, metavar="DOUT",
                     help="instead: time the expert grouped GEMM (D -> DOUT) on the receive rows")
-    ap.add_argument("--mode", choices=["step", "dedup", "backward"], default="step",
+    ap.add_argument("--mode", choices=["step", "dedup", "backward", "ceilings"], default="step",
                     help="step: layout+dispatch+combine (the benchmark); dedup: the per-rank "
-                         "dedupe dispatch alone; backward: combine and dispatch backward")
+                         "dedupe dispatch alone; backward: combine and dispatch backward; "
+                         "ceilings: the HBM ceiling of each access pattern the step uses")
     ap.add_argument("--seed", type=int, default=None,
                     help="routing and hidden-state seed (default: the workload's own)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph-leg", action="store_true",
                     help="skip the extra captured-graph timing of the same step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="approximate CPU time spent timing the oracle")
-    return ap.parse_args()
+    ap.add_argument("--cpu-repeats", type=int, default=3,
+                    help="oracle runs of the benched step for the CPU baseline (median taken)")
+    args = ap.parse_args()
+    # The oracle takes about 2 s per DeepSeek-shaped step on one host core: its
+    # defaults keep an unflagged run within a minute or so.
+    ref = args.impl == "reference"
+    if args.steps is None:
+        args.steps = 5 if ref else 2000
+    if args.warmup is None:
+        args.warmup = 1 if ref else 20
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -84,6 +109,16 @@ def workload_desc(w: W.Workload, T: int, N: int) -> dict:
         "T": T, "D": w.D, "E": w.E, "K": w.K, "R": w.R, "num_tokens_per_rank": N,
         "num_max_tokens_per_rank": w.N_max,
     }
+
+
+def step_config(args, w: W.Workload, inps: list[dict], N: int) -> dict:
+    """The `config` both arms print: the workload of one benched step."""
+    cfg = workload_desc(w, sum(c["T"] for c in inps), N)
+    if len(inps) > 1:
+        cfg["workload"] += f" ({len(inps)} calls per step: T = {[c['T'] for c in inps]})"
+    if args.fresh_routing:
+        cfg["workload"] += ", fresh routing per step"
+    return cfg
 
 
 def workload_tokens(args, w: W.Workload) -> tuple[int, int]:
@@ -222,33 +257,30 @@ class ClockSampler:
 # CPU oracle timing (baseline and --impl reference)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_run(w: W.Workload, inp: dict, seconds: float, tokens_per_call: int) -> dict:
-    """Time the oracle (as it stands) on consecutive slices of the workload's
-    tokens until about `seconds` of CPU time have been spent."""
+def oracle_step_seconds(w: W.Workload, inps: list[dict], N: int) -> float:
+    """Seconds the oracle, as it stands (single-threaded C), takes for one
+    benched step: its dispatch and combine of every call of the step, on the
+    step's own inputs (the same T, N and routing the GPU arm times)."""
     import oracle
     o = oracle.get()
-    x, ids, sc = inp["x"], inp["ids"], inp["scores"]
-    T = ids.shape[0]
-    done = 0
     t0 = time.perf_counter()
-    start = 0
-    calls = 0
-    while True:
-        n = min(tokens_per_call, T - start)
-        xs, ids_s, sc_s = x[start:start + n], ids[start:start + n], sc[start:start + n]
-        d = o.dispatch(xs, sc_s, ids_s, n, w.E, w.R)
-        o.combine(d["recv_x"], sc_s, d["pos"], d["rank_prefix"], d["S"], w.R)
-        done += n
-        calls += 1
-        start = (start + n) % T
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"tokens": done, "seconds": el, "calls": calls, "tokens_per_call": tokens_per_call}
+    for c in inps:
+        d = o.dispatch(c["x"], c["scores"], c["ids"], N, w.E, w.R)
+        o.combine(d["recv_x"], c["scores"], d["pos"], d["rank_prefix"], d["S"], w.R)
+        del d
+    return time.perf_counter() - t0
 
 
-def oracle_tokens_per_call(w: W.Workload) -> int:
-    return 256 if w.D * w.K >= 4096 * 8 else 1024
+def oracle_baseline(w: W.Workload, inps: list[dict], N: int, repeats: int) -> dict:
+    """The oracle on the benched step, `repeats` times; the median is reported."""
+    secs = [oracle_step_seconds(w, inps, N) for _ in range(max(1, repeats))]
+    T_step = sum(c["T"] for c in inps)
+    med = statistics.median(secs)
+    return {"value": T_step / med, "unit": "tokens/s", "cores": 1,
+            "host_cores": os.cpu_count(), "kind": "oracle",
+            "sample": (f"the whole benched step ({len(inps)} call(s), {T_step} tokens, the same "
+                       f"inputs as the GPU arm), {len(secs)} runs on one host thread, median "
+                       f"{med:.2f} s (runs: {', '.join(f'{x:.2f}' for x in secs)} s)")}
 
 
 # ---------------------------------------------------------------------------
@@ -291,6 +323,47 @@ def barrier(world: int):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+
+def make_l2_flush(args, dev):
+    """The L2 flush run before every timed step, outside its events. read: a
+    read-only sweep over 4x L2 (a sum), after which L2 holds only clean lines,
+    so the step pays for no earlier write-back; memset: a 2x L2 memset, which
+    leaves about L2's size of dirty lines for the step to write back."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    if args.flush == "read":
+        # fp32 so that the sum reads the buffer in place (an integer sum would
+        # first write a widened copy)
+        buf = torch.zeros(max(4 * l2, 512 << 20) // 4, dtype=torch.float32, device=dev)
+        return lambda: buf.sum()
+    buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    return lambda: buf.zero_()
+
+
+def _routing_job(job):
+    name, rank, T, seed, replay = job
+    inp = W.make(name, rank=rank, T=T, seed=seed, replay=replay, with_x=False)
+    return inp["ids"], inp["scores"]
+
+
+def fresh_routings(args, w: W.Workload, Ts: list[int]) -> list:
+    """Pinned host copies of a fresh routing (ids, scores) per call for up to
+    100 replays (replay i of the workload's graph schedule), drawn in a pool
+    of spawned processes."""
+    import multiprocessing as mp
+
+    import torch
+    n = max(1, min(args.steps, 100))
+    jobs = [(args.workload, c, T, args.seed, i) for i in range(n) for c, T in enumerate(Ts)]
+    with mp.get_context("spawn").Pool(min(16, os.cpu_count() or 1)) as pool:
+        flat = pool.map(_routing_job, jobs)
+    out = []
+    for i in range(n):
+        calls = flat[i * len(Ts):(i + 1) * len(Ts)]
+        out.append([(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory())
+                    for a, b in calls])
+    return out
+
 
 def step_calls(args, w: W.Workload) -> tuple[list[dict], int]:
     """The dispatch+combine calls of one step and their shared N: one call, or
@@ -362,8 +435,8 @@ def run_gb300(args) -> dict | None:
     assert buf.device_error() == 0
     ref_outs = [o.clone() for o in outs]
 
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    l2_flush = make_l2_flush(args, dev)
+    routes = fresh_routings(args, w, Ts) if args.fresh_routing else None
 
     def step_kernels(stream_ptr):
         for i in range(n_calls):
@@ -386,7 +459,7 @@ def run_gb300(args) -> dict | None:
     graph = capture() if args.graph else None
 
     for _ in range(args.warmup):
-        flush.zero_()
+        l2_flush()
         if graph is not None:
             graph.replay()
         else:
@@ -405,7 +478,12 @@ def run_gb300(args) -> dict | None:
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     for it in range(K):
-        flush.zero_()                       # L2 flush, outside the events
+        if routes is not None:              # fresh routing into the captured inputs
+            r = routes[it % len(routes)]
+            for i in range(n_calls):
+                idss[i].copy_(r[i][0], non_blocking=True)
+                scs[i].copy_(r[i][1], non_blocking=True)
+        l2_flush()                          # L2 flush, outside the events
         e = ev[it]
         e[0].record(stream)
         if graph is not None:
@@ -425,8 +503,22 @@ def run_gb300(args) -> dict | None:
     if graph is not None:
         launches = K * per_step_launches
     assert buf.device_error() == 0
-    for o, r in zip(outs, ref_outs):
-        assert torch.equal(o.view(raw), r.view(raw)), "timed steps changed the output"
+    if routes is None:
+        for o, r in zip(outs, ref_outs):
+            assert torch.equal(o.view(raw), r.view(raw)), "timed steps changed the output"
+    else:
+        # the last replay's outputs against an eager step on the same routing
+        last = [o.clone() for o in outs]
+        step_kernels(sptr)
+        torch.cuda.synchronize(dev)
+        assert buf.device_error() == 0
+        for o, r in zip(outs, last):
+            assert torch.equal(o.view(raw), r.view(raw)), "replay differs from an eager step"
+        for i in range(n_calls):            # back to the first routing for the legs below
+            idss[i].copy_(idh[i])
+            scs[i].copy_(sch[i])
+        step_kernels(sptr)
+        torch.cuda.synchronize(dev)
 
     step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
     total_ms = sum(step_ms)
@@ -469,6 +561,9 @@ def run_gb300(args) -> dict | None:
                            "peak_source": peak_src,
                            "traffic": profiled_traffic(kname, args.workload),
                            "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
+    if routes is not None:
+        res["fresh_routing"] = {"routings": len(routes), "replays": K,
+                                "copied_per_replay_bytes": sum(8 * T * w.K for T in Ts)}
     res["bytes"] = nbytes
     res["pairs"] = sum(pairs)
     res["info"] = buf.info()
@@ -478,7 +573,7 @@ def run_gb300(args) -> dict | None:
     if graph is None and not args.no_graph_leg:
         g = capture()
         for _ in range(3):
-            flush.zero_()
+            l2_flush()
             g.replay()
         Kg = max(3, min(K, 300))
         evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -486,7 +581,7 @@ def run_gb300(args) -> dict | None:
         barrier(world)
         torch.cuda.synchronize(dev)
         for a, c in evg:
-            flush.zero_()
+            l2_flush()
             a.record(stream)
             g.replay()
             c.record(stream)
@@ -716,10 +811,9 @@ def run_aux(args) -> None:
             ep.ep_combine_backward(h, g, d.recv_x, sc, T, gy, gs)
             ep.ep_dispatch_backward(h, gy, None, T, gx, code)
         extra = {"pairs": pairs}
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    l2_flush = make_l2_flush(args, dev)
     for _ in range(args.warmup):
-        flush.zero_()
+        l2_flush()
         op()
     torch.cuda.synchronize(dev)
     Ks = args.steps
@@ -729,7 +823,7 @@ def run_aux(args) -> None:
     clocks.start()
     launches0 = buf.info()["kernel_launches"]
     for e0, e1 in ev:
-        flush.zero_()
+        l2_flush()
         e0.record()
         op()
         e1.record()
@@ -751,8 +845,70 @@ def run_aux(args) -> None:
     print(json.dumps(line))
 
 
+def run_ceilings(args) -> None:
+    """The HBM ceiling of each access pattern the step uses, on the workload's
+    row size: ep_pattern_probe moves the rows of one call (T tokens, K = fan)
+    in each shape alone in a kernel, L2 flushed before every launch, CUDA
+    events around it; bytes are the rows read plus the rows written."""
+    import torch
+
+    import combine_topk_ids_expert_gb300 as ep
+    from combine_topk_ids_expert_gb300.build import build as build_lib
+    build_lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = W.WORKLOADS[args.workload]
+    T, _ = workload_tokens(args, w)
+    row, fan = w.D * w.elem_bytes, w.K
+    src = torch.zeros(T * fan * row // 4, dtype=torch.int32, device=dev)
+    dst = torch.zeros(T * fan * row // 4, dtype=torch.int32, device=dev)
+    shapes = {   # name: (pattern, rows, bytes moved)
+        "read": (ep._abi.EP_PATTERN_READ, T * fan, T * fan * (row + 16)),
+        "write": (ep._abi.EP_PATTERN_WRITE, T * fan, T * fan * row),
+        "copy": (ep._abi.EP_PATTERN_COPY, T * fan, 2 * T * fan * row),
+        f"fanout_1to{fan}": (ep._abi.EP_PATTERN_FANOUT, T, (1 + fan) * T * row),
+        f"gather_{fan}to1": (ep._abi.EP_PATTERN_GATHER, T, (1 + fan) * T * row),
+    }
+    l2_flush = make_l2_flush(args, dev)
+    peak, src_name = measured_peak_hbm()
+    steps = max(3, min(args.steps, 200))
+    clocks = ClockSampler(0)
+    clocks.start()
+    out = {}
+    for name, (pat, rows, nbytes) in shapes.items():
+        def op():
+            ep.ep_pattern_probe(pat, src, dst, rows, row, fan)
+        for _ in range(max(3, args.warmup)):
+            l2_flush()
+            op()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            l2_flush()
+            a.record()
+            op()
+            b.record()
+        torch.cuda.synchronize(dev)
+        us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+        avg = sum(us) / len(us)
+        gbs = nbytes / (avg / 1e6) / 1e9
+        out[name] = {"bytes": nbytes, "avg_us": round(avg, 2),
+                     "median_us": round(statistics.median(us), 2), "gbs": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4)}
+    clk = clocks.stop()
+    line = {"metric": "HBM ceiling of each access pattern of the step (GB/s)", "unit": "GB/s",
+            "n_gpus": 1, "steps": steps, "warmup": args.warmup, "higher_is_better": True,
+            "data": "synthetic", "row_bytes": row, "fan": fan, "rows": T,
+            "workload": w.name, "patterns": out, "peak": peak, "peak_source": src_name,
+            "l2": f"flushed before every launch ({args.flush})", "clocks": clk}
+    print(json.dumps(line))
+
+
 def main():
     args = parse_args()
+    if args.mode == "ceilings":
+        run_ceilings(args)
+        return
     if args.gemm and args.impl == "gb300":
         run_gemm(args)
         return
@@ -765,23 +921,20 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        T, N = workload_tokens(args, w)
-        inp = W.make(args.workload, rank=0, T=T, seed=args.seed)
-        tpc = oracle_tokens_per_call(w)
-        budget = max(1.0, min(args.cpu_seconds, 20.0)) / max(1, args.steps + args.warmup)
+        inps, N = step_calls(args, w)
+        T_step = sum(c["T"] for c in inps)
         for _ in range(args.warmup):
-            oracle_sample_run(w, inp, budget, tpc)
-        runs = [oracle_sample_run(w, inp, budget, tpc) for _ in range(args.steps)]
-        tokens = sum(r["tokens"] for r in runs)
-        secs = sum(r["seconds"] for r in runs)
-        v = tokens / secs
-        sample = (f"{args.steps} steps of about {budget:.2f} s, each the oracle's dispatch+combine "
-                  f"over consecutive {tpc}-token slices of the workload (N = slice size)")
+            oracle_step_seconds(w, inps, N)
+        secs = [oracle_step_seconds(w, inps, N) for _ in range(args.steps)]
+        v = T_step * len(secs) / sum(secs)
+        sample = (f"each step the oracle's dispatch+combine of the whole benched step "
+                  f"({len(inps)} call(s), {T_step} tokens: the GPU arm's workload and inputs), "
+                  f"one host thread")
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": secs / len(runs) * 1e3, "higher_is_better": True,
+                "ms_per_step": sum(secs) / len(secs) * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-                "config": workload_desc(w, T, N),
+                "config": step_config(args, w, inps, N),
                 "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1,
                                  "host_cores": os.cpu_count(), "kind": "oracle",
                                  "sample": sample},
@@ -794,43 +947,34 @@ def main():
     res = run_gb300(args)
     if rank != 0:
         return
-    T, N = workload_tokens(args, w)
-    if res.get("calls_per_step", 1) > 1:
-        T = res["T_step"]
-    cfg = workload_desc(w, T, N)
-    cfg["calls_per_step"] = res.get("calls_per_step", 1)
-    cfg.update({"l2": "flushed between timed steps (memset of 2x L2)",
-                "expert": "identity (y = recv_x), not timed",
-                "permute_impl": {1: "vec", 2: "bulk"}.get(res["info"]["permute_impl"]),
-                "timing": "CUDA graph replay" if args.graph else "eager, per-kernel CUDA events",
-                "parallelism": f"replicas x{args.gpus}"})
+    inps, N = step_calls(args, w)
+    cfg = step_config(args, w, inps, N)
+    setup = {"calls_per_step": res.get("calls_per_step", 1),
+             "l2": {"read": "flushed before every timed step by a read-only sweep over 4x L2 "
+                            "(every dirty line written back before the step starts)",
+                    "memset": "flushed before every timed step by a memset of 2x L2 (its dirty "
+                              "lines are written back inside the step)"}[args.flush],
+             "expert": "identity (y = recv_x), not timed",
+             "permute_impl": {1: "vec", 2: "bulk"}.get(res["info"]["permute_impl"]),
+             "timing": ("CUDA graph replay" if args.graph else "eager, per-kernel CUDA events")
+             + (", fresh routing copied in before every replay (outside the events)"
+                if args.fresh_routing else ""),
+             "parallelism": f"replicas x{args.gpus}"}
     line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.dtype, "data": "synthetic", "config": cfg,
+            "dtype": w.dtype, "data": "synthetic", "config": cfg, "setup": setup,
             "achieved_hbm_gbs": round(res["hbm_gbs_step"], 1),
             "hbm_frac_step": round(res["hbm_gbs_step"] / measured_peak_hbm()[0], 4),
             "step_ms": {"median": res["step_ms_median"], "p10": res["step_ms_p10"],
                         "p90": res["step_ms_p90"]}}
-    if "roofline" in res:
-        line["roofline"] = res["roofline"]
-        line["kernels"] = res["kernels"]
-    if "e2e" in res:
-        line["e2e"] = res["e2e"]
-    if "graph_replay" in res:
-        line["graph_replay"] = res["graph_replay"]
+    for key in ("roofline", "kernels", "e2e", "graph_replay", "fresh_routing"):
+        if key in res:
+            line[key] = res[key]
     line["gpu_launches"] = res["launches"]
     line["clocks"] = res["clocks"]
     if not args.no_cpu_baseline:
-        inp = W.make(args.workload, rank=0, T=T, seed=args.seed)
-        tpc = oracle_tokens_per_call(w)
-        r = oracle_sample_run(w, inp, args.cpu_seconds, tpc)
-        line["cpu_baseline"] = {
-            "value": r["tokens"] / r["seconds"], "unit": "tokens/s", "cores": 1,
-            "host_cores": os.cpu_count(), "kind": "oracle",
-            "sample": (f"{r['calls']} oracle dispatch+combine calls over consecutive "
-                       f"{tpc}-token slices of the same workload ({r['tokens']} tokens, "
-                       f"{r['seconds']:.1f} s, single thread)")}
+        line["cpu_baseline"] = oracle_baseline(w, inps, N, args.cpu_repeats)
     print(json.dumps(line))
 
 

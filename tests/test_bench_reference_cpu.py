@@ -19,7 +19,9 @@ def _run(env_extra, *args):
 
 
 def test_reference_arm_prints_one_contract_line():
-    lines = _run({}, "--steps", "2", "--warmup", "1", "--cpu-seconds", "1")
+    # A 512-token call of the DeepSeek shape keeps the CPU test short; the
+    # default run times the full 8192-token call the GPU arm times.
+    lines = _run({}, "--steps", "2", "--warmup", "1", "--tokens", "512")
     assert len(lines) == 1
     d = json.loads(lines[0])
     import bench
@@ -31,12 +33,31 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
-    assert d["config"]["workload"].startswith("deepseek: T=8192 D=7168 bf16 E=256 K=8 R=8")
+    assert d["config"]["workload"].startswith("deepseek: T=512 D=7168 bf16 E=256 K=8 R=8")
+    assert "512 tokens" in d["cpu_baseline"]["sample"]
+
+
+def test_both_arms_print_the_same_config():
+    # The GPU arm and the reference arm build `config` from the same step
+    # description (run-specific facts go under the GPU arm's `setup`).
+    import argparse
+
+    import bench
+    import workloads as W
+    for name in ("deepseek", "ragged", "mixtral"):
+        args = argparse.Namespace(workload=name, tokens=0, seed=None, fresh_routing=False)
+        w = W.WORKLOADS[name]
+        inps, N = bench.step_calls(args, w)
+        cfg = bench.step_config(args, w, inps, N)
+        assert set(cfg) == {"workload", "T", "D", "E", "K", "R", "num_tokens_per_rank",
+                            "num_max_tokens_per_rank"}
+        assert cfg["T"] == sum(c["T"] for c in inps)
+        assert cfg["workload"].startswith(f"{name}: T={cfg['T']} ")
 
 
 def test_reference_arm_other_ranks_print_nothing():
     lines = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"},
-                 "--steps", "1", "--warmup", "0", "--cpu-seconds", "1")
+                 "--steps", "1", "--warmup", "0", "--tokens", "64")
     assert lines == []
 
 
