@@ -39,7 +39,9 @@ struct ep_buffer {
     bool debug;             // EP_DEBUG: sentinel fill and checks of the receive rows
     bool nvtx;              // EP_NVTX: an NVTX range around every call
     bool coop_pdl;          // cooperative launches take programmatic serialization
-    uint32_t* gbar;         // [2] the one-pass dispatch's grid barrier
+    uint32_t* gbar;         // [3] the one-pass dispatch's grid barrier and token-pool counter
+    uint32_t* tile_ready;   // [max_tiles] the one-pass dispatch's per-tile ready words
+    int dispatch_pool_pct;  // share of each tile's tokens in the one-pass dispatch's pool
     int gemm_kernel;        // last expert GEMM: 0 none, 1 single-CTA, 2 two-SM
     int gemm_grid;
     int64_t test_skip_load; // test hook (EP_TEST_SKIP_LOAD), -1 = off
@@ -77,6 +79,9 @@ constexpr size_t kAlign = 256;
 // Expert GEMM schedule: experts with at most this many rows are light (their
 // weights feed one or two 128-row tiles, so those tiles wait on HBM).
 constexpr int kGemmLightRows = 256;
+// One-pass dispatch: percent of each tile's tokens in the shared token pool
+// (CTAs that finish their own share early copy the rest of the others').
+constexpr int kDispatchPoolPct = 25;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -123,8 +128,8 @@ struct Carve {
 
 struct Offsets {
     size_t recv_x, recv_scores, recv_src, pos, cnt, expert_offset, rows_per_rank, rank_prefix,
-        tokens_in_rank, tile_cnt, tile_pre, tile_tok, tile_tok_pre, tok_pos, tok_src, gbar, err,
-        total;
+        tokens_in_rank, tile_cnt, tile_pre, tile_tok, tile_tok_pre, tok_pos, tok_src, tile_ready,
+        gbar, err, total;
 };
 
 Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, int64_t max_tiles)
@@ -149,7 +154,8 @@ Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, i
     o.tile_tok_pre = cv.take((size_t)max_tiles * R * 4);
     o.tok_pos = cv.take((size_t)c->num_max_tokens_per_rank * R * 4);
     o.tok_src = cv.take(R * (size_t)pad4(c->num_max_tokens_per_rank) * 4);
-    o.gbar = cv.take(8);
+    o.tile_ready = cv.take((size_t)max_tiles * 4);
+    o.gbar = cv.take(12);
     o.err = cv.take(4);   // last: the workspace ends after the error word
     o.total = cv.off;
     return o;
@@ -263,6 +269,7 @@ ep::LayoutArgs layout_args(ep_buffer* b, const int32_t* ids, int64_t T, int64_t 
     a.pos = b->pos;
     a.err = b->err;
     a.gbar = b->gbar;
+    a.tile_ready = b->tile_ready;
     a.packed = b->cfg.layout_mode == EP_LAYOUT_PACKED;
     return a;
 }
@@ -316,8 +323,8 @@ ep_status enqueue_dispatch(ep_buffer* b, const void* x, const float* scores, con
     const ep::LaunchOpts o = opts(b, s);
     if (b->permute.impl == EP_PERMUTE_BULK) {
         if (b->onepass) {
-            const cudaError_t e1 = ep::launch_dispatch_onepass(la, permute_args(b, x, scores),
-                                                               b->permute, o, b->coop_pdl);
+            const cudaError_t e1 = ep::launch_dispatch_onepass(
+                la, permute_args(b, x, scores), b->permute, o, b->coop_pdl, b->dispatch_pool_pct);
             if (e1 == cudaSuccess) {
                 remember_layout(b, T, N);
                 return EP_OK;
@@ -376,6 +383,10 @@ void read_knobs(ep_buffer* b)
     b->dedup_fused = !env_is("EP_DEDUP_FUSED", "0");
     // EP_DISPATCH_ONEPASS=0 keeps the dispatch as count + scan + fused.
     b->onepass = !env_is("EP_DISPATCH_ONEPASS", "0");
+    // EP_DISPATCH_POOL=p: percent of each tile's tokens the one-pass dispatch
+    // puts in its shared pool (0: every CTA copies only its own tile).
+    const int64_t pool = env_int("EP_DISPATCH_POOL", kDispatchPoolPct);
+    b->dispatch_pool_pct = (int)std::min<int64_t>(std::max<int64_t>(pool, 0), 100);
     // Debugging: EP_DEBUG=1 (sentinel checks), EP_NVTX=1 (NVTX ranges).
     b->debug = env_is("EP_DEBUG", "1");
     b->nvtx = env_is("EP_NVTX", "1");
@@ -449,6 +460,7 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     b->tok_src = reinterpret_cast<int32_t*>(w + o.tok_src);
     b->err = reinterpret_cast<uint32_t*>(w + o.err);
     b->gbar = reinterpret_cast<uint32_t*>(w + o.gbar);
+    b->tile_ready = reinterpret_cast<uint32_t*>(w + o.tile_ready);
     b->coop_pdl = ep::probe_cooperative_pdl();
 
     const int impl = cfg->permute_impl == EP_PERMUTE_DEFAULT ? EP_PERMUTE_BULK : cfg->permute_impl;
@@ -457,7 +469,8 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
         ep::plan_combine(cfg->dtype == EP_BF16 ? 0 : 1, b->num_sms, &b->combine_grid) !=
             cudaSuccess ||
         cudaMemset(b->err, 0, sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(b->gbar, 0, 2 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(b->gbar, 0, 3 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(b->tile_ready, 0, (size_t)b->max_tiles * 4) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         delete b;
         return EP_ERR_CUDA;
@@ -759,9 +772,12 @@ ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flag
         cudaMemsetAsync(buf->err, 0, sizeof v, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return EP_ERR_CUDA;
-    // A timed-out grid barrier leaves its arrival count behind: start it over.
+    // A timed-out grid barrier leaves its arrival count behind: start it over
+    // (generation, pool counter and the tiles' ready words with it, so that no
+    // ready word of an earlier call can match a generation counted anew).
     if ((v & EP_DEVERR_TIMEOUT) &&
-        (cudaMemsetAsync(buf->gbar, 0, 2 * sizeof(uint32_t), s) != cudaSuccess ||
+        (cudaMemsetAsync(buf->gbar, 0, 3 * sizeof(uint32_t), s) != cudaSuccess ||
+         cudaMemsetAsync(buf->tile_ready, 0, (size_t)buf->max_tiles * 4, s) != cudaSuccess ||
          cudaStreamSynchronize(s) != cudaSuccess))
         return EP_ERR_CUDA;
     *flags = v;

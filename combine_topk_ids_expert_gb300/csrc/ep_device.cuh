@@ -299,11 +299,13 @@ __device__ __forceinline__ void tile_histogram(const LayoutArgs& a, int tile, in
 // the generation. Called by one thread per CTA after the CTA's writes are
 // fenced; false if the others have not arrived within the wait limit (the
 // count is then left inconsistent: the host resets both words when it reads
-// the timeout bit).
-__device__ __forceinline__ bool grid_barrier(uint32_t* bar, uint32_t n)
+// the timeout bit). *epoch receives the generation this barrier opens (the
+// one bar[1] holds once every CTA has arrived).
+__device__ __forceinline__ bool grid_barrier(uint32_t* bar, uint32_t n, uint32_t* epoch)
 {
     uint32_t gen, old;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(bar + 1) : "memory");
+    *epoch = gen + 1u;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(bar) : "memory");
     if (old == n - 1) {
         asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(bar) : "memory");

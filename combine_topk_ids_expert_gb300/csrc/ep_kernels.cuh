@@ -72,7 +72,10 @@ struct LayoutArgs {
     int32_t* tokens_in_rank;   // [R]
     int32_t* pos;              // [T][K]
     uint32_t* err;
-    uint32_t* gbar;            // [2] grid barrier of the one-pass dispatch, or null
+    uint32_t* gbar;            // [3] one-pass dispatch: barrier arrivals, generation, and
+                               // the counter of its shared token pool; or null
+    uint32_t* tile_ready;      // [tiles] one-pass dispatch: the generation in which each
+                               // tile's positions were published; or null
     bool packed;               // ranks back to back instead of r*S
 };
 
@@ -131,8 +134,11 @@ cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
 // barrier, prefix, positions, copies); cudaErrorNotSupported where a tile does
 // not fit or the tiles cannot all be resident. pdl_ok: cooperative launches
 // accept the programmatic-serialization attribute (probe_cooperative_pdl).
+// pool_pct: the share (percent) of each tile's tokens whose rows go to a pool
+// that any CTA may copy once its own share is done (needs l.tile_ready).
 cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
-                                    const PermutePlan& plan, const LaunchOpts& o, bool pdl_ok);
+                                    const PermutePlan& plan, const LaunchOpts& o, bool pdl_ok,
+                                    int pool_pct);
 // Synchronous: whether a cooperative launch with programmatic serialization runs.
 bool probe_cooperative_pdl();
 

@@ -176,6 +176,7 @@ extern "C" ep_status ep_dispatch_layout_noalloc(
     // Without a caller word, bad-id reports land in a scratch word nobody reads.
     a.err = error_flags ? error_flags : reinterpret_cast<uint32_t*>(p);
     a.gbar = nullptr;
+    a.tile_ready = nullptr;
     a.packed = false;
     int64_t launches = 0;
     const ep::LaunchOpts o{static_cast<cudaStream_t>(stream), true, &launches};

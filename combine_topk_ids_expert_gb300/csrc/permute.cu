@@ -202,18 +202,28 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
 // s_rank[2][r] = tokens_in_rank[r]. Global writes: this tile's rows of the
 // count tables and the barrier words only, which no earlier kernel in the
 // stream reads. False if the barrier timed out. s_work: kLayoutWarps * Ep ints.
+template <typename IssueRows>
 __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* s_seed, int* s_tot,
                                int* s_off, int (*s_rank)[kMaxRanks], int* s_tok, int* s_wsum,
-                               int* s_flag)
+                               int* s_flag, uint32_t* s_epoch, IssueRows issue_rows)
 {
     const int Ep = L.Ep, E = L.E, R = L.R, G = (int)gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The ids first: issued behind the tile's row loads they would wait for
+    // those; the rows are started right after the histogram instead (they are
+    // in by the time the positions are known).
     tile_histogram(L, tile, s_tot, s_tok);   // ends with __syncthreads
+    if (threadIdx.x == 0) issue_rows();
     for (int e = threadIdx.x; e < Ep; e += blockDim.x) L.tile_cnt[(int64_t)tile * Ep + e] = s_tot[e];
     if (threadIdx.x < R) L.tile_tok[(int64_t)tile * R + threadIdx.x] = s_tok[threadIdx.x];
+    // The token pool's counter starts over for this call. Every CTA of the
+    // previous kernel in the stream has finished taking from it (dependents
+    // start only after all of its CTAs allow them, at their very end), and no
+    // CTA of this call takes from it before the barrier.
+    if (tile == 0 && threadIdx.x == 0) L.gbar[2] = 0u;
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) *s_flag = grid_barrier(L.gbar, (uint32_t)G) ? 1 : 0;
+    if (threadIdx.x == 0) *s_flag = grid_barrier(L.gbar, (uint32_t)G, s_epoch) ? 1 : 0;
     __syncthreads();
     if (!*s_flag) return false;
 
@@ -226,14 +236,23 @@ __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* 
     if (NG < 1) NG = 1;
     const int g = threadIdx.x / Q, q = threadIdx.x % Q;
     if (g < NG && q < Q) {
+        // Loads in batches of kSumBatch rows, all in flight before the adds.
+        constexpr int kSumBatch = 16;
         const int4* tc = reinterpret_cast<const int4*>(L.tile_cnt);
         int4 bef = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
-#pragma unroll 8
-        for (int t = g; t < G; t += NG) {
-            const int4 v = ld_cg_v4(tc + (int64_t)t * Q + q);
-            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
-            if (t < tile) {
-                bef.x += v.x; bef.y += v.y; bef.z += v.z; bef.w += v.w;
+        for (int tb = g; tb < G; tb += kSumBatch * NG) {
+            int4 v[kSumBatch];
+#pragma unroll
+            for (int u = 0; u < kSumBatch; ++u) {
+                const int t = tb + u * NG;
+                v[u] = (t < G) ? ld_cg_v4(tc + (int64_t)t * Q + q) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kSumBatch; ++u) {
+                tot.x += v[u].x; tot.y += v[u].y; tot.z += v[u].z; tot.w += v[u].w;
+                if (tb + u * NG < tile) {
+                    bef.x += v[u].x; bef.y += v[u].y; bef.z += v[u].z; bef.w += v[u].w;
+                }
             }
         }
         int* b = s_work + (2 * g) * Ep + 4 * q;
@@ -327,17 +346,48 @@ __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* 
     return true;
 }
 
+// Receive rows of pool token t for lane k < K: read from the positions its
+// owner tile published (L.pos), once that tile's ready word holds this call's
+// generation. -1 if the word does not come within the wait limit (then
+// kErrTimeout is set and the row is skipped).
+__device__ __forceinline__ int pool_pos(const LayoutArgs& L, int64_t t, int k, uint32_t epoch,
+                                        uint32_t* err)
+{
+    const uint32_t* flag = L.tile_ready + t / L.tpt;
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+    while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v == epoch) break;
+        if (globaltimer_ns() > deadline) {
+            atomicOr(err, kErrTimeout);
+            return -1;
+        }
+        __nanosleep(32);
+    }
+    return __ldcg(L.pos + t * L.K + k);
+}
+
 // Positions + permute of one layout tile per CTA (see the file comment).
 // ONEPASS: the layout is computed here too (onepass_layout; launched
 // cooperatively, so every tile's CTA is resident for the grid barrier).
 // Shared memory: [stages slots of slot_bytes][kLayoutWarps * Ep ints][tile pairs
 // ints] (+ ONEPASS: [3 * Ep ints]).
+//
+// Rows are copied in a sequence of tokens through the ring: the tile's own
+// tokens first, then (ONEPASS with pool_d > 0) tokens taken from a pool shared
+// by all CTAs, so that CTAs which finish early take over the others' last
+// rows. The pool holds the last d = min(pool_d, n - stages) tokens of every
+// tile of n tokens; pool entry c is token c / ntiles of tile c % ntiles's
+// share. Whoever copies a row, the owner tile writes its scores and sources
+// and publishes its positions (L.pos) for the others.
 template <bool ONEPASS>
 __global__ void __launch_bounds__(kLayoutThreads, 1)
-dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
+dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, int pool_d)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kBulkMaxStages];
+    __shared__ int s_seq[kBulkMaxStages];   // pool token in each ring slot, -1: none
     int* s_base = reinterpret_cast<int*>(smem + (size_t)stages * slot_bytes);
     int* s_pos = s_base + kLayoutWarps * L.Ep;
     const int tile = blockIdx.x;
@@ -352,35 +402,73 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
     const uint32_t bar0 = smem_u32(bars);
     const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
     uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
-    const int n_pro = n_my < stages ? n_my : stages;
+    const bool pooled = ONEPASS && pool_d > 0;
+    // This tile's pool share and the tokens it keeps.
+    auto share = [&](int n) { return pooled ? min(pool_d, max(0, n - stages)) : 0; };
+    const int n_static = n_my - share(n_my);
+    const int n_pro = n_static < stages ? n_static : stages;
+    const uint32_t pool_total = pooled ? (uint32_t)L.ntiles * (uint32_t)pool_d : 0u;
+    bool pool_empty = !pooled;   // thread 0 only
 
     const int64_t skipped = (tile == 0) ? a.skip_load : -1;
-    auto issue_load = [&](int i) {
-        if (i == skipped) return;
-        const int s = i % stages;
+    // Starts the load of sequence index q into its slot: an own token, or the
+    // next pool token (recorded in s_seq; -1 once the pool is empty).
+    auto issue = [&](int q) {
+        const int s = q % stages;
+        int64_t t = -1;
+        if (q < n_static) {
+            if (q == skipped) return;
+            t = t0 + q;
+        } else {
+            while (!pool_empty) {
+                const uint32_t c = atomicAdd(L.gbar + 2, 1u);
+                if (c >= pool_total) {
+                    pool_empty = true;
+                    break;
+                }
+                const int ot = (int)(c % (uint32_t)L.ntiles), j = (int)(c / (uint32_t)L.ntiles);
+                const int64_t o0 = (int64_t)ot * L.tpt;
+                const int on = (int)(min(L.T, o0 + L.tpt) - o0);
+                const int od = share(on);
+                if (j < od) {
+                    t = o0 + (on - od) + j;
+                    break;
+                }
+            }
+            s_seq[s] = (int)t;
+            if (t < 0) return;
+        }
         const uint32_t bar = bar0 + 8u * s;
         mbar_expect_tx(bar, bytes);
-        bulk_g2s(slot0 + (uint32_t)s * (uint32_t)slot_bytes, x + (t0 + i) * a.row_bytes, bytes,
-                 bar);
+        bulk_g2s(slot0 + (uint32_t)s * (uint32_t)slot_bytes, x + t * a.row_bytes, bytes, bar);
     };
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) mbar_init(bar0 + 8u * s, 1u);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(bar0 + 8u * s, 1u);
+            s_seq[s] = -1;
+        }
         fence_mbar_init();
-        // The rows do not depend on the layout: start them before waiting for it.
-        for (int i = 0; i < n_pro; ++i) issue_load(i);
+        // The rows do not depend on the layout: the fused form starts them
+        // before waiting for it (the one-pass form right after its histogram).
+        if constexpr (!ONEPASS)
+            for (int i = 0; i < n_pro; ++i) issue(i);
     }
 
+    uint32_t epoch = 0;
     if constexpr (ONEPASS) {
         __shared__ int s_rank[3][kMaxRanks];
         __shared__ int s_tok[kMaxRanks];
         __shared__ int s_wsum[kLayoutWarps];
         __shared__ int s_flag;
+        __shared__ uint32_t s_epoch;
         const int tile_pairs = (int)(L.tpt * L.K);
         int* s_seed = s_pos + tile_pairs;
         int* s_tot = s_seed + L.Ep;
         int* s_off = s_tot + L.Ep;
         const bool ok = onepass_layout(L, tile, s_base, s_seed, s_tot, s_off, s_rank, s_tok, s_wsum,
-                                       &s_flag);
+                                       &s_flag, &s_epoch, [&] {
+                                           for (int i = 0; i < n_pro; ++i) issue(i);
+                                       });
         if (!ok) {   // barrier timed out: report, let this CTA's loads land, leave
             if (threadIdx.x == 0) {
                 atomicOr(a.err, kErrTimeout);
@@ -389,6 +477,7 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
             griddep_launch_dependents();
             return;
         }
+        epoch = s_epoch;
         griddep_wait();   // the previous kernel in the stream may read what follows
         if (tile == 0) {
             for (int e = threadIdx.x; e < L.E; e += blockDim.x) {
@@ -402,6 +491,19 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
             }
         }
         tile_positions(L, tile, s_base, L.pos, s_pos, s_seed);   // ends with __syncthreads
+        if (pooled) {
+            // Publish this tile's positions for the CTAs that copy its pool rows.
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(L.tile_ready + tile),
+                             "r"(epoch)
+                             : "memory");
+                // A tile shorter than the ring fills its free slots from the pool.
+                for (int q = n_pro; q < stages; ++q) issue(q);
+            }
+            __syncthreads();
+        }
     } else {
         griddep_wait();                                   // counts and offsets are ready
         tile_positions(L, tile, s_base, L.pos, s_pos);    // ends with __syncthreads
@@ -410,32 +512,50 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes)
     if (warp == 0) {
         bool ok = true;
         int i = 0;
-        for (; i < n_my; ++i) {
+        for (;; ++i) {
             const int s = i % stages;
+            int64_t t = -1;
+            if (i < n_static) {
+                t = t0 + i;
+            } else if (pooled) {
+                t = s_seq[s];
+            }
+            if (t < 0) break;
             if (!mbar_wait(bar0 + 8u * s, (uint32_t)((i / stages) & 1))) {
                 ok = false;
                 break;
             }
             if (lane < K) {
-                const int p = s_pos[i * K + lane];
+                const int p = (i < n_static) ? s_pos[i * K + lane]
+                                             : pool_pos(L, t, lane, epoch, a.err);
                 if (p >= 0)
                     bulk_s2g(rx + (int64_t)p * a.row_bytes,
                              slot0 + (uint32_t)s * (uint32_t)slot_bytes, bytes);
             }
             bulk_commit();
             const int j = i - kBulkLag;
-            if (j >= 0 && j + stages < n_my) {
+            if (j >= 0 && (pooled || j + stages < n_my)) {
                 bulk_wait_read<kBulkLag>();
                 __syncwarp();
-                if (lane == 0) issue_load(j + stages);
+                if (lane == 0) issue(j + stages);
             }
+            __syncwarp();
         }
         bulk_wait_all();
         if (!ok && lane == 0) {
             atomicOr(a.err, kErrTimeout);
-            int issued_hi = (i - kBulkLag) + stages;
-            if (issued_hi < n_pro) issued_hi = n_pro;
-            drain_loads(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my, skipped);
+            // Loads were issued for sequence indices below max(n_pro, i - lag + stages);
+            // pool indices whose slot holds no token had none.
+            int hi = (i - kBulkLag) + stages;
+            const int issued_first = pooled ? stages : n_pro;   // before the loop began
+            if (hi < issued_first) hi = issued_first;
+            const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+            for (int m = i; m < hi; ++m) {
+                if (m >= n_static && (!pooled || s_seq[m % stages] < 0)) continue;
+                if (m == skipped) continue;
+                mbar_wait_until(bar0 + 8u * (uint32_t)(m % stages), (uint32_t)((m / stages) & 1),
+                                deadline);
+            }
         }
     } else {
         const int np = n_my * K;
@@ -547,11 +667,12 @@ cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
     if (stages < kBulkLag + 2) return cudaErrorNotSupported;
     const size_t smem = (size_t)(stages * slot + fixed);
     return launch_kernel(dispatch_tile_kernel<false>, dim3(l.ntiles), dim3(kLayoutThreads), smem, o,
-                         l, p, (int)stages, slot);
+                         l, p, (int)stages, slot, 0);
 }
 
 cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
-                                    const PermutePlan& plan, const LaunchOpts& o, bool pdl_ok)
+                                    const PermutePlan& plan, const LaunchOpts& o, bool pdl_ok,
+                                    int pool_pct)
 {
     if (plan.impl != 2 || plan.fused_smem_cap <= 0 || l.K > 32 || !l.gbar || l.ntiles <= 0)
         return cudaErrorNotSupported;
@@ -583,7 +704,17 @@ cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (o.pdl && pdl_ok) ? 2 : 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, dispatch_tile_kernel<true>, l, p, (int)stages, slot);
+    // Tokens of each full tile given to the shared pool. A tile keeps at least
+    // a ring's worth of its own tokens (those are loaded before the layout is
+    // known), so tiles that fit the ring give none and there is no pool.
+    int64_t pool_d = 0;
+    if (l.tile_ready && pool_pct > 0) {
+        pool_d = l.tpt * (pool_pct < 100 ? pool_pct : 100) / 100;
+        if (pool_d > l.tpt - stages) pool_d = l.tpt - stages;
+        if (pool_d < 0) pool_d = 0;
+    }
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, dispatch_tile_kernel<true>, l, p, (int)stages, slot, (int)pool_d);
     if (e == cudaErrorCooperativeLaunchTooLarge) {   // fewer SMs than the device reports (MPS)
         cudaGetLastError();
         return cudaErrorNotSupported;
