@@ -35,6 +35,7 @@ namespace {
 
 constexpr int kVecThreads = 128;
 constexpr int kBulkLag = 4;            // store groups in flight before a slot is reused
+constexpr int kPoolAhead = 2;          // pool tokens taken ahead of the one being copied
 constexpr int kBulkMaxStages = 32;
 constexpr int kBulkSmemBudget = 200 * 1024;
 constexpr int kFusedSmemCap = 227 * 1024 - 1024;   // dynamic shared memory of the fused kernel
@@ -409,6 +410,8 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
     const int n_pro = n_static < stages ? n_static : stages;
     const uint32_t pool_total = pooled ? (uint32_t)L.ntiles * (uint32_t)pool_d : 0u;
     bool pool_empty = !pooled;   // thread 0 only
+    // Sequence indices issued before the copy loop starts.
+    const int pool_first_issue = pooled ? max(n_pro, min(stages, kPoolAhead + 1)) : n_pro;
 
     const int64_t skipped = (tile == 0) ? a.skip_load : -1;
     // Starts the load of sequence index q into its slot: an own token, or the
@@ -499,8 +502,8 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
                 asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(L.tile_ready + tile),
                              "r"(epoch)
                              : "memory");
-                // A tile shorter than the ring fills its free slots from the pool.
-                for (int q = n_pro; q < stages; ++q) issue(q);
+                // A tile shorter than the ring takes its first pool tokens now.
+                for (int q = n_pro; q < pool_first_issue; ++q) issue(q);
             }
             __syncthreads();
         }
@@ -512,6 +515,7 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
     if (warp == 0) {
         bool ok = true;
         int i = 0;
+        int next = pool_first_issue;   // next sequence index to issue (the same in every lane)
         for (;; ++i) {
             const int s = i % stages;
             int64_t t = -1;
@@ -533,22 +537,29 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
                              slot0 + (uint32_t)s * (uint32_t)slot_bytes, bytes);
             }
             bulk_commit();
-            const int j = i - kBulkLag;
-            if (j >= 0 && (pooled || j + stages < n_my)) {
-                bulk_wait_read<kBulkLag>();
+            // Loads up to the last index whose slot is free: own tokens as far
+            // ahead as the ring allows (a slot is reused once the stores of
+            // kBulkLag groups back have read it), pool tokens only kPoolAhead
+            // ahead, so that no CTA holds many pool tokens when the pool runs
+            // dry (a token's stores take longer than a row load).
+            int target = (i >= kBulkLag) ? i - kBulkLag + stages : stages - 1;
+            target = pooled ? min(target, max(n_static - 1, i + kPoolAhead))
+                            : min(target, n_my - 1);
+            if (next <= target) {
+                if (target >= stages) bulk_wait_read<kBulkLag>();
                 __syncwarp();
-                if (lane == 0) issue(j + stages);
+                if (lane == 0)
+                    for (int q = next; q <= target; ++q) issue(q);
+                next = target + 1;
             }
             __syncwarp();
         }
         bulk_wait_all();
         if (!ok && lane == 0) {
             atomicOr(a.err, kErrTimeout);
-            // Loads were issued for sequence indices below max(n_pro, i - lag + stages);
-            // pool indices whose slot holds no token had none.
-            int hi = (i - kBulkLag) + stages;
-            const int issued_first = pooled ? stages : n_pro;   // before the loop began
-            if (hi < issued_first) hi = issued_first;
+            // Loads were issued for sequence indices below `next`; pool indices
+            // whose slot holds no token had none.
+            const int hi = next;
             const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
             for (int m = i; m < hi; ++m) {
                 if (m >= n_static && (!pooled || s_seq[m % stages] < 0)) continue;
