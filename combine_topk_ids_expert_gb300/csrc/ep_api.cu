@@ -42,6 +42,7 @@ struct ep_buffer {
     uint32_t* gbar;         // [3] the one-pass dispatch's grid barrier and token-pool counter
     uint32_t* tile_ready;   // [max_tiles] the one-pass dispatch's per-tile ready words
     int dispatch_pool_pct;  // share of each tile's tokens in the one-pass dispatch's pool
+    int64_t dispatch_small_pairs;   // calls this small count every id in every CTA, no barrier
     int gemm_kernel;        // last expert GEMM: 0 none, 1 single-CTA, 2 two-SM
     int gemm_grid;
     int64_t test_skip_load; // test hook (EP_TEST_SKIP_LOAD), -1 = off
@@ -82,6 +83,9 @@ constexpr int kGemmLightRows = 256;
 // One-pass dispatch: percent of each tile's tokens in the shared token pool
 // (CTAs that finish their own share early copy the rest of the others').
 constexpr int kDispatchPoolPct = 25;
+// One-pass dispatch: calls of at most this many (token, k) pairs count all of
+// their ids in every CTA instead of meeting at the grid barrier.
+constexpr int64_t kDispatchSmallPairs = 4096;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -324,7 +328,8 @@ ep_status enqueue_dispatch(ep_buffer* b, const void* x, const float* scores, con
     if (b->permute.impl == EP_PERMUTE_BULK) {
         if (b->onepass) {
             const cudaError_t e1 = ep::launch_dispatch_onepass(
-                la, permute_args(b, x, scores), b->permute, o, b->coop_pdl, b->dispatch_pool_pct);
+                la, permute_args(b, x, scores), b->permute, o, b->coop_pdl, b->dispatch_pool_pct,
+                b->dispatch_small_pairs);
             if (e1 == cudaSuccess) {
                 remember_layout(b, T, N);
                 return EP_OK;
@@ -387,6 +392,10 @@ void read_knobs(ep_buffer* b)
     // puts in its shared pool (0: every CTA copies only its own tile).
     const int64_t pool = env_int("EP_DISPATCH_POOL", kDispatchPoolPct);
     b->dispatch_pool_pct = (int)std::min<int64_t>(std::max<int64_t>(pool, 0), 100);
+    // EP_DISPATCH_SMALL_PAIRS=n: one-pass dispatches of at most n (token, k)
+    // pairs count every id in every CTA instead of meeting at the grid barrier.
+    b->dispatch_small_pairs = std::max<int64_t>(env_int("EP_DISPATCH_SMALL_PAIRS",
+                                                        kDispatchSmallPairs), 0);
     // Debugging: EP_DEBUG=1 (sentinel checks), EP_NVTX=1 (NVTX ranges).
     b->debug = env_is("EP_DEBUG", "1");
     b->nvtx = env_is("EP_NVTX", "1");

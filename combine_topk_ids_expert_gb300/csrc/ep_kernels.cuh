@@ -136,9 +136,11 @@ cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
 // accept the programmatic-serialization attribute (probe_cooperative_pdl).
 // pool_pct: the share (percent) of each tile's tokens whose rows go to a pool
 // that any CTA may copy once its own share is done (needs l.tile_ready).
+// small_pairs: calls of at most this many (token, k) pairs skip the grid
+// barrier: every CTA counts all of the call's ids itself.
 cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
                                     const PermutePlan& plan, const LaunchOpts& o, bool pdl_ok,
-                                    int pool_pct);
+                                    int pool_pct, int64_t small_pairs);
 // Synchronous: whether a cooperative launch with programmatic serialization runs.
 bool probe_cooperative_pdl();
 

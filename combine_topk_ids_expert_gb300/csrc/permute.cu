@@ -203,13 +203,171 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
 // s_rank[2][r] = tokens_in_rank[r]. Global writes: this tile's rows of the
 // count tables and the barrier words only, which no earlier kernel in the
 // stream reads. False if the barrier timed out. s_work: kLayoutWarps * Ep ints.
+// Second half of the layout, from the call's per-expert totals s_tot[e] and
+// this tile's counts of earlier pairs s_seed[e]: s_off[e] = expert_offset[e],
+// s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r] (inclusive),
+// and s_seed[e] += expert_offset[e] (this tile's first receive row of e).
+// s_work: at least E ints. Ends with __syncthreads.
+__device__ void layout_offsets(const LayoutArgs& L, int* s_work, int* s_seed, const int* s_tot,
+                               int* s_off, int (*s_rank)[kMaxRanks], int* s_wsum)
+{
+    const int Ep = L.Ep, E = L.E, R = L.R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Inclusive prefix of the totals over experts (C consecutive experts per
+    // thread, then warps, then the block) into s_off.
+    const int C = (Ep + kLayoutThreads - 1) / kLayoutThreads;
+    const int e0 = threadIdx.x * C;
+    int run = 0;
+    for (int j = 0; j < C; ++j) {
+        const int e = e0 + j;
+        if (e < E) run += s_tot[e];
+    }
+    int v = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += n;
+    }
+    if (lane == 31) s_wsum[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int c = s_wsum[w];
+            s_wsum[w] = acc;
+            acc += c;
+        }
+    }
+    __syncthreads();
+    int incl = v - run + s_wsum[warp];   // exclusive prefix of this thread's first expert
+    for (int j = 0; j < C; ++j) {
+        const int e = e0 + j;
+        if (e < E) {
+            incl += s_tot[e];
+            s_off[e] = incl;
+        }
+    }
+    __syncthreads();
+
+    // Offsets: ranks own contiguous expert blocks (packed: back to back).
+    const int eloc = E / R;
+    if (threadIdx.x < R) {
+        const int r = threadIdx.x;
+        const int hi = s_off[(r + 1) * eloc - 1];
+        const int lo = (r > 0) ? s_off[r * eloc - 1] : 0;
+        s_rank[0][r] = hi - lo;
+        s_rank[1][r] = hi;
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int excl = s_off[e] - s_tot[e];
+        int off;
+        if (L.packed) {
+            off = excl;
+        } else {
+            const int r = e / eloc;
+            const int lo = (r > 0) ? s_off[r * eloc - 1] : 0;
+            off = (int)((int64_t)r * L.S + (excl - lo));
+        }
+        s_work[e] = off;   // s_off still holds the inclusive prefix other threads read
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        s_off[e] = s_work[e];
+        s_seed[e] += s_work[e];
+    }
+    __syncthreads();
+}
+
+// Layout of a small call without a grid barrier: every CTA counts all of the
+// call's pairs itself (its ids stay in L2 after the first CTA reads them), so
+// the CTAs never wait for one another. s_tot[e] = pairs of expert e in the
+// call; s_seed[e] = those before this tile's first pair; tile 0 also counts
+// each rank's distinct tokens into s_rank[2] and reports invalid ids.
+// Ends with __syncthreads.
+__device__ void redundant_counts(const LayoutArgs& L, int tile, int* s_seed, int* s_tot,
+                                 int (*s_rank)[kMaxRanks])
+{
+    const int64_t np = L.T * L.K;
+    const int64_t p0 = (int64_t)tile * L.tpt * L.K;   // this tile's first pair
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = threadIdx.x; e < L.Ep; e += blockDim.x) {
+        s_seed[e] = 0;
+        s_tot[e] = 0;
+    }
+    if (threadIdx.x < L.R) s_rank[2][threadIdx.x] = 0;
+    __syncthreads();
+    const int64_t np32 = (np + 31) & ~(int64_t)31;
+    bool bad = false;
+    // Warp w takes the 32-pair chunks w, w + 8, ...; each lane loads the ids of
+    // kRedBatch chunks before matching them, so the loads are in flight together.
+    constexpr int kRedBatch = 16;
+    for (int64_t cb = (int64_t)warp * 32; cb < np32; cb += (int64_t)kRedBatch * kLayoutThreads) {
+        int raw[kRedBatch];
+#pragma unroll
+        for (int u = 0; u < kRedBatch; ++u) {
+            const int64_t i = cb + (int64_t)u * kLayoutThreads + lane;
+            raw[u] = (i < np) ? __ldcg(L.ids + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kRedBatch; ++u) {
+            const int64_t c = cb + (int64_t)u * kLayoutThreads;
+            if (c >= np32) break;   // the same for every lane of the warp
+            const int e = valid_id(raw[u], L.E);
+            bad |= (e != raw[u]);
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && lane == __ffs(peers) - 1) {
+                atomicAdd(&s_tot[e], __popc(peers));
+                // lanes of this chunk whose pair comes before the tile
+                const unsigned before = (c + 32 <= p0) ? 0xffffffffu
+                                        : (c >= p0)    ? 0u
+                                                       : (1u << (unsigned)(p0 - c)) - 1u;
+                const int nb = __popc(peers & before);
+                if (nb) atomicAdd(&s_seed[e], nb);
+            }
+        }
+    }
+    if (tile == 0) {
+        if (bad) atomicOr(L.err, kErrBadId);
+        // Distinct tokens per rank over the call: the rank set of every token,
+        // kTokBatch tokens per thread with their first 8 ids loaded together.
+        constexpr int kTokBatch = 4;
+        const int eloc = L.E / L.R;
+        for (int64_t tb = threadIdx.x; tb < L.T; tb += (int64_t)kTokBatch * kLayoutThreads) {
+            unsigned long long mask[kTokBatch];
+#pragma unroll
+            for (int u = 0; u < kTokBatch; ++u) {
+                mask[u] = 0ull;
+                const int64_t t = tb + (int64_t)u * kLayoutThreads;
+                if (t >= L.T) continue;
+                int e8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    e8[k] = (k < L.K) ? valid_id(__ldcg(L.ids + t * L.K + k), L.E) : -1;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (e8[k] >= 0) mask[u] |= 1ull << (e8[k] / eloc);
+                for (int k = 8; k < L.K; ++k) {
+                    const int e = valid_id(__ldcg(L.ids + t * L.K + k), L.E);
+                    if (e >= 0) mask[u] |= 1ull << (e / eloc);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kTokBatch; ++u)
+                while (mask[u]) {
+                    atomicAdd(&s_rank[2][__ffsll((long long)mask[u]) - 1], 1);
+                    mask[u] &= mask[u] - 1ull;
+                }
+        }
+    }
+    __syncthreads();
+}
+
 template <typename IssueRows>
 __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* s_seed, int* s_tot,
                                int* s_off, int (*s_rank)[kMaxRanks], int* s_tok, int* s_wsum,
                                int* s_flag, uint32_t* s_epoch, IssueRows issue_rows)
 {
-    const int Ep = L.Ep, E = L.E, R = L.R, G = (int)gridDim.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Ep = L.Ep, R = L.R, G = (int)gridDim.x;
     // The ids first: issued behind the tile's row loads they would wait for
     // those; the rows are started right after the histogram instead (they are
     // in by the time the positions are known).
@@ -281,69 +439,7 @@ __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* 
     __syncthreads();
     if (g2 < NG2 && tsum) atomicAdd(&s_rank[2][r2], tsum);
 
-    // Inclusive prefix of the totals over experts (C consecutive experts per
-    // thread, then warps, then the block) into s_off.
-    const int C = (Ep + kLayoutThreads - 1) / kLayoutThreads;
-    const int e0 = threadIdx.x * C;
-    int run = 0;
-    for (int j = 0; j < C; ++j) {
-        const int e = e0 + j;
-        if (e < E) run += s_tot[e];
-    }
-    int v = run;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, v, d);
-        if (lane >= d) v += n;
-    }
-    if (lane == 31) s_wsum[warp] = v;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int w = 0; w < kLayoutWarps; ++w) {
-            const int c = s_wsum[w];
-            s_wsum[w] = acc;
-            acc += c;
-        }
-    }
-    __syncthreads();
-    int incl = v - run + s_wsum[warp];   // exclusive prefix of this thread's first expert
-    for (int j = 0; j < C; ++j) {
-        const int e = e0 + j;
-        if (e < E) {
-            incl += s_tot[e];
-            s_off[e] = incl;
-        }
-    }
-    __syncthreads();
-
-    // Offsets: ranks own contiguous expert blocks (packed: back to back).
-    const int eloc = E / R;
-    if (threadIdx.x < R) {
-        const int r = threadIdx.x;
-        const int hi = s_off[(r + 1) * eloc - 1];
-        const int lo = (r > 0) ? s_off[r * eloc - 1] : 0;
-        s_rank[0][r] = hi - lo;
-        s_rank[1][r] = hi;
-    }
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int excl = s_off[e] - s_tot[e];
-        int off;
-        if (L.packed) {
-            off = excl;
-        } else {
-            const int r = e / eloc;
-            const int lo = (r > 0) ? s_off[r * eloc - 1] : 0;
-            off = (int)((int64_t)r * L.S + (excl - lo));
-        }
-        s_work[e] = off;   // s_off still holds the inclusive prefix other threads read
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        s_off[e] = s_work[e];
-        s_seed[e] += s_work[e];
-    }
-    __syncthreads();
+    layout_offsets(L, s_work, s_seed, s_tot, s_off, s_rank, s_wsum);
     return true;
 }
 
@@ -384,7 +480,8 @@ __device__ __forceinline__ int pool_pos(const LayoutArgs& L, int64_t t, int k, u
 // and publishes its positions (L.pos) for the others.
 template <bool ONEPASS>
 __global__ void __launch_bounds__(kLayoutThreads, 1)
-dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, int pool_d)
+dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, int pool_d,
+                     int small)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kBulkMaxStages];
@@ -403,7 +500,7 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
     const uint32_t bar0 = smem_u32(bars);
     const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
     uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
-    const bool pooled = ONEPASS && pool_d > 0;
+    const bool pooled = ONEPASS && pool_d > 0 && !small;
     // This tile's pool share and the tokens it keeps.
     auto share = [&](int n) { return pooled ? min(pool_d, max(0, n - stages)) : 0; };
     const int n_static = n_my - share(n_my);
@@ -468,10 +565,20 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
         int* s_seed = s_pos + tile_pairs;
         int* s_tot = s_seed + L.Ep;
         int* s_off = s_tot + L.Ep;
-        const bool ok = onepass_layout(L, tile, s_base, s_seed, s_tot, s_off, s_rank, s_tok, s_wsum,
-                                       &s_flag, &s_epoch, [&] {
-                                           for (int i = 0; i < n_pro; ++i) issue(i);
-                                       });
+        bool ok = true;
+        if (small) {
+            // A small call: no grid barrier (see redundant_counts), no pool.
+            redundant_counts(L, tile, s_seed, s_tot, s_rank);
+            if (threadIdx.x == 0)
+                for (int i = 0; i < n_pro; ++i) issue(i);
+            layout_offsets(L, s_base, s_seed, s_tot, s_off, s_rank, s_wsum);
+            s_epoch = 0u;
+        } else {
+            ok = onepass_layout(L, tile, s_base, s_seed, s_tot, s_off, s_rank, s_tok, s_wsum,
+                                &s_flag, &s_epoch, [&] {
+                                    for (int i = 0; i < n_pro; ++i) issue(i);
+                                });
+        }
         if (!ok) {   // barrier timed out: report, let this CTA's loads land, leave
             if (threadIdx.x == 0) {
                 atomicOr(a.err, kErrTimeout);
@@ -678,12 +785,12 @@ cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
     if (stages < kBulkLag + 2) return cudaErrorNotSupported;
     const size_t smem = (size_t)(stages * slot + fixed);
     return launch_kernel(dispatch_tile_kernel<false>, dim3(l.ntiles), dim3(kLayoutThreads), smem, o,
-                         l, p, (int)stages, slot, 0);
+                         l, p, (int)stages, slot, 0, 0);
 }
 
 cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
                                     const PermutePlan& plan, const LaunchOpts& o, bool pdl_ok,
-                                    int pool_pct)
+                                    int pool_pct, int64_t small_pairs)
 {
     if (plan.impl != 2 || plan.fused_smem_cap <= 0 || l.K > 32 || !l.gbar || l.ntiles <= 0)
         return cudaErrorNotSupported;
@@ -718,14 +825,18 @@ cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
     // Tokens of each full tile given to the shared pool. A tile keeps at least
     // a ring's worth of its own tokens (those are loaded before the layout is
     // known), so tiles that fit the ring give none and there is no pool.
+    // A call of at most small_pairs pairs counts all its ids in every CTA
+    // instead of meeting at the grid barrier (and then has no pool).
+    const int small = (l.T * l.K <= small_pairs) ? 1 : 0;
     int64_t pool_d = 0;
-    if (l.tile_ready && pool_pct > 0) {
+    if (!small && l.tile_ready && pool_pct > 0) {
         pool_d = l.tpt * (pool_pct < 100 ? pool_pct : 100) / 100;
         if (pool_d > l.tpt - stages) pool_d = l.tpt - stages;
         if (pool_d < 0) pool_d = 0;
     }
     const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, dispatch_tile_kernel<true>, l, p, (int)stages, slot, (int)pool_d);
+        cudaLaunchKernelEx(&cfg, dispatch_tile_kernel<true>, l, p, (int)stages, slot, (int)pool_d,
+                           small);
     if (e == cudaErrorCooperativeLaunchTooLarge) {   // fewer SMs than the device reports (MPS)
         cudaGetLastError();
         return cudaErrorNotSupported;

@@ -18,12 +18,16 @@ def orc():
     return oracle.get()
 
 
-@pytest.fixture(params=["onepass", "fused", "vec"])
+@pytest.fixture(params=["onepass", "onepass_barrier", "fused", "vec"])
 def path(request, monkeypatch):
     """Each dispatch path in turn: the one-pass cooperative bulk dispatch (the
-    default), the bulk dispatch as count + scan + fused kernels, and the 16-byte
-    vector permute. Returns the permute_impl to build the Buffer with."""
+    default; small calls count every id in every CTA), the same with every call
+    meeting at the grid barrier (EP_DISPATCH_SMALL_PAIRS=0), the bulk dispatch as
+    count + scan + fused kernels, and the 16-byte vector permute. Returns the
+    permute_impl to build the Buffer with."""
     import combine_topk_ids_expert_gb300 as ep
+    if request.param == "onepass_barrier":
+        monkeypatch.setenv("EP_DISPATCH_SMALL_PAIRS", "0")
     if request.param == "fused":
         monkeypatch.setenv("EP_DISPATCH_ONEPASS", "0")
     return ep.EP_PERMUTE_VEC if request.param == "vec" else ep.EP_PERMUTE_BULK

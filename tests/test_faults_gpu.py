@@ -194,13 +194,15 @@ def test_bounded_wait_runs_out_and_reports(orc, monkeypatch):
     good.close()
 
 
-def test_grid_barrier_runs_out_and_recovers(orc):
+def test_grid_barrier_runs_out_and_recovers(orc, monkeypatch):
     # The one-pass dispatch meets all its CTAs at a grid barrier (two words at
     # the end of the workspace: arrivals, generation) with a 2 s limit. Seeding
     # the arrival count past the grid size means no CTA is ever the last to
     # arrive, so every CTA's wait runs out: the kernel must report
     # EP_DEVERR_TIMEOUT and return; reading the flag starts the barrier over,
-    # and the next dispatch on the same buffer is oracle-exact.
+    # and the next dispatch on the same buffer is oracle-exact. (A call this
+    # small would skip the barrier: EP_DISPATCH_SMALL_PAIRS=0 keeps it.)
+    monkeypatch.setenv("EP_DISPATCH_SMALL_PAIRS", "0")
     buf = ep.Buffer(64, D, E, R, K, dtype=torch.bfloat16, permute_impl=ep.EP_PERMUTE_BULK)
     x, ids, sc = small(T=40, seed=9)
     xd, idd, scd = to_dev(x), to_dev(ids), to_dev(sc)

@@ -19,9 +19,12 @@ from gpu_util import (assert_combine_equal, assert_layout_equal, assert_recv_equ
 pytestmark = pytest.mark.gpu
 
 # vec: 16-byte vector permute; bulk: the default bulk dispatch (one cooperative
-# kernel: counts, grid barrier, prefix, positions, copies); fused: the bulk
-# dispatch as count + scan + fused positions/copy kernels (EP_DISPATCH_ONEPASS=0)
-IMPLS = ["vec", "bulk", "fused"]
+# kernel: counts, grid barrier, prefix, positions, copies; calls of up to 4096
+# pairs count every id in every CTA instead of meeting at the barrier);
+# bulk_barrier: the same with every call meeting at the barrier
+# (EP_DISPATCH_SMALL_PAIRS=0); fused: the bulk dispatch as count + scan + fused
+# positions/copy kernels (EP_DISPATCH_ONEPASS=0)
+IMPLS = ["vec", "bulk", "bulk_barrier", "fused"]
 IMPL_IDS = IMPLS
 
 
@@ -29,6 +32,8 @@ IMPL_IDS = IMPLS
 def impl(request, monkeypatch):
     if request.param == "fused":
         monkeypatch.setenv("EP_DISPATCH_ONEPASS", "0")
+    if request.param == "bulk_barrier":
+        monkeypatch.setenv("EP_DISPATCH_SMALL_PAIRS", "0")
     return ep.EP_PERMUTE_VEC if request.param == "vec" else ep.EP_PERMUTE_BULK
 
 # id: (seed, T, N, N_max, D, dtype, E, K, R, ids, scores)

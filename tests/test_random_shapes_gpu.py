@@ -42,7 +42,7 @@ def draw_configs(n: int = 24, seed: int = 0x5EED5, max_recv_bytes: int = 128 << 
 
 
 CONFIGS = draw_configs()
-PATHS = ["onepass", "fused", "vec"]
+PATHS = ["onepass", "onepass_barrier", "fused", "vec"]
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -51,6 +51,8 @@ def test_random_shape(orc, monkeypatch, cfg, path):
     seed, T, N, N_max, D, dtype, E, K, R, ik, layout = cfg
     if path == "fused":
         monkeypatch.setenv("EP_DISPATCH_ONEPASS", "0")
+    if path == "onepass_barrier":
+        monkeypatch.setenv("EP_DISPATCH_SMALL_PAIRS", "0")
     impl = ep.EP_PERMUTE_VEC if path == "vec" else ep.EP_PERMUTE_BULK
     x = W.hidden(seed, T, D, dtype)
     ids, sc = W.routing(seed, T, E, K, ik, "sigmoid_norm")
