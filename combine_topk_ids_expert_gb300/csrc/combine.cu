@@ -123,23 +123,30 @@ combine_vec_kernel(CombineArgs a)
     griddep_wait();
     const int64_t V = a.D / N;
     const int4* __restrict__ y = static_cast<const int4*>(a.y);
+    // Work item w = (token w / vsplit, vector chunk w % vsplit): a call with
+    // fewer tokens than CTAs spreads each token's row over vsplit CTAs, so that
+    // each thread has fewer dependent load rounds.
+    const int64_t nch = a.vsplit;
+    const int64_t per = (V + nch - 1) / nch;   // vectors per chunk
 
-    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+    for (int64_t w = blockIdx.x; w < a.T * nch; w += gridDim.x) {
+        const int64_t t = w / nch, ch = w % nch;
         if (threadIdx.x < a.K) {
             const int64_t q = t * a.K + threadIdx.x;
             int p = __ldcg(a.pos + q);
             // Keep the row only if it lies inside its rank's true total.
             if (p >= 0 && !row_valid(p, a.S, a.R, a.rank_prefix, a.packed)) {
-                atomicOr(a.err, kErrRowOob);
+                if (ch == 0) atomicOr(a.err, kErrRowOob);
                 p = -1;
             }
             s_pos[threadIdx.x] = p;
             s_w[threadIdx.x] = a.unit_weights ? 1.0f : __ldcg(a.scores + q);
-            if (a.gather_out)
+            if (a.gather_out && ch == 0)
                 a.gather_out[q] = (p >= 0 && a.gather_in) ? __ldcg(a.gather_in + p) : 0.0f;
         }
         __syncthreads();
-        for (int64_t v = threadIdx.x; v < V; v += kCombineThreads) {
+        const int64_t v_end = min(V, (ch + 1) * per);
+        for (int64_t v = ch * per + threadIdx.x; v < v_end; v += kCombineThreads) {
             float acc[N];
 #pragma unroll
             for (int i = 0; i < N; ++i) acc[i] = 0.0f;
@@ -309,16 +316,29 @@ cudaError_t plan_combine(int in_dtype, int num_sms, int* grid)
     return cudaSuccess;
 }
 
-cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& opts)
+cudaError_t launch_combine(const CombineArgs& args, int grid, const LaunchOpts& opts)
 {
-    if (a.T <= 0) return cudaSuccess;
+    if (args.T <= 0) return cudaSuccess;
     // The combine follows the expert (or, with an identity expert, the permute)
     // and would only start early to wait: launch it in plain stream order. In a
     // captured graph an early-launched combine behind the bulk permute measured
     // slower than a plain dependency.
     LaunchOpts o = opts;
     o.pdl = false;
-    const dim3 g((unsigned)(a.T < grid ? a.T : grid)), b(kCombineThreads);
+    // Fewer tokens than CTAs: split each token's row into chunks of at least one
+    // vector per thread, as many as the grid has room for.
+    CombineArgs a = args;
+    const int64_t V = a.D / (a.in_dtype == 0 ? 8 : 4);
+    int64_t nch = 1;
+    if (a.T < grid) {
+        const int64_t by_grid = grid / a.T;
+        const int64_t by_row = (V + kCombineThreads - 1) / kCombineThreads;
+        nch = by_grid < by_row ? by_grid : by_row;
+        if (nch < 1) nch = 1;
+    }
+    a.vsplit = (int)nch;
+    const int64_t items = a.T * nch;
+    const dim3 g((unsigned)(items < grid ? items : grid)), b(kCombineThreads);
     if (a.in_dtype == 0 && a.out_dtype == 0) return launch_kernel(combine_vec_kernel<0, 0>, g, b, 0, o, a);
     if (a.in_dtype == 0 && a.out_dtype == 1) return launch_kernel(combine_vec_kernel<0, 1>, g, b, 0, o, a);
     if (a.in_dtype == 1 && a.out_dtype == 0) return launch_kernel(combine_vec_kernel<1, 0>, g, b, 0, o, a);

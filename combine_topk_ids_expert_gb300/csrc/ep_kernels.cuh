@@ -162,6 +162,9 @@ struct CombineArgs {
     bool unit_weights;
     const float* gather_in;    // [R*S] or null
     float* gather_out;         // [T][K] or null
+    // Set by launch_combine: CTAs (vector chunks) per token, 1 unless the call
+    // has fewer tokens than the grid has CTAs.
+    int vsplit;
 };
 cudaError_t plan_combine(int in_dtype, int num_sms, int* grid);
 cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& o);
