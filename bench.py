@@ -567,6 +567,9 @@ def run_gb300(args) -> dict | None:
     res["bytes"] = nbytes
     res["pairs"] = sum(pairs)
     res["info"] = buf.info()
+    props = torch.cuda.get_device_properties(dev)
+    res["device"] = {"name": props.name, "sms": props.multi_processor_count,
+                     "l2_bytes": props.L2_cache_size, "dispatch_ctas": buf.info()["permute_grid"]}
 
     # The same step replayed from a captured CUDA graph (events around each
     # replay, L2 flushed before each), reported beside the eager timing.
@@ -959,7 +962,8 @@ def main():
              "timing": ("CUDA graph replay" if args.graph else "eager, per-kernel CUDA events")
              + (", fresh routing copied in before every replay (outside the events)"
                 if args.fresh_routing else ""),
-             "parallelism": f"replicas x{args.gpus}"}
+             "parallelism": f"replicas x{args.gpus}",
+             "device": res.get("device")}
     line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
