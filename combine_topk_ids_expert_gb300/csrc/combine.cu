@@ -307,11 +307,12 @@ cudaError_t occupancy(int* per_sm)
 
 }  // namespace
 
-cudaError_t plan_combine(int in_dtype, int num_sms, int* grid)
+cudaError_t plan_combine(int in_dtype, int num_sms, int per_sm_cap, int* grid)
 {
     int per_sm = 0;
     cudaError_t e = in_dtype == 0 ? occupancy<0, 0>(&per_sm) : occupancy<1, 1>(&per_sm);
     if (e != cudaSuccess) return e;
+    if (per_sm_cap > 0 && per_sm > per_sm_cap) per_sm = per_sm_cap;
     *grid = num_sms * (per_sm > 0 ? per_sm : 1);
     return cudaSuccess;
 }

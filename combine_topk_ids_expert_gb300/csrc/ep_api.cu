@@ -43,6 +43,7 @@ struct ep_buffer {
     uint32_t* tile_ready;   // [max_tiles] the one-pass dispatch's per-tile ready words
     int dispatch_pool_pct;  // share of each tile's tokens in the one-pass dispatch's pool
     int64_t dispatch_small_pairs;   // calls this small count every id in every CTA, no barrier
+    int combine_per_sm;     // combine CTAs per SM at most (0: as many as fit)
     int gemm_kernel;        // last expert GEMM: 0 none, 1 single-CTA, 2 two-SM
     int gemm_grid;
     int64_t test_skip_load; // test hook (EP_TEST_SKIP_LOAD), -1 = off
@@ -86,6 +87,8 @@ constexpr int kDispatchPoolPct = 25;
 // One-pass dispatch: calls of at most this many (token, k) pairs count all of
 // their ids in every CTA instead of meeting at the grid barrier.
 constexpr int64_t kDispatchSmallPairs = 4096;
+// Combine CTAs per SM at most (0: as many as fit).
+constexpr int kCombinePerSm = 0;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -392,6 +395,9 @@ void read_knobs(ep_buffer* b)
     // puts in its shared pool (0: every CTA copies only its own tile).
     const int64_t pool = env_int("EP_DISPATCH_POOL", kDispatchPoolPct);
     b->dispatch_pool_pct = (int)std::min<int64_t>(std::max<int64_t>(pool, 0), 100);
+    // EP_COMBINE_PER_SM=n: at most n combine CTAs per SM (0: as many as fit).
+    b->combine_per_sm = (int)std::min<int64_t>(std::max<int64_t>(env_int("EP_COMBINE_PER_SM",
+                                                                         kCombinePerSm), 0), 64);
     // EP_DISPATCH_SMALL_PAIRS=n: one-pass dispatches of at most n (token, k)
     // pairs count every id in every CTA instead of meeting at the grid barrier.
     b->dispatch_small_pairs = std::max<int64_t>(env_int("EP_DISPATCH_SMALL_PAIRS",
@@ -475,7 +481,8 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
     const int impl = cfg->permute_impl == EP_PERMUTE_DEFAULT ? EP_PERMUTE_BULK : cfg->permute_impl;
     if (ep::plan_permute(impl, rb, cfg->topk, cfg->num_experts, b->num_sms, b->tiles_per_sm,
                          &b->permute) != cudaSuccess ||
-        ep::plan_combine(cfg->dtype == EP_BF16 ? 0 : 1, b->num_sms, &b->combine_grid) !=
+        ep::plan_combine(cfg->dtype == EP_BF16 ? 0 : 1, b->num_sms, b->combine_per_sm,
+                         &b->combine_grid) !=
             cudaSuccess ||
         cudaMemset(b->err, 0, sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(b->gbar, 0, 3 * sizeof(uint32_t)) != cudaSuccess ||

@@ -166,7 +166,8 @@ struct CombineArgs {
     // has fewer tokens than the grid has CTAs.
     int vsplit;
 };
-cudaError_t plan_combine(int in_dtype, int num_sms, int* grid);
+// grid: num_sms times the CTAs per SM that fit, at most per_sm_cap (0: no cap).
+cudaError_t plan_combine(int in_dtype, int num_sms, int per_sm_cap, int* grid);
 cudaError_t launch_combine(const CombineArgs& a, int grid, const LaunchOpts& o);
 
 struct CombineBwdArgs {
