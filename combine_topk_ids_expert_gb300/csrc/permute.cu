@@ -201,8 +201,8 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
 // receive row of expert e, s_tot[e] = cnt[e], s_off[e] = expert_offset[e],
 // s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r],
 // s_rank[2][r] = tokens_in_rank[r]. Global writes: this tile's rows of the
-// count tables and the barrier words only, which no earlier kernel in the
-// stream reads. False if the barrier timed out. s_work: kLayoutWarps * Ep ints.
+// count tables and the barrier words only. False if the barrier timed out.
+// s_work: kLayoutWarps * Ep ints.
 // Second half of the layout, from the call's per-expert totals s_tot[e] and
 // this tile's counts of earlier pairs s_seed[e]: s_off[e] = expert_offset[e],
 // s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r] (inclusive),
@@ -375,10 +375,9 @@ __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* 
     if (threadIdx.x == 0) issue_rows();
     for (int e = threadIdx.x; e < Ep; e += blockDim.x) L.tile_cnt[(int64_t)tile * Ep + e] = s_tot[e];
     if (threadIdx.x < R) L.tile_tok[(int64_t)tile * R + threadIdx.x] = s_tok[threadIdx.x];
-    // The token pool's counter starts over for this call. Every CTA of the
-    // previous kernel in the stream has finished taking from it (dependents
-    // start only after all of its CTAs allow them, at their very end), and no
-    // CTA of this call takes from it before the barrier.
+    // The token pool's counter starts over for this call: the previous kernel
+    // in the stream has completed (the kernel waited for it on entry), and no
+    // CTA of this call takes from the pool before the barrier.
     if (tile == 0 && threadIdx.x == 0) L.gbar[2] = 0u;
     __threadfence();
     __syncthreads();
@@ -549,13 +548,20 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
         }
         fence_mbar_init();
         // The rows do not depend on the layout: the fused form starts them
-        // before waiting for it (the one-pass form right after its histogram).
+        // before waiting for it. Its predecessors are this call's count and
+        // scan kernels, which allow it to start only after their own waits,
+        // so every kernel before them has completed by then. (The one-pass
+        // form waits on entry and starts them right after its histogram.)
         if constexpr (!ONEPASS)
             for (int i = 0; i < n_pro; ++i) issue(i);
     }
 
     uint32_t epoch = 0;
     if constexpr (ONEPASS) {
+        // Inputs (ids, x, scores) may come from the previous kernel in the
+        // stream: wait for it before the first read (this costs nothing
+        // measurable, as the previous kernel is at its end by then).
+        griddep_wait();
         __shared__ int s_rank[3][kMaxRanks];
         __shared__ int s_tok[kMaxRanks];
         __shared__ int s_wsum[kLayoutWarps];
@@ -588,7 +594,6 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
             return;
         }
         epoch = s_epoch;
-        griddep_wait();   // the previous kernel in the stream may read what follows
         if (tile == 0) {
             for (int e = threadIdx.x; e < L.E; e += blockDim.x) {
                 L.cnt[e] = s_tot[e];
