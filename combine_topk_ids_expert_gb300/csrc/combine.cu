@@ -113,7 +113,7 @@ __device__ __forceinline__ void store_out(void* out, int64_t t, int64_t D, int64
     }
 }
 
-template <int IN, int OUT>
+template <int IN, int OUT, bool SPLIT>
 __global__ void __launch_bounds__(kCombineThreads)
 combine_vec_kernel(CombineArgs a)
 {
@@ -124,9 +124,10 @@ combine_vec_kernel(CombineArgs a)
     const int64_t V = a.D / N;
     const int4* __restrict__ y = static_cast<const int4*>(a.y);
     // Work item w = (token w / vsplit, vector chunk w % vsplit): a call with
-    // fewer tokens than CTAs spreads each token's row over vsplit CTAs, so that
-    // each thread has fewer dependent load rounds.
-    const int64_t nch = a.vsplit;
+    // fewer tokens than CTAs (SPLIT) spreads each token's row over vsplit CTAs,
+    // so that each thread has fewer dependent load rounds. Without SPLIT the
+    // chunk is the whole row, resolved at compile time.
+    const int64_t nch = SPLIT ? a.vsplit : 1;
     const int64_t per = (V + nch - 1) / nch;   // vectors per chunk
 
     for (int64_t w = blockIdx.x; w < a.T * nch; w += gridDim.x) {
@@ -301,7 +302,7 @@ combine_backward_kernel(CombineBwdArgs a)
 template <int IN, int OUT>
 cudaError_t occupancy(int* per_sm)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, combine_vec_kernel<IN, OUT>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, combine_vec_kernel<IN, OUT, false>,
                                                          kCombineThreads, 0);
 }
 
@@ -340,10 +341,22 @@ cudaError_t launch_combine(const CombineArgs& args, int grid, const LaunchOpts& 
     a.vsplit = (int)nch;
     const int64_t items = a.T * nch;
     const dim3 g((unsigned)(items < grid ? items : grid)), b(kCombineThreads);
-    if (a.in_dtype == 0 && a.out_dtype == 0) return launch_kernel(combine_vec_kernel<0, 0>, g, b, 0, o, a);
-    if (a.in_dtype == 0 && a.out_dtype == 1) return launch_kernel(combine_vec_kernel<0, 1>, g, b, 0, o, a);
-    if (a.in_dtype == 1 && a.out_dtype == 0) return launch_kernel(combine_vec_kernel<1, 0>, g, b, 0, o, a);
-    return launch_kernel(combine_vec_kernel<1, 1>, g, b, 0, o, a);
+    if (nch > 1) {
+        if (a.in_dtype == 0 && a.out_dtype == 0)
+            return launch_kernel(combine_vec_kernel<0, 0, true>, g, b, 0, o, a);
+        if (a.in_dtype == 0 && a.out_dtype == 1)
+            return launch_kernel(combine_vec_kernel<0, 1, true>, g, b, 0, o, a);
+        if (a.in_dtype == 1 && a.out_dtype == 0)
+            return launch_kernel(combine_vec_kernel<1, 0, true>, g, b, 0, o, a);
+        return launch_kernel(combine_vec_kernel<1, 1, true>, g, b, 0, o, a);
+    }
+    if (a.in_dtype == 0 && a.out_dtype == 0)
+        return launch_kernel(combine_vec_kernel<0, 0, false>, g, b, 0, o, a);
+    if (a.in_dtype == 0 && a.out_dtype == 1)
+        return launch_kernel(combine_vec_kernel<0, 1, false>, g, b, 0, o, a);
+    if (a.in_dtype == 1 && a.out_dtype == 0)
+        return launch_kernel(combine_vec_kernel<1, 0, false>, g, b, 0, o, a);
+    return launch_kernel(combine_vec_kernel<1, 1, false>, g, b, 0, o, a);
 }
 
 cudaError_t launch_combine_backward(const CombineBwdArgs& a, int grid, const LaunchOpts& opts)

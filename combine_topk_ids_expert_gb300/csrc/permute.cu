@@ -477,10 +477,9 @@ __device__ __forceinline__ int pool_pos(const LayoutArgs& L, int64_t t, int k, u
 // tile of n tokens; pool entry c is token c / ntiles of tile c % ntiles's
 // share. Whoever copies a row, the owner tile writes its scores and sources
 // and publishes its positions (L.pos) for the others.
-template <bool ONEPASS>
+template <bool ONEPASS, bool SMALL>
 __global__ void __launch_bounds__(kLayoutThreads, 1)
-dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, int pool_d,
-                     int small)
+dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, int pool_d)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kBulkMaxStages];
@@ -499,7 +498,7 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
     const uint32_t bar0 = smem_u32(bars);
     const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
     uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
-    const bool pooled = ONEPASS && pool_d > 0 && !small;
+    const bool pooled = ONEPASS && !SMALL && pool_d > 0;
     // This tile's pool share and the tokens it keeps.
     auto share = [&](int n) { return pooled ? min(pool_d, max(0, n - stages)) : 0; };
     const int n_static = n_my - share(n_my);
@@ -572,7 +571,7 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
         int* s_tot = s_seed + L.Ep;
         int* s_off = s_tot + L.Ep;
         bool ok = true;
-        if (small) {
+        if constexpr (SMALL) {
             // A small call: no grid barrier (see redundant_counts), no pool.
             redundant_counts(L, tile, s_seed, s_tot, s_rank);
             if (threadIdx.x == 0)
@@ -725,10 +724,14 @@ cudaError_t plan_permute(int impl, int64_t row_bytes, int K, int E, int num_sms,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  plan->smem_bytes);
             if (e != cudaSuccess) return e;
-            e = cudaFuncSetAttribute(dispatch_tile_kernel<false>,
+            e = cudaFuncSetAttribute(dispatch_tile_kernel<false, false>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemCap);
             if (e != cudaSuccess) return e;
-            e = cudaFuncSetAttribute(dispatch_tile_kernel<true>,
+            e = cudaFuncSetAttribute(dispatch_tile_kernel<true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kFusedSmemCap - kOnepassStaticReserve);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(dispatch_tile_kernel<true, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kFusedSmemCap - kOnepassStaticReserve);
             if (e != cudaSuccess) return e;
@@ -789,8 +792,8 @@ cudaError_t launch_dispatch_fused(const LayoutArgs& l, const PermuteArgs& p,
     if (stages > kBulkMaxStages) stages = kBulkMaxStages;
     if (stages < kBulkLag + 2) return cudaErrorNotSupported;
     const size_t smem = (size_t)(stages * slot + fixed);
-    return launch_kernel(dispatch_tile_kernel<false>, dim3(l.ntiles), dim3(kLayoutThreads), smem, o,
-                         l, p, (int)stages, slot, 0, 0);
+    return launch_kernel(dispatch_tile_kernel<false, false>, dim3(l.ntiles), dim3(kLayoutThreads),
+                         smem, o, l, p, (int)stages, slot, 0);
 }
 
 cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
@@ -807,12 +810,18 @@ cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
     if (stages > kBulkMaxStages) stages = kBulkMaxStages;
     if (stages < kBulkLag + 2) return cudaErrorNotSupported;
     const size_t smem = (size_t)(stages * slot + fixed);
+    // A call of at most small_pairs pairs counts all its ids in every CTA
+    // instead of meeting at the grid barrier (and then has no pool): a kernel
+    // of its own, so that the barrier form carries none of its code.
+    const bool small = l.T * l.K <= small_pairs;
+    void (*kernel)(LayoutArgs, PermuteArgs, int, int, int) =
+        small ? dispatch_tile_kernel<true, true> : dispatch_tile_kernel<true, false>;
     // Every CTA must be resident at once for the grid barrier.
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_tile_kernel<true>,
-                                                      kLayoutThreads, smem) != cudaSuccess)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kLayoutThreads, smem) !=
+            cudaSuccess)
         return cudaErrorNotSupported;
     if ((int64_t)per_sm * sms < l.ntiles) return cudaErrorNotSupported;
     cudaLaunchConfig_t cfg = {};
@@ -830,18 +839,13 @@ cudaError_t launch_dispatch_onepass(const LayoutArgs& l, const PermuteArgs& p,
     // Tokens of each full tile given to the shared pool. A tile keeps at least
     // a ring's worth of its own tokens (those are loaded before the layout is
     // known), so tiles that fit the ring give none and there is no pool.
-    // A call of at most small_pairs pairs counts all its ids in every CTA
-    // instead of meeting at the grid barrier (and then has no pool).
-    const int small = (l.T * l.K <= small_pairs) ? 1 : 0;
     int64_t pool_d = 0;
     if (!small && l.tile_ready && pool_pct > 0) {
         pool_d = l.tpt * (pool_pct < 100 ? pool_pct : 100) / 100;
         if (pool_d > l.tpt - stages) pool_d = l.tpt - stages;
         if (pool_d < 0) pool_d = 0;
     }
-    const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, dispatch_tile_kernel<true>, l, p, (int)stages, slot, (int)pool_d,
-                           small);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, l, p, (int)stages, slot, (int)pool_d);
     if (e == cudaErrorCooperativeLaunchTooLarge) {   // fewer SMs than the device reports (MPS)
         cudaGetLastError();
         return cudaErrorNotSupported;
