@@ -86,7 +86,7 @@ constexpr int kGemmLightRows = 256;
 constexpr int kDispatchPoolPct = 25;
 // One-pass dispatch: calls of at most this many (token, k) pairs count all of
 // their ids in every CTA instead of meeting at the grid barrier.
-constexpr int64_t kDispatchSmallPairs = 4096;
+constexpr int64_t kDispatchSmallPairs = 2048;
 // Combine CTAs per SM at most (0: as many as fit).
 constexpr int kCombinePerSm = 0;
 

@@ -22,7 +22,7 @@ LAYERS = 4
 
 CASES = {
     # name: (T, N, D, E, K, R, dtype) -- the grid-barrier path (many tiles, token
-    # pool) and the small-call path (at most 4096 pairs) of the one-pass dispatch
+    # pool) and the small-call path (at most 2048 pairs) of the one-pass dispatch
     "barrier_bf16": (2000, 2003, 1024, 64, 8, 8, "bf16"),
     "barrier_f32": (1500, 1500, 512, 32, 4, 4, "f32"),
     "small_bf16": (200, 203, 7168, 256, 8, 8, "bf16"),
