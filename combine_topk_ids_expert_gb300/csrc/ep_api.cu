@@ -39,7 +39,7 @@ struct ep_buffer {
     bool debug;             // EP_DEBUG: sentinel fill and checks of the receive rows
     bool nvtx;              // EP_NVTX: an NVTX range around every call
     bool coop_pdl;          // cooperative launches take programmatic serialization
-    uint32_t* gbar;         // [3] the one-pass dispatch's grid barrier and token-pool counter
+    uint32_t* gbar;         // [4] the one-pass dispatch's grid barrier and token-pool counter
     uint32_t* tile_ready;   // [max_tiles] the one-pass dispatch's per-tile ready words
     int dispatch_pool_pct;  // share of each tile's tokens in the one-pass dispatch's pool
     int64_t dispatch_small_pairs;   // calls this small count every id in every CTA, no barrier
@@ -162,7 +162,7 @@ Offsets layout_workspace(const ep_config* c, int64_t row_bytes, int64_t s_max, i
     o.tok_pos = cv.take((size_t)c->num_max_tokens_per_rank * R * 4);
     o.tok_src = cv.take(R * (size_t)pad4(c->num_max_tokens_per_rank) * 4);
     o.tile_ready = cv.take((size_t)max_tiles * 4);
-    o.gbar = cv.take(12);
+    o.gbar = cv.take(16);
     o.err = cv.take(4);   // last: the workspace ends after the error word
     o.total = cv.off;
     return o;
@@ -485,7 +485,7 @@ ep_status ep_buffer_init(const ep_config* cfg, void* workspace, size_t workspace
                          &b->combine_grid) !=
             cudaSuccess ||
         cudaMemset(b->err, 0, sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(b->gbar, 0, 3 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(b->gbar, 0, 4 * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(b->tile_ready, 0, (size_t)b->max_tiles * 4) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         delete b;
@@ -788,11 +788,11 @@ ep_status ep_get_device_error(ep_buffer* buf, ep_stream_t stream, uint32_t* flag
         cudaMemsetAsync(buf->err, 0, sizeof v, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return EP_ERR_CUDA;
-    // A timed-out grid barrier leaves its arrival count behind: start it over
-    // (generation, pool counter and the tiles' ready words with it, so that no
+    // A timed-out grid barrier leaves its arrival counts behind: start them over
+    // (generation, pool counter and the tiles' ready words with them, so that no
     // ready word of an earlier call can match a generation counted anew).
     if ((v & EP_DEVERR_TIMEOUT) &&
-        (cudaMemsetAsync(buf->gbar, 0, 3 * sizeof(uint32_t), s) != cudaSuccess ||
+        (cudaMemsetAsync(buf->gbar, 0, 4 * sizeof(uint32_t), s) != cudaSuccess ||
          cudaMemsetAsync(buf->tile_ready, 0, (size_t)buf->max_tiles * 4, s) != cudaSuccess ||
          cudaStreamSynchronize(s) != cudaSuccess))
         return EP_ERR_CUDA;

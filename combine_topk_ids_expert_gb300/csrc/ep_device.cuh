@@ -294,29 +294,46 @@ __device__ __forceinline__ void tile_histogram(const LayoutArgs& a, int tile, in
 
 // ---- grid barrier ----------------------------------------------------------
 //
-// For a cooperative launch (every CTA resident). bar[0] counts arrivals,
-// bar[1] is the generation; the last arrival resets the count and advances
-// the generation. Called by one thread per CTA after the CTA's writes are
-// fenced; false if the others have not arrived within the wait limit (the
-// count is then left inconsistent: the host resets both words when it reads
-// the timeout bit). *epoch receives the generation this barrier opens (the
-// one bar[1] holds once every CTA has arrived).
-__device__ __forceinline__ bool grid_barrier(uint32_t* bar, uint32_t n, uint32_t* epoch)
+// For a cooperative launch (every CTA resident). bar[1] is the generation of
+// the next barrier; bar[0] and bar[3] count the arrivals of even and odd
+// generations. A barrier of generation g is complete once its counter holds
+// n: the last arrival's own atomic completes it, and the waiters poll the
+// counter itself (one round trip after the last arrival). The last arrival
+// also sets the other counter to zero for the next barrier (nothing uses it
+// during this one: the kernel that used it has completed) and advances bar[1].
+// A waiter tests for exactly n, so a counter left above n never opens.
+//
+// gen: bar[1] as read by this CTA at the kernel's start (grid_generation),
+// which stays unchanged until every CTA of this launch has arrived. Called by
+// one thread per CTA after the CTA's writes are fenced; false if the others
+// have not arrived within the wait limit (the counters are then inconsistent:
+// the host resets every word when it reads the timeout bit). *epoch receives
+// gen + 1, the generation this barrier opens.
+__device__ __forceinline__ uint32_t grid_generation(const uint32_t* bar)
 {
-    uint32_t gen, old;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(bar + 1) : "memory");
+    uint32_t g;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(bar + 1) : "memory");
+    return g;
+}
+
+__device__ __forceinline__ bool grid_barrier(uint32_t* bar, uint32_t n, uint32_t gen,
+                                             uint32_t* epoch)
+{
     *epoch = gen + 1u;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(bar) : "memory");
-    if (old == n - 1) {
-        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(bar) : "memory");
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar + 1) : "memory");
+    uint32_t* cnt = bar + ((gen & 1u) ? 3 : 0);
+    uint32_t* next = bar + ((gen & 1u) ? 0 : 3);
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
+    if (old + 1u == n) {
+        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(next) : "memory");
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(bar + 1) : "memory");
         return true;
     }
     const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
     while (true) {
-        uint32_t g;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(bar + 1) : "memory");
-        if (g != gen) return true;
+        uint32_t c;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(cnt) : "memory");
+        if (c == n) return true;
         if (globaltimer_ns() > deadline) return false;
         __nanosleep(64);
     }

@@ -72,8 +72,9 @@ struct LayoutArgs {
     int32_t* tokens_in_rank;   // [R]
     int32_t* pos;              // [T][K]
     uint32_t* err;
-    uint32_t* gbar;            // [3] one-pass dispatch: barrier arrivals, generation, and
-                               // the counter of its shared token pool; or null
+    uint32_t* gbar;            // [4] one-pass dispatch: even-generation arrivals,
+                               // generation, the counter of its shared token pool,
+                               // odd-generation arrivals; or null
     uint32_t* tile_ready;      // [tiles] one-pass dispatch: the generation in which each
                                // tile's positions were published; or null
     bool packed;               // ranks back to back instead of r*S

@@ -368,6 +368,9 @@ __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* 
                                int* s_flag, uint32_t* s_epoch, IssueRows issue_rows)
 {
     const int Ep = L.Ep, R = L.R, G = (int)gridDim.x;
+    // The barrier's generation, read now so that its latency hides behind the
+    // histogram (it cannot change before every CTA of this launch arrives).
+    const uint32_t gen = threadIdx.x == 0 ? grid_generation(L.gbar) : 0u;
     // The ids first: issued behind the tile's row loads they would wait for
     // those; the rows are started right after the histogram instead (they are
     // in by the time the positions are known).
@@ -381,7 +384,7 @@ __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* 
     if (tile == 0 && threadIdx.x == 0) L.gbar[2] = 0u;
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) *s_flag = grid_barrier(L.gbar, (uint32_t)G, s_epoch) ? 1 : 0;
+    if (threadIdx.x == 0) *s_flag = grid_barrier(L.gbar, (uint32_t)G, gen, s_epoch) ? 1 : 0;
     __syncthreads();
     if (!*s_flag) return false;
 

@@ -195,10 +195,11 @@ def test_bounded_wait_runs_out_and_reports(orc, monkeypatch):
 
 
 def test_grid_barrier_runs_out_and_recovers(orc, monkeypatch):
-    # The one-pass dispatch meets all its CTAs at a grid barrier (two words at
-    # the end of the workspace: arrivals, generation) with a 2 s limit. Seeding
-    # the arrival count past the grid size means no CTA is ever the last to
-    # arrive, so every CTA's wait runs out: the kernel must report
+    # The one-pass dispatch meets all its CTAs at a grid barrier (words at the
+    # end of the workspace: even-generation arrivals, generation, pool counter,
+    # odd-generation arrivals) with a 2 s limit. Seeding the first arrival
+    # count past the grid size means the count never equals the grid size, so
+    # every CTA's wait runs out: the kernel must report
     # EP_DEVERR_TIMEOUT and return; reading the flag starts the barrier over,
     # and the next dispatch on the same buffer is oracle-exact. (A call this
     # small would skip the barrier: EP_DISPATCH_SMALL_PAIRS=0 keeps it.)
@@ -208,14 +209,14 @@ def test_grid_barrier_runs_out_and_recovers(orc, monkeypatch):
     xd, idd, scd = to_dev(x), to_dev(ids), to_dev(sc)
     ws = buf.workspace
     align = 256                      # workspace carve granularity
-    gbar = ws.numel() - 2 * align    # [arrivals, generation], then the error word
+    gbar = ws.numel() - 2 * align    # the barrier's four words, then the error word
     ws[gbar:gbar + 4].view(torch.int32).fill_(1 << 20)
     n0 = buf.info()["kernel_launches"]
     buf.dispatch(xd, scd, idd, 40)
     torch.cuda.synchronize()
     assert buf.info()["kernel_launches"] - n0 == 1, "expected the one-pass dispatch"
     assert buf.device_error() & ep.EP_DEVERR_TIMEOUT
-    assert int(ws[gbar:gbar + 8].view(torch.int32).abs().sum().item()) == 0
+    assert int(ws[gbar:gbar + 16].view(torch.int32).abs().sum().item()) == 0
     d = buf.dispatch(xd, scd, idd, 40)
     out = buf.combine(d.recv_x, scd)
     torch.cuda.synchronize()
