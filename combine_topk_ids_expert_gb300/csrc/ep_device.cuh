@@ -167,10 +167,14 @@ __device__ __forceinline__ void bulk_wait_all()
 // so the order is the flat pair order t*K + k. Called by all kLayoutThreads
 // threads of the block; s_base holds kLayoutWarps * Ep ints. Writes the rows
 // to pos_out (global) and, if s_pos is given, to s_pos[i] (shared). If s_seed
-// is given, s_seed[e] replaces expert_offset[e] + tile_pre[tile][e].
+// is given, s_seed[e] replaces expert_offset[e] + tile_pre[tile][e]. If s_ids
+// is given, it holds the tile's ids as tile_histogram kept them, and they are
+// read from there instead of from global memory (s_ids may be s_pos: each
+// entry is read before its position is written over it).
 __device__ __forceinline__ void tile_positions(const LayoutArgs& a, int tile, int* s_base,
                                                int32_t* pos_out, int* s_pos,
-                                               const int* s_seed = nullptr)
+                                               const int* s_seed = nullptr,
+                                               const int* s_ids = nullptr)
 {
     const int64_t t0 = (int64_t)tile * a.tpt;
     const int64_t t1 = min(a.T, t0 + a.tpt);
@@ -189,7 +193,7 @@ __device__ __forceinline__ void tile_positions(const LayoutArgs& a, int tile, in
     // Pass 1: per-warp histogram (one writer per row, one add per peer group).
     for (int c = w_begin; c < w_begin + seg; c += 32) {
         const int i = c + lane;
-        const int e = (i < w_end) ? valid_id(__ldcg(a.ids + p0 + i), E) : -1;
+        const int e = (i >= w_end) ? -1 : s_ids ? s_ids[i] : valid_id(__ldcg(a.ids + p0 + i), E);
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
         __syncwarp();
@@ -214,7 +218,7 @@ __device__ __forceinline__ void tile_positions(const LayoutArgs& a, int tile, in
     for (int c = w_begin; c < w_begin + seg; c += 32) {
         const int i = c + lane;
         const bool in = i < w_end;
-        const int e = in ? valid_id(__ldcg(a.ids + p0 + i), E) : -1;
+        const int e = !in ? -1 : s_ids ? s_ids[i] : valid_id(__ldcg(a.ids + p0 + i), E);
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int b = (e >= 0) ? mine[e] : 0;
         if (in) {
@@ -235,12 +239,14 @@ __device__ __forceinline__ void tile_positions(const LayoutArgs& a, int tile, in
 // = tokens of the tile with at least one expert on rank r. Full warps walk the
 // tile so every lane takes part in __match_any_sync (equal ids are grouped and
 // one lane per group adds the group size); each thread loads kHistUnroll ids
-// before matching them. Invalid ids count as none and set kErrBadId. Ends
-// with __syncthreads.
+// before matching them. Invalid ids count as none and set kErrBadId. If s_ids
+// is given, the tile's ids (invalid ones as -1) are also kept there, s_ids[i]
+// for the tile's pair i, and the rank sets are taken from them. Ends with
+// __syncthreads.
 constexpr int kHistUnroll = 4;
 
 __device__ __forceinline__ void tile_histogram(const LayoutArgs& a, int tile, int* s_hist,
-                                               int* s_tok)
+                                               int* s_tok, int* s_ids = nullptr)
 {
     const int64_t t0 = (int64_t)tile * a.tpt;
     const int64_t t1 = min(a.T, t0 + a.tpt);
@@ -263,6 +269,7 @@ __device__ __forceinline__ void tile_histogram(const LayoutArgs& a, int tile, in
             const int raw = (i < np) ? __ldcg(a.ids + p0 + i) : -1;
             e[j] = valid_id(raw, a.E);
             bad |= (e[j] != raw);
+            if (s_ids && i < np) s_ids[i] = e[j];
         }
 #pragma unroll
         for (int j = 0; j < kHistUnroll; ++j) {
@@ -274,6 +281,7 @@ __device__ __forceinline__ void tile_histogram(const LayoutArgs& a, int tile, in
         }
     }
     if (bad) atomicOr(a.err, kErrBadId);
+    if (s_ids) __syncthreads();
 
     // Distinct tokens per logical rank: one 64-bit rank set per token.
     const int eloc = a.E / a.R;
@@ -281,7 +289,8 @@ __device__ __forceinline__ void tile_histogram(const LayoutArgs& a, int tile, in
         unsigned long long mask = 0ull;
 #pragma unroll 8
         for (int k = 0; k < a.K; ++k) {
-            const int e = valid_id(__ldcg(a.ids + t * a.K + k), a.E);
+            const int e = s_ids ? s_ids[(t - t0) * a.K + k]
+                                : valid_id(__ldcg(a.ids + t * a.K + k), a.E);
             if (e >= 0) mask |= 1ull << (e / eloc);
         }
         while (mask) {

@@ -195,14 +195,6 @@ permute_bulk_kernel(PermuteArgs a, int stages, int slot_bytes)
     griddep_launch_dependents();
 }
 
-// One-pass layout of tile `tile` (dispatch_onepass): this tile's counts, a
-// grid barrier, then every tile's counts summed per expert (before this tile,
-// and in all) and scanned over experts. Leaves s_seed[e] = this tile's first
-// receive row of expert e, s_tot[e] = cnt[e], s_off[e] = expert_offset[e],
-// s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r],
-// s_rank[2][r] = tokens_in_rank[r]. Global writes: this tile's rows of the
-// count tables and the barrier words only. False if the barrier timed out.
-// s_work: kLayoutWarps * Ep ints.
 // Second half of the layout, from the call's per-expert totals s_tot[e] and
 // this tile's counts of earlier pairs s_seed[e]: s_off[e] = expert_offset[e],
 // s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r] (inclusive),
@@ -362,10 +354,19 @@ __device__ void redundant_counts(const LayoutArgs& L, int tile, int* s_seed, int
     __syncthreads();
 }
 
+// One-pass layout of tile `tile` (dispatch_onepass): this tile's counts, a
+// grid barrier, then every tile's counts summed per expert (before this tile,
+// and in all) and scanned over experts. Leaves s_seed[e] = this tile's first
+// receive row of expert e, s_tot[e] = cnt[e], s_off[e] = expert_offset[e],
+// s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r],
+// s_rank[2][r] = tokens_in_rank[r]. Global writes: this tile's rows of the
+// count tables and the barrier words only. False if the barrier timed out.
+// s_work: kLayoutWarps * Ep ints. s_ids: the tile's pairs' ids are kept there
+// (tile_histogram) for the positions.
 template <typename IssueRows>
 __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* s_seed, int* s_tot,
                                int* s_off, int (*s_rank)[kMaxRanks], int* s_tok, int* s_wsum,
-                               int* s_flag, uint32_t* s_epoch, IssueRows issue_rows)
+                               int* s_flag, uint32_t* s_epoch, int* s_ids, IssueRows issue_rows)
 {
     const int Ep = L.Ep, R = L.R, G = (int)gridDim.x;
     // The barrier's generation, read now so that its latency hides behind the
@@ -374,7 +375,7 @@ __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* 
     // The ids first: issued behind the tile's row loads they would wait for
     // those; the rows are started right after the histogram instead (they are
     // in by the time the positions are known).
-    tile_histogram(L, tile, s_tot, s_tok);   // ends with __syncthreads
+    tile_histogram(L, tile, s_tot, s_tok, s_ids);   // ends with __syncthreads
     if (threadIdx.x == 0) issue_rows();
     for (int e = threadIdx.x; e < Ep; e += blockDim.x) L.tile_cnt[(int64_t)tile * Ep + e] = s_tot[e];
     if (threadIdx.x < R) L.tile_tok[(int64_t)tile * R + threadIdx.x] = s_tok[threadIdx.x];
@@ -583,7 +584,7 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
             s_epoch = 0u;
         } else {
             ok = onepass_layout(L, tile, s_base, s_seed, s_tot, s_off, s_rank, s_tok, s_wsum,
-                                &s_flag, &s_epoch, [&] {
+                                &s_flag, &s_epoch, s_pos, [&] {
                                     for (int i = 0; i < n_pro; ++i) issue(i);
                                 });
         }
@@ -607,7 +608,9 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
                 L.tokens_in_rank[threadIdx.x] = s_rank[2][threadIdx.x];
             }
         }
-        tile_positions(L, tile, s_base, L.pos, s_pos, s_seed);   // ends with __syncthreads
+        // The barrier form kept the tile's ids in s_pos (onepass_layout).
+        tile_positions(L, tile, s_base, L.pos, s_pos, s_seed,
+                       SMALL ? nullptr : s_pos);   // ends with __syncthreads
         if (pooled) {
             // Publish this tile's positions for the CTAs that copy its pool rows.
             __threadfence();
