@@ -513,6 +513,17 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
     const int pool_first_issue = pooled ? max(n_pro, min(stages, kPoolAhead + 1)) : n_pro;
 
     const int64_t skipped = (tile == 0) ? a.skip_load : -1;
+    // Whether receive row p is to be written: p >= 0 and inside the call's
+    // R * S rows. Positions always are when the layout is sound; one outside
+    // (possible only if the grid barrier's words were corrupted and it opened
+    // early) is skipped and reported, so that no store leaves the buffer.
+    const int64_t rows_cap = (int64_t)L.R * L.S;
+    auto in_rows = [&](int p) {
+        if (p < 0) return false;
+        if ((int64_t)p < rows_cap) return true;
+        atomicOr(a.err, kErrRowOob);
+        return false;
+    };
     // Starts the load of sequence index q into its slot: an own token, or the
     // next pool token (recorded in s_seq; -1 once the pool is empty).
     auto issue = [&](int q) {
@@ -649,7 +660,7 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
             if (lane < K) {
                 const int p = (i < n_static) ? s_pos[i * K + lane]
                                              : pool_pos(L, t, lane, epoch, a.err);
-                if (p >= 0)
+                if (in_rows(p))
                     bulk_s2g(rx + (int64_t)p * a.row_bytes,
                              slot0 + (uint32_t)s * (uint32_t)slot_bytes, bytes);
             }
@@ -689,7 +700,7 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
         const int np = n_my * K;
         for (int j = threadIdx.x - 32; j < np; j += kLayoutThreads - 32) {
             const int p = s_pos[j];
-            if (p >= 0) {
+            if (in_rows(p)) {
                 a.recv_scores[p] = __ldcg(a.scores + p0 + j);
                 a.recv_src[p] = (int32_t)(p0 + j);
             }

@@ -90,7 +90,10 @@ typedef enum {
 
 /* Device error word bits (sticky until ep_get_device_error clears them). */
 #define EP_DEVERR_BAD_ID 0x1u     /* an id outside [-1, E) was seen; treated as -1 */
-#define EP_DEVERR_ROW_OOB 0x2u    /* combine met a row outside its rank's true total; skipped */
+#define EP_DEVERR_ROW_OOB 0x2u    /* combine met a row outside its rank's true total, or the
+                                     one-pass dispatch computed a row outside the call's R*S
+                                     rows (only after its barrier words were corrupted);
+                                     skipped */
 #define EP_DEVERR_TIMEOUT 0x4u    /* a bounded device-side wait gave up; outputs invalid */
 /* Only with EP_DEBUG=1 (read at ep_buffer_init): the dispatch fills its receive
  * rows with 0xFF before the permute and checks them after it; the combine

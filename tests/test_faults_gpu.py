@@ -225,3 +225,37 @@ def test_grid_barrier_runs_out_and_recovers(orc, monkeypatch):
     want, _ = orc.combine(ref["recv_x"], sc, ref["pos"], ref["rank_prefix"], ref["S"], R)
     assert_combine_equal(to_np(out), want)
     buf.close()
+
+
+def test_grid_barrier_opened_early_stays_in_bounds(orc, monkeypatch):
+    # Corrupted barrier words can open the barrier before every CTA has
+    # counted its tile: seeding the arrival count at three below the grid size
+    # (a 40-token call runs 40 CTAs, one token each) lets the first three CTAs
+    # through with the tile tables of nobody else. Their layout is garbage,
+    # but every store stays inside the receive buffer (rows outside the call's
+    # R * S are skipped and reported as EP_DEVERR_ROW_OOB), the other CTAs'
+    # waits run out (EP_DEVERR_TIMEOUT: their count passes the grid size), and
+    # after the host resets the words the next dispatch is oracle-exact.
+    monkeypatch.setenv("EP_DISPATCH_SMALL_PAIRS", "0")
+    buf = ep.Buffer(64, D, E, R, K, dtype=torch.bfloat16, permute_impl=ep.EP_PERMUTE_BULK)
+    x, ids, sc = small(T=40, seed=11)
+    xd, idd, scd = to_dev(x), to_dev(ids), to_dev(sc)
+    ws = buf.workspace
+    gbar = ws.numel() - 2 * 256      # the barrier's four words, then the error word
+    ws[gbar:gbar + 4].view(torch.int32).fill_(40 - 3)
+    n0 = buf.info()["kernel_launches"]
+    buf.dispatch(xd, scd, idd, 40)
+    torch.cuda.synchronize()
+    assert buf.info()["kernel_launches"] - n0 == 1, "expected the one-pass dispatch"
+    flags = buf.device_error()
+    assert flags & ep.EP_DEVERR_TIMEOUT
+    assert flags & ~(ep.EP_DEVERR_TIMEOUT | ep.EP_DEVERR_ROW_OOB) == 0
+    assert int(ws[gbar:gbar + 16].view(torch.int32).abs().sum().item()) == 0
+    d = buf.dispatch(xd, scd, idd, 40)
+    out = buf.combine(d.recv_x, scd)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch(x, sc, ids, 40, E, R)
+    want, _ = orc.combine(ref["recv_x"], sc, ref["pos"], ref["rank_prefix"], ref["S"], R)
+    assert_combine_equal(to_np(out), want)
+    buf.close()
