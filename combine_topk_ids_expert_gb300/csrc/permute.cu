@@ -399,7 +399,7 @@ __device__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work, int* 
     const int g = threadIdx.x / Q, q = threadIdx.x % Q;
     if (g < NG && q < Q) {
         // Loads in batches of kSumBatch rows, all in flight before the adds.
-        constexpr int kSumBatch = 16;
+        constexpr int kSumBatch = 20;
         const int4* tc = reinterpret_cast<const int4*>(L.tile_cnt);
         int4 bef = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
         for (int tb = g; tb < G; tb += kSumBatch * NG) {
@@ -623,17 +623,21 @@ dispatch_tile_kernel(LayoutArgs L, PermuteArgs a, int stages, int slot_bytes, in
         tile_positions(L, tile, s_base, L.pos, s_pos, s_seed,
                        SMALL ? nullptr : s_pos);   // ends with __syncthreads
         if (pooled) {
-            // Publish this tile's positions for the CTAs that copy its pool rows.
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) {
+            // Publish this tile's positions for the CTAs that copy its pool rows:
+            // the block barrier that ends tile_positions orders every thread's
+            // position writes before thread 32's fence and release (cumulativity),
+            // so warp 0 starts copying without waiting for the fence.
+            if (threadIdx.x == 32) {
+                __threadfence();
                 asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(L.tile_ready + tile),
                              "r"(epoch)
                              : "memory");
-                // A tile shorter than the ring takes its first pool tokens now.
-                for (int q = n_pro; q < pool_first_issue; ++q) issue(q);
             }
-            __syncthreads();
+            // A tile shorter than the ring takes its first pool tokens now (the
+            // pool's rows do not depend on any position).
+            if (threadIdx.x == 0)
+                for (int q = n_pro; q < pool_first_issue; ++q) issue(q);
+            if (warp == 0) __syncwarp();   // s_seq, written by lane 0, is read by the warp
         }
     } else {
         griddep_wait();                                   // counts and offsets are ready
