@@ -34,7 +34,7 @@ namespace ep {
 namespace {
 
 constexpr int kVecThreads = 128;
-constexpr int kBulkLag = 4;            // store groups in flight before a slot is reused
+constexpr int kBulkLag = 2;            // store groups in flight before a slot is reused
 constexpr int kPoolAhead = 2;          // pool tokens taken ahead of the one being copied
 constexpr int kBulkMaxStages = 32;
 constexpr int kBulkSmemBudget = 200 * 1024;
