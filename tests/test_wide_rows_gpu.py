@@ -1,9 +1,11 @@
 """Wide hidden rows on every dispatch path, the combine and the dedupe dispatch.
 
-The bulk dispatch stages whole rows in a shared-memory ring: 32 KB rows still
-leave it six slots, while 40 KB rows leave too few and the dispatch falls back
-to the 16-byte vector kernel, which loops over a row wider than its CTA's
-vectors (256 KB fp32 rows). Each case is compared with the oracle bit for bit.
+The bulk dispatch stages whole rows in a shared-memory ring and needs four
+slots (two tokens' stores may still be reading the ring while two more rows
+load): 32 KB rows leave it six, 40 KB rows five, while 56 KB rows leave too few
+and the dispatch falls back to the 16-byte vector kernel, which loops over a
+row wider than its CTA's vectors (also 256 KB fp32 rows). Each case is
+compared with the oracle bit for bit.
 """
 import numpy as np
 import pytest
@@ -20,10 +22,11 @@ CASES = {
     # name: (seed, T, N, D, dtype, E, K, R)
     "bf16_32k_rows": (170, 61, 64, 16384, "bf16", 8, 2, 2),
     "bf16_40k_rows": (171, 45, 45, 20480, "bf16", 8, 3, 4),
+    "bf16_56k_rows": (173, 37, 40, 28672, "bf16", 8, 2, 2),
     "f32_256k_rows": (172, 23, 25, 65536, "f32", 4, 2, 2),
 }
 # Ring slots the bulk dispatch keeps for each case (0: falls back to the vector kernel).
-BULK_STAGES = {"bf16_32k_rows": 6, "bf16_40k_rows": 0, "f32_256k_rows": 0}
+BULK_STAGES = {"bf16_32k_rows": 6, "bf16_40k_rows": 5, "bf16_56k_rows": 0, "f32_256k_rows": 0}
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
