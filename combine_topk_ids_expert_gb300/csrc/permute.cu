@@ -7,20 +7,24 @@
 // stride).
 //
 // HBM-bound: reads T rows and writes up to T*K rows. Kernels:
-//   dispatch_tile<ONEPASS> : one CTA (8 warps) per layout tile, about one per
-//                    SM. Thread 0 starts bulk async loads of the tile's rows
-//                    into a shared-memory ring before the layout is known
-//                    (the rows do not depend on it). The one-pass form (the
-//                    default, a cooperative launch) then counts its tile,
+//   dispatch_tile<ONEPASS, SMALL> : one CTA (8 warps) per layout tile, about
+//                    one per SM. Thread 0 starts bulk async loads of the
+//                    tile's rows into a shared-memory ring before the layout
+//                    is known (the rows do not depend on it). The one-pass
+//                    form (the default, a cooperative launch; it first waits
+//                    for the previous kernel in the stream) counts its tile,
 //                    meets every other CTA at a grid barrier and derives its
-//                    prefixes from all tiles' counts; the fused form waits
-//                    for the separate count and scan kernels instead. Then
-//                    all warps compute the tile's positions into shared
-//                    memory, and warp 0 streams the rows out: lane k issues
-//                    the bulk store of destination k; warps 1-7 write scores
-//                    and sources. Completion of loads is tracked by mbarriers
-//                    (bounded waits); a slot is reused only after its stores
-//                    have read it (cp.async.bulk.wait_group.read).
+//                    prefixes from all tiles' counts; with SMALL (calls of
+//                    few pairs) every CTA counts all of the call's ids instead
+//                    and there is no barrier; the fused form waits for the
+//                    separate count and scan kernels. Then all warps compute
+//                    the tile's positions into shared memory, and warp 0
+//                    streams the rows out: lane k issues the bulk store of
+//                    destination k; warps 1-7 write scores and sources. CTAs
+//                    that finish their own tokens take the last ones of the
+//                    others from a shared pool. Completion of loads is tracked
+//                    by mbarriers (bounded waits); a slot is reused only after
+//                    its stores have read it (cp.async.bulk.wait_group.read).
 //   permute_bulk   : the same ring for a standalone permute (positions from
 //                    global memory, prefetched two tokens ahead), one warp per
 //                    CTA, one CTA per SM, tokens strided by the grid.
