@@ -379,10 +379,10 @@ def run_gb300(args) -> dict | None:
     import torch
 
     world, rank, local = dist_env()
+    torch.cuda.set_device(local)          # before NCCL, so its communicator binds this GPU
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
     import combine_topk_ids_expert_gb300 as ep
