@@ -35,6 +35,7 @@ constexpr int kCopyThreads = 128;
 constexpr int kLag = 4;                            // store groups in flight before a slot is reused
 constexpr int kMaxStages = 32;
 constexpr int kFusedSmemCap = 227 * 1024 - 1024;   // dynamic shared memory of the fused kernel
+constexpr int kOnepassStatic = 2048;               // the one-pass kernel's extra static arrays
 
 int slot_bytes_of(int64_t row_bytes) { return (int)((row_bytes + 127) / 128 * 128); }
 
@@ -53,9 +54,12 @@ __device__ __forceinline__ unsigned long long rank_mask(const int32_t* ids, int6
 // Dedupe row of each (token, rank) of layout tile `tile`: written to
 // a.tok_pos[t][r] and, if s_tok is given, to s_tok[i * R + r] (i = token in the
 // tile); -1 where the token selects none of rank r's experts. s_rbase holds
-// kLayoutWarps * kMaxRanks ints. Ends with __syncthreads.
+// kLayoutWarps * kMaxRanks ints. The distinct tokens per rank of the tiles
+// before this one come from s_tokpre[r] if given, else from the scan's
+// l.tile_tok_pre. Ends with __syncthreads.
 __device__ __forceinline__ void tile_dedup_rows(const LayoutArgs& l, const DedupArgs& a, int tile,
-                                                int (*s_rbase)[kMaxRanks], int* s_tok)
+                                                int (*s_rbase)[kMaxRanks], int* s_tok,
+                                                const int* s_tokpre = nullptr)
 {
     const int64_t t0 = (int64_t)tile * l.tpt;
     const int64_t t1 = min(l.T, t0 + l.tpt);
@@ -86,7 +90,8 @@ __device__ __forceinline__ void tile_dedup_rows(const LayoutArgs& l, const Dedup
     // distinct tokens of all earlier tiles.
     if (threadIdx.x < R) {
         const int r = threadIdx.x;
-        int base = (int)((int64_t)r * a.P) + __ldcg(l.tile_tok_pre + (int64_t)tile * R + r);
+        int base = (int)((int64_t)r * a.P) +
+                   (s_tokpre ? s_tokpre[r] : __ldcg(l.tile_tok_pre + (int64_t)tile * R + r));
         for (int w = 0; w < kLayoutWarps; ++w) {
             const int c = s_rbase[w][r];
             s_rbase[w][r] = base;
@@ -284,6 +289,139 @@ dedup_fused_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
     griddep_launch_dependents();
 }
 
+// The dedupe dispatch in one cooperative kernel: the one-pass layout (this
+// tile's counts, a grid barrier, every tile's counts summed from L2) replaces
+// the count and scan kernels, then the same positions, dedupe rows and copies
+// as dedup_fused. Thread 0 starts the tile's first row loads right after the
+// histogram. Shared memory: dedup_fused's, then [3 * Ep ints].
+__global__ void __launch_bounds__(kLayoutThreads, 1)
+dedup_onepass_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kMaxStages];
+    __shared__ int s_rank[3][kMaxRanks];
+    __shared__ int s_tk[kMaxRanks];
+    __shared__ int s_tokpre[kMaxRanks];
+    __shared__ int s_wsum[kLayoutWarps];
+    __shared__ int s_flag;
+    __shared__ uint32_t s_epoch;
+    int* s_base = reinterpret_cast<int*>(smem + (size_t)stages * slot_bytes);
+    int (*s_rbase)[kMaxRanks] = reinterpret_cast<int (*)[kMaxRanks]>(s_base + kLayoutWarps * L.Ep);
+    int* s_tok = s_base + kLayoutWarps * L.Ep + kLayoutWarps * kMaxRanks;
+    int* s_seed = s_tok + L.tpt * a.R;
+    int* s_tot = s_seed + L.Ep;
+    int* s_off = s_tot + L.Ep;
+    const int tile = blockIdx.x;
+    const int64_t t0 = (int64_t)tile * L.tpt;
+    const int64_t t1 = min(L.T, t0 + L.tpt);
+    const int n_my = (int)(t1 - t0);
+    const int R = a.R, K = a.K, eloc = a.E / a.R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bytes = static_cast<uint32_t>(a.row_bytes);
+    const uint32_t slot0 = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
+    uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
+    const int n_pro = n_my < stages ? n_my : stages;
+    // Whether dedupe row q is to be written: q >= 0 and inside the call's R * P
+    // rows. Rows always are when the layout is sound; one outside (possible
+    // only if the grid barrier's words were corrupted and it opened early) is
+    // skipped and reported, so that no store leaves the buffer.
+    const int64_t rows_cap = (int64_t)R * a.P;
+    auto in_rows = [&](int q) {
+        if (q < 0) return false;
+        if ((int64_t)q < rows_cap) return true;
+        atomicOr(a.err, kErrRowOob);
+        return false;
+    };
+
+    auto issue_load = [&](int i) {
+        const int s = i % stages;
+        const uint32_t bar = bar0 + 8u * s;
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(slot0 + (uint32_t)s * (uint32_t)slot_bytes, x + (t0 + i) * a.row_bytes, bytes, bar);
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(bar0 + 8u * s, 1u);
+        fence_mbar_init();
+    }
+    // Inputs may come from the previous kernel in the stream.
+    griddep_wait();
+    const bool ok_layout =
+        onepass_layout(L, tile, s_base, s_seed, s_tot, s_off, s_rank, s_tk, s_wsum, &s_flag,
+                       &s_epoch, nullptr, s_tokpre, [&] {
+                           for (int i = 0; i < n_pro; ++i) issue_load(i);
+                       });
+    if (!ok_layout) {   // barrier timed out: report, let this CTA's loads land, leave
+        if (threadIdx.x == 0) {
+            atomicOr(a.err, kErrTimeout);
+            drain_ring(bar0, stages, 0, n_pro);
+        }
+        griddep_launch_dependents();
+        return;
+    }
+    if (tile == 0) {
+        for (int e = threadIdx.x; e < L.E; e += blockDim.x) {
+            L.cnt[e] = s_tot[e];
+            L.expert_offset[e] = s_off[e];
+        }
+        if (threadIdx.x < L.R) {
+            L.rows_per_rank[threadIdx.x] = s_rank[0][threadIdx.x];
+            L.rank_prefix[threadIdx.x] = s_rank[1][threadIdx.x];
+            L.tokens_in_rank[threadIdx.x] = s_rank[2][threadIdx.x];
+        }
+    }
+    tile_positions(L, tile, s_base, L.pos, nullptr, s_seed);   // per-expert rows, for the expansion
+    tile_dedup_rows(L, a, tile, s_rbase, s_tok, s_tokpre);     // ends with __syncthreads
+
+    if (warp == 0) {
+        bool ok = true;
+        int i = 0;
+        for (; i < n_my; ++i) {
+            const int s = i % stages;
+            if (!mbar_wait(bar0 + 8u * s, (uint32_t)((i / stages) & 1))) {
+                ok = false;
+                break;
+            }
+            for (int r = lane; r < R; r += 32) {
+                const int q = s_tok[i * R + r];
+                if (in_rows(q))
+                    bulk_s2g(rx + (int64_t)q * a.row_bytes, slot0 + (uint32_t)s * (uint32_t)slot_bytes,
+                             bytes);
+            }
+            bulk_commit();
+            const int j = i - kLag;
+            if (j >= 0 && j + stages < n_my) {
+                bulk_wait_read<kLag>();
+                __syncwarp();
+                if (lane == 0) issue_load(j + stages);
+            }
+        }
+        bulk_wait_all();
+        if (!ok && lane == 0) {
+            atomicOr(a.err, kErrTimeout);
+            int issued_hi = (i - kLag) + stages;   // loads issued for tokens < issued_hi
+            if (issued_hi < n_pro) issued_hi = n_pro;
+            drain_ring(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my);
+        }
+    } else {
+        // Per dedupe row: source token, and per k the local expert index and score.
+        const int per_tok = R * K;
+        for (int j = threadIdx.x - 32; j < n_my * per_tok; j += kLayoutThreads - 32) {
+            const int i = j / per_tok, r = (j / K) % R, k = j % K;
+            const int q = s_tok[i * R + r];
+            if (!in_rows(q)) continue;
+            const int64_t t = t0 + i;
+            const int e = valid_id(__ldcg(a.ids + t * K + k), a.E);
+            const bool mine = e >= 0 && e / eloc == r;
+            a.recv_topk_idx[(int64_t)q * K + k] = mine ? e - r * eloc : -1;
+            a.recv_topk_w[(int64_t)q * K + k] = mine ? __ldcg(a.scores + t * K + k) : 0.0f;
+            if (k == 0) a.recv_tok_src[q] = (int32_t)t;
+        }
+    }
+    griddep_launch_dependents();
+}
+
 __global__ void __launch_bounds__(kCopyThreads)
 dedup_expand_kernel(DedupArgs a, const int32_t* pos, void* y)
 {
@@ -374,6 +512,56 @@ cudaError_t launch_dedup_fused(const LayoutArgs& l, const DedupArgs& a, const La
     const size_t smem = (size_t)(stages * slot + fixed);
     return launch_kernel(dedup_fused_kernel, dim3(l.ntiles), dim3(kLayoutThreads), smem, o, l, a,
                          (int)stages, slot);
+}
+
+cudaError_t launch_dedup_onepass(const LayoutArgs& l, const DedupArgs& a, const LaunchOpts& o,
+                                 bool pdl_ok)
+{
+    // An empty call still writes its (zero) layout: the separate kernels do that.
+    if (l.ntiles <= 0 || a.T <= 0 || !l.gbar) return cudaErrorNotSupported;
+    static bool attr_set = false;
+    if (!attr_set) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(dedup_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kFusedSmemCap - kOnepassStatic);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int slot = slot_bytes_of(a.row_bytes);
+    const int64_t fixed = ((int64_t)kLayoutWarps * l.Ep + (int64_t)kLayoutWarps * kMaxRanks +
+                           l.tpt * a.R + 3 * (int64_t)l.Ep) * 4;
+    int64_t stages = (kFusedSmemCap - kOnepassStatic - fixed) / slot;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (a.row_bytes > (1 << 20) || stages < kLag + 2) return cudaErrorNotSupported;
+    const size_t smem = (size_t)(stages * slot + fixed);
+    // Every CTA must be resident at once for the grid barrier.
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dedup_onepass_kernel,
+                                                      kLayoutThreads, smem) != cudaSuccess)
+        return cudaErrorNotSupported;
+    if ((int64_t)per_sm * sms < l.ntiles) return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(l.ntiles);
+    cfg.blockDim = dim3(kLayoutThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = o.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (o.pdl && pdl_ok) ? 2 : 1;
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, dedup_onepass_kernel, l, a, (int)stages, slot);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {   // fewer SMs than the device reports (MPS)
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+    if (e == cudaSuccess && o.launches) ++*o.launches;
+    return e;
 }
 
 cudaError_t launch_dedup_expand(const DedupArgs& a, const int32_t* pos, void* y,

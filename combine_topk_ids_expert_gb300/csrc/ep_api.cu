@@ -691,17 +691,25 @@ ep_status ep_dispatch_dedup(ep_buffer* buf, const void* x, const float* scores, 
     la.tile_tok_pre = buf->tile_tok_pre;
     const ep::LaunchOpts o = opts(buf, s);
     const ep::DedupArgs da = dedup_args(buf, x, scores, ids, T, N);
-    if (ep::launch_layout_counts(la, o) != cudaSuccess) return EP_ERR_CUDA;
-    remember_layout(buf, T, N);
-    const cudaError_t e =
-        buf->dedup_fused ? ep::launch_dedup_fused(la, da, o) : cudaErrorNotSupported;
-    if (e == cudaErrorNotSupported) {
-        if (ep::launch_layout_positions(la, o) != cudaSuccess ||
-            ep::launch_dedup(la, da, o) != cudaSuccess)
+    // One cooperative kernel where it fits; else count + scan, then the fused
+    // kernel (or positions + copies).
+    const cudaError_t e0 = (buf->onepass && buf->dedup_fused)
+                               ? ep::launch_dedup_onepass(la, da, o, buf->coop_pdl)
+                               : cudaErrorNotSupported;
+    if (e0 != cudaSuccess && e0 != cudaErrorNotSupported) return EP_ERR_CUDA;
+    if (e0 == cudaErrorNotSupported) {
+        if (ep::launch_layout_counts(la, o) != cudaSuccess) return EP_ERR_CUDA;
+        const cudaError_t e =
+            buf->dedup_fused ? ep::launch_dedup_fused(la, da, o) : cudaErrorNotSupported;
+        if (e == cudaErrorNotSupported) {
+            if (ep::launch_layout_positions(la, o) != cudaSuccess ||
+                ep::launch_dedup(la, da, o) != cudaSuccess)
+                return EP_ERR_CUDA;
+        } else if (e != cudaSuccess) {
             return EP_ERR_CUDA;
-    } else if (e != cudaSuccess) {
-        return EP_ERR_CUDA;
+        }
     }
+    remember_layout(buf, T, N);
     buf->last_dedup = true;
     if (out) {
         out->recv_x = buf->recv_x;

@@ -348,4 +348,187 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* bar, uint32_t n, uint32_t
     }
 }
 
+// ---- one-pass layout ----------------------------------------------------------
+
+// Second half of the layout, from the call's per-expert totals s_tot[e] and
+// this tile's counts of earlier pairs s_seed[e]: s_off[e] = expert_offset[e],
+// s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r] (inclusive),
+// and s_seed[e] += expert_offset[e] (this tile's first receive row of e).
+// s_work: at least E ints. Ends with __syncthreads.
+__device__ __forceinline__ void layout_offsets(const LayoutArgs& L, int* s_work, int* s_seed,
+                                               const int* s_tot, int* s_off,
+                                               int (*s_rank)[kMaxRanks], int* s_wsum)
+{
+    const int Ep = L.Ep, E = L.E, R = L.R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Inclusive prefix of the totals over experts (C consecutive experts per
+    // thread, then warps, then the block) into s_off.
+    const int C = (Ep + kLayoutThreads - 1) / kLayoutThreads;
+    const int e0 = threadIdx.x * C;
+    int run = 0;
+    for (int j = 0; j < C; ++j) {
+        const int e = e0 + j;
+        if (e < E) run += s_tot[e];
+    }
+    int v = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += n;
+    }
+    if (lane == 31) s_wsum[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int c = s_wsum[w];
+            s_wsum[w] = acc;
+            acc += c;
+        }
+    }
+    __syncthreads();
+    int incl = v - run + s_wsum[warp];   // exclusive prefix of this thread's first expert
+    for (int j = 0; j < C; ++j) {
+        const int e = e0 + j;
+        if (e < E) {
+            incl += s_tot[e];
+            s_off[e] = incl;
+        }
+    }
+    __syncthreads();
+
+    // Offsets: ranks own contiguous expert blocks (packed: back to back).
+    const int eloc = E / R;
+    if (threadIdx.x < R) {
+        const int r = threadIdx.x;
+        const int hi = s_off[(r + 1) * eloc - 1];
+        const int lo = (r > 0) ? s_off[r * eloc - 1] : 0;
+        s_rank[0][r] = hi - lo;
+        s_rank[1][r] = hi;
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int excl = s_off[e] - s_tot[e];
+        int off;
+        if (L.packed) {
+            off = excl;
+        } else {
+            const int r = e / eloc;
+            const int lo = (r > 0) ? s_off[r * eloc - 1] : 0;
+            off = (int)((int64_t)r * L.S + (excl - lo));
+        }
+        s_work[e] = off;   // s_off still holds the inclusive prefix other threads read
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        s_off[e] = s_work[e];
+        s_seed[e] += s_work[e];
+    }
+    __syncthreads();
+}
+
+// One-pass layout of tile `tile` (the one-pass dispatch and dedupe): this tile's counts, a
+// grid barrier, then every tile's counts summed per expert (before this tile,
+// and in all) and scanned over experts. Leaves s_seed[e] = this tile's first
+// receive row of expert e, s_tot[e] = cnt[e], s_off[e] = expert_offset[e],
+// s_rank[0][r] = rows_per_rank[r], s_rank[1][r] = rank_prefix[r],
+// s_rank[2][r] = tokens_in_rank[r]. Global writes: this tile's rows of the
+// count tables and the barrier words only. False if the barrier timed out.
+// s_work: kLayoutWarps * Ep ints. s_ids: the tile's pairs' ids are kept there
+// (tile_histogram) for the positions, or null. s_tokpre, if given, receives
+// each rank's distinct tokens in the tiles before this one (kMaxRanks ints).
+// issue_rows runs on thread 0 right after the histogram.
+template <typename IssueRows>
+__device__ __forceinline__ bool onepass_layout(const LayoutArgs& L, int tile, int* s_work,
+                                               int* s_seed, int* s_tot, int* s_off,
+                                               int (*s_rank)[kMaxRanks], int* s_tok,
+                                               int* s_wsum, int* s_flag, uint32_t* s_epoch,
+                                               int* s_ids, int* s_tokpre, IssueRows issue_rows)
+{
+    const int Ep = L.Ep, R = L.R, G = (int)gridDim.x;
+    // The barrier's generation, read now so that its latency hides behind the
+    // histogram (it cannot change before every CTA of this launch arrives).
+    const uint32_t gen = threadIdx.x == 0 ? grid_generation(L.gbar) : 0u;
+    // The ids first: issued behind the tile's row loads they would wait for
+    // those; the rows are started right after the histogram instead (they are
+    // in by the time the positions are known).
+    tile_histogram(L, tile, s_tot, s_tok, s_ids);   // ends with __syncthreads
+    if (threadIdx.x == 0) issue_rows();
+    for (int e = threadIdx.x; e < Ep; e += blockDim.x) L.tile_cnt[(int64_t)tile * Ep + e] = s_tot[e];
+    if (threadIdx.x < R) L.tile_tok[(int64_t)tile * R + threadIdx.x] = s_tok[threadIdx.x];
+    // The token pool's counter starts over for this call: the previous kernel
+    // in the stream has completed (the kernel waited for it on entry), and no
+    // CTA of this call takes from the pool before the barrier.
+    if (tile == 0 && threadIdx.x == 0) L.gbar[2] = 0u;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *s_flag = grid_barrier(L.gbar, (uint32_t)G, gen, s_epoch) ? 1 : 0;
+    __syncthreads();
+    if (!*s_flag) return false;
+
+    // Column sums of all tiles' counts: thread (g, q) adds the 4-expert column
+    // q over tiles g, g + NG, ... into s_work[2g][.] (tiles before this one)
+    // and s_work[2g + 1][.] (all tiles).
+    const int Q = Ep / 4;
+    int NG = kLayoutThreads / Q;
+    if (NG > kLayoutWarps / 2) NG = kLayoutWarps / 2;
+    if (NG < 1) NG = 1;
+    const int g = threadIdx.x / Q, q = threadIdx.x % Q;
+    if (g < NG && q < Q) {
+        // Loads in batches of kSumBatch rows, all in flight before the adds.
+        constexpr int kSumBatch = 20;
+        const int4* tc = reinterpret_cast<const int4*>(L.tile_cnt);
+        int4 bef = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+        for (int tb = g; tb < G; tb += kSumBatch * NG) {
+            int4 v[kSumBatch];
+#pragma unroll
+            for (int u = 0; u < kSumBatch; ++u) {
+                const int t = tb + u * NG;
+                v[u] = (t < G) ? ld_cg_v4(tc + (int64_t)t * Q + q) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kSumBatch; ++u) {
+                tot.x += v[u].x; tot.y += v[u].y; tot.z += v[u].z; tot.w += v[u].w;
+                if (tb + u * NG < tile) {
+                    bef.x += v[u].x; bef.y += v[u].y; bef.z += v[u].z; bef.w += v[u].w;
+                }
+            }
+        }
+        int* b = s_work + (2 * g) * Ep + 4 * q;
+        int* a = s_work + (2 * g + 1) * Ep + 4 * q;
+        b[0] = bef.x; b[1] = bef.y; b[2] = bef.z; b[3] = bef.w;
+        a[0] = tot.x; a[1] = tot.y; a[2] = tot.z; a[3] = tot.w;
+    }
+    // Distinct tokens per rank over all tiles (and over the tiles before this
+    // one): thread (g2, r) adds rows g2, g2 + NG2, ...
+    const int NG2 = kLayoutThreads / R;
+    const int g2 = threadIdx.x / R, r2 = threadIdx.x % R;
+    int tsum = 0, tbef = 0;
+    if (g2 < NG2)
+        for (int t = g2; t < G; t += NG2) {
+            const int c = __ldcg(L.tile_tok + (int64_t)t * R + r2);
+            tsum += c;
+            if (t < tile) tbef += c;
+        }
+    __syncthreads();
+    for (int e = threadIdx.x; e < Ep; e += blockDim.x) {
+        int b = 0, a = 0;
+        for (int gg = 0; gg < NG; ++gg) {
+            b += s_work[(2 * gg) * Ep + e];
+            a += s_work[(2 * gg + 1) * Ep + e];
+        }
+        s_seed[e] = b;
+        s_tot[e] = a;
+    }
+    if (threadIdx.x < R) {
+        s_rank[2][threadIdx.x] = 0;
+        if (s_tokpre) s_tokpre[threadIdx.x] = 0;
+    }
+    __syncthreads();
+    if (g2 < NG2 && tsum) atomicAdd(&s_rank[2][r2], tsum);
+    if (s_tokpre && g2 < NG2 && tbef) atomicAdd(&s_tokpre[r2], tbef);
+
+    layout_offsets(L, s_work, s_seed, s_tot, s_off, s_rank, s_wsum);
+    return true;
+}
+
 }  // namespace ep

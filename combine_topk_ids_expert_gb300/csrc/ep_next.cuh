@@ -29,6 +29,12 @@ cudaError_t launch_dedup(const LayoutArgs& l, const DedupArgs& a, const LaunchOp
 // per-expert positions + dedupe rows + copies in one kernel (after
 // launch_layout_counts); cudaErrorNotSupported if a tile's tables do not fit.
 cudaError_t launch_dedup_fused(const LayoutArgs& l, const DedupArgs& a, const LaunchOpts& o);
+// The dedupe dispatch as one cooperative kernel (layout with a grid barrier,
+// positions, dedupe rows, copies); needs l.gbar. cudaErrorNotSupported where
+// the rows do not fit its ring or the tiles cannot all be resident. pdl_ok as
+// for launch_dispatch_onepass.
+cudaError_t launch_dedup_onepass(const LayoutArgs& l, const DedupArgs& a, const LaunchOpts& o,
+                                 bool pdl_ok);
 // y[pos[t][k]] = recv_x[tok_pos[t][r(e)]] for every routed pair.
 cudaError_t launch_dedup_expand(const DedupArgs& a, const int32_t* pos, void* y,
                                 const LaunchOpts& o);

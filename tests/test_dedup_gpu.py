@@ -11,7 +11,7 @@ import torch
 
 import combine_topk_ids_expert_gb300 as ep
 import workloads as W
-from gpu_util import assert_combine_equal, bits, to_dev, to_np, torch_dtype
+from gpu_util import assert_combine_equal, assert_layout_equal, bits, to_dev, to_np, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -27,12 +27,15 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("fused", ["1", "0"])
+@pytest.mark.parametrize("form", ["onepass", "fused", "separate"])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_dedup_parity_and_expand(orc, monkeypatch, case, fused):
-    # fused: one kernel after the counts (positions, dedupe rows, bulk copies);
-    # "0": positions, dedupe rows and vector copies as separate kernels
-    monkeypatch.setenv("EP_DEDUP_FUSED", fused)
+def test_dedup_parity_and_expand(orc, monkeypatch, case, form):
+    # onepass (the default): one cooperative kernel (layout with a grid
+    # barrier, positions, dedupe rows, bulk copies); fused: the same kernel
+    # body after separate count and scan kernels; separate: positions, dedupe
+    # rows and vector copies as separate kernels
+    monkeypatch.setenv("EP_DEDUP_FUSED", "0" if form == "separate" else "1")
+    monkeypatch.setenv("EP_DISPATCH_ONEPASS", "1" if form == "onepass" else "0")
     seed, T, N, N_max, D, dtype, E, K, R, ik = CASES[case]
     x = W.hidden(seed, T, D, dtype)
     ids, sc = W.routing(seed, T, E, K, ik, "sigmoid_norm")
@@ -49,6 +52,7 @@ def test_dedup_parity_and_expand(orc, monkeypatch, case, fused):
     ref = orc.dispatch_dedup(x, sc, ids, N, E, R)
     P = ref["P"]
     tir = ref["tokens_in_rank"]
+    assert_layout_equal(dd.layout, orc.layout(ids, N, E, R))   # counts, offsets, positions
     assert np.array_equal(to_np(dd.layout.tokens_in_rank), tir)
     assert np.array_equal(to_np(dd.tok_pos), ref["tok_pos"])
     rx = to_np(dd.recv_x.reshape(R * P, D))
