@@ -259,3 +259,29 @@ def test_grid_barrier_opened_early_stays_in_bounds(orc, monkeypatch):
     want, _ = orc.combine(ref["recv_x"], sc, ref["pos"], ref["rank_prefix"], ref["S"], R)
     assert_combine_equal(to_np(out), want)
     buf.close()
+
+
+def test_dedupe_grid_barrier_runs_out_and_recovers(orc):
+    # The one-pass dedupe meets its CTAs at the same grid barrier as the
+    # dispatch: with the arrival count seeded past the grid size every wait
+    # runs out, the kernel reports EP_DEVERR_TIMEOUT after its loads land,
+    # and after the host resets the words the next dedupe is oracle-exact.
+    buf = ep.Buffer(64, D, E, R, K, dtype=torch.bfloat16)
+    x, ids, sc = small(T=40, seed=13)
+    xd, idd, scd = to_dev(x), to_dev(ids), to_dev(sc)
+    ws = buf.workspace
+    gbar = ws.numel() - 2 * 256      # the barrier's four words, then the error word
+    ws[gbar:gbar + 4].view(torch.int32).fill_(1 << 20)
+    n0 = buf.info()["kernel_launches"]
+    buf.dispatch_dedup(xd, scd, idd, 40)
+    torch.cuda.synchronize()
+    assert buf.info()["kernel_launches"] - n0 == 1, "expected the one-pass dedupe"
+    assert buf.device_error() & ep.EP_DEVERR_TIMEOUT
+    assert int(ws[gbar:gbar + 16].view(torch.int32).abs().sum().item()) == 0
+    dd = buf.dispatch_dedup(xd, scd, idd, 40)
+    torch.cuda.synchronize()
+    assert buf.device_error() == 0
+    ref = orc.dispatch_dedup(x, sc, ids, 40, E, R)
+    assert np.array_equal(to_np(dd.tok_pos), ref["tok_pos"])
+    assert np.array_equal(to_np(dd.layout.tokens_in_rank), ref["tokens_in_rank"])
+    buf.close()
