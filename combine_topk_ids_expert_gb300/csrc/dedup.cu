@@ -200,47 +200,23 @@ __device__ void drain_ring(uint32_t bar0, int stages, int from, int to)
         mbar_wait_until(bar0 + 8u * (uint32_t)(m % stages), (uint32_t)((m / stages) & 1), deadline);
 }
 
-// Positions + dedupe rows + copies of one layout tile per CTA (file comment).
-// Shared memory: [stages slots][kLayoutWarps * Ep ints][kLayoutWarps * kMaxRanks
-// ints][tile tokens * R ints].
-__global__ void __launch_bounds__(kLayoutThreads, 1)
-dedup_fused_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
+// Streams the tile's rows out of the shared-memory ring (warp 0: lane r issues
+// the bulk store of the token's row for rank r) while warps 1-7 write each
+// dedupe row's source token, local expert indices and scores. keep(q): whether
+// dedupe row q is written. The ring's first n_pro loads were issued already;
+// issue_load(i) starts the load of the tile's token i. On a timed-out wait it
+// reports EP_DEVERR_TIMEOUT and lets the loads in flight land.
+template <typename Keep, typename IssueLoad>
+__device__ __forceinline__ void dedup_stream_tile(const DedupArgs& a, int64_t t0, int n_my,
+                                                  int n_pro, int stages, int slot_bytes,
+                                                  uint32_t slot0, uint32_t bar0,
+                                                  const int* s_tok, Keep keep,
+                                                  IssueLoad issue_load)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[kMaxStages];
-    int* s_base = reinterpret_cast<int*>(smem + (size_t)stages * slot_bytes);
-    int (*s_rbase)[kMaxRanks] = reinterpret_cast<int (*)[kMaxRanks]>(s_base + kLayoutWarps * L.Ep);
-    int* s_tok = s_base + kLayoutWarps * L.Ep + kLayoutWarps * kMaxRanks;
-    const int tile = blockIdx.x;
-    const int64_t t0 = (int64_t)tile * L.tpt;
-    const int64_t t1 = min(L.T, t0 + L.tpt);
-    const int n_my = (int)(t1 - t0);
     const int R = a.R, K = a.K, eloc = a.E / a.R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bytes = static_cast<uint32_t>(a.row_bytes);
-    const uint32_t slot0 = smem_u32(smem);
-    const uint32_t bar0 = smem_u32(bars);
-    const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
     uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
-    const int n_pro = n_my < stages ? n_my : stages;
-
-    auto issue_load = [&](int i) {
-        const int s = i % stages;
-        const uint32_t bar = bar0 + 8u * s;
-        mbar_expect_tx(bar, bytes);
-        bulk_g2s(slot0 + (uint32_t)s * (uint32_t)slot_bytes, x + (t0 + i) * a.row_bytes, bytes, bar);
-    };
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) mbar_init(bar0 + 8u * s, 1u);
-        fence_mbar_init();
-        // The rows do not depend on the layout: start them before waiting for it.
-        for (int i = 0; i < n_pro; ++i) issue_load(i);
-    }
-
-    griddep_wait();                                   // counts and offsets are ready
-    tile_positions(L, tile, s_base, L.pos, nullptr);  // per-expert rows, for the expansion
-    tile_dedup_rows(L, a, tile, s_rbase, s_tok);      // ends with __syncthreads
-
     if (warp == 0) {
         bool ok = true;
         int i = 0;
@@ -252,7 +228,7 @@ dedup_fused_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
             }
             for (int r = lane; r < R; r += 32) {
                 const int q = s_tok[i * R + r];
-                if (q >= 0)
+                if (keep(q))
                     bulk_s2g(rx + (int64_t)q * a.row_bytes, slot0 + (uint32_t)s * (uint32_t)slot_bytes,
                              bytes);
             }
@@ -277,7 +253,7 @@ dedup_fused_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
         for (int j = threadIdx.x - 32; j < n_my * per_tok; j += kLayoutThreads - 32) {
             const int i = j / per_tok, r = (j / K) % R, k = j % K;
             const int q = s_tok[i * R + r];
-            if (q < 0) continue;
+            if (!keep(q)) continue;
             const int64_t t = t0 + i;
             const int e = valid_id(__ldcg(a.ids + t * K + k), a.E);
             const bool mine = e >= 0 && e / eloc == r;
@@ -286,6 +262,48 @@ dedup_fused_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
             if (k == 0) a.recv_tok_src[q] = (int32_t)t;
         }
     }
+}
+
+// Positions + dedupe rows + copies of one layout tile per CTA (file comment).
+// Shared memory: [stages slots][kLayoutWarps * Ep ints][kLayoutWarps * kMaxRanks
+// ints][tile tokens * R ints].
+__global__ void __launch_bounds__(kLayoutThreads, 1)
+dedup_fused_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kMaxStages];
+    int* s_base = reinterpret_cast<int*>(smem + (size_t)stages * slot_bytes);
+    int (*s_rbase)[kMaxRanks] = reinterpret_cast<int (*)[kMaxRanks]>(s_base + kLayoutWarps * L.Ep);
+    int* s_tok = s_base + kLayoutWarps * L.Ep + kLayoutWarps * kMaxRanks;
+    const int tile = blockIdx.x;
+    const int64_t t0 = (int64_t)tile * L.tpt;
+    const int64_t t1 = min(L.T, t0 + L.tpt);
+    const int n_my = (int)(t1 - t0);
+    const uint32_t bytes = static_cast<uint32_t>(a.row_bytes);
+    const uint32_t slot0 = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
+    const int n_pro = n_my < stages ? n_my : stages;
+
+    auto issue_load = [&](int i) {
+        const int s = i % stages;
+        const uint32_t bar = bar0 + 8u * s;
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(slot0 + (uint32_t)s * (uint32_t)slot_bytes, x + (t0 + i) * a.row_bytes, bytes, bar);
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(bar0 + 8u * s, 1u);
+        fence_mbar_init();
+        // The rows do not depend on the layout: start them before waiting for it.
+        for (int i = 0; i < n_pro; ++i) issue_load(i);
+    }
+
+    griddep_wait();                                   // counts and offsets are ready
+    tile_positions(L, tile, s_base, L.pos, nullptr);  // per-expert rows, for the expansion
+    tile_dedup_rows(L, a, tile, s_rbase, s_tok);      // ends with __syncthreads
+
+    dedup_stream_tile(a, t0, n_my, n_pro, stages, slot_bytes, slot0, bar0, s_tok,
+                      [](int q) { return q >= 0; }, issue_load);
     griddep_launch_dependents();
 }
 
@@ -315,13 +333,11 @@ dedup_onepass_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
     const int64_t t0 = (int64_t)tile * L.tpt;
     const int64_t t1 = min(L.T, t0 + L.tpt);
     const int n_my = (int)(t1 - t0);
-    const int R = a.R, K = a.K, eloc = a.E / a.R;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = a.R;
     const uint32_t bytes = static_cast<uint32_t>(a.row_bytes);
     const uint32_t slot0 = smem_u32(smem);
     const uint32_t bar0 = smem_u32(bars);
     const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
-    uint8_t* __restrict__ rx = static_cast<uint8_t*>(a.recv_x);
     const int n_pro = n_my < stages ? n_my : stages;
     // Whether dedupe row q is to be written: q >= 0 and inside the call's R * P
     // rows. Rows always are when the layout is sound; one outside (possible
@@ -374,51 +390,8 @@ dedup_onepass_kernel(LayoutArgs L, DedupArgs a, int stages, int slot_bytes)
     tile_positions(L, tile, s_base, L.pos, nullptr, s_seed);   // per-expert rows, for the expansion
     tile_dedup_rows(L, a, tile, s_rbase, s_tok, s_tokpre);     // ends with __syncthreads
 
-    if (warp == 0) {
-        bool ok = true;
-        int i = 0;
-        for (; i < n_my; ++i) {
-            const int s = i % stages;
-            if (!mbar_wait(bar0 + 8u * s, (uint32_t)((i / stages) & 1))) {
-                ok = false;
-                break;
-            }
-            for (int r = lane; r < R; r += 32) {
-                const int q = s_tok[i * R + r];
-                if (in_rows(q))
-                    bulk_s2g(rx + (int64_t)q * a.row_bytes, slot0 + (uint32_t)s * (uint32_t)slot_bytes,
-                             bytes);
-            }
-            bulk_commit();
-            const int j = i - kLag;
-            if (j >= 0 && j + stages < n_my) {
-                bulk_wait_read<kLag>();
-                __syncwarp();
-                if (lane == 0) issue_load(j + stages);
-            }
-        }
-        bulk_wait_all();
-        if (!ok && lane == 0) {
-            atomicOr(a.err, kErrTimeout);
-            int issued_hi = (i - kLag) + stages;   // loads issued for tokens < issued_hi
-            if (issued_hi < n_pro) issued_hi = n_pro;
-            drain_ring(bar0, stages, i, issued_hi < n_my ? issued_hi : n_my);
-        }
-    } else {
-        // Per dedupe row: source token, and per k the local expert index and score.
-        const int per_tok = R * K;
-        for (int j = threadIdx.x - 32; j < n_my * per_tok; j += kLayoutThreads - 32) {
-            const int i = j / per_tok, r = (j / K) % R, k = j % K;
-            const int q = s_tok[i * R + r];
-            if (!in_rows(q)) continue;
-            const int64_t t = t0 + i;
-            const int e = valid_id(__ldcg(a.ids + t * K + k), a.E);
-            const bool mine = e >= 0 && e / eloc == r;
-            a.recv_topk_idx[(int64_t)q * K + k] = mine ? e - r * eloc : -1;
-            a.recv_topk_w[(int64_t)q * K + k] = mine ? __ldcg(a.scores + t * K + k) : 0.0f;
-            if (k == 0) a.recv_tok_src[q] = (int32_t)t;
-        }
-    }
+    dedup_stream_tile(a, t0, n_my, n_pro, stages, slot_bytes, slot0, bar0, s_tok, in_rows,
+                      issue_load);
     griddep_launch_dependents();
 }
 
