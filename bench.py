@@ -551,6 +551,8 @@ def run_gb300(args) -> dict | None:
             avg = sum(arr) / len(arr)
             kern[name] = {"avg_us": avg * 1e3, "median_us": statistics.median(arr) * 1e3,
                           "algorithmic_bytes": nbk, "achieved_gbs": nbk / (avg / 1e3) / 1e9}
+        for k in kern.values():   # each kernel against the same measured peak
+            k["frac_of_peak"] = round(k["achieved_gbs"] / peak, 4)
         dom = "dispatch" if kern["dispatch"]["avg_us"] >= kern["combine"]["avg_us"] else "combine"
         ach = kern[dom]["achieved_gbs"]
         impl_name = {1: "vec", 2: "bulk"}[buf.info()["permute_impl"]]
